@@ -1,0 +1,438 @@
+"""Decode-step benchmark: one JSON line on rank 0.
+
+A step is one decode step (the whole per-layer kernel sequence, final norm, LM
+head and greedy arg-max) for one batch of sequences, replayed from the captured
+CUDA graph. Default workload: the 8B-class BF16 decoder at batch 1 with a
+per-sequence context drawn uniformly from [256, 2048] (random-init weights and
+random cache contents), each step feeding back the previous step's token ids and
+advancing every position by one.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 8b] [--batch 1]
+                  [--impl reference]
+
+Under torchrun every rank runs its own replica on its own GPU (the decode step
+has no cross-sequence exchange, so there is no collective on the data path);
+rank 0 prints the whole-job tokens/s over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from memory_bound_transformer_gb300 import blob as mblob  # noqa: E402
+from memory_bound_transformer_gb300 import capi, ledger  # noqa: E402
+from memory_bound_transformer_gb300.engine import Engine  # noqa: E402
+from synth import WORKLOADS, SynthModel, random_contexts, random_kv_pool, seeded_block_tables  # noqa: E402
+
+L2_BYTES = 126 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the gate/up GEMV
+# (8B shape, batch 1) from the ncu capture summarised in
+# profiles/gemv_swiglu_8b_b1.md; None until that capture matches this kernel.
+GEMV_TRAFFIC_BYTES = None
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="8b", choices=sorted(WORKLOADS))
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-kernel-timing", action="store_true")
+    ap.add_argument("--ladder", default=None, help="comma-separated graph ladder (default: the workload's)")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def build_case(wl, B, steps_total, device="cuda"):
+    cfg = wl.model
+    ctx = random_contexts(B, wl.context[0], wl.context[1], wl.seed + 2000)
+    cap = ctx + steps_total + 1
+    nb = int(sum(-(-int(c) // 16) for c in cap)) + 1
+    tables = seeded_block_tables(cap, 16, nb, wl.seed + 3000)
+    tables[tables < 0] = nb
+    model = SynthModel(cfg, wl.seed, device=device, cache=False)
+    blob = mblob.pack(cfg, model.tensors(), device=device)
+    eng = Engine(blob, nb)
+    del blob
+    torch.cuda.empty_cache()
+    pool = random_kv_pool(cfg, nb, wl.seed + 4000, device=device)
+    eng.pool().copy_(pool.view(torch.uint8).reshape(-1))
+    del pool
+    return cfg, ctx, tables, nb, eng
+
+
+def time_native(args, rank, world):
+    wl = WORKLOADS[args.workload]
+    B = args.batch or wl.batches[0]
+    K, W = args.steps, args.warmup
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cfg, ctx, tables, nb, eng = build_case(wl, B, K + W + (0 if args.no_e2e else K + 2))
+    mbs = tables.shape[1]
+    ladder = [int(x) for x in args.ladder.split(",")] if args.ladder else list(wl.ladder)
+    if B > max(ladder):
+        ladder = sorted(set(ladder) | {B})
+    eng.capture(ladder=ladder, max_blocks_per_seq=mbs)
+    kernels_per_step, uses_graph = eng.stats(B)
+    S = torch.cuda.current_stream()
+
+    total = K + W
+    pos_all = torch.tensor(np.stack([ctx + t for t in range(total)]), dtype=torch.int32, device=dev)
+    sl_all = pos_all + 1
+    bt = torch.tensor(tables, device=dev)
+    ids = [torch.randint(0, cfg.vocab, (B,), dtype=torch.int32, device=dev) for _ in range(2)]
+
+    def step(t):
+        eng.step(ids[t % 2], pos_all[t], bt, sl_all[t], ids[(t + 1) % 2])
+
+    for t in range(W):
+        step(t)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = Clocks(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(S)
+    for t in range(K):
+        step(W + t)
+        ev[t + 1].record(S)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ck = clocks.stop()
+    per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(K)]
+    total_ms = ev[0].elapsed_time(ev[K])
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # algorithmic bytes per step over the timed steps (contexts grow by one per step)
+    byte_steps = [ledger.step_bytes(cfg, ctx + W + t + 1) for t in range(K)]
+    avg_bytes = float(np.mean(byte_steps))
+
+    # dominant kernel: the fused gate/up + SwiGLU GEMV (largest matrix of the layer),
+    # timed on its launching stream over all layers' matrices (each > L2)
+    kern = None if args.no_kernel_timing else time_gemv_swiglu(cfg, wl, B, dev)
+
+    e2e = None if args.no_e2e else time_e2e(eng, cfg, ctx + W + K, bt, B, K, dev, tables)
+    eng.close()
+    return dict(cfg=cfg, B=B, K=K, W=W, total_ms=total_ms, per_step=per_step, avg_bytes=avg_bytes,
+                clocks=ck, kernels_per_step=kernels_per_step, uses_graph=uses_graph, kern=kern,
+                e2e=e2e, ctx=ctx, wl=wl)
+
+
+def time_gemv_swiglu(cfg, wl, B, dev, reps=3):
+    """Average duration of the gate/up GEMV (SwiGLU epilogue) on its own stream
+    with CUDA events, cycling through every layer's matrix."""
+    model = SynthModel(cfg, wl.seed + 17, device=dev, cache=False)
+    nl = min(cfg.n_layers, max(2, int(24e9 // (2 * cfg.ffn * cfg.hidden * (1 if cfg.weight_dtype == "fp8" else 2)))))
+    mats = [model.get("w_gu", l) for l in range(nl)]
+    x = torch.randn((B, cfg.hidden), device=dev).to(torch.bfloat16)
+    act = torch.empty((B, cfg.ffn), dtype=torch.bfloat16, device=dev)
+    wdt = capi.DTYPE_E4M3 if cfg.weight_dtype == "fp8" else capi.DTYPE_BF16
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        for m in mats[:2]:
+            capi.op_gemv(capi.EPI_SWIGLU, wdt, m["w"], m.get("s"), cfg.ffn, cfg.hidden, x, B, act=act, stream=s)
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        n = 0
+        for _ in range(reps):
+            for m in mats:
+                capi.op_gemv(capi.EPI_SWIGLU, wdt, m["w"], m.get("s"), cfg.ffn, cfg.hidden, x, B, act=act,
+                             stream=s)
+                n += 1
+        e1.record(s)
+        s.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    w = 1 if cfg.weight_dtype == "fp8" else 2
+    nbytes = 2 * cfg.ffn * cfg.hidden * w + (2 * cfg.ffn * 4 if cfg.weight_dtype == "fp8" else 0) \
+        + B * cfg.hidden * 2 + B * cfg.ffn * 2
+    del mats
+    torch.cuda.empty_cache()
+    return {"ms": ms, "bytes": nbytes, "launches": n}
+
+
+def time_e2e(eng, cfg, ctx0, bt, B, K, dev, tables):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs from pinned host memory and reads the next ids back."""
+    h_tok = torch.randint(0, cfg.vocab, (B,), dtype=torch.int32).pin_memory()
+    h_pos = torch.zeros(B, dtype=torch.int32).pin_memory()
+    h_sl = torch.zeros(B, dtype=torch.int32).pin_memory()
+    h_bt = torch.tensor(tables).pin_memory()
+    h_out = torch.zeros(B, dtype=torch.int32).pin_memory()
+    d_tok = torch.empty(B, dtype=torch.int32, device=dev)
+    d_pos, d_sl = torch.empty_like(d_tok), torch.empty_like(d_tok)
+    d_bt = torch.empty_like(bt)
+    d_out = torch.empty_like(d_tok)
+    S = torch.cuda.current_stream()
+    h2d = (3 * B + h_bt.numel()) * 4
+    d2h = B * 4
+
+    def one(t):
+        h_pos.copy_(torch.from_numpy(ctx0 + t))
+        h_sl.copy_(h_pos + 1)
+        d_tok.copy_(h_tok, non_blocking=True)
+        d_pos.copy_(h_pos, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        eng.step(d_tok, d_pos, d_bt, d_sl, d_out)
+        h_out.copy_(d_out, non_blocking=True)
+        S.synchronize()
+        h_tok.copy_(h_out)
+
+    one(0)
+    one(1)
+    t0 = time.perf_counter()
+    for t in range(K):
+        one(2 + t)
+    dt = time.perf_counter() - t0
+    return {"value": B * K / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def cpu_baseline(wl, B, budget_s=20.0):
+    """The fp64 oracle on this host's cores, on a bounded sample of the workload:
+    embedding + final norm + LM head, plus as many decoder layers as fit the
+    budget, extrapolated to the full depth. Weights are copied to host memory
+    before the clock starts."""
+    from oracle.decode import OracleKV, decode_step
+    from synth import raw_numpy
+
+    cfg = wl.model
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    ctx = random_contexts(B, wl.context[0], wl.context[1], wl.seed + 2000)
+    rows = min(B, 1)
+    ctx_s = ctx[:rows]
+    cap = ctx_s + 1
+    nb = int(sum(-(-int(c) // 16) for c in cap)) + 1
+    tables = seeded_block_tables(cap, 16, nb, wl.seed + 3000)
+    model = SynthModel(cfg, wl.seed, device=dev, cache=False)
+    cache = {}
+
+    def W(name, layer):
+        k = (name, layer)
+        if k not in cache:
+            cache[k] = {a: raw_numpy(v) for a, v in model.get(name, layer).items()}
+        return cache[k]
+
+    def run(nl):
+        one = random_kv_pool(cfg.replace(n_layers=max(nl, 1)), nb, wl.seed + 4000, device="cpu")
+        raw = one.numpy().view(np.uint16) if one.dtype == torch.int16 else one.numpy()
+        kv = OracleKV(raw, np.ones(max(nl, 1)), np.ones(max(nl, 1)))
+        t0 = time.perf_counter()
+        decode_step(W, cfg, kv, [1] * rows, ctx_s, tables, ctx_s + 1, layers=range(nl))
+        return time.perf_counter() - t0
+
+    W("embed", -1), W("g_final", -1), W("lm_head", -1)
+    t0 = run(0)
+    nl = 1
+    for n in ("g_attn", "w_qkv", "w_o", "g_ffn", "w_gu", "w_down"):
+        W(n, 0)
+    t1 = run(1)
+    per_layer = max(t1 - t0, 1e-9)
+    extra = int(max(0, min(cfg.n_layers - 1, (budget_s - t0 - t1) // max(per_layer, 1e-3))))
+    if extra >= 1:
+        nl = 1 + min(extra, 3)
+        for l in range(1, nl):
+            for n in ("g_attn", "w_qkv", "w_o", "g_ffn", "w_gu", "w_down"):
+                W(n, l)
+        tn = run(nl)
+        per_layer = max((tn - t0) / nl, 1e-9)
+    t_step = t0 + cfg.n_layers * per_layer
+    threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+    cores = int(threads) if threads else (os.cpu_count() or 1)
+    return {"value": rows / t_step, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"1 sequence of the {cfg.name} workload: embedding, final norm and LM head "
+                      f"plus {nl} of {cfg.n_layers} layers timed, per-layer time extrapolated to "
+                      f"the full depth; fp64 NumPy, {t_step:.2f} s per token-step"}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        return main_reference(args)
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    capi.load()
+    r = time_native(args, rank, world)
+    cfg, B, K = r["cfg"], r["B"], r["K"]
+    tok_s = world * B * K / (r["total_ms"] / 1e3)
+    peak, src = peaks()
+    kern = r["kern"] or {"bytes": 0, "ms": float("nan"), "launches": 0}
+    k_gbs = kern["bytes"] / (kern["ms"] / 1e3) / 1e9
+    step_ms = r["total_ms"] / K
+    step_gbs = r["avg_bytes"] / (step_ms * 1e-3) / 1e9
+    ps = sorted(r["per_step"])
+    line = {
+        "metric": "decode tokens/s (batch %d); achieved HBM GB/s as %% of GB300 peak" % B,
+        "value": round(tok_s, 2), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": r["W"],
+        "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if cfg.weight_dtype == "bf16" else "fp8-e4m3 weights, fp32 math",
+        "data": "synthetic (seeded random-init weights N(0,0.02), random KV contents and token ids)",
+        "config": {"workload": f"{r['wl'].key}: {r['wl'].description}", "model": cfg.name, "batch": B,
+                   "context_start": [int(c) for c in r["ctx"][:8]], "graph": r["uses_graph"],
+                   "l2": "weights of every step (%.1f GB) exceed L2; no flush needed" % (r["avg_bytes"] / 1e9),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "latency_ms": {"p50": round(ps[len(ps) // 2], 4), "p99": round(ps[min(len(ps) - 1, int(0.99 * len(ps)))], 4)},
+        "step_roofline": {"bytes_per_step": int(r["avg_bytes"]), "achieved_gbs": round(step_gbs, 1),
+                          "frac_of_peak": round(step_gbs / peak, 4), "frac_of_8tbs": round(step_gbs / 8000, 4)},
+        "roofline": {"kernel": "gemv_kernel<NB,WT,EPI_SWIGLU> (fused gate/up + SiLU x mul)", "bound": "hbm",
+                     "achieved": round(k_gbs, 1), "peak": peak, "peak_source": src, "unit": "GB/s",
+                     "frac": round(k_gbs / peak, 4), "traffic": GEMV_TRAFFIC_BYTES,
+                     "algorithmic_bytes_per_launch": kern["bytes"], "avg_launch_ms": round(kern["ms"], 5)},
+        "gpu_launches": int(r["kernels_per_step"] * K),
+        "kernels_per_step": r["kernels_per_step"],
+    }
+    if r["clocks"]:
+        line["clocks"] = r["clocks"]
+    if r["e2e"]:
+        e = dict(r["e2e"])
+        e["value"] = round(e["value"] * world, 2)
+        line["e2e"] = e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(r["wl"], B)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main_reference(args):
+    """The oracle, as it stands, on this host's cores, for the same workload.
+    Each step is a bounded sample sized so that warm-up plus steps take about
+    two minutes: the oracle's own row-chunked projection over a slice of one
+    layer's gate/up rows, its cost per weight byte extrapolated to the whole
+    step's algorithmic bytes (weights + KV read)."""
+    from oracle.decode import matmul
+    from synth import raw_numpy
+
+    wl = WORKLOADS[args.workload]
+    cfg = wl.model
+    B = args.batch or wl.batches[0]
+    n = max(1, args.steps + args.warmup)
+    per_step_s = max(0.05, 120.0 / n)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = SynthModel(cfg, wl.seed, device=dev, cache=False).get("w_gu", 0)
+    gu = {k: raw_numpy(v) for k, v in t.items()}
+    x = np.random.default_rng(0).normal(size=(B, cfg.hidden))
+    wbytes_row = cfg.hidden * (1 if cfg.weight_dtype == "fp8" else 2)
+    rows = 64
+    while True:                                   # size the slice to the per-step budget
+        sl = {k: v[:rows] for k, v in gu.items()}
+        t0 = time.perf_counter()
+        matmul(sl, x)
+        dt = time.perf_counter() - t0
+        if dt > per_step_s / 2 or rows >= gu["w"].shape[0]:
+            break
+        rows = min(gu["w"].shape[0], rows * 2)
+    ctx = random_contexts(B, wl.context[0], wl.context[1], wl.seed + 2000)
+    step_b = ledger.step_bytes(cfg, ctx)
+    sl = {k: v[:rows] for k, v in gu.items()}
+    for _ in range(args.warmup):
+        matmul(sl, x)
+    vals = []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        matmul(sl, x)
+        dt = time.perf_counter() - t0
+        vals.append(B / (dt / (rows * wbytes_row) * step_b))
+    wall = time.perf_counter() - t_all
+    v = float(np.mean(vals))
+    threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+    cores = int(threads) if threads else (os.cpu_count() or 1)
+    line = {"impl": "reference", "metric": "decode tokens/s (batch %d); achieved HBM GB/s as %% of GB300 peak" % B,
+            "value": round(v, 6), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(wall / max(args.steps, 1) * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{wl.key}: {wl.description}", "model": cfg.name, "batch": B},
+            "cpu_baseline": {"value": round(v, 6), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"per step: the oracle's fp64 projection over {rows} rows of layer 0's "
+                                       f"gate/up matrix for {B} row(s), cost per weight byte scaled to the "
+                                       f"step's {step_b / 1e9:.2f} GB of algorithmic bytes"},
+            "e2e": {"value": round(v, 6), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

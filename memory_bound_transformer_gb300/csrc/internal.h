@@ -1,0 +1,93 @@
+// Launch interfaces between the runtime and the kernels (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace mbt {
+
+typedef __nv_bfloat16 bf16;
+
+enum Epilogue { EPI_PARTIAL = 0, EPI_SWIGLU = 1, EPI_ARGMAX = 2 };
+
+struct ArgmaxPart { float v; int i; };
+
+// y = W x for up to 8 batch rows (weight-streaming GEMV, CUDA cores).
+struct GemvArgs {
+  const void* W;            // [rows][K] row-major, BF16 or e4m3 codes
+  const float* scale;       // per-row scale for e4m3 weights, else null
+  int wtype;                // W_BF16 / W_E4M3
+  int N;                    // output channels (SWIGLU: ffn; W holds 2N rows)
+  int K;                    // multiple of 16
+  const bf16* x; int ldx;   // [nb][ldx] BF16 input rows, 16-byte aligned
+  int nb;                   // batch rows, 1..8
+  // EPI_PARTIAL: out[split * split_stride + b * ldo + n] (fp32, no accumulate)
+  float* out; long long split_stride; int ldo;
+  // EPI_SWIGLU: act[b * lda + n] = bf16(silu(gate_n) * up_n)
+  bf16* act; int lda;
+  // EPI_ARGMAX: per-CTA best (value, index) per row into part[cta * part_ld + b];
+  // logits[b * ldl + n] written when logits != null
+  float* logits; int ldl;
+  ArgmaxPart* part; int part_ld;
+  uint32_t* err;
+};
+
+struct GemvLaunch { int nb_tmpl; int nsplit; int grid; size_t smem; };
+
+// Launch geometry for a GEMV of this shape (deterministic: the same inputs give
+// the same geometry, so eager runs and graph replays do the same arithmetic).
+GemvLaunch gemv_plan(int epi, int wtype, int nb, int N, int K, int num_sms, int force_nsplit);
+cudaError_t gemv_launch(int epi, const GemvArgs& a, const GemvLaunch& g, cudaStream_t s);
+cudaError_t gemv_init();   // raise dynamic shared-memory limits (once per process)
+
+// r <- E[token] (fp32); y <- bf16(rmsnorm(r) * gamma)
+struct EmbedNormArgs {
+  int B, H, vocab; const int* tokens; const bf16* embed;
+  float* r; const bf16* gamma; float eps; bf16* y; uint32_t* err;
+};
+cudaError_t launch_embed_rmsnorm(const EmbedNormArgs& a, cudaStream_t s);
+
+// r <- r + sum_s delta[s]; y <- bf16(rmsnorm(r) * gamma)
+struct AddNormArgs {
+  int B, H; float* r; const float* delta; int n_delta; long long delta_stride;
+  const bf16* gamma; float eps; bf16* y;
+};
+cudaError_t launch_add_rmsnorm(const AddNormArgs& a, cudaStream_t s);
+
+// RoPE on q and k, q to q_out (fp32), k and v into the paged cache.
+struct RopeKvArgs {
+  int B; const float* qkv; int nsplit; long long split_stride; int ld_qkv;
+  int nq, nkv, d; const int* positions; const int* bt; int bt_stride; int max_pos;
+  const float2* rope;       // [max_pos][d/2] (cos, sin)
+  float* q_out;             // [B][nq][d]
+  void* kpool; void* vpool; // this layer's K and V pools [nb+1][nkv][16][d]
+  int num_blocks;           // caller blocks; id num_blocks = null block
+  int kv_fp8; float k_scale, v_scale; uint32_t* err;
+};
+cudaError_t launch_rope_kv_write(const RopeKvArgs& a, cudaStream_t s);
+
+// Split-K paged decode attention + combine.
+struct AttnArgs {
+  int B; const float* q; int nq, nkv, d;
+  const void* kpool; const void* vpool; int kv_fp8; float k_scale, v_scale;
+  const int* bt; int bt_stride; const int* seq_lens; int num_blocks;
+  int bps; int nsplit;      // KV blocks per split, splits per (row, kv head)
+  float* part_o; float2* part_ml; bf16* out; uint32_t* err;
+};
+void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nsplit);
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
+cudaError_t attn_init();
+
+// next_ids[b] = index of the best of part[0..G)[b]
+cudaError_t launch_argmax_reduce(int B, const ArgmaxPart* part, int part_ld, int G,
+                                 int* next_ids, uint32_t* err, cudaStream_t s);
+
+// Copy B caller rows into the graph's static buffers and fill pad rows [B, R).
+struct StageArgs {
+  int B, R; const int* tok; const int* pos; const int* bt; int bt_stride; const int* sl;
+  int* s_tok; int* s_pos; int* s_bt; int s_stride; int* s_sl; int null_block;
+};
+cudaError_t launch_stage_inputs(const StageArgs& a, cudaStream_t s);
+
+}  // namespace mbt

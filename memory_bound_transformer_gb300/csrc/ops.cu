@@ -1,0 +1,156 @@
+// Kernel-level entry points (include/mbt_ops.h): one decode-step kernel per
+// call on caller buffers, with the decode step's launch geometry.
+#include <algorithm>
+#include <cmath>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+#include "../../include/mbt_ops.h"
+
+using namespace mbt;
+
+namespace {
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+bool inited = false;
+int init_once() {
+  if (inited) return MBT_OK;
+  if (gemv_init() != cudaSuccess || attn_init() != cudaSuccess) return MBT_ERR_CUDA;
+  inited = true;
+  return MBT_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int op_embed_rmsnorm(int B, int H, int vocab, const int32_t* tokens, const uint16_t* embed,
+                     const uint16_t* gamma, float eps, float* r, uint16_t* y, uint32_t* err,
+                     void* stream) {
+  if (B < 1 || H < 1 || vocab < 1 || !tokens || !embed || !gamma || !r || !y) return MBT_ERR_BAD_ARG;
+  EmbedNormArgs a{B, H, vocab, tokens, (const bf16*)embed, r, (const bf16*)gamma, eps, (bf16*)y, err};
+  return launch_embed_rmsnorm(a, (cudaStream_t)stream) == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
+}
+
+int op_add_rmsnorm(int B, int H, float* r, const float* delta, int n_delta,
+                   const uint16_t* gamma, float eps, uint16_t* y, void* stream) {
+  if (B < 1 || H < 1 || !r || !gamma || !y || n_delta < 0 || (n_delta && !delta)) return MBT_ERR_BAD_ARG;
+  AddNormArgs a{B, H, r, delta, n_delta, (long long)B * H, (const bf16*)gamma, eps, (bf16*)y};
+  return launch_add_rmsnorm(a, (cudaStream_t)stream) == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
+}
+
+int op_gemv_nsplit(int epi, int w_dtype, int B, int N, int K) {
+  const int n = sm_count();
+  if (n <= 0 || B < 1 || N < 1 || K < 16) return 1;
+  return gemv_plan(epi, w_dtype == MBT_DTYPE_E4M3 ? W_E4M3 : W_BF16, std::min(B, 8), N, K, n, 0).nsplit;
+}
+
+int op_gemv(int epi, int w_dtype, const void* W, const float* scales, int N, int K,
+            const uint16_t* x, int B, int force_nsplit, float* out, uint16_t* act,
+            float* logits, int32_t* next_ids, int* nsplit_used, uint32_t* err, void* stream) {
+  if (epi < 0 || epi > 2 || (w_dtype != MBT_DTYPE_BF16 && w_dtype != MBT_DTYPE_E4M3)) return MBT_ERR_BAD_ARG;
+  if (!W || !x || B < 1 || N < 1 || K < 16 || K % 16) return MBT_ERR_BAD_ARG;
+  if (w_dtype == MBT_DTYPE_E4M3 && !scales) return MBT_ERR_BAD_ARG;
+  if ((epi == EPI_PARTIAL && !out) || (epi == EPI_SWIGLU && !act) || (epi == EPI_ARGMAX && !next_ids))
+    return MBT_ERR_BAD_ARG;
+  int rc = init_once();
+  if (rc != MBT_OK) return rc;
+  const int nsm = sm_count();
+  const int wt = w_dtype == MBT_DTYPE_E4M3 ? W_E4M3 : W_BF16;
+  cudaStream_t s = (cudaStream_t)stream;
+  const GemvLaunch g0 = gemv_plan(epi, wt, std::min(B, 8), N, K, nsm, epi == EPI_PARTIAL ? force_nsplit : 0);
+  if (nsplit_used) *nsplit_used = g0.nsplit;
+  ArgmaxPart* part = nullptr;
+  if (epi == EPI_ARGMAX &&
+      cudaMallocAsync((void**)&part, (size_t)g0.grid * B * sizeof(ArgmaxPart), s) != cudaSuccess)
+    return MBT_ERR_OOM;
+  for (int b0 = 0; b0 < B && rc == MBT_OK; b0 += 8) {
+    const int nb = std::min(8, B - b0);
+    GemvLaunch g = gemv_plan(epi, wt, nb, N, K, nsm, epi == EPI_PARTIAL ? g0.nsplit : 0);
+    if (epi == EPI_ARGMAX) g.grid = g0.grid;
+    GemvArgs a = {};
+    a.W = W; a.scale = scales; a.wtype = wt; a.N = N; a.K = K;
+    a.x = (const bf16*)x + (size_t)b0 * K; a.ldx = K; a.nb = nb;
+    a.out = out ? out + (size_t)b0 * N : nullptr; a.split_stride = (long long)B * N; a.ldo = N;
+    a.act = act ? (bf16*)act + (size_t)b0 * N : nullptr; a.lda = N;
+    a.logits = logits ? logits + (size_t)b0 * N : nullptr; a.ldl = N;
+    a.part = part ? part + b0 : nullptr; a.part_ld = B;
+    a.err = err;
+    if (gemv_launch(epi, a, g, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  }
+  if (rc == MBT_OK && epi == EPI_ARGMAX &&
+      launch_argmax_reduce(B, part, B, g0.grid, next_ids, err, s) != cudaSuccess)
+    rc = MBT_ERR_CUDA;
+  if (part) cudaFreeAsync(part, s);
+  return rc;
+}
+
+int op_rope_kv_write(int B, const float* qkv, int nq, int nkv, int d, const int32_t* positions,
+                     const int32_t* bt, int bt_stride, int max_pos, float theta, void* kpool,
+                     void* vpool, int num_blocks, int kv_dtype, float k_scale, float v_scale,
+                     float* q_out, uint32_t* err, void* stream) {
+  if (B < 1 || !qkv || nq < 1 || nkv < 1 || (d != 64 && d != 128) || !positions || !bt ||
+      bt_stride < 1 || max_pos < 1 || !kpool || !vpool || num_blocks < 1 || !q_out ||
+      !(k_scale > 0.f) || !(v_scale > 0.f) || (kv_dtype != MBT_DTYPE_BF16 && kv_dtype != MBT_DTYPE_E4M3))
+    return MBT_ERR_BAD_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int half = d / 2;
+  std::vector<float2> tab((size_t)max_pos * half);
+  for (int p = 0; p < max_pos; ++p)
+    for (int i = 0; i < half; ++i) {
+      const double ang = (double)p * std::pow((double)theta, -2.0 * i / (double)d);
+      tab[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+    }
+  float2* rope = nullptr;
+  if (cudaMallocAsync((void**)&rope, tab.size() * sizeof(float2), s) != cudaSuccess) return MBT_ERR_OOM;
+  int rc = MBT_OK;
+  if (cudaMemcpyAsync(rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice, s) != cudaSuccess)
+    rc = MBT_ERR_CUDA;
+  RopeKvArgs a;
+  a.B = B; a.qkv = qkv; a.nsplit = 1; a.split_stride = 0; a.ld_qkv = (nq + 2 * nkv) * d;
+  a.nq = nq; a.nkv = nkv; a.d = d; a.positions = positions; a.bt = bt; a.bt_stride = bt_stride;
+  a.max_pos = max_pos; a.rope = rope; a.q_out = q_out; a.kpool = kpool; a.vpool = vpool;
+  a.num_blocks = num_blocks; a.kv_fp8 = kv_dtype == MBT_DTYPE_E4M3; a.k_scale = k_scale;
+  a.v_scale = v_scale; a.err = err;
+  if (rc == MBT_OK && launch_rope_kv_write(a, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  // the table must outlive the kernel: free in stream order, then wait for the
+  // host vector's copy to finish before it goes out of scope
+  cudaFreeAsync(rope, s);
+  if (cudaStreamSynchronize(s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  return rc;
+}
+
+int op_paged_attention(int B, const float* q, int nq, int nkv, int d, const void* kpool,
+                       const void* vpool, int kv_dtype, float k_scale, float v_scale,
+                       const int32_t* bt, int bt_stride, const int32_t* seq_lens, int num_blocks,
+                       uint16_t* out, uint32_t* err, void* stream) {
+  if (B < 1 || !q || nq < 1 || nkv < 1 || nq % nkv || nq / nkv > 16 || (d != 64 && d != 128) ||
+      !kpool || !vpool || !bt || bt_stride < 1 || !seq_lens || num_blocks < 1 || !out ||
+      (kv_dtype != MBT_DTYPE_BF16 && kv_dtype != MBT_DTYPE_E4M3))
+    return MBT_ERR_BAD_ARG;
+  int rc = init_once();
+  if (rc != MBT_OK) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  AttnArgs a;
+  a.B = B; a.q = q; a.nq = nq; a.nkv = nkv; a.d = d; a.kpool = kpool; a.vpool = vpool;
+  a.kv_fp8 = kv_dtype == MBT_DTYPE_E4M3; a.k_scale = k_scale; a.v_scale = v_scale;
+  a.bt = bt; a.bt_stride = bt_stride; a.seq_lens = seq_lens; a.num_blocks = num_blocks;
+  attn_plan(B, nkv, bt_stride, sm_count(), &a.bps, &a.nsplit);
+  a.out = (bf16*)out; a.err = err;
+  const size_t heads = (size_t)B * nq * a.nsplit;
+  if (cudaMallocAsync((void**)&a.part_o, heads * d * sizeof(float), s) != cudaSuccess) return MBT_ERR_OOM;
+  if (cudaMallocAsync((void**)&a.part_ml, heads * sizeof(float2), s) != cudaSuccess) {
+    cudaFreeAsync(a.part_o, s);
+    return MBT_ERR_OOM;
+  }
+  if (launch_attention(a, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  cudaFreeAsync(a.part_o, s);
+  cudaFreeAsync(a.part_ml, s);
+  return rc;
+}
+
+}  // extern "C"

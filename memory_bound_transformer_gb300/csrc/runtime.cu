@@ -1,0 +1,644 @@
+// Decode-step executor and the C ABI (include/mbt.h).
+//
+// The executor issues the per-layer kernel sequence of one decode step
+// ("CUDA graphs & kernel fusion", "Direct answer": norms, QKV/O projections,
+// attention, gate/up/down, activations, residual adds, repeated per layer) and
+// captures it as one CUDA graph per batch size of a ladder, padding the live
+// batch to the next captured size ("Kernels, Fusion & CUDA Graphs", "Fix 2:
+// CUDA graphs"; "CUDA graphs & kernel fusion", "Deep dive": warm-up before
+// capture, static input buffers, eager fallback).
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace mbt;
+
+namespace {
+
+struct Layer {
+  const void* w_qkv; const float* s_qkv;
+  const void* w_o; const float* s_o;
+  const void* w_gu; const float* s_gu;
+  const void* w_down; const float* s_down;
+  const bf16* g_attn; const bf16* g_ffn;
+};
+
+// Launch geometry of one step at R rows and block tables of `mbs` entries.
+struct Plan {
+  int R = 0, mbs = 0;
+  int attn_bps = 0, attn_nsplit = 0;
+  int ns_qkv = 1, ns_o = 1, ns_down = 1;
+  int g_lm = 1;
+  int kernels = 0;
+};
+
+// Device workspace for up to `cap` rows.
+struct Workspace {
+  int cap = 0, mbs_cap = 0;
+  size_t part_o_elems = 0, part_ml_elems = 0;
+  int ns_qkv_cap = 0, ns_delta_cap = 0, g_lm_cap = 0;
+  void* mem = nullptr;
+  float* r = nullptr; bf16* y = nullptr; float* qkv = nullptr; float* q = nullptr;
+  float* part_o = nullptr; float2* part_ml = nullptr; bf16* o = nullptr;
+  float* delta = nullptr; bf16* act = nullptr; ArgmaxPart* lm_part = nullptr;
+};
+
+struct Graph {
+  int R = 0;
+  cudaGraphExec_t exec[2] = {nullptr, nullptr};   // [without logits, with logits]
+  int nodes = 0;
+};
+
+}  // namespace
+
+struct mbt_model {
+  mbt_blob_header h;
+  int device = 0, num_sms = 0;
+  int wtype = W_BF16, kv8 = 0;
+  void* wmem = nullptr;
+  size_t wbytes = 0;
+  const bf16* embed = nullptr; const bf16* g_final = nullptr;
+  const void* lm = nullptr; const float* s_lm = nullptr;
+  std::vector<Layer> layers;
+  float2* rope = nullptr;
+  uint32_t* err = nullptr;
+  Workspace ws;
+  // graphs
+  std::vector<Graph> graphs;
+  mbt_kv* graph_kv = nullptr;
+  int graph_mbs = 0;
+  int eager = 0;
+  void* statics = nullptr;
+  int* s_tok = nullptr; int* s_pos = nullptr; int* s_sl = nullptr; int* s_bt = nullptr;
+  int* s_next = nullptr; float* s_logits = nullptr;
+};
+
+struct mbt_kv {
+  mbt_model* m = nullptr;
+  int num_blocks = 0;
+  void* pool = nullptr;
+  size_t bytes = 0;
+  bool owned = false;
+  std::vector<float> k_scale, v_scale;
+};
+
+namespace {
+
+#define MBT_CUDA(x)                                   \
+  do {                                                \
+    cudaError_t e_ = (x);                             \
+    if (e_ != cudaSuccess) return MBT_ERR_CUDA;       \
+  } while (0)
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t kv_layer_half_bytes(const mbt_model* m, int num_blocks) {
+  const size_t esz = m->kv8 ? 1 : 2;
+  return (size_t)(num_blocks + 1) * m->h.n_kv_heads * kBlockTokens * m->h.head_dim * esz;
+}
+
+Plan make_plan(const mbt_model* m, int R, int mbs) {
+  Plan p;
+  p.R = R;
+  p.mbs = mbs;
+  attn_plan(R, (int)m->h.n_kv_heads, mbs, m->num_sms, &p.attn_bps, &p.attn_nsplit);
+  const int nb0 = std::min(R, 8);
+  const int H = (int)m->h.hidden, Q = (int)(m->h.n_q_heads * m->h.head_dim), F = (int)m->h.ffn;
+  const int QKV = (int)((m->h.n_q_heads + 2 * m->h.n_kv_heads) * m->h.head_dim);
+  p.ns_qkv = gemv_plan(EPI_PARTIAL, m->wtype, nb0, QKV, H, m->num_sms, 0).nsplit;
+  p.ns_o = gemv_plan(EPI_PARTIAL, m->wtype, nb0, H, Q, m->num_sms, 0).nsplit;
+  p.ns_down = gemv_plan(EPI_PARTIAL, m->wtype, nb0, H, F, m->num_sms, 0).nsplit;
+  p.g_lm = gemv_plan(EPI_ARGMAX, m->wtype, nb0, (int)m->h.vocab, H, m->num_sms, 0).grid;
+  const int chunks = (R + 7) / 8;
+  p.kernels = 1 + (int)m->h.n_layers * (4 * chunks + 5) + chunks + 1;
+  return p;
+}
+
+void free_ws(Workspace& w) {
+  if (w.mem) cudaFree(w.mem);
+  w = Workspace();
+}
+
+// Grow the workspace to serve R rows with block tables of mbs entries.
+int ensure_ws(mbt_model* m, int R, int mbs) {
+  Workspace& w = m->ws;
+  int cap = std::max(R, w.cap);
+  int mbs_cap = std::max(mbs, w.mbs_cap);
+  size_t po = 0, pml = 0;
+  int ns_qkv = 1, ns_delta = 1, g_lm = 1;
+  for (int r = 1; r <= cap; ++r) {
+    Plan p = make_plan(m, r, mbs_cap);
+    // attn_plan never uses more splits than this, whatever the table width
+    const int pairs = r * (int)m->h.n_kv_heads;
+    const int split_bound = std::max(1, (2 * m->num_sms + pairs - 1) / pairs);
+    pml = std::max(pml, (size_t)r * m->h.n_q_heads * split_bound);
+    ns_qkv = std::max(ns_qkv, p.ns_qkv);
+    ns_delta = std::max({ns_delta, p.ns_o, p.ns_down});
+    g_lm = std::max(g_lm, p.g_lm);
+  }
+  po = pml * m->h.head_dim;
+  if (w.mem && cap <= w.cap && po <= w.part_o_elems && ns_qkv <= w.ns_qkv_cap &&
+      ns_delta <= w.ns_delta_cap && g_lm <= w.g_lm_cap)
+    return MBT_OK;
+  // growing invalidates captured graphs (they hold the old addresses)
+  if (cudaDeviceSynchronize() != cudaSuccess) return MBT_ERR_CUDA;
+  for (auto& g : m->graphs)
+    for (auto& e : g.exec) if (e) cudaGraphExecDestroy(e);
+  m->graphs.clear();
+  m->graph_kv = nullptr;
+  free_ws(w);
+  const size_t H = m->h.hidden, Q = (size_t)m->h.n_q_heads * m->h.head_dim, F = m->h.ffn;
+  const size_t QKV = (size_t)(m->h.n_q_heads + 2 * m->h.n_kv_heads) * m->h.head_dim;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off += align256(bytes); return o; };
+  const size_t o_r = take((size_t)cap * H * 4), o_y = take((size_t)cap * H * 2);
+  const size_t o_qkv = take((size_t)ns_qkv * cap * QKV * 4), o_q = take((size_t)cap * Q * 4);
+  const size_t o_po = take(po * 4), o_pml = take(pml * 8), o_o = take((size_t)cap * Q * 2);
+  const size_t o_d = take((size_t)ns_delta * cap * H * 4), o_a = take((size_t)cap * F * 2);
+  const size_t o_lp = take((size_t)g_lm * cap * sizeof(ArgmaxPart));
+  void* mem = nullptr;
+  if (cudaMalloc(&mem, off) != cudaSuccess) { cudaGetLastError(); return MBT_ERR_OOM; }
+  char* base = (char*)mem;
+  w.mem = mem; w.cap = cap; w.mbs_cap = mbs_cap;
+  w.part_o_elems = po; w.part_ml_elems = pml;
+  w.ns_qkv_cap = ns_qkv; w.ns_delta_cap = ns_delta; w.g_lm_cap = g_lm;
+  w.r = (float*)(base + o_r); w.y = (bf16*)(base + o_y); w.qkv = (float*)(base + o_qkv);
+  w.q = (float*)(base + o_q); w.part_o = (float*)(base + o_po); w.part_ml = (float2*)(base + o_pml);
+  w.o = (bf16*)(base + o_o); w.delta = (float*)(base + o_d); w.act = (bf16*)(base + o_a);
+  w.lm_part = (ArgmaxPart*)(base + o_lp);
+  return MBT_OK;
+}
+
+// One GEMV over R rows, issued in chunks of at most 8 rows.
+cudaError_t gemv_rows(const mbt_model* m, int epi, const void* W, const float* sc, int N, int K,
+                      const bf16* x, int R, int nsplit, int grid_fixed, float* out,
+                      long long split_stride, int ldo, bf16* act, int lda, float* logits,
+                      ArgmaxPart* part, int part_ld, cudaStream_t s) {
+  for (int b0 = 0; b0 < R; b0 += 8) {
+    const int nb = std::min(8, R - b0);
+    GemvLaunch g = gemv_plan(epi, m->wtype, nb, N, K, m->num_sms, epi == EPI_PARTIAL ? nsplit : 0);
+    if (grid_fixed > 0) g.grid = grid_fixed;
+    GemvArgs a;
+    memset(&a, 0, sizeof(a));
+    a.W = W; a.scale = sc; a.wtype = m->wtype; a.N = N; a.K = K;
+    a.x = x + (size_t)b0 * K; a.ldx = K; a.nb = nb;
+    a.out = out ? out + (size_t)b0 * ldo : nullptr; a.split_stride = split_stride; a.ldo = ldo;
+    a.act = act ? act + (size_t)b0 * lda : nullptr; a.lda = lda;
+    a.logits = logits ? logits + (size_t)b0 * m->h.vocab : nullptr; a.ldl = (int)m->h.vocab;
+    a.part = part ? part + b0 : nullptr; a.part_ld = part_ld;
+    a.err = m->err;
+    cudaError_t e = gemv_launch(epi, a, g, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// The decode step over R rows whose inputs are already in device memory.
+int run_step(mbt_model* m, mbt_kv* kv, const Plan& p, const int* tok, const int* pos,
+             const int* bt, int bt_stride, const int* sl, int* next_ids, float* logits,
+             cudaStream_t s) {
+  const Workspace& w = m->ws;
+  const int R = p.R;
+  const int H = (int)m->h.hidden, d = (int)m->h.head_dim;
+  const int nq = (int)m->h.n_q_heads, nkv = (int)m->h.n_kv_heads;
+  const int Q = nq * d, F = (int)m->h.ffn, V = (int)m->h.vocab;
+  const int QKV = (nq + 2 * nkv) * d;
+  const size_t half = kv_layer_half_bytes(m, kv->num_blocks);
+
+  EmbedNormArgs en{R, H, V, tok, m->embed, w.r, m->layers[0].g_attn, m->h.eps, w.y, m->err};
+  MBT_CUDA(launch_embed_rmsnorm(en, s));
+  for (int l = 0; l < (int)m->h.n_layers; ++l) {
+    const Layer& L = m->layers[l];
+    char* kbase = (char*)kv->pool + 2 * half * (size_t)l;
+    // fused QKV projection
+    MBT_CUDA(gemv_rows(m, EPI_PARTIAL, L.w_qkv, L.s_qkv, QKV, H, w.y, R, p.ns_qkv, 0, w.qkv,
+                       (long long)R * QKV, QKV, nullptr, 0, nullptr, nullptr, 0, s));
+    // RoPE + paged KV write
+    RopeKvArgs rk;
+    rk.B = R; rk.qkv = w.qkv; rk.nsplit = p.ns_qkv; rk.split_stride = (long long)R * QKV; rk.ld_qkv = QKV;
+    rk.nq = nq; rk.nkv = nkv; rk.d = d; rk.positions = pos; rk.bt = bt; rk.bt_stride = bt_stride;
+    rk.max_pos = (int)m->h.max_pos; rk.rope = m->rope; rk.q_out = w.q;
+    rk.kpool = kbase; rk.vpool = kbase + half; rk.num_blocks = kv->num_blocks;
+    rk.kv_fp8 = m->kv8; rk.k_scale = kv->k_scale[l]; rk.v_scale = kv->v_scale[l]; rk.err = m->err;
+    MBT_CUDA(launch_rope_kv_write(rk, s));
+    // paged attention
+    AttnArgs at;
+    at.B = R; at.q = w.q; at.nq = nq; at.nkv = nkv; at.d = d;
+    at.kpool = kbase; at.vpool = kbase + half; at.kv_fp8 = m->kv8;
+    at.k_scale = kv->k_scale[l]; at.v_scale = kv->v_scale[l];
+    at.bt = bt; at.bt_stride = bt_stride; at.seq_lens = sl; at.num_blocks = kv->num_blocks;
+    at.bps = p.attn_bps; at.nsplit = p.attn_nsplit;
+    at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = w.o; at.err = m->err;
+    MBT_CUDA(launch_attention(at, s));
+    // O projection (partials), then residual add + RMSNorm
+    MBT_CUDA(gemv_rows(m, EPI_PARTIAL, L.w_o, L.s_o, H, Q, w.o, R, p.ns_o, 0, w.delta,
+                       (long long)R * H, H, nullptr, 0, nullptr, nullptr, 0, s));
+    AddNormArgs an{R, H, w.r, w.delta, p.ns_o, (long long)R * H, L.g_ffn, m->h.eps, w.y};
+    MBT_CUDA(launch_add_rmsnorm(an, s));
+    // gate + up with the SwiGLU epilogue
+    MBT_CUDA(gemv_rows(m, EPI_SWIGLU, L.w_gu, L.s_gu, F, H, w.y, R, 1, 0, nullptr, 0, 0,
+                       w.act, F, nullptr, nullptr, 0, s));
+    // down projection, then residual add + the next norm
+    MBT_CUDA(gemv_rows(m, EPI_PARTIAL, L.w_down, L.s_down, H, F, w.act, R, p.ns_down, 0, w.delta,
+                       (long long)R * H, H, nullptr, 0, nullptr, nullptr, 0, s));
+    const bf16* gnext = l + 1 < (int)m->h.n_layers ? m->layers[l + 1].g_attn : m->g_final;
+    AddNormArgs an2{R, H, w.r, w.delta, p.ns_down, (long long)R * H, gnext, m->h.eps, w.y};
+    MBT_CUDA(launch_add_rmsnorm(an2, s));
+  }
+  // LM head with the arg-max epilogue, then the cross-CTA reduction
+  MBT_CUDA(gemv_rows(m, EPI_ARGMAX, m->lm, m->s_lm, V, H, w.y, R, 1, p.g_lm, nullptr, 0, 0,
+                     nullptr, 0, logits, w.lm_part, R, s));
+  MBT_CUDA(launch_argmax_reduce(R, w.lm_part, R, p.g_lm, next_ids, m->err, s));
+  return MBT_OK;
+}
+
+int find_tensor(const mbt_blob_tensor* t, uint32_t n, uint32_t kind, int layer) {
+  for (uint32_t i = 0; i < n; ++i)
+    if (t[i].kind == kind && t[i].layer == layer) return (int)i;
+  return -1;
+}
+
+void destroy_graphs(mbt_model* m) {
+  for (auto& g : m->graphs)
+    for (auto& e : g.exec) if (e) cudaGraphExecDestroy(e);
+  m->graphs.clear();
+  m->graph_kv = nullptr;
+  if (m->statics) cudaFree(m->statics);
+  m->statics = nullptr;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+
+extern "C" {
+
+const char* status_string(int code) {
+  switch (code) {
+    case MBT_OK: return "ok";
+    case MBT_ERR_BAD_ARG: return "bad argument";
+    case MBT_ERR_BATCH: return "batch size must be >= 1";
+    case MBT_ERR_CUDA: return "CUDA error";
+    case MBT_ERR_OOM: return "out of device memory";
+    case MBT_ERR_BLOB: return "malformed weight/config blob";
+    case MBT_ERR_UNSUPPORTED: return "unsupported model shape";
+    case MBT_ERR_NO_DEVICE: return "no usable CUDA device";
+    default: return "unknown status";
+  }
+}
+
+int model_create(const void* blob, size_t bytes, int blob_is_device, void* stream, mbt_model** out) {
+  if (!blob || !out || bytes < sizeof(mbt_blob_header)) return MBT_ERR_BAD_ARG;
+  *out = nullptr;
+  cudaStream_t s = (cudaStream_t)stream;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return MBT_ERR_NO_DEVICE; }
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MBT_ERR_NO_DEVICE;
+  if (prop.major != 10 || prop.minor != 3) return MBT_ERR_NO_DEVICE;
+
+  // header and table to host
+  mbt_blob_header h;
+  std::vector<unsigned char> hostcopy;
+  const unsigned char* hb = nullptr;
+  if (blob_is_device) {
+    if (cudaMemcpy(&h, blob, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MBT_ERR_CUDA;
+  } else {
+    memcpy(&h, blob, sizeof(h));
+    hb = (const unsigned char*)blob;
+  }
+  if (memcmp(h.magic, MBT_BLOB_MAGIC, 8) != 0 || h.version != MBT_BLOB_VERSION) return MBT_ERR_BLOB;
+  if (h.n_layers < 1 || h.hidden < 16 || h.n_q_heads < 1 || h.n_kv_heads < 1 || h.ffn < 16 ||
+      h.vocab < 1 || h.max_pos < 1 || h.n_tensors == 0 || h.n_tensors > 100000)
+    return MBT_ERR_BLOB;
+  if (!(h.eps > 0.f) || !(h.rope_theta > 1.f)) return MBT_ERR_BLOB;
+  if (h.weight_dtype > 1 || h.kv_dtype > 1) return MBT_ERR_BLOB;
+  if (h.block_size != (uint32_t)kBlockTokens) return MBT_ERR_UNSUPPORTED;
+  if (h.head_dim != 64 && h.head_dim != 128) return MBT_ERR_UNSUPPORTED;
+  if (h.n_q_heads % h.n_kv_heads != 0 || h.n_q_heads / h.n_kv_heads > 16) return MBT_ERR_UNSUPPORTED;
+  if (h.hidden % 16 || (h.n_q_heads * h.head_dim) % 16 || h.ffn % 16) return MBT_ERR_UNSUPPORTED;
+  if (h.hidden > 65536 || h.ffn > 262144 || h.vocab > (1u << 30)) return MBT_ERR_UNSUPPORTED;
+  const size_t table_bytes = (size_t)h.n_tensors * sizeof(mbt_blob_tensor);
+  if (h.table_offset > bytes || table_bytes > bytes - h.table_offset) return MBT_ERR_BLOB;
+  std::vector<mbt_blob_tensor> tab(h.n_tensors);
+  if (blob_is_device) {
+    if (cudaMemcpy(tab.data(), (const char*)blob + h.table_offset, table_bytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return MBT_ERR_CUDA;
+  } else {
+    memcpy(tab.data(), hb + h.table_offset, table_bytes);
+  }
+
+  // expected tensors: (kind, layer, dtype, rows, cols)
+  struct Want { uint32_t kind; int layer; uint32_t dtype; uint64_t rows, cols; };
+  std::vector<Want> want;
+  const uint64_t H = h.hidden, Qd = (uint64_t)h.n_q_heads * h.head_dim, F = h.ffn, V = h.vocab;
+  const uint64_t QKV = (uint64_t)(h.n_q_heads + 2 * h.n_kv_heads) * h.head_dim;
+  const bool fp8 = h.weight_dtype == MBT_DTYPE_E4M3;
+  const uint32_t wdt = fp8 ? MBT_DTYPE_E4M3 : MBT_DTYPE_BF16;
+  want.push_back({MBT_T_EMBED, -1, MBT_DTYPE_BF16, V, H});
+  for (int l = 0; l < (int)h.n_layers; ++l) {
+    want.push_back({MBT_T_G_ATTN, l, MBT_DTYPE_BF16, H, 1});
+    want.push_back({MBT_T_W_QKV, l, wdt, QKV, H});
+    want.push_back({MBT_T_W_O, l, wdt, H, Qd});
+    want.push_back({MBT_T_G_FFN, l, MBT_DTYPE_BF16, H, 1});
+    want.push_back({MBT_T_W_GU, l, wdt, 2 * F, H});
+    want.push_back({MBT_T_W_DOWN, l, wdt, H, F});
+    if (fp8) {
+      want.push_back({MBT_T_S_QKV, l, MBT_DTYPE_F32, QKV, 1});
+      want.push_back({MBT_T_S_O, l, MBT_DTYPE_F32, H, 1});
+      want.push_back({MBT_T_S_GU, l, MBT_DTYPE_F32, 2 * F, 1});
+      want.push_back({MBT_T_S_DOWN, l, MBT_DTYPE_F32, H, 1});
+    }
+  }
+  want.push_back({MBT_T_G_FINAL, -1, MBT_DTYPE_BF16, H, 1});
+  want.push_back({MBT_T_LM_HEAD, -1, wdt, V, H});
+  if (fp8) want.push_back({MBT_T_S_LM, -1, MBT_DTYPE_F32, V, 1});
+
+  std::vector<int> idx(want.size());
+  std::vector<size_t> dst(want.size());
+  size_t total = 0;
+  for (size_t i = 0; i < want.size(); ++i) {
+    const Want& w = want[i];
+    const int j = find_tensor(tab.data(), h.n_tensors, w.kind, w.layer);
+    if (j < 0) return MBT_ERR_BLOB;
+    const mbt_blob_tensor& t = tab[j];
+    const uint64_t esz = w.dtype == MBT_DTYPE_BF16 ? 2 : w.dtype == MBT_DTYPE_E4M3 ? 1 : 4;
+    if (t.dtype != w.dtype || t.rows != w.rows || t.cols != w.cols || t.bytes != w.rows * w.cols * esz)
+      return MBT_ERR_BLOB;
+    if (t.offset % 16 || t.offset > bytes || t.bytes > bytes - t.offset) return MBT_ERR_BLOB;
+    idx[i] = j;
+    dst[i] = total;
+    total += align256(t.bytes);
+  }
+
+  mbt_model* m = new (std::nothrow) mbt_model();
+  if (!m) return MBT_ERR_OOM;
+  m->h = h;
+  m->h.n_tensors = 0;
+  m->h.table_offset = 0;
+  m->device = dev;
+  m->num_sms = prop.multiProcessorCount;
+  m->wtype = fp8 ? W_E4M3 : W_BF16;
+  m->kv8 = h.kv_dtype == MBT_DTYPE_E4M3;
+  int rc = MBT_OK;
+  if (gemv_init() != cudaSuccess || attn_init() != cudaSuccess) rc = MBT_ERR_CUDA;
+  if (rc == MBT_OK && cudaMalloc(&m->wmem, total) != cudaSuccess) { cudaGetLastError(); rc = MBT_ERR_OOM; }
+  if (rc == MBT_OK && cudaMalloc(&m->err, 256) != cudaSuccess) { cudaGetLastError(); rc = MBT_ERR_OOM; }
+  const size_t rope_bytes = (size_t)h.max_pos * (h.head_dim / 2) * sizeof(float2);
+  if (rc == MBT_OK && cudaMalloc(&m->rope, rope_bytes) != cudaSuccess) { cudaGetLastError(); rc = MBT_ERR_OOM; }
+  if (rc != MBT_OK) { model_destroy(m); return rc; }
+  m->wbytes = total;
+  char* base = (char*)m->wmem;
+  for (size_t i = 0; i < want.size() && rc == MBT_OK; ++i) {
+    const mbt_blob_tensor& t = tab[idx[i]];
+    const cudaMemcpyKind k = blob_is_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+    if (cudaMemcpyAsync(base + dst[i], (const char*)blob + t.offset, t.bytes, k, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  }
+  if (rc == MBT_OK && cudaMemsetAsync(m->err, 0, 256, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  // RoPE table: angle p * theta^(-2i/d), evaluated in double precision
+  {
+    const int half = (int)h.head_dim / 2;
+    std::vector<float2> tabl((size_t)h.max_pos * half);
+    for (uint32_t p = 0; p < h.max_pos; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double ang = (double)p * std::pow((double)h.rope_theta, -2.0 * i / (double)h.head_dim);
+        tabl[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    if (rc == MBT_OK && cudaMemcpyAsync(m->rope, tabl.data(), rope_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      rc = MBT_ERR_CUDA;
+    if (rc == MBT_OK && cudaStreamSynchronize(s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  }
+  if (rc != MBT_OK) { model_destroy(m); return rc; }
+
+  auto at = [&](uint32_t kind, int layer) -> void* {
+    for (size_t i = 0; i < want.size(); ++i)
+      if (want[i].kind == kind && want[i].layer == layer) return base + dst[i];
+    return nullptr;
+  };
+  m->embed = (const bf16*)at(MBT_T_EMBED, -1);
+  m->g_final = (const bf16*)at(MBT_T_G_FINAL, -1);
+  m->lm = at(MBT_T_LM_HEAD, -1);
+  m->s_lm = (const float*)at(MBT_T_S_LM, -1);
+  m->layers.resize(h.n_layers);
+  for (int l = 0; l < (int)h.n_layers; ++l) {
+    Layer& L = m->layers[l];
+    L.w_qkv = at(MBT_T_W_QKV, l); L.s_qkv = (const float*)at(MBT_T_S_QKV, l);
+    L.w_o = at(MBT_T_W_O, l); L.s_o = (const float*)at(MBT_T_S_O, l);
+    L.w_gu = at(MBT_T_W_GU, l); L.s_gu = (const float*)at(MBT_T_S_GU, l);
+    L.w_down = at(MBT_T_W_DOWN, l); L.s_down = (const float*)at(MBT_T_S_DOWN, l);
+    L.g_attn = (const bf16*)at(MBT_T_G_ATTN, l); L.g_ffn = (const bf16*)at(MBT_T_G_FFN, l);
+  }
+  *out = m;
+  return MBT_OK;
+}
+
+int model_destroy(mbt_model* m) {
+  if (!m) return MBT_OK;
+  cudaDeviceSynchronize();
+  destroy_graphs(m);
+  free_ws(m->ws);
+  if (m->wmem) cudaFree(m->wmem);
+  if (m->err) cudaFree(m->err);
+  if (m->rope) cudaFree(m->rope);
+  delete m;
+  return MBT_OK;
+}
+
+int model_info(const mbt_model* m, mbt_blob_header* out) {
+  if (!m || !out) return MBT_ERR_BAD_ARG;
+  *out = m->h;
+  return MBT_OK;
+}
+
+size_t kv_bytes(const mbt_model* m, int num_blocks) {
+  if (!m || num_blocks < 1) return 0;
+  return 2 * kv_layer_half_bytes(m, num_blocks) * m->h.n_layers;
+}
+
+int kv_alloc(mbt_model* m, int num_blocks, void* mem, mbt_kv** out) {
+  if (!m || !out || num_blocks < 1) return MBT_ERR_BAD_ARG;
+  *out = nullptr;
+  mbt_kv* kv = new (std::nothrow) mbt_kv();
+  if (!kv) return MBT_ERR_OOM;
+  kv->m = m;
+  kv->num_blocks = num_blocks;
+  kv->bytes = kv_bytes(m, num_blocks);
+  if (mem) {
+    if ((uintptr_t)mem % 16) { delete kv; return MBT_ERR_BAD_ARG; }
+    kv->pool = mem;
+  } else {
+    if (cudaMalloc(&kv->pool, kv->bytes) != cudaSuccess) { cudaGetLastError(); delete kv; return MBT_ERR_OOM; }
+    kv->owned = true;
+  }
+  kv->k_scale.assign(m->h.n_layers, 1.0f);
+  kv->v_scale.assign(m->h.n_layers, 1.0f);
+  *out = kv;
+  return MBT_OK;
+}
+
+int kv_free(mbt_kv* kv) {
+  if (!kv) return MBT_OK;
+  if (kv->m && kv->m->graph_kv == kv) destroy_graphs(kv->m);
+  if (kv->owned && kv->pool) { cudaDeviceSynchronize(); cudaFree(kv->pool); }
+  delete kv;
+  return MBT_OK;
+}
+
+int kv_pool(const mbt_kv* kv, void** pool, size_t* bytes) {
+  if (!kv || !pool || !bytes) return MBT_ERR_BAD_ARG;
+  *pool = kv->pool;
+  *bytes = kv->bytes;
+  return MBT_OK;
+}
+
+int kv_set_scales(mbt_kv* kv, const float* ks, const float* vs) {
+  if (!kv || !ks || !vs) return MBT_ERR_BAD_ARG;
+  const int L = (int)kv->m->h.n_layers;
+  for (int l = 0; l < L; ++l)
+    if (!(ks[l] > 0.f) || !(vs[l] > 0.f) || !std::isfinite(ks[l]) || !std::isfinite(vs[l])) return MBT_ERR_BAD_ARG;
+  kv->k_scale.assign(ks, ks + L);
+  kv->v_scale.assign(vs, vs + L);
+  if (kv->m->graph_kv == kv) destroy_graphs(kv->m);
+  return MBT_OK;
+}
+
+int model_set_eager(mbt_model* m, int eager) {
+  if (!m) return MBT_ERR_BAD_ARG;
+  m->eager = eager ? 1 : 0;
+  return MBT_OK;
+}
+
+int model_capture(mbt_model* m, mbt_kv* kv, const int* ladder, int n, int mbs, void* stream) {
+  if (!m || !kv || kv->m != m || mbs < 1) return MBT_ERR_BAD_ARG;
+  std::vector<int> rungs;
+  if (ladder) {
+    if (n < 1) return MBT_ERR_BAD_ARG;
+    for (int i = 0; i < n; ++i) {
+      if (ladder[i] < 1 || (i && ladder[i] <= ladder[i - 1])) return MBT_ERR_BAD_ARG;
+      rungs.push_back(ladder[i]);
+    }
+  } else {
+    rungs = {1, 2, 4};
+    for (int r = 8; r <= 64; r += 8) rungs.push_back(r);
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  destroy_graphs(m);
+  const int Rmax = rungs.back();
+  int rc = ensure_ws(m, Rmax, mbs);
+  if (rc != MBT_OK) return rc;
+  // static input buffers
+  size_t off = 0;
+  auto take = [&](size_t b) { size_t o = off; off += align256(b); return o; };
+  const size_t o_tok = take(Rmax * 4), o_pos = take(Rmax * 4), o_sl = take(Rmax * 4);
+  const size_t o_bt = take((size_t)Rmax * mbs * 4), o_next = take(Rmax * 4);
+  const size_t o_lg = take((size_t)Rmax * m->h.vocab * 4);
+  if (cudaMalloc(&m->statics, off) != cudaSuccess) { cudaGetLastError(); return MBT_ERR_OOM; }
+  char* b = (char*)m->statics;
+  m->s_tok = (int*)(b + o_tok); m->s_pos = (int*)(b + o_pos); m->s_sl = (int*)(b + o_sl);
+  m->s_bt = (int*)(b + o_bt); m->s_next = (int*)(b + o_next); m->s_logits = (float*)(b + o_lg);
+  m->graph_mbs = mbs;
+
+  cudaStream_t cs;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return MBT_ERR_CUDA;
+  for (int R : rungs) {
+    // all rows padding: token 0, position 0, the null block
+    StageArgs st{0, R, nullptr, nullptr, nullptr, 1, nullptr, m->s_tok, m->s_pos, m->s_bt, mbs,
+                 m->s_sl, kv->num_blocks};
+    if (launch_stage_inputs(st, s) != cudaSuccess) { rc = MBT_ERR_CUDA; break; }
+    Plan p = make_plan(m, R, mbs);
+    // warm-up run outside capture
+    rc = run_step(m, kv, p, m->s_tok, m->s_pos, m->s_bt, mbs, m->s_sl, m->s_next, m->s_logits, s);
+    if (rc != MBT_OK) break;
+    if (cudaStreamSynchronize(s) != cudaSuccess) { rc = MBT_ERR_CUDA; break; }
+    Graph g;
+    g.R = R;
+    for (int v = 0; v < 2 && rc == MBT_OK; ++v) {
+      cudaGraph_t graph;
+      if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) { rc = MBT_ERR_CUDA; break; }
+      int rr = run_step(m, kv, p, m->s_tok, m->s_pos, m->s_bt, mbs, m->s_sl, m->s_next,
+                        v ? m->s_logits : nullptr, cs);
+      cudaError_t ce = cudaStreamEndCapture(cs, &graph);
+      if (rr != MBT_OK || ce != cudaSuccess) { rc = MBT_ERR_CUDA; if (ce == cudaSuccess) cudaGraphDestroy(graph); break; }
+      size_t nn = 0;
+      cudaGraphGetNodes(graph, nullptr, &nn);
+      g.nodes = (int)nn;
+      if (cudaGraphInstantiate(&g.exec[v], graph, 0) != cudaSuccess) rc = MBT_ERR_CUDA;
+      cudaGraphDestroy(graph);
+    }
+    if (rc != MBT_OK) {
+      for (auto& e : g.exec) if (e) cudaGraphExecDestroy(e);
+      break;
+    }
+    m->graphs.push_back(g);
+  }
+  cudaStreamDestroy(cs);
+  if (rc != MBT_OK) { cudaGetLastError(); destroy_graphs(m); return rc; }
+  if (cudaMemsetAsync(m->err, 0, 4, s) != cudaSuccess) return MBT_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MBT_ERR_CUDA;
+  m->graph_kv = kv;
+  return MBT_OK;
+}
+
+static const Graph* pick_graph(const mbt_model* m, const mbt_kv* kv, int B, int bt_stride) {
+  (void)bt_stride;
+  if (m->eager || m->graph_kv != kv) return nullptr;
+  for (const Graph& g : m->graphs)
+    if (g.R >= B) return &g;
+  return nullptr;
+}
+
+int decode_step(mbt_model* m, mbt_kv* kv, int B, const int32_t* tok, const int32_t* pos,
+                const int32_t* bt, int bt_stride, const int32_t* sl, int32_t* next_ids,
+                float* logits, void* stream) {
+  if (!m || !kv) return MBT_ERR_BAD_ARG;
+  if (B <= 0) return MBT_ERR_BATCH;
+  if (kv->m != m || !tok || !pos || !bt || !sl || !next_ids || bt_stride < 1) return MBT_ERR_BAD_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const Graph* g = pick_graph(m, kv, B, bt_stride);
+  if (g) {
+    StageArgs st{B, g->R, tok, pos, bt, bt_stride, sl, m->s_tok, m->s_pos, m->s_bt, m->graph_mbs,
+                 m->s_sl, kv->num_blocks};
+    MBT_CUDA(launch_stage_inputs(st, s));
+    MBT_CUDA(cudaGraphLaunch(g->exec[logits ? 1 : 0], s));
+    MBT_CUDA(cudaMemcpyAsync(next_ids, m->s_next, (size_t)B * 4, cudaMemcpyDeviceToDevice, s));
+    if (logits)
+      MBT_CUDA(cudaMemcpyAsync(logits, m->s_logits, (size_t)B * m->h.vocab * 4, cudaMemcpyDeviceToDevice, s));
+    return MBT_OK;
+  }
+  int rc = ensure_ws(m, B, bt_stride);
+  if (rc != MBT_OK) return rc;
+  Plan p = make_plan(m, B, bt_stride);
+  return run_step(m, kv, p, tok, pos, bt, bt_stride, sl, next_ids, logits, s);
+}
+
+int model_poll_errors(mbt_model* m, void* stream, uint32_t* bits) {
+  if (!m || !bits) return MBT_ERR_BAD_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t v = 0;
+  MBT_CUDA(cudaStreamSynchronize(s));
+  MBT_CUDA(cudaMemcpy(&v, m->err, 4, cudaMemcpyDeviceToHost));
+  MBT_CUDA(cudaMemset(m->err, 0, 4));
+  *bits = v;
+  return MBT_OK;
+}
+
+int model_stats(mbt_model* m, int B, int* kernels, int* uses_graph) {
+  if (!m || !kernels || !uses_graph || B < 1) return MBT_ERR_BAD_ARG;
+  const Graph* g = pick_graph(m, m->graph_kv, B, m->graph_mbs);
+  if (g) {
+    *kernels = g->nodes + 1;   // graph kernel nodes + the staging kernel
+    *uses_graph = 1;
+  } else {
+    *kernels = make_plan(m, B, std::max(1, m->graph_mbs)).kernels;
+    *uses_graph = 0;
+  }
+  return MBT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,240 @@
+"""Whole decode-step parity through the C ABI (include/mbt.h) against the oracle.
+
+Acceptance: max |logit - oracle| <= 3e-2 for BF16 models and 1.5e-1 for FP8
+models over every checked row and step; greedy ids equal wherever the oracle's
+top-2 margin exceeds 1e-2; the set of cache bytes a step writes is exactly the
+slots of the rows' positions (sentinel bytes elsewhere unchanged, padding rows
+only in the null block), and the written values agree with the oracle's to the
+tolerance of the values that produce them.
+
+Both sides start from the same random cache and each keeps its own cache across
+steps (the oracle never reads GPU results); tokens are random at every step, so
+a disagreement in one step's id cannot cascade."""
+import numpy as np
+import pytest
+import torch
+
+from memory_bound_transformer_gb300 import blob as mblob
+from memory_bound_transformer_gb300 import capi
+from memory_bound_transformer_gb300.engine import Engine
+from oracle.decode import OracleKV, decode_step
+from oracle.numerics import bf16_decode, e4m3_decode
+from synth import (EIGHT_B, ONE_B, TINY, SynthModel, random_kv_pool, random_tokens,
+                   seeded_block_tables)
+from tests.helpers import SMALL, SMALL_D128, SMALL_FP8, SMALL_G5, kv_numpy, oracle_weights
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def tol_logits(cfg):
+    return 1.5e-1 if cfg.weight_dtype == "fp8" or cfg.kv_dtype == "fp8" else 3e-2
+
+
+class Case:
+    """Model + cache + block tables shared by the GPU engine and the oracle."""
+
+    def __init__(self, cfg, seed, B, ctx, steps, cache_weights=True, ladder=None, graph=False):
+        self.cfg, self.B, self.steps = cfg, B, steps
+        self.model = SynthModel(cfg, seed, device=DEV, cache=cache_weights)
+        self.blob = mblob.pack(cfg, self.model.tensors(), device=DEV)
+        self.ctx = np.asarray(ctx, np.int32)
+        cap = self.ctx + steps
+        self.nb = int(sum(-(-int(c) // 16) for c in cap)) + 2
+        self.tables = seeded_block_tables(cap, 16, self.nb, seed + 1)
+        self.tables[self.tables < 0] = self.nb
+        self.eng = Engine(self.blob, self.nb)
+        del self.blob
+        pool0 = random_kv_pool(cfg, self.nb, seed + 2, device=DEV)
+        self.eng.pool().copy_(pool0.view(torch.uint8).reshape(-1))
+        self.pool0 = kv_numpy(pool0)
+        self.toks = random_tokens(B * steps, cfg.vocab, seed + 3).reshape(steps, B)
+        if graph:
+            self.eng.capture(ladder, max_blocks_per_seq=self.tables.shape[1])
+        self.bt_dev = torch.tensor(self.tables, device=DEV)
+
+    def gpu_step(self, t, logits=True):
+        B = self.B
+        pos = self.ctx + t
+        tok = torch.tensor(self.toks[t], device=DEV)
+        posd = torch.tensor(pos, device=DEV)
+        sl = torch.tensor(pos + 1, device=DEV)
+        ids = torch.full((B,), -1, dtype=torch.int32, device=DEV)
+        lg = torch.zeros((B, self.cfg.vocab), device=DEV) if logits else None
+        self.eng.step(tok, posd, self.bt_dev, sl, ids, lg)
+        torch.cuda.synchronize()
+        return ids.cpu().numpy(), (lg.double().cpu().numpy() if logits else None)
+
+    def gpu_pool(self):
+        raw = self.eng.pool().cpu().numpy()
+        dt = np.uint8 if self.cfg.kv_dtype == "fp8" else np.uint16
+        return raw.view(dt).reshape(self.pool0.shape)
+
+
+def _check_step(cfg, ids, lg, res):
+    tol = tol_logits(cfg)
+    err = np.abs(lg - res.logits).max()
+    assert err <= tol, f"max logit error {err}"
+    srt = np.sort(res.logits, axis=1)
+    clear = (srt[:, -1] - srt[:, -2]) > 1e-2
+    assert np.array_equal(ids[clear], res.next_ids[clear])
+    assert np.array_equal(ids, np.argmax(lg, axis=1))
+    return err
+
+
+def _check_pool(case, okv, written):
+    """written: set of (block, slot). Bytes elsewhere equal the initial pool on
+    both sides; written values close to the oracle's."""
+    gp = case.gpu_pool()
+    mask = np.zeros(gp.shape[2:5], bool)                 # [nb+1][nkv][16] per layer/kv
+    for blk, slot in written:
+        mask[blk, :, slot] = True
+    for arr, skip_null in ((gp, True), (okv.raw, False)):
+        same = np.all(arr == case.pool0, axis=-1)        # [L][2][nb+1][nkv][16]
+        keep = ~mask
+        if skip_null:                                    # graph padding rows write the null block
+            keep[case.nb] = False
+        assert np.all(same[:, :, keep]), "a byte outside the written slots changed"
+    dec = e4m3_decode if case.cfg.kv_dtype == "fp8" else bf16_decode
+    g = dec(gp[:, :, mask])
+    o = dec(okv.raw[:, :, mask])
+    scale = np.abs(o).max(axis=-1, keepdims=True) + 1e-30
+    rel = 0.25 if case.cfg.kv_dtype == "fp8" else 3e-2
+    assert np.all(np.abs(g - o) <= rel * scale)
+
+
+def _run(case, W, okv, steps):
+    cfg = case.cfg
+    written = set()
+    worst = 0.0
+    for t in range(steps):
+        pos = case.ctx + t
+        ids, lg = case.gpu_step(t)
+        res = decode_step(W, cfg, okv, case.toks[t], pos, case.tables, pos + 1)
+        worst = max(worst, _check_step(cfg, ids, lg, res))
+        for b in range(case.B):
+            written.add((int(case.tables[b][pos[b] // 16]), int(pos[b] % 16)))
+    assert case.eng.errors() == 0
+    _check_pool(case, okv, written)
+    return worst
+
+
+def test_tiny_layer_workload(cuda_lib):
+    """Single decoder layer + LM head, batch 1, 128 tokens of random KV, 8 decode
+    steps from random token ids, replayed from a captured graph."""
+    cfg = TINY
+    case = Case(cfg, 1235, 1, [128], 8, ladder=[1], graph=True)
+    okv = OracleKV(case.pool0.copy(), np.ones(cfg.n_layers), np.ones(cfg.n_layers))
+    assert case.eng.stats(1)[1]
+    _run(case, oracle_weights(case.model), okv, 8)
+
+
+@pytest.mark.parametrize("cfg", [SMALL, SMALL_FP8, SMALL_D128, SMALL_G5], ids=lambda c: c.name)
+@pytest.mark.parametrize("B", [1, 3, 13])
+def test_small_models_eager(cuda_lib, cfg, B):
+    rng = np.random.default_rng(B)
+    ctx = rng.integers(0, 300, size=B)
+    ctx[0] = 0
+    if B > 2:
+        ctx[1], ctx[2] = 15, 16
+    case = Case(cfg, 77 + B, B, ctx, 3)
+    okv = OracleKV(case.pool0.copy(), np.ones(cfg.n_layers), np.ones(cfg.n_layers))
+    _run(case, oracle_weights(case.model), okv, 3)
+
+
+def test_fp8_cache_scales(cuda_lib):
+    cfg = SMALL_FP8
+    case = Case(cfg, 5, 3, [40, 1, 70], 2)
+    ks, vs = [0.5, 1.5], [2.0, 0.75]
+    case.eng.set_kv_scales(ks, vs)
+    okv = OracleKV(case.pool0.copy(), np.array(ks), np.array(vs))
+    _run(case, oracle_weights(case.model), okv, 2)
+
+
+def test_graph_replay_bit_identical_to_eager(cuda_lib):
+    """Graphs change how the step is launched, not what it computes: replaying
+    the rung-4 graph for 4 rows gives the eager run's bits exactly."""
+    cfg = SMALL
+    B = 4
+    ctx = [20, 47, 5, 160]
+    a = Case(cfg, 9, B, ctx, 3)
+    b = Case(cfg, 9, B, ctx, 3, ladder=[1, 2, 4, 8], graph=True)
+    assert b.eng.stats(B)[1] and not a.eng.stats(B)[1]
+    for t in range(3):
+        ia, la = a.gpu_step(t)
+        ib, lb = b.gpu_step(t)
+        assert np.array_equal(ia, ib)
+        assert np.array_equal(la, lb)
+    assert np.array_equal(a.gpu_pool(), b.gpu_pool())
+    assert a.eng.errors() == 0 and b.eng.errors() == 0
+
+
+def test_graph_ladder_padding_and_fallback(cuda_lib):
+    """13 live rows replay the graph captured for 16; 70 rows exceed the top
+    rung and run eagerly; both match the oracle."""
+    cfg = SMALL
+    for B, expect_graph in ((13, True), (70, False)):
+        rng = np.random.default_rng(B)
+        case = Case(cfg, 31, B, rng.integers(1, 100, size=B), 1, ladder=[1, 2, 4, 8, 16], graph=True)
+        assert case.eng.stats(B)[1] == expect_graph
+        okv = OracleKV(case.pool0.copy(), np.ones(cfg.n_layers), np.ones(cfg.n_layers))
+        _run(case, oracle_weights(case.model), okv, 1)
+
+
+def test_1b_workload(cuda_lib):
+    """1B-class decoder at batch 8 with graphs, two steps after a 512-token
+    (random) context."""
+    cfg = ONE_B
+    case = Case(cfg, 1236, 8, [512] * 8, 2, ladder=[1, 2, 4, 8], graph=True)
+    okv = OracleKV(case.pool0.copy(), np.ones(cfg.n_layers), np.ones(cfg.n_layers))
+    _run(case, oracle_weights(case.model), okv, 2)
+
+
+def test_8b_full_size_batch1(cuda_lib):
+    """8B-class decoder, batch 1, one step at a 300-token context."""
+    cfg = EIGHT_B
+    case = Case(cfg, 1237, 1, [300], 1, cache_weights=False, ladder=[1], graph=True)
+    okv = OracleKV(case.pool0.copy(), np.ones(cfg.n_layers), np.ones(cfg.n_layers))
+    model = SynthModel(cfg, 1237, device=DEV, cache=False)
+
+    def W(name, layer):
+        from synth import raw_numpy
+        return {k: raw_numpy(v) for k, v in model.get(name, layer).items()}
+    _run(case, W, okv, 1)
+
+
+def test_host_detected_errors(cuda_lib):
+    cfg = SMALL
+    case = Case(cfg, 3, 2, [5, 9], 1)
+    m, kv = case.eng.model, case.eng.kv
+    d = torch.zeros(4, dtype=torch.int32, device=DEV)
+    bt = case.bt_dev
+    assert capi.decode_step_raw(m, kv, 0, d, d, bt, bt.shape[1], d, d) == -2        # MBT_ERR_BATCH
+    assert capi.decode_step_raw(m, kv, 2, None, d, bt, bt.shape[1], d, d) == -1     # MBT_ERR_BAD_ARG
+    assert capi.decode_step_raw(m, kv, 2, d, d, bt, 0, d, d) == -1
+    assert capi.decode_step_raw(m, None, 2, d, d, bt, bt.shape[1], d, d) == -1
+    assert capi.status_string(-2) == "batch size must be >= 1"
+
+
+def test_device_detected_errors(cuda_lib):
+    cfg = SMALL
+    case = Case(cfg, 4, 2, [5, 9], 1)
+    bt = case.bt_dev
+    ids = torch.zeros(2, dtype=torch.int32, device=DEV)
+    ok_pos = torch.tensor([5, 9], dtype=torch.int32, device=DEV)
+    # token out of range
+    case.eng.step(torch.tensor([cfg.vocab, 1], dtype=torch.int32, device=DEV), ok_pos, bt,
+                  ok_pos + 1, ids)
+    assert case.eng.errors() & capi.DEV_TOKEN_RANGE
+    # seq_len beyond the block table
+    case.eng.step(torch.tensor([1, 1], dtype=torch.int32, device=DEV), ok_pos, bt,
+                  torch.tensor([6, 10 ** 6], dtype=torch.int32, device=DEV), ids)
+    assert case.eng.errors() & capi.DEV_SEQLEN_RANGE
+    # block id out of range: nothing written
+    before = case.gpu_pool().copy()
+    bad = bt.clone()
+    bad[:, :] = case.nb + 7
+    case.eng.step(torch.tensor([1, 1], dtype=torch.int32, device=DEV), ok_pos, bad, ok_pos + 1, ids)
+    assert case.eng.errors() & capi.DEV_BLOCK_RANGE
+    assert np.array_equal(before, case.gpu_pool())
+    assert case.eng.errors() == 0
