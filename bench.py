@@ -200,8 +200,8 @@ def time_gemv_swiglu(cfg, wl, B, dev, reps=3):
     model = SynthModel(cfg, wl.seed + 17, device=dev, cache=False)
     nl = min(cfg.n_layers, max(2, int(24e9 // (2 * cfg.ffn * cfg.hidden * (1 if cfg.weight_dtype == "fp8" else 2)))))
     mats = [model.get("w_gu", l) for l in range(nl)]
-    x = torch.randn((B, cfg.hidden), device=dev).to(torch.bfloat16)
-    act = torch.empty((B, cfg.ffn), dtype=torch.bfloat16, device=dev)
+    x = torch.randn((B, cfg.hidden), device=dev)
+    act = torch.empty((B, cfg.ffn), device=dev)
     wdt = capi.DTYPE_E4M3 if cfg.weight_dtype == "fp8" else capi.DTYPE_BF16
     s = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(s):
@@ -221,7 +221,7 @@ def time_gemv_swiglu(cfg, wl, B, dev, reps=3):
     ms = e0.elapsed_time(e1) / n
     w = 1 if cfg.weight_dtype == "fp8" else 2
     nbytes = 2 * cfg.ffn * cfg.hidden * w + (2 * cfg.ffn * 4 if cfg.weight_dtype == "fp8" else 0) \
-        + B * cfg.hidden * 2 + B * cfg.ffn * 2
+        + B * cfg.hidden * 4 + B * cfg.ffn * 4
     del mats
     torch.cuda.empty_cache()
     return {"ms": ms, "bytes": nbytes, "launches": n}

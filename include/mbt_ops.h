@@ -8,7 +8,8 @@
  * on `stream`. Calls that need scratch space take it from the stream-ordered
  * allocator (cudaMallocAsync / cudaFreeAsync on `stream`). `err` is a device
  * uint32 the kernels OR MBT_DEV_* bits into (may be NULL).
- * BF16 arrays are passed as uint16 bit patterns.
+ * BF16 arrays (weights, gains) are passed as uint16 bit patterns; activations
+ * are fp32.
  */
 #ifndef MBT_OPS_H_
 #define MBT_OPS_H_
@@ -21,22 +22,24 @@ extern "C" {
 #endif
 
 #define MBT_EPI_PARTIAL 0   /* fp32 split-K partial sums out[split][B][N]              */
-#define MBT_EPI_SWIGLU  1   /* act[B][N] = bf16(silu(gate) * up), W has 2N rows        */
+#define MBT_EPI_SWIGLU  1   /* act[B][N] = silu(gate) * up (fp32), W has 2N rows       */
 #define MBT_EPI_ARGMAX  2   /* next_ids[B] = argmax_n (W x)_n, logits[B][N] if non-NULL */
 
-/* op_embed_rmsnorm: r[b] = E[tokens[b]] (fp32), y[b] = bf16(r / sqrt(mean(r^2)
- * + eps) * gamma). RMSNorm as defined in "Root Mean Square Layer
+/* op_embed_rmsnorm: r[b] = E[tokens[b]] (fp32), y[b] = r / sqrt(mean(r^2) + eps)
+ * * gamma (fp32). RMSNorm as defined in "Root Mean Square Layer
  * Normalization" (reference 9 of "Kernel Fusion for Large-Scale LLM
- * Inference"). embed [vocab][H] and gamma [H] BF16; r [B][H] fp32; y [B][H]. */
+ * Inference"). embed [vocab][H] and gamma [H] BF16; r, y [B][H] fp32; H a
+ * multiple of 4. */
 int op_embed_rmsnorm(int B, int H, int vocab, const int32_t* tokens, const uint16_t* embed,
-                     const uint16_t* gamma, float eps, float* r, uint16_t* y, uint32_t* err,
+                     const uint16_t* gamma, float eps, float* r, float* y, uint32_t* err,
                      void* stream);
 
-/* op_add_rmsnorm: r[b] += sum_s delta[s][b]; y[b] = bf16(rmsnorm(r[b]) * gamma)
+/* op_add_rmsnorm: r[b] += sum_s delta[s][b]; y[b] = rmsnorm(r[b]) * gamma
  * ("Kernels, Fusion & CUDA Graphs", "Fix 1: kernel fusion": residual add +
- * RMSNorm in one pass). delta [n_delta][B][H] fp32 (n_delta may be 0). */
+ * RMSNorm in one pass). delta [n_delta][B][H] fp32 (n_delta may be 0); r, y
+ * fp32; gamma BF16. */
 int op_add_rmsnorm(int B, int H, float* r, const float* delta, int n_delta,
-                   const uint16_t* gamma, float eps, uint16_t* y, void* stream);
+                   const uint16_t* gamma, float eps, float* y, void* stream);
 
 /* op_gemv_nsplit: split-K count op_gemv uses for this shape (1 unless PARTIAL). */
 int op_gemv_nsplit(int epi, int w_dtype, int B, int N, int K);
@@ -44,15 +47,16 @@ int op_gemv_nsplit(int epi, int w_dtype, int B, int N, int K);
 /* op_gemv: the weight-streaming projection for B rows (any B >= 1; rows are
  * processed 8 at a time). W [rows][K] row-major, BF16 or e4m3 codes (w_dtype
  * MBT_DTYPE_BF16 / MBT_DTYPE_E4M3) with fp32 per-row scales (NULL for BF16);
- * x [B][K] BF16; K a multiple of 16.
+ * x [B][K] fp32; K a multiple of 16.
  *   PARTIAL: out [nsplit][B][N] fp32, nsplit = op_gemv_nsplit(...) unless
- *            force_nsplit > 0; *nsplit_used receives it (may be NULL).
- *   SWIGLU:  W has 2N rows (gate rows then up rows); act [B][N] BF16.
+ *            force_nsplit > 0 (clamped to K / 8 for BF16, K / 16 for e4m3);
+ *            *nsplit_used receives it (may be NULL).
+ *   SWIGLU:  W has 2N rows (gate rows then up rows); act [B][N] fp32.
  *   ARGMAX:  next_ids [B] int32; logits [B][N] fp32 or NULL.
  * Dequantisation is fused into the projection ("Kernel Fusion for Large-Scale
  * LLM Inference", section 11, "Epilogue and dequant fusion"). */
 int op_gemv(int epi, int w_dtype, const void* W, const float* scales, int N, int K,
-            const uint16_t* x, int B, int force_nsplit, float* out, uint16_t* act,
+            const float* x, int B, int force_nsplit, float* out, float* act,
             float* logits, int32_t* next_ids, int* nsplit_used, uint32_t* err, void* stream);
 
 /* op_rope_kv_write: rotate q and k of qkv [B][(nq + 2 nkv) d] (fp32; q heads,
@@ -70,14 +74,14 @@ int op_rope_kv_write(int B, const float* qkv, int nq, int nkv, int d, const int3
 /* op_paged_attention: out[b][h] = sum_t softmax_t(q[b][h] . K_t / sqrt(d)) V_t
  * over t < seq_lens[b], K_t and V_t (times k_scale, v_scale) gathered through
  * bt; query head h reads KV head h / (nq / nkv). q [B][nq][d] fp32; out
- * [B][nq * d] BF16. Split-K over the context with the launch geometry the
+ * [B][nq * d] fp32. Split-K over the context with the launch geometry the
  * decode step uses for a table of bt_stride entries. ("GPU Inference
  * Internals", "The KV-Cache Ledger" and "Kernels: FlashAttention and the Memory
  * Hierarchy".) */
 int op_paged_attention(int B, const float* q, int nq, int nkv, int d, const void* kpool,
                        const void* vpool, int kv_dtype, float k_scale, float v_scale,
                        const int32_t* bt, int bt_stride, const int32_t* seq_lens, int num_blocks,
-                       uint16_t* out, uint32_t* err, void* stream);
+                       float* out, uint32_t* err, void* stream);
 
 #ifdef __cplusplus
 }

@@ -12,8 +12,9 @@
 // incrementally, no score matrix in HBM). One CTA per (split of the context,
 // KV head, row) so that a batch-1 step still spreads the KV stream over all SMs;
 // each CTA reads its KV blocks once for all query heads of the group, keeps a
-// running max and sum per head and writes an unnormalised partial; a second
-// kernel merges the splits.
+// running max and sum per head and writes an unnormalised partial. The last
+// CTA of a (row, KV head) to finish -- found with an atomic ticket, nothing
+// waits -- merges that group's splits.
 #include "common.cuh"
 #include "internal.h"
 
@@ -63,10 +64,12 @@ __device__ __forceinline__ void chunk_to_float<1>(const uint4& c, float* f) {
   }
 }
 
+// One split of one (row, KV head): stream its KV blocks once for all query
+// heads of the group and leave (unnormalised o, running max m, sum l) per head.
 template <int D, int KV8>
-__global__ void __launch_bounds__(kAttnThreads, 2) attn_split_kernel(const AttnArgs a) {
+__device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, int b, int h, int sp,
+                                       int G, size_t head0, int seq, int blk0, int blk1) {
   using S = AttnShape<D, KV8>;
-  extern __shared__ __align__(16) unsigned char smem[];
   float* qs = reinterpret_cast<float*>(smem);                        // [group][D]
   unsigned char* kt = smem + (size_t)kMaxGroup * D * 4;               // [2][tile][ROWB] swizzled
   unsigned char* vt = kt + 2 * (size_t)kAttnTile * S::ROWB;           // [2][tile][ROWB]
@@ -74,29 +77,32 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_split_kernel(const AttnA
   float* st_m = sc + kMaxGroup * kAttnTile;
   float* st_l = st_m + kMaxGroup;
   float* st_a = st_l + kMaxGroup;
-
-  const int sp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int G = a.nq / a.nkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const size_t head0 = (size_t)b * a.nq + (size_t)h * G;             // first query head of the group
-  const int seq = a.seq_lens[b];
-
-  auto write_empty = [&]() {
-    if (tid < G) a.part_ml[(head0 + tid) * a.nsplit + sp] = make_float2(-INFINITY, 0.f);
-  };
-  if (seq < 1 || seq > a.bt_stride * kBlockTokens) {
-    if (tid == 0 && sp == 0 && h == 0) set_err(a.err, MBT_DEV_SEQLEN_RANGE);
-    write_empty();
-    return;
-  }
-  const int nblk = (seq + kBlockTokens - 1) / kBlockTokens;
-  const int blk0 = sp * a.bps;
-  const int blk1 = min(nblk, blk0 + a.bps);
-  if (blk0 >= nblk) { write_empty(); return; }
 
   // queries of the group, pre-scaled into the log2 domain with the K dequant scale
   const float qscale = 1.4426950408889634f / sqrtf((float)D) * a.k_scale;
-  for (int i = tid; i < G * D; i += kAttnThreads) qs[i] = a.q[head0 * D + i] * qscale;
+  if (a.qkv) {
+    // RoPE (rotate-half: element i pairs with i + D/2) straight from the QKV
+    // projection's partial sums
+    const int half = D / 2;
+    int pos = a.positions[b];
+    if (pos < 0 || pos >= a.max_pos) pos = 0;
+    const float* src = a.qkv + (size_t)b * a.ld_qkv + (size_t)h * G * D;
+    const float2* cs = a.rope + (size_t)pos * half;
+    for (int e = tid; e < G * half; e += kAttnThreads) {
+      const int g = e / half, i = e - g * half;
+      float x1 = 0.f, x2 = 0.f;
+      for (int s2 = 0; s2 < a.qkv_nsplit; ++s2) {
+        x1 += src[(size_t)s2 * a.qkv_split_stride + g * D + i];
+        x2 += src[(size_t)s2 * a.qkv_split_stride + g * D + i + half];
+      }
+      const float2 t = cs[i];
+      qs[g * D + i] = (x1 * t.x - x2 * t.y) * qscale;
+      qs[g * D + i + half] = (x2 * t.x + x1 * t.y) * qscale;
+    }
+  } else {
+    for (int i = tid; i < G * D; i += kAttnThreads) qs[i] = a.q[head0 * D + i] * qscale;
+  }
   if (tid < G) { st_m[tid] = -INFINITY; st_l[tid] = 0.f; }
 
   const unsigned char* kpool = reinterpret_cast<const unsigned char*>(a.kpool);
@@ -238,24 +244,131 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_split_kernel(const AttnA
   if (tid < G) a.part_ml[(head0 + tid) * a.nsplit + sp] = make_float2(st_m[tid], st_l[tid]);
 }
 
-// Merge the splits of one (row, query head): rescale each partial to the
+// Merge the splits of the group's G query heads: rescale each partial to the
 // common maximum, sum, divide by the total softmax mass, apply the V scale.
-__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a) {
-  const int qh = blockIdx.x, b = blockIdx.y;
-  const size_t head = (size_t)b * a.nq + qh;
-  const float2* ml = a.part_ml + head * a.nsplit;
-  float M = -INFINITY;
-  for (int s = 0; s < a.nsplit; ++s) if (ml[s].y > 0.f) M = fmaxf(M, ml[s].x);
-  float L = 0.f;
-  for (int s = 0; s < a.nsplit; ++s) if (ml[s].y > 0.f) L += exp2f(ml[s].x - M) * ml[s].y;
-  const float inv = L > 0.f ? a.v_scale / L : 0.f;
-  for (int d = threadIdx.x; d < a.d; d += blockDim.x) {
+__device__ __forceinline__ void merge_splits(const AttnArgs& a, float* wsm, int G, size_t head0, int D) {
+  const int tid = threadIdx.x;
+  const int ns = a.nsplit;
+  // per (head, split) weight exp2(m_s - M) / L in shared memory
+  for (int g = tid; g < G; g += blockDim.x) {
+    const float2* ml = a.part_ml + (head0 + g) * ns;
+    float M = -INFINITY;
+    for (int s = 0; s < ns; ++s) if (ml[s].y > 0.f) M = fmaxf(M, ml[s].x);
+    float L = 0.f;
+    for (int s = 0; s < ns; ++s) if (ml[s].y > 0.f) L += exp2f(ml[s].x - M) * ml[s].y;
+    const float inv = L > 0.f ? a.v_scale / L : 0.f;
+    for (int s = 0; s < ns; ++s) wsm[g * ns + s] = ml[s].y > 0.f ? exp2f(ml[s].x - M) * inv : 0.f;
+  }
+  __syncthreads();
+  for (int e = tid; e < G * D; e += blockDim.x) {
+    const int g = e / D, d = e - g * D;
+    const float* po = a.part_o + (head0 + g) * ns * D + d;
     float acc = 0.f;
-    for (int s = 0; s < a.nsplit; ++s)
-      if (ml[s].y > 0.f) acc += exp2f(ml[s].x - M) * a.part_o[(head * a.nsplit + s) * a.d + d];
-    a.out[head * a.d + d] = __float2bfloat16_rn(acc * inv);
+    for (int s = 0; s < ns; ++s) {
+      const float w = wsm[g * ns + s];
+      if (w != 0.f) acc += w * po[(size_t)s * D];
+    }
+    a.out[(head0 + g) * D + d] = acc;
   }
 }
+
+// Fused "RoPE + KV-cache write" ("Kernels, Fusion & CUDA Graphs", "Fix 1:
+// kernel fusion"): rotate the new token's key for KV head h and store it and its
+// value at block bt[p / 16], slot p % 16, rounded to the cache format.
+template <int D, int KV8>
+__device__ __forceinline__ void write_new_kv(const AttnArgs& a, int b, int h, int pos, int blk) {
+  const int half = D / 2;
+  const float* src = a.qkv + (size_t)b * a.ld_qkv;
+  const int kcol = (a.nq + h) * D, vcol = (a.nq + a.nkv + h) * D;
+  const float2* cs = a.rope + (size_t)pos * half;
+  const size_t base = (((size_t)blk * a.nkv + h) * kBlockTokens + pos % kBlockTokens) * D;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) {
+    float k1 = 0.f, k2 = 0.f, v = 0.f;
+    const int ip = i < half ? i : i - half;
+    for (int s2 = 0; s2 < a.qkv_nsplit; ++s2) {
+      const float* p = src + (size_t)s2 * a.qkv_split_stride;
+      k1 += p[kcol + ip];
+      k2 += p[kcol + ip + half];
+      v += p[vcol + i];
+    }
+    const float2 t = cs[ip];
+    const float k = i < half ? k1 * t.x - k2 * t.y : k2 * t.x + k1 * t.y;
+    const float ks = __fdiv_rn(k, a.k_scale), vs = __fdiv_rn(v, a.v_scale);
+    if (KV8) {
+      reinterpret_cast<uint8_t*>(const_cast<void*>(a.kpool))[base + i] = f32_to_e4m3(ks);
+      reinterpret_cast<uint8_t*>(const_cast<void*>(a.vpool))[base + i] = f32_to_e4m3(vs);
+    } else {
+      reinterpret_cast<uint16_t*>(const_cast<void*>(a.kpool))[base + i] = f32_to_bf16_bits(ks);
+      reinterpret_cast<uint16_t*>(const_cast<void*>(a.vpool))[base + i] = f32_to_bf16_bits(vs);
+    }
+  }
+}
+
+template <int D, int KV8>
+__global__ void __launch_bounds__(kAttnThreads, 2) attn_split_kernel(const AttnArgs a) {
+  using S = AttnShape<D, KV8>;
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int sp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int G = a.nq / a.nkv;
+  const int tid = threadIdx.x;
+  const size_t head0 = (size_t)b * a.nq + (size_t)h * G;             // first query head of the group
+  const int seq = a.seq_lens[b];
+  pdl_launch_dependents();
+
+  // The cached context is not produced by the previous kernel: pull this
+  // split's K and V blocks into L2 before waiting for it.
+  if (seq >= 1 && seq <= a.bt_stride * kBlockTokens) {
+    const int nb_all = (seq + kBlockTokens - 1) / kBlockTokens;
+    const int j = sp * a.bps + (tid >> 1);
+    if ((tid >> 1) < a.bps && j < nb_all) {
+      const int blk = a.bt[(size_t)b * a.bt_stride + j];
+      if (blk >= 0 && blk <= a.num_blocks) {
+        const size_t off = ((size_t)blk * a.nkv + h) * kBlockTokens * S::ROWB;
+        prefetch_l2((const unsigned char*)((tid & 1) ? a.vpool : a.kpool) + off, kBlockTokens * S::ROWB);
+      }
+    }
+  }
+  pdl_wait();
+
+  if (a.qkv) {
+    // the split holding the new token's block writes its K and V first
+    int pos = a.positions[b];
+    const bool pos_ok = pos >= 0 && pos < a.max_pos;
+    if (!pos_ok && tid == 0 && sp == 0 && h == 0) set_err(a.err, MBT_DEV_POS_RANGE);
+    const int jb = pos_ok ? pos / kBlockTokens : -1;
+    if (pos_ok && jb < a.bt_stride && sp == jb / a.bps) {
+      const int blk = a.bt[(size_t)b * a.bt_stride + jb];
+      if (blk >= 0 && blk <= a.num_blocks) write_new_kv<D, KV8>(a, b, h, pos, blk);
+      else if (tid == 0) set_err(a.err, MBT_DEV_BLOCK_RANGE);
+    } else if (pos_ok && jb >= a.bt_stride && tid == 0 && sp == 0) {
+      set_err(a.err, MBT_DEV_BLOCK_RANGE);
+    }
+    __syncthreads();
+  }
+  const bool seq_ok = seq >= 1 && seq <= a.bt_stride * kBlockTokens;
+  if (!seq_ok && tid == 0 && sp == 0 && h == 0) set_err(a.err, MBT_DEV_SEQLEN_RANGE);
+  const int nblk = seq_ok ? (seq + kBlockTokens - 1) / kBlockTokens : 0;
+  const int blk0 = sp * a.bps;
+  const int blk1 = min(nblk, blk0 + a.bps);
+  if (blk0 < nblk) attend<D, KV8>(a, smem, b, h, sp, G, head0, seq, blk0, blk1);
+  else if (tid < G) a.part_ml[(head0 + tid) * a.nsplit + sp] = make_float2(-INFINITY, 0.f);
+
+  // ticket: the last CTA of this (row, KV head) merges the splits
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int t = atomicAdd(a.tickets + (size_t)b * a.nkv + h, 1);
+    last = (t == a.nsplit - 1);
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  merge_splits(a, reinterpret_cast<float*>(smem), G, head0, D);
+  if (tid == 0) a.tickets[(size_t)b * a.nkv + h] = 0;     // ready for the next launch
+}
+
+
 
 void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nsplit) {
   const int target = 2 * num_sms;
@@ -297,10 +410,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
   void* fn = attn_pick(a.d, a.kv_fp8, &sm);
   AttnArgs args = a;
   void* params[] = {&args};
-  cudaError_t e = cudaLaunchKernel(fn, dim3(a.nsplit, a.nkv, a.B), dim3(kAttnThreads), params, sm, s);
-  if (e != cudaSuccess) return e;
-  attn_combine_kernel<<<dim3(a.nq, a.B), 128, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(fn, dim3(a.nsplit, a.nkv, a.B), dim3(kAttnThreads), sm, s, params);
 }
 
 }  // namespace mbt

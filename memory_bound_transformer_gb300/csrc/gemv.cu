@@ -7,7 +7,8 @@
 //   * every weight byte is loaded once with 16-byte streaming loads (L1 bypass),
 //     a warp instruction covering 512 contiguous bytes of one row, several rows
 //     and vectors per thread in flight;
-//   * the activation rows x (BF16) sit in shared memory for the whole CTA;
+//   * the activation rows x (fp32: rounding them to BF16 would move 16-layer
+//     logits by ~5e-2) sit in shared memory for the whole CTA;
 //   * rows are split over CTAs in equal contiguous ranges (the grid is a
 //     multiple of the SM count), so every SM streams the same number of bytes;
 //   * FP8-e4m3 weights are converted in registers and the per-output-channel
@@ -59,67 +60,134 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[M], int lane, int
   return v[0];
 }
 
+// Four weights of a 16-byte vector (quarter q) widened to fp32, exactly.
 template <int WT>
-__device__ __forceinline__ void widen8(const uint4& w, int half, float (&f)[8]);
+__device__ __forceinline__ void widen4(const uint4& w, int q, float (&f)[4]);
 
 template <>
-__device__ __forceinline__ void widen8<W_BF16>(const uint4& w, int, float (&f)[8]) {
-  f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
-  f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z); f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
+__device__ __forceinline__ void widen4<W_BF16>(const uint4& w, int q, float (&f)[4]) {
+  const uint32_t a = q ? w.z : w.x, b = q ? w.w : w.y;
+  f[0] = bf16_lo(a); f[1] = bf16_hi(a); f[2] = bf16_lo(b); f[3] = bf16_hi(b);
 }
 
 template <>
-__device__ __forceinline__ void widen8<W_E4M3>(const uint4& w, int half, float (&f)[8]) {
-  const uint32_t a = half ? w.z : w.x, b = half ? w.w : w.y;
-  float2 t;
-  t = e4m3x2_to_float2(a);        f[0] = t.x; f[1] = t.y;
-  t = e4m3x2_to_float2(a >> 16);  f[2] = t.x; f[3] = t.y;
-  t = e4m3x2_to_float2(b);        f[4] = t.x; f[5] = t.y;
-  t = e4m3x2_to_float2(b >> 16);  f[6] = t.x; f[7] = t.y;
+__device__ __forceinline__ void widen4<W_E4M3>(const uint4& w, int q, float (&f)[4]) {
+  const uint32_t a = q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w;
+  const float2 lo = e4m3x2_to_float2(a), hi = e4m3x2_to_float2(a >> 16);
+  f[0] = lo.x; f[1] = lo.y; f[2] = hi.x; f[3] = hi.y;
 }
 
-template <int NB, int WT, int EPI>
+template <int NB, int WT, int EPI, int PRO>
 __global__ void __launch_bounds__(kGemvThreads, GemvShape<NB>::MINB)
 gemv_kernel(const GemvArgs a) {
   constexpr int RG = GemvShape<NB>::RG;          // weight rows per group
   constexpr int U = GemvShape<NB>::U;            // 16-B vectors per row per thread in flight
   constexpr int EPV = (WT == W_BF16) ? 8 : 16;   // elements per 16-B weight vector
-  constexpr int HALVES = EPV / 8;                // 8-element halves per vector
+  constexpr int QN = EPV / 4;                    // fp32 quarters (float4) of x per vector
   constexpr int M = RG * NB;                     // dot products per group
   constexpr int CH = (EPI == EPI_SWIGLU) ? RG / 2 : RG;   // output channels per group
   static_assert(M <= 32 && (M & (M - 1)) == 0, "M must be a power of two <= 32");
 
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_launch_dependents();
 
   // this CTA's split of K, in 16-byte weight vectors
   const int nvec_all = a.K / EPV;
   const int split = blockIdx.y, nsplit = gridDim.y;
   const int v0 = (int)((long long)nvec_all * split / nsplit);
   const int nvec = (int)((long long)nvec_all * (split + 1) / nsplit) - v0;
-
-  // x tile: [NB][HALVES][nvec] uint4 (8 BF16 each): thread-contiguous reads
-  uint4* xs = reinterpret_cast<uint4*>(smem);
-  const int xrow = nvec * HALVES;
-  float* red = reinterpret_cast<float*>(smem + (size_t)NB * xrow * 16);   // [2][warps][32]
-  float* fin = red + 2 * kGemvWarps * 32;                                  // [M]
-  {
-    const bf16* xb = a.x + (size_t)v0 * EPV;
-    for (int i = tid; i < NB * xrow; i += kGemvThreads) {
-      const int b = i / xrow, j = i - b * xrow;          // j = h * nvec + v
-      const int h = j / nvec, v = j - h * nvec;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (b < a.nb) val = *reinterpret_cast<const uint4*>(xb + (size_t)b * a.ldx + (size_t)v * EPV + h * 8);
-      xs[i] = val;
-    }
-  }
-  __syncthreads();
-
   const int G = gridDim.x, c = blockIdx.x;
   const int r_begin = (int)((long long)a.N * c / G);
   const int r_end = (int)((long long)a.N * (c + 1) / G);
   const size_t row_bytes = (size_t)a.K * (WT == W_BF16 ? 2 : 1);
   const unsigned char* Wb = reinterpret_cast<const unsigned char*>(a.W) + (size_t)v0 * 16;
+
+  // The weights do not depend on the previous kernel: start pulling this CTA's
+  // first rows into L2 while that kernel drains.
+  if (tid < RG && r_begin < r_end) {
+    const int i = tid;
+    const int ch = min(r_begin + (i % CH), r_end - 1);
+    const int wr = (EPI == EPI_SWIGLU && i >= CH) ? a.N + ch : ch;
+    const uint32_t bytes = (uint32_t)min((size_t)nvec * 16, (size_t)32768);
+    prefetch_l2(Wb + (size_t)wr * row_bytes, bytes);
+  }
+  pdl_wait();
+
+  // x tile (fp32): [NB][QN][nvec] float4, so that a warp reads 512 contiguous bytes
+  float4* xs = reinterpret_cast<float4*>(smem);
+  const int xrow = nvec * QN;
+  float* red = reinterpret_cast<float*>(smem + (size_t)NB * xrow * 16);   // [2][warps][32]
+  float* fin = red + 2 * kGemvWarps * 32;                                  // [M]
+  if (PRO == PRO_X) {
+    const float* xb = a.x + (size_t)v0 * EPV;
+    for (int i = tid; i < NB * xrow; i += kGemvThreads) {
+      const int b = i / xrow, j = i - b * xrow;          // j = q * nvec + v
+      const int q = j / nvec, v = j - q * nvec;
+      float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (b < a.nb) val = *reinterpret_cast<const float4*>(xb + (size_t)b * a.ldx + (size_t)v * EPV + q * 4);
+      xs[i] = val;
+    }
+  } else {
+    // RMSNorm prologue (nsplit == 1): x = (r_in + sum_s delta_s) / rms * gamma.
+    // "Residual add + RMSNorm" ("Kernels, Fusion & CUDA Graphs", "Fix 1: kernel
+    // fusion") done by every CTA into its own x tile; CTA 0 stores the new residual.
+    const int k4n = a.K / 4;
+    const bool store_r = (c == 0 && split == 0);
+    float ss[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      ss[b] = 0.f;
+      if (b < a.nb) {
+        const float4* __restrict__ r4 = reinterpret_cast<const float4*>(a.r_in + (size_t)b * a.K);
+        const float4* __restrict__ d4 = reinterpret_cast<const float4*>(a.delta + (size_t)b * a.K);
+        float4* __restrict__ o4 = reinterpret_cast<float4*>(a.r_out + (size_t)b * a.K);
+        for (int k4 = tid; k4 < k4n; k4 += kGemvThreads) {
+          float4 x = r4[k4];
+          for (int sidx = 0; sidx < a.n_delta; ++sidx) {
+            const float4 t = d4[(size_t)sidx * (a.delta_stride / 4) + k4];
+            x.x += t.x; x.y += t.y; x.z += t.z; x.w += t.w;
+          }
+          if (store_r) o4[k4] = x;
+          ss[b] += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+          const int v = k4 / QN, q = k4 - v * QN;
+          xs[(b * QN + q) * nvec + v] = x;
+        }
+      } else {
+        for (int k4 = tid; k4 < k4n; k4 += kGemvThreads) {
+          const int v = k4 / QN, q = k4 - v * QN;
+          xs[(b * QN + q) * nvec + v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      ss[b] = warp_sum(ss[b]);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int b = 0; b < NB; ++b) red[warp * NB + b] = ss[b];
+    }
+    __syncthreads();
+    float inv[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      float t = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < kGemvWarps; ++w2) t += red[w2 * NB + b];
+      inv[b] = 1.0f / sqrtf(t / (float)a.K + a.eps);
+    }
+    const uint2* g2 = reinterpret_cast<const uint2*>(a.gamma);
+    for (int k4 = tid; k4 < k4n; k4 += kGemvThreads) {
+      const uint2 g = g2[k4];
+      const float g0 = bf16_lo(g.x), g1 = bf16_hi(g.x), gg2 = bf16_lo(g.y), g3 = bf16_hi(g.y);
+      const int v = k4 / QN, q = k4 - v * QN;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        float4& x = xs[(b * QN + q) * nvec + v];
+        x.x = x.x * inv[b] * g0; x.y = x.y * inv[b] * g1;
+        x.z = x.z * inv[b] * gg2; x.w = x.w * inv[b] * g3;
+      }
+    }
+  }
+  __syncthreads();
 
   float best_v = -INFINITY;
   int best_i = 0x7fffffff;
@@ -152,22 +220,21 @@ gemv_kernel(const GemvArgs a) {
         const int vv = v + u * kGemvThreads;
         if (vv < nvec) {
 #pragma unroll
-          for (int h = 0; h < HALVES; ++h) {
-            float xf[NB][8];
+          for (int q = 0; q < QN; ++q) {
+            float4 xq[NB];
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-              const uint4 xv = xs[b * xrow + h * nvec + vv];
-              widen8<W_BF16>(xv, 0, xf[b]);
-            }
+            for (int b = 0; b < NB; ++b) xq[b] = xs[(b * QN + q) * nvec + vv];
 #pragma unroll
             for (int i = 0; i < RG; ++i) {
-              float wf[8];
-              widen8<WT>(w[u][i], h, wf);
+              float wf[4];
+              widen4<WT>(w[u][i], q, wf);
 #pragma unroll
               for (int b = 0; b < NB; ++b) {
                 float s = acc[i * NB + b];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) s = fmaf(wf[e], xf[b][e], s);
+                s = fmaf(wf[0], xq[b].x, s);
+                s = fmaf(wf[1], xq[b].y, s);
+                s = fmaf(wf[2], xq[b].z, s);
+                s = fmaf(wf[3], xq[b].w, s);
                 acc[i * NB + b] = s;
               }
             }
@@ -205,8 +272,7 @@ gemv_kernel(const GemvArgs a) {
         }
         if (ch < r_end && b < a.nb) {
           if (WT == W_E4M3) { g *= a.scale[ch]; u *= a.scale[a.N + ch]; }
-          const float act = g / (1.f + expf(-g)) * u;
-          a.act[(size_t)b * a.lda + ch] = __float2bfloat16_rn(act);
+          a.act[(size_t)b * a.lda + ch] = g / (1.f + expf(-g)) * u;
         }
       }
     } else {  // EPI_ARGMAX
@@ -243,8 +309,8 @@ gemv_kernel(const GemvArgs a) {
 // host side
 
 namespace {
-constexpr size_t kXsBudgetShared = 96 * 1024;    // 2 CTAs per SM
-constexpr size_t kXsBudgetSolo = 192 * 1024;     // 1 CTA per SM (NB = 8)
+constexpr size_t kXsBudgetShared = 96 * 1024;    // x tile that still lets 2 CTAs share an SM
+constexpr size_t kXsMax = 216 * 1024;            // largest x tile (1 CTA per SM)
 
 int nb_template(int nb) { return nb <= 1 ? 1 : nb <= 2 ? 2 : nb <= 4 ? 4 : 8; }
 
@@ -261,14 +327,16 @@ int rows_per_group(int nbt, int epi) {
 }
 
 template <int NB, int WT, int EPI>
-void* kernel_ptr() { return (void*)gemv_kernel<NB, WT, EPI>; }
+void* kernel_ptr(int pro) {
+  return pro == PRO_NORM ? (void*)gemv_kernel<NB, WT, EPI, PRO_NORM> : (void*)gemv_kernel<NB, WT, EPI, PRO_X>;
+}
 
-void* pick(int nbt, int wt, int epi) {
+void* pick(int nbt, int wt, int epi, int pro) {
 #define MBT_PICK_E(NB, WT)                                               \
   switch (epi) {                                                         \
-    case EPI_PARTIAL: return kernel_ptr<NB, WT, EPI_PARTIAL>();          \
-    case EPI_SWIGLU: return kernel_ptr<NB, WT, EPI_SWIGLU>();            \
-    default: return kernel_ptr<NB, WT, EPI_ARGMAX>();                    \
+    case EPI_PARTIAL: return kernel_ptr<NB, WT, EPI_PARTIAL>(pro);       \
+    case EPI_SWIGLU: return kernel_ptr<NB, WT, EPI_SWIGLU>(pro);         \
+    default: return kernel_ptr<NB, WT, EPI_ARGMAX>(pro);                 \
   }
 #define MBT_PICK_W(NB) \
   if (wt == W_BF16) { MBT_PICK_E(NB, W_BF16) } else { MBT_PICK_E(NB, W_E4M3) }
@@ -283,48 +351,58 @@ void* pick(int nbt, int wt, int epi) {
 }
 }  // namespace
 
-GemvLaunch gemv_plan(int epi, int wtype, int nb, int N, int K, int num_sms, int force_nsplit) {
+int gemv_max_rows(int epi, int K, int pro) {
+  if (epi == EPI_PARTIAL && pro == PRO_X) return 8;
+  const size_t per_row = (size_t)K * 4;
+  for (int nb = 8; nb > 1; nb >>= 1)
+    if ((size_t)nb * per_row <= kXsMax) return nb;
+  return 1;
+}
+
+GemvLaunch gemv_plan(int epi, int wtype, int nb, int N, int K, int num_sms, int force_nsplit, int pro) {
   GemvLaunch g;
   g.nb_tmpl = nb_template(nb);
   const int epv = wtype == W_BF16 ? 8 : 16;
   const int nvec_all = K / epv;
-  const size_t budget = g.nb_tmpl == 8 ? kXsBudgetSolo : kXsBudgetShared;
-  const size_t xs_full = (size_t)g.nb_tmpl * K * 2;
-  int ns = (int)((xs_full + budget - 1) / budget);
+  const size_t xs_full = (size_t)g.nb_tmpl * K * 4;
+  int ns = (int)((xs_full + kXsBudgetShared - 1) / kXsBudgetShared);
+  if (g.nb_tmpl == 8) ns = (int)((xs_full + kXsMax - 1) / kXsMax);
   if (epi != EPI_PARTIAL) ns = 1;
   if (force_nsplit > 0) ns = force_nsplit;
+  if (pro == PRO_NORM) ns = 1;              // the norm needs the whole row in one CTA
   if (ns > nvec_all) ns = nvec_all;
   if (ns < 1) ns = 1;
   g.nsplit = ns;
-  const int per_sm = g.nb_tmpl == 8 ? 1 : 2;
+  const size_t nvec_max = (size_t)(nvec_all + ns - 1) / ns;
+  g.smem = (size_t)g.nb_tmpl * nvec_max * 16 * (epv / 4) + 2 * kGemvWarps * 32 * 4 + 32 * 4;
+  const int per_sm = (g.nb_tmpl < 8 && g.smem <= 110 * 1024) ? 2 : 1;
   int grid = num_sms * per_sm / ns;
   if (grid < 1) grid = 1;
   const int rg = rows_per_group(g.nb_tmpl, epi);
   const int max_grid = (N + rg - 1) / rg;
   if (grid > max_grid) grid = max_grid;
   g.grid = grid;
-  const size_t nvec_max = (size_t)(nvec_all + ns - 1) / ns;
-  g.smem = (size_t)g.nb_tmpl * nvec_max * 16 * (epv / 8) + 2 * kGemvWarps * 32 * 4 + 32 * 4;
   return g;
 }
 
-cudaError_t gemv_launch(int epi, const GemvArgs& a, const GemvLaunch& g, cudaStream_t s) {
-  void* fn = pick(g.nb_tmpl, a.wtype, epi);
+cudaError_t gemv_launch(int epi, int pro, const GemvArgs& a, const GemvLaunch& g, cudaStream_t s) {
+  void* fn = pick(g.nb_tmpl, a.wtype, epi, pro);
   GemvArgs args = a;
   void* params[] = {&args};
-  return cudaLaunchKernel(fn, dim3(g.grid, g.nsplit), dim3(kGemvThreads), params, g.smem, s);
+  return launch_pdl(fn, dim3(g.grid, g.nsplit), dim3(kGemvThreads), g.smem, s, params);
 }
 
 cudaError_t gemv_init() {
   const int nbs[4] = {1, 2, 4, 8};
   for (int i = 0; i < 4; ++i)
     for (int wt = 0; wt < 2; ++wt)
-      for (int epi = 0; epi < 3; ++epi) {
-        const int lim = nbs[i] == 8 ? 227 * 1024 : 113 * 1024;
-        cudaError_t e = cudaFuncSetAttribute(pick(nbs[i], wt, epi),
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-        if (e != cudaSuccess) return e;
-      }
+      for (int epi = 0; epi < 3; ++epi)
+        for (int pro = 0; pro < 2; ++pro) {
+          const int lim = 227 * 1024;
+          cudaError_t e = cudaFuncSetAttribute(pick(nbs[i], wt, epi, pro),
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+          if (e != cudaSuccess) return e;
+        }
   return cudaSuccess;
 }
 

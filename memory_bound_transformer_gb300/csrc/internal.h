@@ -10,6 +10,11 @@ namespace mbt {
 typedef __nv_bfloat16 bf16;
 
 enum Epilogue { EPI_PARTIAL = 0, EPI_SWIGLU = 1, EPI_ARGMAX = 2 };
+enum Prologue { PRO_X = 0, PRO_NORM = 1 };
+
+// Launch with the programmatic-stream-serialization attribute (PDL) so that the
+// kernel's independent prologue overlaps the previous kernel's tail.
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args);
 
 struct ArgmaxPart { float v; int i; };
 
@@ -20,12 +25,16 @@ struct GemvArgs {
   int wtype;                // W_BF16 / W_E4M3
   int N;                    // output channels (SWIGLU: ffn; W holds 2N rows)
   int K;                    // multiple of 16
-  const bf16* x; int ldx;   // [nb][ldx] BF16 input rows, 16-byte aligned
+  const float* x; int ldx;  // PRO_X: [nb][ldx] fp32 input rows, 16-byte aligned
   int nb;                   // batch rows, 1..8
+  // PRO_NORM: x = rmsnorm(r_in + sum_s delta[s]) * gamma over rows of K
+  // elements; the CTA at (0, 0) stores r_in + sum_s delta[s] to r_out
+  const float* r_in; const float* delta; int n_delta; long long delta_stride;
+  const bf16* gamma; float eps; float* r_out;
   // EPI_PARTIAL: out[split * split_stride + b * ldo + n] (fp32, no accumulate)
   float* out; long long split_stride; int ldo;
-  // EPI_SWIGLU: act[b * lda + n] = bf16(silu(gate_n) * up_n)
-  bf16* act; int lda;
+  // EPI_SWIGLU: act[b * lda + n] = silu(gate_n) * up_n (fp32)
+  float* act; int lda;
   // EPI_ARGMAX: per-CTA best (value, index) per row into part[cta * part_ld + b];
   // logits[b * ldl + n] written when logits != null
   float* logits; int ldl;
@@ -37,21 +46,25 @@ struct GemvLaunch { int nb_tmpl; int nsplit; int grid; size_t smem; };
 
 // Launch geometry for a GEMV of this shape (deterministic: the same inputs give
 // the same geometry, so eager runs and graph replays do the same arithmetic).
-GemvLaunch gemv_plan(int epi, int wtype, int nb, int N, int K, int num_sms, int force_nsplit);
-cudaError_t gemv_launch(int epi, const GemvArgs& a, const GemvLaunch& g, cudaStream_t s);
+GemvLaunch gemv_plan(int epi, int wtype, int nb, int N, int K, int num_sms, int force_nsplit,
+                     int pro = PRO_X);
+// Most batch rows one launch may take for this epilogue and prologue (the fp32
+// x tile must fit in shared memory when K cannot be split).
+int gemv_max_rows(int epi, int K, int pro = PRO_X);
+cudaError_t gemv_launch(int epi, int pro, const GemvArgs& a, const GemvLaunch& g, cudaStream_t s);
 cudaError_t gemv_init();   // raise dynamic shared-memory limits (once per process)
 
-// r <- E[token] (fp32); y <- bf16(rmsnorm(r) * gamma)
+// r <- E[token] (fp32); y <- rmsnorm(r) * gamma (fp32)
 struct EmbedNormArgs {
   int B, H, vocab; const int* tokens; const bf16* embed;
-  float* r; const bf16* gamma; float eps; bf16* y; uint32_t* err;
+  float* r; const bf16* gamma; float eps; float* y; uint32_t* err;
 };
 cudaError_t launch_embed_rmsnorm(const EmbedNormArgs& a, cudaStream_t s);
 
-// r <- r + sum_s delta[s]; y <- bf16(rmsnorm(r) * gamma)
+// r <- r + sum_s delta[s]; y <- rmsnorm(r) * gamma (fp32)
 struct AddNormArgs {
   int B, H; float* r; const float* delta; int n_delta; long long delta_stride;
-  const bf16* gamma; float eps; bf16* y;
+  const bf16* gamma; float eps; float* y;
 };
 cudaError_t launch_add_rmsnorm(const AddNormArgs& a, cudaStream_t s);
 
@@ -67,13 +80,19 @@ struct RopeKvArgs {
 };
 cudaError_t launch_rope_kv_write(const RopeKvArgs& a, cudaStream_t s);
 
-// Split-K paged decode attention + combine.
+// Split-K paged decode attention; the last CTA of each (row, KV head) merges
+// the splits (ticket counters in `tickets`, zero between launches).
 struct AttnArgs {
   int B; const float* q; int nq, nkv, d;
+  // Fused RoPE + KV write (when qkv != null, q is ignored): the queries are
+  // rotated from the QKV projection's split-K partials in the prologue, and the
+  // CTA whose split holds the new token's block first writes its K and V.
+  const float* qkv; int qkv_nsplit; long long qkv_split_stride; int ld_qkv;
+  const int* positions; const float2* rope; int max_pos;
   const void* kpool; const void* vpool; int kv_fp8; float k_scale, v_scale;
   const int* bt; int bt_stride; const int* seq_lens; int num_blocks;
   int bps; int nsplit;      // KV blocks per split, splits per (row, kv head)
-  float* part_o; float2* part_ml; bf16* out; uint32_t* err;
+  float* part_o; float2* part_ml; float* out; int* tickets; uint32_t* err;
 };
 void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nsplit);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);

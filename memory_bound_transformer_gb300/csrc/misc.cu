@@ -7,59 +7,132 @@
 namespace mbt {
 
 constexpr int kRowThreads = 256;
+constexpr int kNormMaxV = 8;        // float4 per thread: H <= 8 * 4 * 1024
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
 
 // RMSNorm ("Root Mean Square Layer Normalization", reference 9 of "Kernel
 // Fusion for Large-Scale LLM Inference"): y = r / sqrt(mean(r^2) + eps) * gamma,
-// computed in fp32 and rounded once to BF16 for the next projection.
-__device__ __forceinline__ void norm_row(const float* r, int H, const bf16* gamma, float eps,
-                                         bf16* y, float* scratch) {
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) { const float v = r[i]; ss = fmaf(v, v, ss); }
+// in fp32. One CTA per row; every thread keeps its slice of the row in
+// registers so the row is read once and written once.
+__device__ __forceinline__ void norm_store(const float4 (&v)[kNormMaxV], float ss, int H,
+                                          const bf16* __restrict__ gamma, float eps,
+                                          float* __restrict__ y, float* scratch) {
   const float tot = block_sum(ss, scratch);
   const float inv = 1.0f / sqrtf(tot / (float)H + eps);
-  for (int i = threadIdx.x; i < H; i += blockDim.x)
-    y[i] = __float2bfloat16_rn(r[i] * inv * __bfloat162float(gamma[i]));
+  const int nv = H / 4;
+  const uint2* g2 = reinterpret_cast<const uint2*>(gamma);
+  float4* y4 = reinterpret_cast<float4*>(y);
+#pragma unroll
+  for (int j = 0; j < kNormMaxV; ++j) {
+    const int i = threadIdx.x + j * blockDim.x;
+    if (i < nv) {
+      const uint2 g = g2[i];
+      float4 o;
+      o.x = v[j].x * inv * bf16_lo(g.x);
+      o.y = v[j].y * inv * bf16_hi(g.x);
+      o.z = v[j].z * inv * bf16_lo(g.y);
+      o.w = v[j].w * inv * bf16_hi(g.y);
+      y4[i] = o;
+    }
+  }
 }
 
-__global__ void __launch_bounds__(kRowThreads) embed_rmsnorm_kernel(const EmbedNormArgs a) {
+__global__ void __launch_bounds__(1024) embed_rmsnorm_kernel(const EmbedNormArgs a) {
   __shared__ float scratch[32];
   const int b = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
   int tok = a.tokens[b];
   if (tok < 0 || tok >= a.vocab) {
     if (threadIdx.x == 0) set_err(a.err, MBT_DEV_TOKEN_RANGE);
     tok = 0;
   }
-  const bf16* e = a.embed + (size_t)tok * a.H;
-  float* r = a.r + (size_t)b * a.H;
-  for (int i = threadIdx.x; i < a.H; i += blockDim.x) r[i] = __bfloat162float(e[i]);
-  __syncthreads();
-  norm_row(r, a.H, a.gamma, a.eps, a.y + (size_t)b * a.H, scratch);
+  const uint2* e = reinterpret_cast<const uint2*>(a.embed + (size_t)tok * a.H);
+  float4* r = reinterpret_cast<float4*>(a.r + (size_t)b * a.H);
+  const int nv = a.H / 4;
+  float4 v[kNormMaxV];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kNormMaxV; ++j) {
+    const int i = threadIdx.x + j * blockDim.x;
+    if (i < nv) {
+      const uint2 u = e[i];
+      v[j] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+      r[i] = v[j];
+      ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+    }
+  }
+  if (a.y) norm_store(v, ss, a.H, a.gamma, a.eps, a.y + (size_t)b * a.H, scratch);
 }
 
 // "Residual add + RMSNorm ... doing both in one pass" ("Kernels, Fusion & CUDA
 // Graphs", "Fix 1: kernel fusion"). The projection before it left its output
 // as split-K partial sums; they are added here too, in a fixed order.
-__global__ void __launch_bounds__(kRowThreads) add_rmsnorm_kernel(const AddNormArgs a) {
+__global__ void __launch_bounds__(1024) add_rmsnorm_kernel(const AddNormArgs a) {
   __shared__ float scratch[32];
   const int b = blockIdx.x;
-  float* r = a.r + (size_t)b * a.H;
-  for (int i = threadIdx.x; i < a.H; i += blockDim.x) {
-    float v = r[i];
-    for (int s = 0; s < a.n_delta; ++s) v += a.delta[(size_t)s * a.delta_stride + (size_t)b * a.H + i];
-    r[i] = v;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int nv = a.H / 4;
+  float4* __restrict__ r = reinterpret_cast<float4*>(a.r + (size_t)b * a.H);
+  const float4* __restrict__ d = reinterpret_cast<const float4*>(a.delta + (size_t)b * a.H);
+  const size_t ds = (size_t)a.delta_stride / 4;
+  float4 v[kNormMaxV];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kNormMaxV; ++j) {
+    const int i = threadIdx.x + j * blockDim.x;
+    if (i < nv) {
+      float4 x = r[i];
+      for (int s = 0; s < a.n_delta; ++s) {
+        const float4 t = d[s * ds + i];
+        x.x += t.x; x.y += t.y; x.z += t.z; x.w += t.w;
+      }
+      v[j] = x;
+      ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+    }
   }
-  __syncthreads();
-  norm_row(r, a.H, a.gamma, a.eps, a.y + (size_t)b * a.H, scratch);
+#pragma unroll
+  for (int j = 0; j < kNormMaxV; ++j) {
+    const int i = threadIdx.x + j * blockDim.x;
+    if (i < nv) r[i] = v[j];
+  }
+  norm_store(v, ss, a.H, a.gamma, a.eps, a.y + (size_t)b * a.H, scratch);
+}
+
+static int norm_threads(int H) {
+  int t = (H / 4 + kNormMaxV - 1) / kNormMaxV;
+  t = ((t + 31) / 32) * 32;
+  if (t < 128) t = 128;
+  if (t > 1024) t = 1024;
+  return t;
 }
 
 cudaError_t launch_embed_rmsnorm(const EmbedNormArgs& a, cudaStream_t s) {
-  embed_rmsnorm_kernel<<<a.B, kRowThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a.H % 4 || a.H > 4 * kNormMaxV * 1024) return cudaErrorInvalidValue;
+  EmbedNormArgs args = a;
+  void* p[] = {&args};
+  return launch_pdl((const void*)embed_rmsnorm_kernel, dim3(a.B), dim3(norm_threads(a.H)), 0, s, p);
 }
 
 cudaError_t launch_add_rmsnorm(const AddNormArgs& a, cudaStream_t s) {
-  add_rmsnorm_kernel<<<a.B, kRowThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a.H % 4 || a.H > 4 * kNormMaxV * 1024) return cudaErrorInvalidValue;
+  AddNormArgs args = a;
+  void* p[] = {&args};
+  return launch_pdl((const void*)add_rmsnorm_kernel, dim3(a.B), dim3(norm_threads(a.H)), 0, s, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -74,13 +147,16 @@ __device__ __forceinline__ void store_kv(void* pool, size_t idx, float v, int fp
   else reinterpret_cast<uint16_t*>(pool)[idx] = f32_to_bf16_bits(v);
 }
 
-__global__ void __launch_bounds__(kRowThreads) rope_kv_write_kernel(const RopeKvArgs a) {
-  const int b = blockIdx.x;
+constexpr int kRopeHeads = 4;      // heads per CTA (q, k or v heads)
+
+__global__ void __launch_bounds__(128) rope_kv_write_kernel(const RopeKvArgs a) {
+  const int b = blockIdx.y;
   const int half = a.d / 2;
+  const int nh = a.nq + 2 * a.nkv;
   int pos = a.positions[b];
   bool write = true;
   if (pos < 0 || pos >= a.max_pos) {
-    if (threadIdx.x == 0) set_err(a.err, MBT_DEV_POS_RANGE);
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_err(a.err, MBT_DEV_POS_RANGE);
     pos = 0;
     write = false;
   }
@@ -89,49 +165,49 @@ __global__ void __launch_bounds__(kRowThreads) rope_kv_write_kernel(const RopeKv
   if (write) {
     blk = jb < a.bt_stride ? a.bt[(size_t)b * a.bt_stride + jb] : -1;
     if (blk < 0 || blk > a.num_blocks) {
-      if (threadIdx.x == 0) set_err(a.err, MBT_DEV_BLOCK_RANGE);
+      if (threadIdx.x == 0 && blockIdx.x == 0) set_err(a.err, MBT_DEV_BLOCK_RANGE);
       write = false;
     }
   }
-  const float* src = a.qkv + (size_t)b * a.ld_qkv;
-  const float2* cs = a.rope + (size_t)pos * half;
-  const int n_rot = (a.nq + a.nkv) * half;
-  for (int e = threadIdx.x; e < n_rot; e += blockDim.x) {
-    const int hh = e / half, i = e - hh * half;
-    const int col = hh * a.d + i;
-    float x1 = 0.f, x2 = 0.f;
-    for (int s = 0; s < a.nsplit; ++s) {
-      x1 += src[(size_t)s * a.split_stride + col];
-      x2 += src[(size_t)s * a.split_stride + col + half];
-    }
-    const float2 t = cs[i];
-    const float y1 = x1 * t.x - x2 * t.y;
-    const float y2 = x2 * t.x + x1 * t.y;
-    if (hh < a.nq) {
-      float* q = a.q_out + ((size_t)b * a.nq + hh) * a.d;
-      q[i] = y1;
-      q[i + half] = y2;
-    } else if (write) {
-      const int kvh = hh - a.nq;
+  const float* __restrict__ src = a.qkv + (size_t)b * a.ld_qkv;
+  const float2* __restrict__ cs = a.rope + (size_t)pos * half;
+  const int h0 = blockIdx.x * kRopeHeads;
+  for (int e = threadIdx.x; e < kRopeHeads * a.d; e += blockDim.x) {
+    const int hh = h0 + e / a.d, i = e % a.d;
+    if (hh >= nh) continue;
+    if (hh < a.nq + a.nkv) {                       // q or k head: rotate pair (i, i + d/2)
+      if (i >= half) continue;
+      const int col = hh * a.d + i;
+      float x1 = 0.f, x2 = 0.f;
+      for (int s = 0; s < a.nsplit; ++s) {
+        x1 += src[(size_t)s * a.split_stride + col];
+        x2 += src[(size_t)s * a.split_stride + col + half];
+      }
+      const float2 t = cs[i];
+      const float y1 = x1 * t.x - x2 * t.y;
+      const float y2 = x2 * t.x + x1 * t.y;
+      if (hh < a.nq) {
+        float* q = a.q_out + ((size_t)b * a.nq + hh) * a.d;
+        q[i] = y1;
+        q[i + half] = y2;
+      } else if (write) {
+        const size_t base = (((size_t)blk * a.nkv + (hh - a.nq)) * kBlockTokens + slot) * a.d;
+        store_kv(a.kpool, base + i, __fdiv_rn(y1, a.k_scale), a.kv_fp8);
+        store_kv(a.kpool, base + i + half, __fdiv_rn(y2, a.k_scale), a.kv_fp8);
+      }
+    } else if (write) {                            // v head: copy
+      const int kvh = hh - a.nq - a.nkv;
+      float v = 0.f;
+      for (int s = 0; s < a.nsplit; ++s) v += src[(size_t)s * a.split_stride + hh * a.d + i];
       const size_t base = (((size_t)blk * a.nkv + kvh) * kBlockTokens + slot) * a.d;
-      store_kv(a.kpool, base + i, __fdiv_rn(y1, a.k_scale), a.kv_fp8);
-      store_kv(a.kpool, base + i + half, __fdiv_rn(y2, a.k_scale), a.kv_fp8);
+      store_kv(a.vpool, base + i, __fdiv_rn(v, a.v_scale), a.kv_fp8);
     }
-  }
-  if (!write) return;
-  const int n_v = a.nkv * a.d;
-  const int vcol0 = (a.nq + a.nkv) * a.d;
-  for (int e = threadIdx.x; e < n_v; e += blockDim.x) {
-    const int kvh = e / a.d, i = e - kvh * a.d;
-    float v = 0.f;
-    for (int s = 0; s < a.nsplit; ++s) v += src[(size_t)s * a.split_stride + vcol0 + e];
-    const size_t base = (((size_t)blk * a.nkv + kvh) * kBlockTokens + slot) * a.d;
-    store_kv(a.vpool, base + i, __fdiv_rn(v, a.v_scale), a.kv_fp8);
   }
 }
 
 cudaError_t launch_rope_kv_write(const RopeKvArgs& a, cudaStream_t s) {
-  rope_kv_write_kernel<<<a.B, kRowThreads, 0, s>>>(a);
+  const int nh = a.nq + 2 * a.nkv;
+  rope_kv_write_kernel<<<dim3((nh + kRopeHeads - 1) / kRopeHeads, a.B), 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -148,6 +224,8 @@ __global__ void __launch_bounds__(kRowThreads) argmax_reduce_kernel(
   __shared__ float sv[32];
   __shared__ int si[32];
   const int b = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
@@ -180,8 +258,8 @@ __global__ void __launch_bounds__(kRowThreads) argmax_reduce_kernel(
 cudaError_t launch_argmax_reduce(int B, const ArgmaxPart* part, int part_ld, int G,
                                  int* next_ids, uint32_t* err, cudaStream_t s) {
   (void)err;
-  argmax_reduce_kernel<<<B, kRowThreads, 0, s>>>(part, part_ld, G, next_ids);
-  return cudaGetLastError();
+  void* p[] = {&part, &part_ld, &G, &next_ids};
+  return launch_pdl((const void*)argmax_reduce_kernel, dim3(B), dim3(kRowThreads), 0, s, p);
 }
 
 // ---------------------------------------------------------------------------

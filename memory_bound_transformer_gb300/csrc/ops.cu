@@ -29,17 +29,17 @@ int init_once() {
 extern "C" {
 
 int op_embed_rmsnorm(int B, int H, int vocab, const int32_t* tokens, const uint16_t* embed,
-                     const uint16_t* gamma, float eps, float* r, uint16_t* y, uint32_t* err,
+                     const uint16_t* gamma, float eps, float* r, float* y, uint32_t* err,
                      void* stream) {
-  if (B < 1 || H < 1 || vocab < 1 || !tokens || !embed || !gamma || !r || !y) return MBT_ERR_BAD_ARG;
-  EmbedNormArgs a{B, H, vocab, tokens, (const bf16*)embed, r, (const bf16*)gamma, eps, (bf16*)y, err};
+  if (B < 1 || H < 4 || H % 4 || vocab < 1 || !tokens || !embed || !gamma || !r || !y) return MBT_ERR_BAD_ARG;
+  EmbedNormArgs a{B, H, vocab, tokens, (const bf16*)embed, r, (const bf16*)gamma, eps, y, err};
   return launch_embed_rmsnorm(a, (cudaStream_t)stream) == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
 }
 
 int op_add_rmsnorm(int B, int H, float* r, const float* delta, int n_delta,
-                   const uint16_t* gamma, float eps, uint16_t* y, void* stream) {
-  if (B < 1 || H < 1 || !r || !gamma || !y || n_delta < 0 || (n_delta && !delta)) return MBT_ERR_BAD_ARG;
-  AddNormArgs a{B, H, r, delta, n_delta, (long long)B * H, (const bf16*)gamma, eps, (bf16*)y};
+                   const uint16_t* gamma, float eps, float* y, void* stream) {
+  if (B < 1 || H < 4 || H % 4 || !r || !gamma || !y || n_delta < 0 || (n_delta && !delta)) return MBT_ERR_BAD_ARG;
+  AddNormArgs a{B, H, r, delta, n_delta, (long long)B * H, (const bf16*)gamma, eps, y};
   return launch_add_rmsnorm(a, (cudaStream_t)stream) == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
 }
 
@@ -50,7 +50,7 @@ int op_gemv_nsplit(int epi, int w_dtype, int B, int N, int K) {
 }
 
 int op_gemv(int epi, int w_dtype, const void* W, const float* scales, int N, int K,
-            const uint16_t* x, int B, int force_nsplit, float* out, uint16_t* act,
+            const float* x, int B, int force_nsplit, float* out, float* act,
             float* logits, int32_t* next_ids, int* nsplit_used, uint32_t* err, void* stream) {
   if (epi < 0 || epi > 2 || (w_dtype != MBT_DTYPE_BF16 && w_dtype != MBT_DTYPE_E4M3)) return MBT_ERR_BAD_ARG;
   if (!W || !x || B < 1 || N < 1 || K < 16 || K % 16) return MBT_ERR_BAD_ARG;
@@ -62,25 +62,27 @@ int op_gemv(int epi, int w_dtype, const void* W, const float* scales, int N, int
   const int nsm = sm_count();
   const int wt = w_dtype == MBT_DTYPE_E4M3 ? W_E4M3 : W_BF16;
   cudaStream_t s = (cudaStream_t)stream;
-  const GemvLaunch g0 = gemv_plan(epi, wt, std::min(B, 8), N, K, nsm, epi == EPI_PARTIAL ? force_nsplit : 0);
+  const GemvLaunch g0 = gemv_plan(epi, wt, std::min(B, gemv_max_rows(epi, K)), N, K, nsm,
+                                  epi == EPI_PARTIAL ? force_nsplit : 0);
   if (nsplit_used) *nsplit_used = g0.nsplit;
   ArgmaxPart* part = nullptr;
   if (epi == EPI_ARGMAX &&
       cudaMallocAsync((void**)&part, (size_t)g0.grid * B * sizeof(ArgmaxPart), s) != cudaSuccess)
     return MBT_ERR_OOM;
-  for (int b0 = 0; b0 < B && rc == MBT_OK; b0 += 8) {
-    const int nb = std::min(8, B - b0);
+  const int step = gemv_max_rows(epi, K);
+  for (int b0 = 0; b0 < B && rc == MBT_OK; b0 += step) {
+    const int nb = std::min(step, B - b0);
     GemvLaunch g = gemv_plan(epi, wt, nb, N, K, nsm, epi == EPI_PARTIAL ? g0.nsplit : 0);
     if (epi == EPI_ARGMAX) g.grid = g0.grid;
     GemvArgs a = {};
     a.W = W; a.scale = scales; a.wtype = wt; a.N = N; a.K = K;
-    a.x = (const bf16*)x + (size_t)b0 * K; a.ldx = K; a.nb = nb;
+    a.x = x + (size_t)b0 * K; a.ldx = K; a.nb = nb;
     a.out = out ? out + (size_t)b0 * N : nullptr; a.split_stride = (long long)B * N; a.ldo = N;
-    a.act = act ? (bf16*)act + (size_t)b0 * N : nullptr; a.lda = N;
+    a.act = act ? act + (size_t)b0 * N : nullptr; a.lda = N;
     a.logits = logits ? logits + (size_t)b0 * N : nullptr; a.ldl = N;
     a.part = part ? part + b0 : nullptr; a.part_ld = B;
     a.err = err;
-    if (gemv_launch(epi, a, g, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+    if (gemv_launch(epi, PRO_X, a, g, s) != cudaSuccess) rc = MBT_ERR_CUDA;
   }
   if (rc == MBT_OK && epi == EPI_ARGMAX &&
       launch_argmax_reduce(B, part, B, g0.grid, next_ids, err, s) != cudaSuccess)
@@ -110,7 +112,7 @@ int op_rope_kv_write(int B, const float* qkv, int nq, int nkv, int d, const int3
   int rc = MBT_OK;
   if (cudaMemcpyAsync(rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice, s) != cudaSuccess)
     rc = MBT_ERR_CUDA;
-  RopeKvArgs a;
+  RopeKvArgs a = {};
   a.B = B; a.qkv = qkv; a.nsplit = 1; a.split_stride = 0; a.ld_qkv = (nq + 2 * nkv) * d;
   a.nq = nq; a.nkv = nkv; a.d = d; a.positions = positions; a.bt = bt; a.bt_stride = bt_stride;
   a.max_pos = max_pos; a.rope = rope; a.q_out = q_out; a.kpool = kpool; a.vpool = vpool;
@@ -127,7 +129,7 @@ int op_rope_kv_write(int B, const float* qkv, int nq, int nkv, int d, const int3
 int op_paged_attention(int B, const float* q, int nq, int nkv, int d, const void* kpool,
                        const void* vpool, int kv_dtype, float k_scale, float v_scale,
                        const int32_t* bt, int bt_stride, const int32_t* seq_lens, int num_blocks,
-                       uint16_t* out, uint32_t* err, void* stream) {
+                       float* out, uint32_t* err, void* stream) {
   if (B < 1 || !q || nq < 1 || nkv < 1 || nq % nkv || nq / nkv > 16 || (d != 64 && d != 128) ||
       !kpool || !vpool || !bt || bt_stride < 1 || !seq_lens || num_blocks < 1 || !out ||
       (kv_dtype != MBT_DTYPE_BF16 && kv_dtype != MBT_DTYPE_E4M3))
@@ -135,21 +137,24 @@ int op_paged_attention(int B, const float* q, int nq, int nkv, int d, const void
   int rc = init_once();
   if (rc != MBT_OK) return rc;
   cudaStream_t s = (cudaStream_t)stream;
-  AttnArgs a;
+  AttnArgs a = {};
   a.B = B; a.q = q; a.nq = nq; a.nkv = nkv; a.d = d; a.kpool = kpool; a.vpool = vpool;
   a.kv_fp8 = kv_dtype == MBT_DTYPE_E4M3; a.k_scale = k_scale; a.v_scale = v_scale;
   a.bt = bt; a.bt_stride = bt_stride; a.seq_lens = seq_lens; a.num_blocks = num_blocks;
   attn_plan(B, nkv, bt_stride, sm_count(), &a.bps, &a.nsplit);
-  a.out = (bf16*)out; a.err = err;
+  a.out = out; a.err = err;
   const size_t heads = (size_t)B * nq * a.nsplit;
-  if (cudaMallocAsync((void**)&a.part_o, heads * d * sizeof(float), s) != cudaSuccess) return MBT_ERR_OOM;
-  if (cudaMallocAsync((void**)&a.part_ml, heads * sizeof(float2), s) != cudaSuccess) {
-    cudaFreeAsync(a.part_o, s);
-    return MBT_ERR_OOM;
-  }
-  if (launch_attention(a, s) != cudaSuccess) rc = MBT_ERR_CUDA;
-  cudaFreeAsync(a.part_o, s);
-  cudaFreeAsync(a.part_ml, s);
+  // scratch: partial outputs, (max, sum) pairs, zeroed tickets
+  const size_t b_po = heads * d * sizeof(float), b_ml = heads * sizeof(float2);
+  const size_t b_tk = (size_t)B * nkv * sizeof(int);
+  char* scratch = nullptr;
+  if (cudaMallocAsync((void**)&scratch, b_po + b_ml + b_tk, s) != cudaSuccess) return MBT_ERR_OOM;
+  a.part_o = (float*)scratch;
+  a.part_ml = (float2*)(scratch + b_po);
+  a.tickets = (int*)(scratch + b_po + b_ml);
+  if (cudaMemsetAsync(a.tickets, 0, b_tk, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  if (rc == MBT_OK && launch_attention(a, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  cudaFreeAsync(scratch, s);
   return rc;
 }
 

@@ -43,9 +43,12 @@ struct Workspace {
   size_t part_o_elems = 0, part_ml_elems = 0;
   int ns_qkv_cap = 0, ns_delta_cap = 0, g_lm_cap = 0;
   void* mem = nullptr;
-  float* r = nullptr; bf16* y = nullptr; float* qkv = nullptr; float* q = nullptr;
-  float* part_o = nullptr; float2* part_ml = nullptr; bf16* o = nullptr;
-  float* delta = nullptr; bf16* act = nullptr; ArgmaxPart* lm_part = nullptr;
+  float* r = nullptr; float* r2 = nullptr;           // residual ping-pong [cap][H]
+  float* qkv = nullptr;                              // QKV partials [splits][cap][QKV]
+  float* part_o = nullptr; float2* part_ml = nullptr; float* o = nullptr;
+  float* delta = nullptr; float* delta2 = nullptr;   // O and down partials [splits][cap][H]
+  float* act = nullptr; ArgmaxPart* lm_part = nullptr;
+  int* tickets = nullptr;
 };
 
 struct Graph {
@@ -109,13 +112,14 @@ Plan make_plan(const mbt_model* m, int R, int mbs) {
   attn_plan(R, (int)m->h.n_kv_heads, mbs, m->num_sms, &p.attn_bps, &p.attn_nsplit);
   const int nb0 = std::min(R, 8);
   const int H = (int)m->h.hidden, Q = (int)(m->h.n_q_heads * m->h.head_dim), F = (int)m->h.ffn;
-  const int QKV = (int)((m->h.n_q_heads + 2 * m->h.n_kv_heads) * m->h.head_dim);
-  p.ns_qkv = gemv_plan(EPI_PARTIAL, m->wtype, nb0, QKV, H, m->num_sms, 0).nsplit;
+  p.ns_qkv = 1;                                          // norm prologue: whole rows per CTA
   p.ns_o = gemv_plan(EPI_PARTIAL, m->wtype, nb0, H, Q, m->num_sms, 0).nsplit;
   p.ns_down = gemv_plan(EPI_PARTIAL, m->wtype, nb0, H, F, m->num_sms, 0).nsplit;
-  p.g_lm = gemv_plan(EPI_ARGMAX, m->wtype, nb0, (int)m->h.vocab, H, m->num_sms, 0).grid;
-  const int chunks = (R + 7) / 8;
-  p.kernels = 1 + (int)m->h.n_layers * (4 * chunks + 5) + chunks + 1;
+  const int mn = gemv_max_rows(EPI_ARGMAX, H, PRO_NORM);
+  p.g_lm = gemv_plan(EPI_ARGMAX, m->wtype, std::min(nb0, mn), (int)m->h.vocab, H, m->num_sms, 0, PRO_NORM).grid;
+  const int c8 = (R + 7) / 8;
+  const int cn = (R + mn - 1) / mn;                      // chunks of the norm-prologue projections
+  p.kernels = 1 + (int)m->h.n_layers * (2 * cn + 2 * c8 + 1) + cn + 1;
   return p;
 }
 
@@ -156,49 +160,76 @@ int ensure_ws(mbt_model* m, int R, int mbs) {
   const size_t QKV = (size_t)(m->h.n_q_heads + 2 * m->h.n_kv_heads) * m->h.head_dim;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off += align256(bytes); return o; };
-  const size_t o_r = take((size_t)cap * H * 4), o_y = take((size_t)cap * H * 2);
-  const size_t o_qkv = take((size_t)ns_qkv * cap * QKV * 4), o_q = take((size_t)cap * Q * 4);
-  const size_t o_po = take(po * 4), o_pml = take(pml * 8), o_o = take((size_t)cap * Q * 2);
-  const size_t o_d = take((size_t)ns_delta * cap * H * 4), o_a = take((size_t)cap * F * 2);
+  const size_t o_r = take((size_t)cap * H * 4), o_r2 = take((size_t)cap * H * 4);
+  const size_t o_qkv = take((size_t)ns_qkv * cap * QKV * 4);
+  const size_t o_po = take(po * 4), o_pml = take(pml * 8), o_o = take((size_t)cap * Q * 4);
+  const size_t o_d = take((size_t)ns_delta * cap * H * 4), o_d2 = take((size_t)ns_delta * cap * H * 4);
+  const size_t o_a = take((size_t)cap * F * 4);
   const size_t o_lp = take((size_t)g_lm * cap * sizeof(ArgmaxPart));
+  const size_t o_tk = take((size_t)cap * m->h.n_kv_heads * 4);
   void* mem = nullptr;
   if (cudaMalloc(&mem, off) != cudaSuccess) { cudaGetLastError(); return MBT_ERR_OOM; }
   char* base = (char*)mem;
   w.mem = mem; w.cap = cap; w.mbs_cap = mbs_cap;
   w.part_o_elems = po; w.part_ml_elems = pml;
   w.ns_qkv_cap = ns_qkv; w.ns_delta_cap = ns_delta; w.g_lm_cap = g_lm;
-  w.r = (float*)(base + o_r); w.y = (bf16*)(base + o_y); w.qkv = (float*)(base + o_qkv);
-  w.q = (float*)(base + o_q); w.part_o = (float*)(base + o_po); w.part_ml = (float2*)(base + o_pml);
-  w.o = (bf16*)(base + o_o); w.delta = (float*)(base + o_d); w.act = (bf16*)(base + o_a);
+  w.r = (float*)(base + o_r); w.r2 = (float*)(base + o_r2); w.qkv = (float*)(base + o_qkv);
+  w.part_o = (float*)(base + o_po); w.part_ml = (float2*)(base + o_pml);
+  w.o = (float*)(base + o_o); w.delta = (float*)(base + o_d); w.delta2 = (float*)(base + o_d2);
+  w.act = (float*)(base + o_a);
   w.lm_part = (ArgmaxPart*)(base + o_lp);
+  w.tickets = (int*)(base + o_tk);
+  // attention tickets start at zero; every launch leaves them at zero
+  if (cudaMemset(w.tickets, 0, (size_t)cap * m->h.n_kv_heads * 4) != cudaSuccess) return MBT_ERR_CUDA;
   return MBT_OK;
 }
 
-// One GEMV over R rows, issued in chunks of at most 8 rows.
-cudaError_t gemv_rows(const mbt_model* m, int epi, const void* W, const float* sc, int N, int K,
-                      const bf16* x, int R, int nsplit, int grid_fixed, float* out,
-                      long long split_stride, int ldo, bf16* act, int lda, float* logits,
+// Inputs of a norm-prologue projection: x = rmsnorm(r_in + sum of n_delta
+// partials) * gamma, new residual to r_out.
+struct NormIn {
+  const float* r_in; const float* delta; int n_delta; const bf16* gamma; float* r_out;
+};
+
+// One GEMV over R rows, issued in chunks of at most 8 rows (fewer when the
+// fp32 x tile of an unsplittable launch would not fit in shared memory).
+cudaError_t gemv_rows(const mbt_model* m, int epi, const NormIn* nin, const void* W, const float* sc,
+                      int N, int K, const float* x, int R, int nsplit, int grid_fixed, float* out,
+                      long long split_stride, int ldo, float* act, int lda, float* logits,
                       ArgmaxPart* part, int part_ld, cudaStream_t s) {
-  for (int b0 = 0; b0 < R; b0 += 8) {
-    const int nb = std::min(8, R - b0);
-    GemvLaunch g = gemv_plan(epi, m->wtype, nb, N, K, m->num_sms, epi == EPI_PARTIAL ? nsplit : 0);
+  const int pro = nin ? PRO_NORM : PRO_X;
+  const int step = gemv_max_rows(epi, K, pro);
+  for (int b0 = 0; b0 < R; b0 += step) {
+    const int nb = std::min(step, R - b0);
+    GemvLaunch g = gemv_plan(epi, m->wtype, nb, N, K, m->num_sms, epi == EPI_PARTIAL ? nsplit : 0, pro);
     if (grid_fixed > 0) g.grid = grid_fixed;
     GemvArgs a;
     memset(&a, 0, sizeof(a));
     a.W = W; a.scale = sc; a.wtype = m->wtype; a.N = N; a.K = K;
-    a.x = x + (size_t)b0 * K; a.ldx = K; a.nb = nb;
+    a.x = x ? x + (size_t)b0 * K : nullptr; a.ldx = K; a.nb = nb;
+    if (nin) {
+      a.r_in = nin->r_in + (size_t)b0 * K;
+      a.delta = nin->delta ? nin->delta + (size_t)b0 * K : nullptr;
+      a.n_delta = nin->n_delta; a.delta_stride = (long long)R * K;
+      a.gamma = nin->gamma; a.eps = m->h.eps;
+      a.r_out = nin->r_out + (size_t)b0 * K;
+    }
     a.out = out ? out + (size_t)b0 * ldo : nullptr; a.split_stride = split_stride; a.ldo = ldo;
     a.act = act ? act + (size_t)b0 * lda : nullptr; a.lda = lda;
     a.logits = logits ? logits + (size_t)b0 * m->h.vocab : nullptr; a.ldl = (int)m->h.vocab;
     a.part = part ? part + b0 : nullptr; a.part_ld = part_ld;
     a.err = m->err;
-    cudaError_t e = gemv_launch(epi, a, g, s);
+    cudaError_t e = gemv_launch(epi, pro, a, g, s);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
 // The decode step over R rows whose inputs are already in device memory.
+// Per layer: QKV projection with the RMSNorm prologue, attention with RoPE +
+// KV write fused in, O projection, gate/up projection with the RMSNorm
+// prologue and SwiGLU epilogue, down projection. The residual lives in two
+// fp32 buffers (read one, write the other); projections with residual
+// outputs leave split-K partials that the next norm prologue adds.
 int run_step(mbt_model* m, mbt_kv* kv, const Plan& p, const int* tok, const int* pos,
              const int* bt, int bt_stride, const int* sl, int* next_ids, float* logits,
              cudaStream_t s) {
@@ -209,49 +240,43 @@ int run_step(mbt_model* m, mbt_kv* kv, const Plan& p, const int* tok, const int*
   const int Q = nq * d, F = (int)m->h.ffn, V = (int)m->h.vocab;
   const int QKV = (nq + 2 * nkv) * d;
   const size_t half = kv_layer_half_bytes(m, kv->num_blocks);
+  const long long rh = (long long)R * H;
 
-  EmbedNormArgs en{R, H, V, tok, m->embed, w.r, m->layers[0].g_attn, m->h.eps, w.y, m->err};
+  EmbedNormArgs en{R, H, V, tok, m->embed, w.r, m->layers[0].g_attn, m->h.eps, nullptr, m->err};
   MBT_CUDA(launch_embed_rmsnorm(en, s));
   for (int l = 0; l < (int)m->h.n_layers; ++l) {
     const Layer& L = m->layers[l];
     char* kbase = (char*)kv->pool + 2 * half * (size_t)l;
-    // fused QKV projection
-    MBT_CUDA(gemv_rows(m, EPI_PARTIAL, L.w_qkv, L.s_qkv, QKV, H, w.y, R, p.ns_qkv, 0, w.qkv,
+    // RMSNorm prologue + fused QKV projection
+    NormIn n1{w.r, l ? w.delta2 : nullptr, l ? p.ns_down : 0, L.g_attn, w.r2};
+    MBT_CUDA(gemv_rows(m, EPI_PARTIAL, &n1, L.w_qkv, L.s_qkv, QKV, H, nullptr, R, 1, 0, w.qkv,
                        (long long)R * QKV, QKV, nullptr, 0, nullptr, nullptr, 0, s));
-    // RoPE + paged KV write
-    RopeKvArgs rk;
-    rk.B = R; rk.qkv = w.qkv; rk.nsplit = p.ns_qkv; rk.split_stride = (long long)R * QKV; rk.ld_qkv = QKV;
-    rk.nq = nq; rk.nkv = nkv; rk.d = d; rk.positions = pos; rk.bt = bt; rk.bt_stride = bt_stride;
-    rk.max_pos = (int)m->h.max_pos; rk.rope = m->rope; rk.q_out = w.q;
-    rk.kpool = kbase; rk.vpool = kbase + half; rk.num_blocks = kv->num_blocks;
-    rk.kv_fp8 = m->kv8; rk.k_scale = kv->k_scale[l]; rk.v_scale = kv->v_scale[l]; rk.err = m->err;
-    MBT_CUDA(launch_rope_kv_write(rk, s));
-    // paged attention
-    AttnArgs at;
-    at.B = R; at.q = w.q; at.nq = nq; at.nkv = nkv; at.d = d;
+    // RoPE + paged KV write + split-K attention + merge
+    AttnArgs at = {};
+    at.B = R; at.q = nullptr; at.nq = nq; at.nkv = nkv; at.d = d;
+    at.qkv = w.qkv; at.qkv_nsplit = 1; at.qkv_split_stride = (long long)R * QKV; at.ld_qkv = QKV;
+    at.positions = pos; at.rope = m->rope; at.max_pos = (int)m->h.max_pos;
     at.kpool = kbase; at.vpool = kbase + half; at.kv_fp8 = m->kv8;
     at.k_scale = kv->k_scale[l]; at.v_scale = kv->v_scale[l];
     at.bt = bt; at.bt_stride = bt_stride; at.seq_lens = sl; at.num_blocks = kv->num_blocks;
     at.bps = p.attn_bps; at.nsplit = p.attn_nsplit;
-    at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = w.o; at.err = m->err;
+    at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = w.o; at.tickets = w.tickets; at.err = m->err;
     MBT_CUDA(launch_attention(at, s));
-    // O projection (partials), then residual add + RMSNorm
-    MBT_CUDA(gemv_rows(m, EPI_PARTIAL, L.w_o, L.s_o, H, Q, w.o, R, p.ns_o, 0, w.delta,
-                       (long long)R * H, H, nullptr, 0, nullptr, nullptr, 0, s));
-    AddNormArgs an{R, H, w.r, w.delta, p.ns_o, (long long)R * H, L.g_ffn, m->h.eps, w.y};
-    MBT_CUDA(launch_add_rmsnorm(an, s));
-    // gate + up with the SwiGLU epilogue
-    MBT_CUDA(gemv_rows(m, EPI_SWIGLU, L.w_gu, L.s_gu, F, H, w.y, R, 1, 0, nullptr, 0, 0,
+    // O projection (residual partials)
+    MBT_CUDA(gemv_rows(m, EPI_PARTIAL, nullptr, L.w_o, L.s_o, H, Q, w.o, R, p.ns_o, 0, w.delta,
+                       rh, H, nullptr, 0, nullptr, nullptr, 0, s));
+    // RMSNorm prologue + gate/up projection + SwiGLU epilogue
+    NormIn n2{w.r2, w.delta, p.ns_o, L.g_ffn, w.r};
+    MBT_CUDA(gemv_rows(m, EPI_SWIGLU, &n2, L.w_gu, L.s_gu, F, H, nullptr, R, 1, 0, nullptr, 0, 0,
                        w.act, F, nullptr, nullptr, 0, s));
-    // down projection, then residual add + the next norm
-    MBT_CUDA(gemv_rows(m, EPI_PARTIAL, L.w_down, L.s_down, H, F, w.act, R, p.ns_down, 0, w.delta,
-                       (long long)R * H, H, nullptr, 0, nullptr, nullptr, 0, s));
-    const bf16* gnext = l + 1 < (int)m->h.n_layers ? m->layers[l + 1].g_attn : m->g_final;
-    AddNormArgs an2{R, H, w.r, w.delta, p.ns_down, (long long)R * H, gnext, m->h.eps, w.y};
-    MBT_CUDA(launch_add_rmsnorm(an2, s));
+    // down projection (residual partials)
+    MBT_CUDA(gemv_rows(m, EPI_PARTIAL, nullptr, L.w_down, L.s_down, H, F, w.act, R, p.ns_down, 0,
+                       w.delta2, rh, H, nullptr, 0, nullptr, nullptr, 0, s));
   }
-  // LM head with the arg-max epilogue, then the cross-CTA reduction
-  MBT_CUDA(gemv_rows(m, EPI_ARGMAX, m->lm, m->s_lm, V, H, w.y, R, 1, p.g_lm, nullptr, 0, 0,
+  // final RMSNorm prologue + LM head with the arg-max epilogue, then the
+  // cross-CTA reduction
+  NormIn nf{w.r, w.delta2, p.ns_down, m->g_final, w.r2};
+  MBT_CUDA(gemv_rows(m, EPI_ARGMAX, &nf, m->lm, m->s_lm, V, H, nullptr, R, 1, p.g_lm, nullptr, 0, 0,
                      nullptr, 0, logits, w.lm_part, R, s));
   MBT_CUDA(launch_argmax_reduce(R, w.lm_part, R, p.g_lm, next_ids, m->err, s));
   return MBT_OK;

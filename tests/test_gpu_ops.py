@@ -1,11 +1,13 @@
 """Per-kernel parity through the C ABI (include/mbt_ops.h) against the oracle.
 
+Activations are fp32 on both sides of every kernel (only weights and the KV
+cache have narrow formats), so the oracle receives exactly the GPU's inputs.
 Tolerances (derived from the arithmetic, written per test):
 * fp32 dot products of length K: |gpu - exact| <= 2e-5 * sum_k |w_k x_k| + 1e-7
   (K <= 28672 products accumulated in fp32 by 256 threads and a tree, each
   partial sum with relative error ~K_partial * 2^-24; 2e-5 is ~3x that bound).
-* a value rounded once to BF16 after fp32 math: relative 2^-8 (half an ulp is
-  2^-9; the fp32 error before rounding can move it by at most one more ulp).
+* RMSNorm in fp32: relative 1e-5 (sum of squares over <= 42 rounding steps,
+  then three multiplications).
 * bit-exact where both sides round the same exact value once (V writes,
   K writes at position 0, arg-max decided on the GPU's own logits)."""
 import numpy as np
@@ -26,6 +28,11 @@ TOL_REL, TOL_ABS = 2e-5, 1e-7
 def _bf16_rand(shape, seed, scale=1.0):
     g = torch.Generator(device="cpu").manual_seed(seed)
     return (torch.randn(shape, generator=g) * scale).to(torch.bfloat16)
+
+
+def _f32_rand(shape, seed, scale=1.0):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    return torch.randn(shape, generator=g) * scale
 
 
 def _np_bits(t):
@@ -57,7 +64,7 @@ def _dtype(wt):
 @pytest.mark.parametrize("N,K", [(1000, 1040), (64, 16), (4099, 2048)])
 def test_gemv_partial(cuda_lib, wt, B, N, K):
     t, raw = _weights(wt, N, K, seed=N + K + B)
-    x = _bf16_rand((B, K), seed=B).to(DEV)
+    x = _f32_rand((B, K), seed=B).to(DEV)
     ns = capi.op_gemv_nsplit(capi.EPI_PARTIAL, _dtype(wt), B, N, K)
     for force in (0, 3):
         out = torch.full((max(force, ns), B, N), float("nan"), device=DEV)
@@ -67,7 +74,7 @@ def test_gemv_partial(cuda_lib, wt, B, N, K):
         assert used == (min(force, K // (8 if wt == "bf16" else 16)) if force else ns)
         got = out[:used].sum(0).double().cpu().numpy()
         W = decode_weight(raw)
-        xv = bf16_decode(_np_bits(x.cpu()))
+        xv = x.double().cpu().numpy()
         ref = xv @ W.T
         bound = TOL_REL * (np.abs(xv) @ np.abs(W).T) + TOL_ABS
         assert np.all(np.abs(got - ref) <= bound)
@@ -78,18 +85,18 @@ def test_gemv_partial(cuda_lib, wt, B, N, K):
 def test_gemv_swiglu(cuda_lib, wt, B):
     F, K = 688, 256
     t, raw = _weights(wt, 2 * F, K, seed=7 + B)
-    x = _bf16_rand((B, K), seed=3 + B, scale=3.0).to(DEV)
-    act = torch.zeros((B, F), dtype=torch.bfloat16, device=DEV)
+    x = _f32_rand((B, K), seed=3 + B, scale=3.0).to(DEV)
+    act = torch.zeros((B, F), device=DEV)
     capi.op_gemv(capi.EPI_SWIGLU, _dtype(wt), t["w"], t.get("s"), F, K, x, B, act=act)
     W = decode_weight(raw)
-    xv = bf16_decode(_np_bits(x.cpu()))
+    xv = x.double().cpu().numpy()
     gu = xv @ W.T
     bound_gu = TOL_REL * (np.abs(xv) @ np.abs(W).T) + TOL_ABS
     g, u = gu[:, :F], gu[:, F:]
     ref = silu(g) * u
-    got = bf16_decode(_np_bits(act.cpu()))
-    # fp32 error of g and u propagated (|silu'| <= 1.1), then one BF16 rounding
-    bound = 2 ** -8 * np.abs(ref) + 1.1 * np.abs(u) * bound_gu[:, :F] + np.abs(silu(g)) * bound_gu[:, F:] + 1e-30
+    got = act.double().cpu().numpy()
+    # fp32 error of g and u propagated (|silu'| <= 1.1), plus fp32 evaluation of silu(g) * u
+    bound = 1e-6 * np.abs(ref) + 1.1 * np.abs(u) * bound_gu[:, :F] + np.abs(silu(g)) * bound_gu[:, F:] + 1e-30
     assert np.all(np.abs(got - ref) <= bound)
 
 
@@ -98,7 +105,7 @@ def test_gemv_swiglu(cuda_lib, wt, B):
 def test_gemv_argmax(cuda_lib, wt, B):
     V, K = 3001, 512
     t, raw = _weights(wt, V, K, seed=11 + B)
-    x = _bf16_rand((B, K), seed=21 + B, scale=2.0).to(DEV)
+    x = _f32_rand((B, K), seed=21 + B, scale=2.0).to(DEV)
     logits = torch.zeros((B, V), device=DEV)
     ids = torch.full((B,), -1, dtype=torch.int32, device=DEV)
     capi.op_gemv(capi.EPI_ARGMAX, _dtype(wt), t["w"], t.get("s"), V, K, x, B, logits=logits, next_ids=ids)
@@ -107,7 +114,7 @@ def test_gemv_argmax(cuda_lib, wt, B):
     # the decision is taken on the GPU's own fp32 logits: first maximum
     assert np.array_equal(got_ids, np.argmax(lg, axis=1))
     W = decode_weight(raw)
-    xv = bf16_decode(_np_bits(x.cpu()))
+    xv = x.double().cpu().numpy()
     ref = xv @ W.T
     bound = TOL_REL * (np.abs(xv) @ np.abs(W).T) + TOL_ABS
     assert np.all(np.abs(lg - ref) <= bound)
@@ -128,7 +135,7 @@ def test_gemv_full_size_sampled(cuda_lib, wt, N, K, B):
     """Full model-size projections (8B gate/up, down, LM head; 70B down,
     gate/up): 64 sampled output rows checked one by one by the oracle."""
     t, _ = _weights(wt, N, K, seed=N ^ K)
-    x = _bf16_rand((B, K), seed=5).to(DEV)
+    x = _f32_rand((B, K), seed=5).to(DEV)
     ns = capi.op_gemv_nsplit(capi.EPI_PARTIAL, _dtype(wt), B, N, K)
     out = torch.zeros((ns, B, N), device=DEV)
     capi.op_gemv(capi.EPI_PARTIAL, _dtype(wt), t["w"], t.get("s"), N, K, x, B, out=out)
@@ -140,7 +147,7 @@ def test_gemv_full_size_sampled(cuda_lib, wt, N, K, B):
     if "s" in t:
         sub["s"] = t["s"][rows].cpu().numpy()
     W = decode_weight(sub)
-    xv = bf16_decode(_np_bits(x.cpu()))
+    xv = x.double().cpu().numpy()
     ref = xv @ W.T
     bound = TOL_REL * (np.abs(xv) @ np.abs(W).T) + TOL_ABS
     assert np.all(np.abs(got[:, rows] - ref) <= bound)
@@ -153,15 +160,15 @@ def test_norms(cuda_lib, H):
     gamma = (1 + 0.1 * torch.randn(H)).to(torch.bfloat16).to(DEV)
     tok = torch.tensor([0, 5, 776, 123, 5], dtype=torch.int32, device=DEV)
     r = torch.zeros((B, H), device=DEV)
-    y = torch.zeros((B, H), dtype=torch.bfloat16, device=DEV)
+    y = torch.zeros((B, H), device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     capi.op_embed_rmsnorm(tok, emb, gamma, 1e-6, r, y, err)
     e = bf16_decode(_np_bits(emb.cpu()))[tok.cpu().numpy()]
     g = bf16_decode(_np_bits(gamma.cpu()))
     assert np.array_equal(r.cpu().numpy().astype(np.float64), e)
     ref = rmsnorm(e, g, 1e-6)
-    got = bf16_decode(_np_bits(y.cpu()))
-    assert np.all(np.abs(got - ref) <= 2 ** -8 * np.abs(ref) + 1e-30)
+    got = y.double().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= 1e-5 * np.abs(ref) + 1e-30)
     assert err.item() == 0
     # residual add of 3 split partials, then the norm
     delta = torch.randn((3, B, H), device=DEV)
@@ -170,8 +177,8 @@ def test_norms(cuda_lib, H):
     rr = r0 + delta.double().cpu().numpy().sum(0)
     np.testing.assert_allclose(r.double().cpu().numpy(), rr, rtol=1e-6, atol=1e-6)
     ref = rmsnorm(rr, g, 1e-6)
-    got = bf16_decode(_np_bits(y.cpu()))
-    assert np.all(np.abs(got - ref) <= 2 ** -8 * np.abs(ref) + 1e-6)
+    got = y.double().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= 1e-5 * np.abs(ref) + 1e-6)
     # out-of-range token: error bit, token 0 used
     bad = torch.tensor([-1, V], dtype=torch.int32, device=DEV)
     capi.op_embed_rmsnorm(bad, emb, gamma, 1e-6, r[:2], y[:2], err)
@@ -280,19 +287,19 @@ def test_paged_attention(cuda_lib, kv, nq, nkv, d, lens):
     rng = np.random.default_rng(B + nq)
     q = rng.normal(size=(B, nq, d)) * 0.6
     qd = torch.tensor(q, dtype=torch.float32, device=DEV)
-    out = torch.zeros((B, nq * d), dtype=torch.bfloat16, device=DEV)
+    out = torch.zeros((B, nq * d), device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     flat = pool.view(torch.uint8).reshape(2, -1)
     capi.op_paged_attention(qd, nkv, flat[0], flat[1], _dtype(kv), ks, vs, torch.tensor(tables, device=DEV),
                             torch.tensor(lens_a, device=DEV), nb, out, err)
     torch.cuda.synchronize()
     assert err.item() == 0
-    got = bf16_decode(_np_bits(out.cpu())).reshape(B, nq, d)
+    got = out.double().cpu().numpy().reshape(B, nq, d)
     for b in range(B):
         ref = paged_attention(qd[b].double().cpu().numpy(), okv, 0, tables[b], int(lens_a[b]))
-        # fp32 softmax and accumulation (relative ~1e-5 of max|V|) + one BF16 rounding
+        # fp32 scores, exp2 and accumulation over <= 2049 tokens: ~1e-5 of max|V|
         vmax = np.abs(okv.decode(0, 1, tables[b][: -(-int(lens_a[b]) // 16)])).max()
-        assert np.all(np.abs(got[b] - ref) <= 2 ** -8 * np.abs(ref) + 2e-5 * vmax)
+        assert np.all(np.abs(got[b] - ref) <= 2e-5 * vmax)
 
 
 def test_paged_attention_bad_seq_len(cuda_lib):
@@ -302,7 +309,7 @@ def test_paged_attention_bad_seq_len(cuda_lib):
     flat = pool.view(torch.uint8).reshape(2, -1)
     q = torch.randn((2, nq, d), device=DEV)
     tables = torch.tensor([[0, 1], [2, 3]], dtype=torch.int32, device=DEV)
-    out = torch.full((2, nq * d), 7.0, dtype=torch.bfloat16, device=DEV)
+    out = torch.full((2, nq * d), 7.0, device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     capi.op_paged_attention(q, nkv, flat[0], flat[1], capi.DTYPE_BF16, 1.0, 1.0, tables,
                             torch.tensor([0, 33], dtype=torch.int32, device=DEV), nb, out, err)

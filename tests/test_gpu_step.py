@@ -165,7 +165,9 @@ def test_graph_replay_bit_identical_to_eager(cuda_lib):
         ib, lb = b.gpu_step(t)
         assert np.array_equal(ia, ib)
         assert np.array_equal(la, lb)
-    assert np.array_equal(a.gpu_pool(), b.gpu_pool())
+    # the capture's warm-up ran padding rows, which write the null block only
+    pa, pb = a.gpu_pool(), b.gpu_pool()
+    assert np.array_equal(pa[:, :, :a.nb], pb[:, :, :b.nb])
     assert a.eng.errors() == 0 and b.eng.errors() == 0
 
 
