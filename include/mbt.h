@@ -54,6 +54,7 @@ extern "C" {
 #define MBT_ERR_BLOB        (-5)   /* malformed weight/config blob */
 #define MBT_ERR_UNSUPPORTED (-6)   /* shape the kernels do not support */
 #define MBT_ERR_NO_DEVICE   (-7)   /* no CUDA device, or not sm_103 */
+#define MBT_ERR_SCRATCH     (-8)   /* request larger than a fixed scratch area */
 
 /* ---- device error word bits (model_poll_errors) ----------------------- */
 #define MBT_DEV_TOKEN_RANGE   0x1u   /* token id < 0 or >= vocab (token 0 used)   */

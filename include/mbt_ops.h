@@ -83,6 +83,36 @@ int op_paged_attention(int B, const float* q, int nq, int nkv, int d, const void
                        const int32_t* bt, int bt_stride, const int32_t* seq_lens, int num_blocks,
                        float* out, uint32_t* err, void* stream);
 
+/* Size in bytes of the device array op_paged_attention_noalloc works in. */
+#define MBT_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* op_paged_attention_noalloc: op_paged_attention for callers that cannot
+ * allocate device memory when they run attention -- processes that reserve
+ * nearly all HBM for their KV pool up front (a new allocation would fail or
+ * fragment it), latency-critical paths where cudaMalloc / cudaFree may
+ * synchronise the device, runtimes that forbid allocation after start-up. The
+ * paper has no counterpart; this is a property of the library, not of the
+ * method.
+ * Same arguments, result and launch geometry as op_paged_attention, but its
+ * scratch (split partials, (max, sum) pairs, merge tickets) is a file-scope
+ * device array of MBT_NOALLOC_SCRATCH_BYTES that every GPU loading the library
+ * holds until the process exits; it calls no cudaMalloc, cudaFree or other
+ * allocating routine. The scratch needed is about B * nq * splits * (4 d + 8)
+ * bytes (splits as op_paged_attention chooses them); a call needing more than
+ * the array returns MBT_ERR_SCRATCH before doing any work.
+ * All calls share the array and it keeps the last call's contents (the
+ * tickets are cleared at every call): calls that overlap on the GPU race, so
+ * keep them in one stream order. The first call on a device also does the
+ * set-up (looks up the array's device address with that device current); make
+ * it before any stream capture. */
+int op_paged_attention_noalloc(int B, const float* q, int nq, int nkv, int d, const void* kpool,
+                               const void* vpool, int kv_dtype, float k_scale, float v_scale,
+                               const int32_t* bt, int bt_stride, const int32_t* seq_lens,
+                               int num_blocks, float* out, uint32_t* err, void* stream);
+
+/* op_paged_attention_noalloc_limit: MBT_NOALLOC_SCRATCH_BYTES, as built. */
+size_t op_paged_attention_noalloc_limit(void);
+
 #ifdef __cplusplus
 }
 #endif

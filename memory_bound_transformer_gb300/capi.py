@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(_PKG, "libmbt.so")
 
 MBT_OK = 0
 STATUS = {0: "MBT_OK", -1: "MBT_ERR_BAD_ARG", -2: "MBT_ERR_BATCH", -3: "MBT_ERR_CUDA",
-          -4: "MBT_ERR_OOM", -5: "MBT_ERR_BLOB", -6: "MBT_ERR_UNSUPPORTED", -7: "MBT_ERR_NO_DEVICE"}
+          -4: "MBT_ERR_OOM", -5: "MBT_ERR_BLOB", -6: "MBT_ERR_UNSUPPORTED", -7: "MBT_ERR_NO_DEVICE",
+          -8: "MBT_ERR_SCRATCH"}
 DEV_TOKEN_RANGE, DEV_BLOCK_RANGE, DEV_POS_RANGE, DEV_SEQLEN_RANGE, DEV_NONFINITE = 1, 2, 4, 8, 16
 EPI_PARTIAL, EPI_SWIGLU, EPI_ARGMAX = 0, 1, 2
 DTYPE_BF16, DTYPE_E4M3, DTYPE_F32 = 0, 1, 2
@@ -48,6 +49,8 @@ SIGNATURES = {
     "op_gemv": (_I, [_I, _I, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _P, ctypes.POINTER(_I), _P, _P]),
     "op_rope_kv_write": (_I, [_I, _P, _I, _I, _I, _P, _P, _I, _I, _F, _P, _P, _I, _I, _F, _F, _P, _P, _P]),
     "op_paged_attention": (_I, [_I, _P, _I, _I, _I, _P, _P, _I, _F, _F, _P, _I, _P, _I, _P, _P, _P]),
+    "op_paged_attention_noalloc": (_I, [_I, _P, _I, _I, _I, _P, _P, _I, _F, _F, _P, _I, _P, _I, _P, _P, _P]),
+    "op_paged_attention_noalloc_limit": (_Z, []),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -239,3 +242,17 @@ def op_paged_attention(q, nkv, kpool, vpool, kv_dtype, k_scale, v_scale, bt, seq
     _check("op_paged_attention", load().op_paged_attention(
         B, _ptr(q), nq, nkv, d, _ptr(kpool), _ptr(vpool), kv_dtype, k_scale, v_scale, _ptr(bt),
         bt.shape[1], _ptr(seq_lens), num_blocks, _ptr(out), _ptr(err), _stream(stream)))
+
+
+def op_paged_attention_noalloc(q, nkv, kpool, vpool, kv_dtype, k_scale, v_scale, bt, seq_lens,
+                               num_blocks, out, err=None, stream=None) -> int:
+    """Allocation-free variant; returns the status code (MBT_ERR_SCRATCH when the
+    request exceeds the fixed scratch array) instead of raising."""
+    B, nq, d = q.shape
+    return load().op_paged_attention_noalloc(
+        B, _ptr(q), nq, nkv, d, _ptr(kpool), _ptr(vpool), kv_dtype, k_scale, v_scale, _ptr(bt),
+        bt.shape[1], _ptr(seq_lens), num_blocks, _ptr(out), _ptr(err), _stream(stream))
+
+
+def op_paged_attention_noalloc_limit() -> int:
+    return load().op_paged_attention_noalloc_limit()

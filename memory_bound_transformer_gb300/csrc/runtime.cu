@@ -314,6 +314,7 @@ const char* status_string(int code) {
     case MBT_ERR_BLOB: return "malformed weight/config blob";
     case MBT_ERR_UNSUPPORTED: return "unsupported model shape";
     case MBT_ERR_NO_DEVICE: return "no usable CUDA device";
+    case MBT_ERR_SCRATCH: return "request exceeds the fixed scratch area";
     default: return "unknown status";
   }
 }

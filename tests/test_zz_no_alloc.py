@@ -1,0 +1,77 @@
+"""The allocation-free attention entry point against the allocating one.
+
+op_paged_attention_noalloc exists for callers that cannot allocate device
+memory when they run attention (a serving process that reserved nearly all
+HBM for its KV pool, a latency-critical path where cudaMalloc may synchronise,
+a runtime that forbids allocation after start-up). It runs the same kernel on
+a fixed device array instead of stream-ordered allocations, so its output must
+match op_paged_attention's; two calls in a row with different inputs check
+that nothing left in the shared array from one call leaks into the next.
+
+This file is collected last so that a run stopping at the first failure has
+already run every other test; it also passes alone in a fresh process."""
+import numpy as np
+import pytest
+import torch
+
+from memory_bound_transformer_gb300 import capi
+from synth import ModelConfig, random_kv_pool, seeded_block_tables
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _case(nq, nkv, d, kv, lens, seed):
+    lens = np.array(lens, np.int32)
+    B = len(lens)
+    nb = int(sum(-(-int(l) // 16) for l in lens)) + 2
+    stride = max(-(-int(l) // 16) for l in lens) + 1
+    tables = seeded_block_tables(lens, 16, nb, seed=seed, stride=stride)
+    tables[tables < 0] = nb
+    cfg = ModelConfig("a", 1, 64, nq, nkv, d, 16, 16, kv_dtype=kv)
+    pool = random_kv_pool(cfg, nb, seed=seed + 1, device=DEV)
+    flat = pool.view(torch.uint8).reshape(2, -1)
+    g = torch.Generator(device="cpu").manual_seed(seed + 2)
+    q = (torch.randn((B, nq, d), generator=g) * 0.6).to(DEV)
+    return dict(q=q, k=flat[0], v=flat[1], bt=torch.tensor(tables, device=DEV),
+                sl=torch.tensor(lens, device=DEV), nb=nb, nkv=nkv,
+                dt=capi.DTYPE_E4M3 if kv == "fp8" else capi.DTYPE_BF16)
+
+
+def _run(c, fn):
+    out = torch.full((c["q"].shape[0], c["q"].shape[1] * c["q"].shape[2]), float("nan"), device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rc = fn(c["q"], c["nkv"], c["k"], c["v"], c["dt"], 0.75, 1.25, c["bt"], c["sl"], c["nb"], out, err)
+    torch.cuda.synchronize()
+    return rc, out, int(err.item())
+
+
+def test_noalloc_matches_allocating_entry_point(cuda_lib):
+    cases = [_case(32, 8, 128, "bf16", [1000, 17, 1], seed=3),
+             _case(64, 8, 128, "fp8", [2049, 65, 300, 16], seed=4)]
+    for c in cases:                                   # two calls in a row, different shapes
+        rc, got, e1 = _run(c, capi.op_paged_attention_noalloc)
+        assert rc == 0 and e1 == 0
+        ref = torch.zeros_like(got)
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        capi.op_paged_attention(c["q"], c["nkv"], c["k"], c["v"], c["dt"], 0.75, 1.25, c["bt"], c["sl"],
+                                c["nb"], ref, err)
+        torch.cuda.synchronize()
+        # same kernel, same geometry: within the attention tests' tolerance
+        # (2e-5 of max |V|; |V| < 5 for these N(0,1) caches times 1.25)
+        assert torch.isfinite(got).all()
+        assert torch.max(torch.abs(got - ref)).item() <= 2e-5 * 5.0 * 1.25
+
+
+def test_noalloc_rejects_oversized_requests(cuda_lib):
+    limit = capi.op_paged_attention_noalloc_limit()
+    assert limit == 8 << 20
+    # 512 rows x 128 query heads x d 128 need > 8 MiB of partials
+    B, nq, nkv, d = 512, 128, 8, 128
+    q = torch.zeros((B, nq, d), device=DEV)
+    tiny = torch.zeros(16, dtype=torch.int32, device=DEV)
+    bt = torch.zeros((B, 1), dtype=torch.int32, device=DEV)
+    out = torch.zeros(1, device=DEV)
+    rc = capi.op_paged_attention_noalloc(q, nkv, tiny, tiny, capi.DTYPE_BF16, 1.0, 1.0, bt, tiny, 1, out)
+    assert rc == -8                                  # MBT_ERR_SCRATCH, nothing launched
+    assert capi.status_string(-8) == "request exceeds the fixed scratch area"
