@@ -246,29 +246,38 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
 
 // Merge the splits of the group's G query heads: rescale each partial to the
 // common maximum, sum, divide by the total softmax mass, apply the V scale.
+// One warp per head finds the maximum and the mass; every thread then sums one
+// output element over the splits with several loads in flight.
 __device__ __forceinline__ void merge_splits(const AttnArgs& a, float* wsm, int G, size_t head0, int D) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ns = a.nsplit;
-  // per (head, split) weight exp2(m_s - M) / L in shared memory
-  for (int g = tid; g < G; g += blockDim.x) {
+  for (int g = warp; g < G; g += kAttnThreads / 32) {
     const float2* ml = a.part_ml + (head0 + g) * ns;
     float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) if (ml[s].y > 0.f) M = fmaxf(M, ml[s].x);
+    for (int s = lane; s < ns; s += 32) if (ml[s].y > 0.f) M = fmaxf(M, ml[s].x);
+    M = warp_max(M);
     float L = 0.f;
-    for (int s = 0; s < ns; ++s) if (ml[s].y > 0.f) L += exp2f(ml[s].x - M) * ml[s].y;
+    for (int s = lane; s < ns; s += 32) if (ml[s].y > 0.f) L += exp2f(ml[s].x - M) * ml[s].y;
+    L = warp_sum(L);
     const float inv = L > 0.f ? a.v_scale / L : 0.f;
-    for (int s = 0; s < ns; ++s) wsm[g * ns + s] = ml[s].y > 0.f ? exp2f(ml[s].x - M) * inv : 0.f;
+    for (int s = lane; s < ns; s += 32) wsm[g * ns + s] = ml[s].y > 0.f ? exp2f(ml[s].x - M) * inv : 0.f;
   }
   __syncthreads();
-  for (int e = tid; e < G * D; e += blockDim.x) {
+  for (int e = tid; e < G * D; e += kAttnThreads) {
     const int g = e / D, d = e - g * D;
     const float* po = a.part_o + (head0 + g) * ns * D + d;
-    float acc = 0.f;
-    for (int s = 0; s < ns; ++s) {
-      const float w = wsm[g * ns + s];
-      if (w != 0.f) acc += w * po[(size_t)s * D];
+    const float* wg = wsm + g * ns;
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    int s = 0;
+    for (; s + 4 <= ns; s += 4) {
+      const float w0 = wg[s], w1 = wg[s + 1], w2 = wg[s + 2], w3 = wg[s + 3];
+      if (w0 != 0.f) acc0 += w0 * po[(size_t)s * D];
+      if (w1 != 0.f) acc1 += w1 * po[(size_t)(s + 1) * D];
+      if (w2 != 0.f) acc2 += w2 * po[(size_t)(s + 2) * D];
+      if (w3 != 0.f) acc3 += w3 * po[(size_t)(s + 3) * D];
     }
-    a.out[(head0 + g) * D + d] = acc;
+    for (; s < ns; ++s) if (wg[s] != 0.f) acc0 += wg[s] * po[(size_t)s * D];
+    a.out[(head0 + g) * D + d] = (acc0 + acc1) + (acc2 + acc3);
   }
 }
 
@@ -371,11 +380,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_split_kernel(const AttnA
 
 
 void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nsplit) {
-  const int target = 2 * num_sms;
+  // Enough CTAs to cover the SMs, but at least two 64-token tiles per split so
+  // that the double buffer overlaps loads with math and the merge stays short.
+  const int target = num_sms;
   const int pairs = B * nkv;
   int want = (target + pairs - 1) / pairs;
   if (want < 1) want = 1;
   int per = (max_blocks + want - 1) / want;
+  const int min_per = 2 * kAttnTile / kBlockTokens;
+  if (per < min_per) per = min_per;
+  if (per > max_blocks) per = max_blocks;
   if (per < 1) per = 1;
   *bps = per;
   *nsplit = (max_blocks + per - 1) / per;

@@ -103,14 +103,20 @@ gemv_kernel(const GemvArgs a) {
   const size_t row_bytes = (size_t)a.K * (WT == W_BF16 ? 2 : 1);
   const unsigned char* Wb = reinterpret_cast<const unsigned char*>(a.W) + (size_t)v0 * 16;
 
-  // The weights do not depend on the previous kernel: start pulling this CTA's
-  // first rows into L2 while that kernel drains.
-  if (tid < RG && r_begin < r_end) {
-    const int i = tid;
-    const int ch = min(r_begin + (i % CH), r_end - 1);
-    const int wr = (EPI == EPI_SWIGLU && i >= CH) ? a.N + ch : ch;
-    const uint32_t bytes = (uint32_t)min((size_t)nvec * 16, (size_t)32768);
-    prefetch_l2(Wb + (size_t)wr * row_bytes, bytes);
+  // The weights do not depend on the previous kernel: pull this CTA's first
+  // rows (all of them when prefetch_bytes says so) into L2 while it drains.
+  if (r_begin < r_end) {
+    const size_t seg = (size_t)nvec * 16;                       // this split's bytes of a row
+    const size_t budget = a.prefetch_bytes ? a.prefetch_bytes : 65536;
+    const int rows = (EPI == EPI_SWIGLU ? 2 : 1) * (r_end - r_begin);
+    const int n_pf = (int)min((size_t)rows, max((size_t)1, budget / seg));
+    for (int i = tid; i < n_pf; i += kGemvThreads) {
+      const int ch = r_begin + (EPI == EPI_SWIGLU ? i / 2 : i);
+      const int wr = (EPI == EPI_SWIGLU && (i & 1)) ? a.N + ch : ch;
+      const unsigned char* rp = Wb + (size_t)wr * row_bytes;
+      for (size_t o = 0; o < seg; o += 65536)
+        prefetch_l2(rp + o, (uint32_t)min(seg - o, (size_t)65536));
+    }
   }
   pdl_wait();
 

@@ -40,6 +40,10 @@ struct GemvArgs {
   float* logits; int ldl;
   ArgmaxPart* part; int part_ld;
   uint32_t* err;
+  // bytes of this CTA's weight rows pulled into L2 before waiting on the
+  // previous kernel (0 = default 64 KB); a kernel that follows a latency-bound
+  // one (attention) prefetches its whole slice
+  uint32_t prefetch_bytes;
 };
 
 struct GemvLaunch { int nb_tmpl; int nsplit; int grid; size_t smem; };

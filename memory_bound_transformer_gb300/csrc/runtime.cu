@@ -195,7 +195,7 @@ struct NormIn {
 cudaError_t gemv_rows(const mbt_model* m, int epi, const NormIn* nin, const void* W, const float* sc,
                       int N, int K, const float* x, int R, int nsplit, int grid_fixed, float* out,
                       long long split_stride, int ldo, float* act, int lda, float* logits,
-                      ArgmaxPart* part, int part_ld, cudaStream_t s) {
+                      ArgmaxPart* part, int part_ld, cudaStream_t s, uint32_t prefetch = 0) {
   const int pro = nin ? PRO_NORM : PRO_X;
   const int step = gemv_max_rows(epi, K, pro);
   for (int b0 = 0; b0 < R; b0 += step) {
@@ -218,6 +218,7 @@ cudaError_t gemv_rows(const mbt_model* m, int epi, const NormIn* nin, const void
     a.logits = logits ? logits + (size_t)b0 * m->h.vocab : nullptr; a.ldl = (int)m->h.vocab;
     a.part = part ? part + b0 : nullptr; a.part_ld = part_ld;
     a.err = m->err;
+    a.prefetch_bytes = prefetch;
     cudaError_t e = gemv_launch(epi, pro, a, g, s);
     if (e != cudaSuccess) return e;
   }
@@ -262,9 +263,10 @@ int run_step(mbt_model* m, mbt_kv* kv, const Plan& p, const int* tok, const int*
     at.bps = p.attn_bps; at.nsplit = p.attn_nsplit;
     at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = w.o; at.tickets = w.tickets; at.err = m->err;
     MBT_CUDA(launch_attention(at, s));
-    // O projection (residual partials)
+    // O projection (residual partials); it starts during attention, whose
+    // batch-1 form leaves HBM idle, so it prefetches all of its weights
     MBT_CUDA(gemv_rows(m, EPI_PARTIAL, nullptr, L.w_o, L.s_o, H, Q, w.o, R, p.ns_o, 0, w.delta,
-                       rh, H, nullptr, 0, nullptr, nullptr, 0, s));
+                       rh, H, nullptr, 0, nullptr, nullptr, 0, s, 0xffffffffu));
     // RMSNorm prologue + gate/up projection + SwiGLU epilogue
     NormIn n2{w.r2, w.delta, p.ns_o, L.g_ffn, w.r};
     MBT_CUDA(gemv_rows(m, EPI_SWIGLU, &n2, L.w_gu, L.s_gu, F, H, nullptr, R, 1, 0, nullptr, 0, 0,
