@@ -131,24 +131,14 @@ def build_case(wl, B, steps_total, device="cuda"):
     return cfg, ctx, tables, nb, eng
 
 
-def time_native(args, rank, world):
-    wl = WORKLOADS[args.workload]
-    B = args.batch or wl.batches[0]
-    K, W = args.steps, args.warmup
-    dev = torch.device("cuda", torch.cuda.current_device())
-    cfg, ctx, tables, nb, eng = build_case(wl, B, K + W + (0 if args.no_e2e else K + 2))
-    mbs = tables.shape[1]
-    ladder = [int(x) for x in args.ladder.split(",")] if args.ladder else list(wl.ladder)
-    if B > max(ladder):
-        ladder = sorted(set(ladder) | {B})
-    eng.capture(ladder=ladder, max_blocks_per_seq=mbs)
-    kernels_per_step, uses_graph = eng.stats(B)
+def timed_steps(eng, cfg, ctx, tables, B, K, W, dev, world, clocks_on):
+    """W untimed then K timed decode steps at batch B (rows 0..B-1 of the case);
+    each step feeds back the previous ids and advances every position by one."""
     S = torch.cuda.current_stream()
-
     total = K + W
-    pos_all = torch.tensor(np.stack([ctx + t for t in range(total)]), dtype=torch.int32, device=dev)
+    pos_all = torch.tensor(np.stack([ctx[:B] + t for t in range(total)]), dtype=torch.int32, device=dev)
     sl_all = pos_all + 1
-    bt = torch.tensor(tables, device=dev)
+    bt = torch.tensor(tables[:B], device=dev)
     ids = [torch.randint(0, cfg.vocab, (B,), dtype=torch.int32, device=dev) for _ in range(2)]
 
     def step(t):
@@ -159,9 +149,10 @@ def time_native(args, rank, world):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    clocks = Clocks(dev.index)
-    clocks.start()
-    time.sleep(0.3)
+    clocks = Clocks(dev.index) if clocks_on else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
     torch.cuda.synchronize()
     ev[0].record(S)
@@ -171,27 +162,42 @@ def time_native(args, rank, world):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    ck = clocks.stop()
+    ck = clocks.stop() if clocks else None
     per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(K)]
     total_ms = ev[0].elapsed_time(ev[K])
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
+    byte_steps = [ledger.step_bytes(cfg, ctx[:B] + W + t + 1) for t in range(K)]
+    kps, graph = eng.stats(B)
+    return dict(B=B, total_ms=total_ms, per_step=per_step, avg_bytes=float(np.mean(byte_steps)),
+                clocks=ck, kernels_per_step=kps, uses_graph=graph)
 
-    # algorithmic bytes per step over the timed steps (contexts grow by one per step)
-    byte_steps = [ledger.step_bytes(cfg, ctx + W + t + 1) for t in range(K)]
-    avg_bytes = float(np.mean(byte_steps))
 
-    # dominant kernel: the fused gate/up + SwiGLU GEMV (largest matrix of the layer),
-    # timed on its launching stream over all layers' matrices (each > L2)
-    kern = None if args.no_kernel_timing else time_gemv_swiglu(cfg, wl, B, dev)
-
-    e2e = None if args.no_e2e else time_e2e(eng, cfg, ctx + W + K, bt, B, K, dev, tables)
+def time_native(args, rank, world):
+    wl = WORKLOADS[args.workload]
+    batches = [args.batch] if args.batch else [b for b in wl.batches if b in (1, 64)] or [wl.batches[0]]
+    Bmax = max(batches)
+    K, W = args.steps, args.warmup
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cfg, ctx, tables, nb, eng = build_case(wl, Bmax, K + W + (0 if args.no_e2e else K + 2))
+    mbs = tables.shape[1]
+    ladder = [int(x) for x in args.ladder.split(",")] if args.ladder else list(wl.ladder)
+    if Bmax > max(ladder):
+        ladder = sorted(set(ladder) | {Bmax})
+    eng.capture(ladder=ladder, max_blocks_per_seq=mbs)
+    runs = [timed_steps(eng, cfg, ctx, tables, B, K, W, dev, world, clocks_on=(i == 0))
+            for i, B in enumerate(batches)]
+    # dominant kernel of the batch-1 step: the fused gate/up + SwiGLU GEMV
+    # (largest matrix of the layer), timed on its own stream over all layers'
+    # matrices (each larger than L2)
+    kern = None if args.no_kernel_timing else time_gemv_swiglu(cfg, wl, batches[0], dev)
+    B0 = batches[0]
+    bt0 = torch.tensor(tables[:B0], device=dev)
+    e2e = None if args.no_e2e else time_e2e(eng, cfg, ctx[:B0] + W + K, bt0, B0, K, dev, tables[:B0])
     eng.close()
-    return dict(cfg=cfg, B=B, K=K, W=W, total_ms=total_ms, per_step=per_step, avg_bytes=avg_bytes,
-                clocks=ck, kernels_per_step=kernels_per_step, uses_graph=uses_graph, kern=kern,
-                e2e=e2e, ctx=ctx, wl=wl)
+    return dict(cfg=cfg, K=K, W=W, runs=runs, kern=kern, e2e=e2e, ctx=ctx, wl=wl)
 
 
 def time_gemv_swiglu(cfg, wl, B, dev, reps=3):
@@ -335,36 +341,49 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     capi.load()
     r = time_native(args, rank, world)
-    cfg, B, K = r["cfg"], r["B"], r["K"]
-    tok_s = world * B * K / (r["total_ms"] / 1e3)
+    cfg, K = r["cfg"], r["K"]
     peak, src = peaks()
     kern = r["kern"] or {"bytes": 0, "ms": float("nan"), "launches": 0}
     k_gbs = kern["bytes"] / (kern["ms"] / 1e3) / 1e9
-    step_ms = r["total_ms"] / K
-    step_gbs = r["avg_bytes"] / (step_ms * 1e-3) / 1e9
-    ps = sorted(r["per_step"])
+
+    def summary(run):
+        step_ms = run["total_ms"] / K
+        gbs = run["avg_bytes"] / (step_ms * 1e-3) / 1e9
+        ps = sorted(run["per_step"])
+        return {"batch": run["B"], "value": round(world * run["B"] * K / (run["total_ms"] / 1e3), 2),
+                "unit": "tokens/s", "ms_per_step": round(step_ms, 4),
+                "latency_ms": {"p50": round(ps[len(ps) // 2], 4),
+                               "p99": round(ps[min(len(ps) - 1, int(0.99 * len(ps)))], 4)},
+                "step_roofline": {"bytes_per_step": int(run["avg_bytes"]), "achieved_gbs": round(gbs, 1),
+                                  "frac_of_peak": round(gbs / peak, 4), "frac_of_8tbs": round(gbs / 8000, 4)},
+                "kernels_per_step": run["kernels_per_step"], "graph": run["uses_graph"]}
+
+    head = summary(r["runs"][0])
+    B = head["batch"]
     line = {
-        "metric": "decode tokens/s (batch %d); achieved HBM GB/s as %% of GB300 peak" % B,
-        "value": round(tok_s, 2), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": r["W"],
-        "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "metric": "decode tokens/s (batch %d; batch 64 in 'batch64'); achieved HBM GB/s as %% of GB300 peak" % B,
+        "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": r["W"],
+        "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if cfg.weight_dtype == "bf16" else "fp8-e4m3 weights, fp32 math",
         "data": "synthetic (seeded random-init weights N(0,0.02), random KV contents and token ids)",
         "config": {"workload": f"{r['wl'].key}: {r['wl'].description}", "model": cfg.name, "batch": B,
-                   "context_start": [int(c) for c in r["ctx"][:8]], "graph": r["uses_graph"],
-                   "l2": "weights of every step (%.1f GB) exceed L2; no flush needed" % (r["avg_bytes"] / 1e9),
+                   "context_start": [int(c) for c in r["ctx"][:8]], "graph": head["graph"],
+                   "l2": "weights of every step (%.1f GB) exceed L2; no flush needed"
+                         % (head["step_roofline"]["bytes_per_step"] / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "latency_ms": {"p50": round(ps[len(ps) // 2], 4), "p99": round(ps[min(len(ps) - 1, int(0.99 * len(ps)))], 4)},
-        "step_roofline": {"bytes_per_step": int(r["avg_bytes"]), "achieved_gbs": round(step_gbs, 1),
-                          "frac_of_peak": round(step_gbs / peak, 4), "frac_of_8tbs": round(step_gbs / 8000, 4)},
-        "roofline": {"kernel": "gemv_kernel<NB,WT,EPI_SWIGLU> (fused gate/up + SiLU x mul)", "bound": "hbm",
-                     "achieved": round(k_gbs, 1), "peak": peak, "peak_source": src, "unit": "GB/s",
-                     "frac": round(k_gbs / peak, 4), "traffic": GEMV_TRAFFIC_BYTES,
+        "latency_ms": head["latency_ms"],
+        "step_roofline": head["step_roofline"],
+        "roofline": {"kernel": "gemv_kernel<NB,WT,EPI_SWIGLU,PRO_NORM> (norm + fused gate/up + SiLU x mul)",
+                     "bound": "hbm", "achieved": round(k_gbs, 1), "peak": peak, "peak_source": src,
+                     "unit": "GB/s", "frac": round(k_gbs / peak, 4), "traffic": GEMV_TRAFFIC_BYTES,
                      "algorithmic_bytes_per_launch": kern["bytes"], "avg_launch_ms": round(kern["ms"], 5)},
-        "gpu_launches": int(r["kernels_per_step"] * K),
-        "kernels_per_step": r["kernels_per_step"],
+        "gpu_launches": int(sum(run["kernels_per_step"] * K for run in r["runs"])),
+        "kernels_per_step": head["kernels_per_step"],
     }
-    if r["clocks"]:
-        line["clocks"] = r["clocks"]
+    for run in r["runs"][1:]:
+        line["batch%d" % run["B"]] = summary(run)
+    if r["runs"][0]["clocks"]:
+        line["clocks"] = r["runs"][0]["clocks"]
     if r["e2e"]:
         e = dict(r["e2e"])
         e["value"] = round(e["value"] * world, 2)

@@ -62,6 +62,7 @@ extern "C" {
 #define MBT_DEV_POS_RANGE     0x4u   /* position < 0 or >= max_pos (write skipped) */
 #define MBT_DEV_SEQLEN_RANGE  0x8u   /* seq_len < 1 or beyond the block table (row output 0) */
 #define MBT_DEV_NONFINITE     0x10u  /* NaN logit met by the arg-max                */
+#define MBT_DEV_WAIT_LIMIT    0x20u  /* a tensor-core kernel's pipeline wait timed out (its output is skipped) */
 
 /* ---- weight/config blob ------------------------------------------------ *
  * A blob is one byte buffer: an mbt_blob_header at offset 0, an array of

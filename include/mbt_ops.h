@@ -59,6 +59,19 @@ int op_gemv(int epi, int w_dtype, const void* W, const float* scales, int N, int
             const float* x, int B, int force_nsplit, float* out, float* act,
             float* logits, int32_t* next_ids, int* nsplit_used, uint32_t* err, void* stream);
 
+/* op_gemm_tc: the tensor-core (tcgen05) projection the decode step uses at
+ * batch 16..128 with BF16 weights: W [rows][K] BF16 (K a multiple of 16,
+ * >= 64), x [B][K] fp32 with 1 <= B <= 128, split internally into BF16
+ * high/low rows so that the product keeps near-fp32 accuracy. Epilogues as
+ * op_gemv: PARTIAL out [ksplit][B][N] (ksplit K-splits), SWIGLU act [B][N]
+ * fp32 (W has 2N rows), ARGMAX next_ids [B] (+ logits [B][N] if non-NULL).
+ * Returns MBT_ERR_UNSUPPORTED where the tensor-map encoder is unavailable.
+ * ("GPU Inference Internals", "Roofline: Why Decode Is Memory-Bound": at batch
+ * B the weight-only intensity is 2B / b_w FLOP per byte.) */
+int op_gemm_tc(int epi, const void* W, const float* scales, int N, int K, const float* x, int B,
+               int ksplit, float* out, float* act, float* logits, int32_t* next_ids, uint32_t* err,
+               void* stream);
+
 /* op_rope_kv_write: rotate q and k of qkv [B][(nq + 2 nkv) d] (fp32; q heads,
  * then k heads, then v heads) at positions[b] with the rotate-half pairing
  * (element i with i + d/2, angle p * theta^(-2i/d)), write rotated q to q_out

@@ -47,6 +47,7 @@ SIGNATURES = {
     "op_add_rmsnorm": (_I, [_I, _I, _P, _P, _I, _P, _F, _P, _P]),
     "op_gemv_nsplit": (_I, [_I, _I, _I, _I, _I]),
     "op_gemv": (_I, [_I, _I, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _P, ctypes.POINTER(_I), _P, _P]),
+    "op_gemm_tc": (_I, [_I, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P]),
     "op_rope_kv_write": (_I, [_I, _P, _I, _I, _I, _P, _P, _I, _I, _F, _P, _P, _I, _I, _F, _F, _P, _P, _P]),
     "op_paged_attention": (_I, [_I, _P, _I, _I, _I, _P, _P, _I, _F, _F, _P, _I, _P, _I, _P, _P, _P]),
     "op_paged_attention_noalloc": (_I, [_I, _P, _I, _I, _I, _P, _P, _I, _F, _F, _P, _I, _P, _I, _P, _P, _P]),
@@ -226,6 +227,12 @@ def op_gemv(epi, w_dtype, W, scales, N, K, x, B, force_nsplit=0, out=None, act=N
                                      _ptr(out), _ptr(act), _ptr(logits), _ptr(next_ids),
                                      ctypes.byref(used), _ptr(err), _stream(stream)))
     return used.value
+
+
+def op_gemm_tc(epi, W, scales, N, K, x, B, ksplit=1, out=None, act=None, logits=None, next_ids=None,
+               err=None, stream=None) -> None:
+    _check("op_gemm_tc", load().op_gemm_tc(epi, _ptr(W), _ptr(scales), N, K, _ptr(x), B, ksplit, _ptr(out),
+                                           _ptr(act), _ptr(logits), _ptr(next_ids), _ptr(err), _stream(stream)))
 
 
 def op_rope_kv_write(qkv, nq, nkv, d, positions, bt, max_pos, theta, kpool, vpool, num_blocks,

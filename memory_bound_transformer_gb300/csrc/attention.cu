@@ -277,7 +277,15 @@ __device__ __forceinline__ void merge_splits(const AttnArgs& a, float* wsm, int 
       if (w3 != 0.f) acc3 += w3 * po[(size_t)(s + 3) * D];
     }
     for (; s < ns; ++s) if (wg[s] != 0.f) acc0 += wg[s] * po[(size_t)s * D];
-    a.out[(head0 + g) * D + d] = (acc0 + acc1) + (acc2 + acc3);
+    const float o = (acc0 + acc1) + (acc2 + acc3);
+    const size_t oi = (head0 + g) * D + d;
+    if (a.out) a.out[oi] = o;
+    if (a.out_hl) {                                // high/low BF16 rows for the tensor-core GEMM
+      const size_t row = oi / ((size_t)a.nq * D), col = oi % ((size_t)a.nq * D);
+      const bf16 h = __float2bfloat16_rn(o);
+      a.out_hl[row * a.nq * D + col] = h;
+      a.out_hl[(a.rp_hl + row) * a.nq * D + col] = __float2bfloat16_rn(o - __bfloat162float(h));
+    }
   }
 }
 

@@ -58,6 +58,26 @@ int gemv_max_rows(int epi, int K, int pro = PRO_X);
 cudaError_t gemv_launch(int epi, int pro, const GemvArgs& a, const GemvLaunch& g, cudaStream_t s);
 cudaError_t gemv_init();   // raise dynamic shared-memory limits (once per process)
 
+// Tensor-core skinny GEMM (batch 16..128, BF16 weights): y = W x with x given
+// as [2 * Rp][K] BF16 rows (rows 0..Rp-1 the high parts, Rp..2Rp-1 the low
+// parts of the fp32 activations). Tensor maps are opaque 128-byte blobs.
+struct TmaMap { alignas(64) unsigned char bytes[128]; };
+struct TcArgs {
+  int N, K, R, Rp;            // output channels (SWIGLU: ffn), K, live rows, padded rows (multiple of 8)
+  const float* scale;         // per-row weight scale or null
+  float* out; long long split_stride; int ldo;       // EPI_PARTIAL: out[split][b][n]
+  bf16* act_hl; int ld_act;                            // EPI_SWIGLU: [2 * Rp][ld_act] hi/lo rows
+  float* logits; int ldl; ArgmaxPart* part; int part_ld;   // EPI_ARGMAX
+  uint32_t* err;
+};
+cudaError_t tc_init();
+cudaError_t tc_make_map(void* map, const void* base, int rows, int K, int box_rows);
+cudaError_t tc_launch(int epi, const void* mapW, const void* mapX, const TcArgs& a, int ksplit, cudaStream_t s);
+int tc_tiles(int epi, int N);
+size_t tc_smem(int Rp);
+cudaError_t tc_to_hl(const float* x, int B, int Rp, int K, bf16* hl, cudaStream_t s);
+cudaError_t tc_from_hl(const bf16* hl, int B, int Rp, int N, float* out, cudaStream_t s);
+
 // r <- E[token] (fp32); y <- rmsnorm(r) * gamma (fp32)
 struct EmbedNormArgs {
   int B, H, vocab; const int* tokens; const bf16* embed;
@@ -65,10 +85,13 @@ struct EmbedNormArgs {
 };
 cudaError_t launch_embed_rmsnorm(const EmbedNormArgs& a, cudaStream_t s);
 
-// r <- r + sum_s delta[s]; y <- rmsnorm(r) * gamma (fp32)
+// r <- r + sum_s delta[s]; y <- rmsnorm(r) * gamma (fp32), or, when y_hl is
+// set, y as BF16 high/low rows [2 * rp][H] for the tensor-core GEMM (rows
+// B..rp-1 written as zeros).
 struct AddNormArgs {
   int B, H; float* r; const float* delta; int n_delta; long long delta_stride;
   const bf16* gamma; float eps; float* y;
+  bf16* y_hl; int rp;
 };
 cudaError_t launch_add_rmsnorm(const AddNormArgs& a, cudaStream_t s);
 
@@ -97,6 +120,7 @@ struct AttnArgs {
   const int* bt; int bt_stride; const int* seq_lens; int num_blocks;
   int bps; int nsplit;      // KV blocks per split, splits per (row, kv head)
   float* part_o; float2* part_ml; float* out; int* tickets; uint32_t* err;
+  bf16* out_hl; int rp_hl;  // optional: output also as BF16 high/low rows [2 * rp_hl][nq * d]
 };
 void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nsplit);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);

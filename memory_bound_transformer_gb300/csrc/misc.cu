@@ -81,11 +81,44 @@ __global__ void __launch_bounds__(1024) embed_rmsnorm_kernel(const EmbedNormArgs
 // "Residual add + RMSNorm ... doing both in one pass" ("Kernels, Fusion & CUDA
 // Graphs", "Fix 1: kernel fusion"). The projection before it left its output
 // as split-K partial sums; they are added here too, in a fixed order.
+// y as BF16 high/low rows (y = hi + lo to ~2^-17) for the tensor-core GEMM.
+__device__ __forceinline__ void norm_store_hl(const float4 (&v)[kNormMaxV], float ss, int H,
+                                             const bf16* __restrict__ gamma, float eps, bf16* hi_row,
+                                             bf16* lo_row, float* scratch) {
+  const float tot = block_sum(ss, scratch);
+  const float inv = 1.0f / sqrtf(tot / (float)H + eps);
+  const int nv = H / 4;
+  const uint2* g2 = reinterpret_cast<const uint2*>(gamma);
+#pragma unroll
+  for (int j = 0; j < kNormMaxV; ++j) {
+    const int i = threadIdx.x + j * blockDim.x;
+    if (i < nv) {
+      const uint2 g = g2[i];
+      const float o[4] = {v[j].x * inv * bf16_lo(g.x), v[j].y * inv * bf16_hi(g.x),
+                          v[j].z * inv * bf16_lo(g.y), v[j].w * inv * bf16_hi(g.y)};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bf16 h = __float2bfloat16_rn(o[e]);
+        hi_row[4 * i + e] = h;
+        lo_row[4 * i + e] = __float2bfloat16_rn(o[e] - __bfloat162float(h));
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(1024) add_rmsnorm_kernel(const AddNormArgs a) {
   __shared__ float scratch[32];
   const int b = blockIdx.x;
   pdl_launch_dependents();
   pdl_wait();
+  if (b >= a.B) {                                   // padding rows of the high/low output
+    const bf16 z = __float2bfloat16_rn(0.f);
+    for (int i = threadIdx.x; i < a.H; i += blockDim.x) {
+      a.y_hl[(size_t)b * a.H + i] = z;
+      a.y_hl[(size_t)(a.rp + b) * a.H + i] = z;
+    }
+    return;
+  }
   const int nv = a.H / 4;
   float4* __restrict__ r = reinterpret_cast<float4*>(a.r + (size_t)b * a.H);
   const float4* __restrict__ d = reinterpret_cast<const float4*>(a.delta + (size_t)b * a.H);
@@ -110,7 +143,10 @@ __global__ void __launch_bounds__(1024) add_rmsnorm_kernel(const AddNormArgs a) 
     const int i = threadIdx.x + j * blockDim.x;
     if (i < nv) r[i] = v[j];
   }
-  norm_store(v, ss, a.H, a.gamma, a.eps, a.y + (size_t)b * a.H, scratch);
+  if (a.y_hl)
+    norm_store_hl(v, ss, a.H, a.gamma, a.eps, a.y_hl + (size_t)b * a.H, a.y_hl + (size_t)(a.rp + b) * a.H, scratch);
+  else
+    norm_store(v, ss, a.H, a.gamma, a.eps, a.y + (size_t)b * a.H, scratch);
 }
 
 static int norm_threads(int H) {
@@ -132,7 +168,8 @@ cudaError_t launch_add_rmsnorm(const AddNormArgs& a, cudaStream_t s) {
   if (a.H % 4 || a.H > 4 * kNormMaxV * 1024) return cudaErrorInvalidValue;
   AddNormArgs args = a;
   void* p[] = {&args};
-  return launch_pdl((const void*)add_rmsnorm_kernel, dim3(a.B), dim3(norm_threads(a.H)), 0, s, p);
+  const int rows = a.y_hl ? a.rp : a.B;
+  return launch_pdl((const void*)add_rmsnorm_kernel, dim3(rows), dim3(norm_threads(a.H)), 0, s, p);
 }
 
 // ---------------------------------------------------------------------------

@@ -39,7 +39,7 @@ int op_embed_rmsnorm(int B, int H, int vocab, const int32_t* tokens, const uint1
 int op_add_rmsnorm(int B, int H, float* r, const float* delta, int n_delta,
                    const uint16_t* gamma, float eps, float* y, void* stream) {
   if (B < 1 || H < 4 || H % 4 || !r || !gamma || !y || n_delta < 0 || (n_delta && !delta)) return MBT_ERR_BAD_ARG;
-  AddNormArgs a{B, H, r, delta, n_delta, (long long)B * H, (const bf16*)gamma, eps, y};
+  AddNormArgs a{B, H, r, delta, n_delta, (long long)B * H, (const bf16*)gamma, eps, y, nullptr, 0};
   return launch_add_rmsnorm(a, (cudaStream_t)stream) == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
 }
 
@@ -88,6 +88,49 @@ int op_gemv(int epi, int w_dtype, const void* W, const float* scales, int N, int
       launch_argmax_reduce(B, part, B, g0.grid, next_ids, err, s) != cudaSuccess)
     rc = MBT_ERR_CUDA;
   if (part) cudaFreeAsync(part, s);
+  return rc;
+}
+
+int op_gemm_tc(int epi, const void* W, const float* scales, int N, int K, const float* x, int B,
+               int ksplit, float* out, float* act, float* logits, int32_t* next_ids, uint32_t* err,
+               void* stream) {
+  if (epi < 0 || epi > 2 || !W || !x || B < 1 || B > 128 || N < 1 || K < 64 || K % 16) return MBT_ERR_BAD_ARG;
+  if ((epi == EPI_PARTIAL && !out) || (epi == EPI_SWIGLU && !act) || (epi == EPI_ARGMAX && !next_ids))
+    return MBT_ERR_BAD_ARG;
+  if (epi != EPI_PARTIAL) ksplit = 1;
+  if (ksplit < 1) ksplit = 1;
+  {
+    const cudaError_t e = tc_init();
+    if (e == cudaErrorNotSupported) return MBT_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return MBT_ERR_CUDA;
+  }
+  int rc = init_once();
+  if (rc != MBT_OK) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int Rp = (B + 7) / 8 * 8;
+  const int wrows = epi == EPI_SWIGLU ? 2 * N : N;
+  const int tiles = tc_tiles(epi, N);
+  const size_t b_x = (size_t)2 * Rp * K * 2, b_a = epi == EPI_SWIGLU ? (size_t)2 * Rp * N * 2 : 0;
+  const size_t b_p = epi == EPI_ARGMAX ? (size_t)tiles * B * sizeof(ArgmaxPart) : 0;
+  char* scratch = nullptr;
+  if (cudaMallocAsync((void**)&scratch, b_x + b_a + b_p + 512, s) != cudaSuccess) return MBT_ERR_OOM;
+  bf16* xhl = (bf16*)scratch;
+  bf16* ahl = (bf16*)(scratch + ((b_x + 255) & ~(size_t)255));
+  ArgmaxPart* part = (ArgmaxPart*)((char*)ahl + ((b_a + 255) & ~(size_t)255));
+  TmaMap wm, xm;
+  if (tc_make_map(&wm, W, wrows, K, 64) != cudaSuccess || tc_make_map(&xm, xhl, 2 * Rp, K, 2 * Rp) != cudaSuccess)
+    rc = MBT_ERR_BAD_ARG;
+  if (rc == MBT_OK && tc_to_hl(x, B, Rp, K, xhl, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  TcArgs a = {};
+  a.N = N; a.K = K; a.R = B; a.Rp = Rp; a.scale = scales;
+  a.out = out; a.split_stride = (long long)B * N; a.ldo = N;
+  a.act_hl = ahl; a.ld_act = N;
+  a.logits = logits; a.ldl = N; a.part = part; a.part_ld = B; a.err = err;
+  if (rc == MBT_OK && tc_launch(epi, &wm, &xm, a, ksplit, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  if (rc == MBT_OK && epi == EPI_SWIGLU && tc_from_hl(ahl, B, Rp, N, act, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  if (rc == MBT_OK && epi == EPI_ARGMAX && launch_argmax_reduce(B, part, B, tiles, next_ids, err, s) != cudaSuccess)
+    rc = MBT_ERR_CUDA;
+  cudaFreeAsync(scratch, s);
   return rc;
 }
 

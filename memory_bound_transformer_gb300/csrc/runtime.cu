@@ -32,8 +32,10 @@ struct Layer {
 struct Plan {
   int R = 0, mbs = 0;
   int attn_bps = 0, attn_nsplit = 0;
-  int ns_qkv = 1, ns_o = 1, ns_down = 1;
-  int g_lm = 1;
+  int ns_qkv = 1, ns_o = 1, ns_down = 1;   // split-K counts of the residual-feeding projections
+  int g_lm = 1;                            // LM-head CTAs (arg-max partials per row)
+  bool use_tc = false;                     // tensor-core GEMMs (batch 16..128, BF16 weights)
+  int rp = 0;                              // rows padded to a multiple of 8 (tensor-core path)
   int kernels = 0;
 };
 
@@ -49,6 +51,8 @@ struct Workspace {
   float* delta = nullptr; float* delta2 = nullptr;   // O and down partials [splits][cap][H]
   float* act = nullptr; ArgmaxPart* lm_part = nullptr;
   int* tickets = nullptr;
+  int rp_cap = 0;                                    // tensor-core path: BF16 high/low rows
+  bf16* x_hl = nullptr; bf16* o_hl = nullptr; bf16* act_hl = nullptr;
 };
 
 struct Graph {
@@ -68,6 +72,8 @@ struct mbt_model {
   const bf16* embed = nullptr; const bf16* g_final = nullptr;
   const void* lm = nullptr; const float* s_lm = nullptr;
   std::vector<Layer> layers;
+  std::vector<TmaMap> wmaps;        // tensor maps of the BF16 weights: [layer][qkv, o, gu, down], lm head
+  bool tc_ok = false;
   float2* rope = nullptr;
   uint32_t* err = nullptr;
   Workspace ws;
@@ -105,6 +111,14 @@ size_t kv_layer_half_bytes(const mbt_model* m, int num_blocks) {
   return (size_t)(num_blocks + 1) * m->h.n_kv_heads * kBlockTokens * m->h.head_dim * esz;
 }
 
+int tc_ksplit(const mbt_model* m, int epi, int N, int K) {
+  const int tiles = tc_tiles(epi, N);
+  int ks = m->num_sms / tiles;
+  const int chunks = (K + 63) / 64;
+  if (ks > chunks / 4) ks = chunks / 4;        // at least 4 stages of K per split
+  return ks < 1 ? 1 : ks;
+}
+
 Plan make_plan(const mbt_model* m, int R, int mbs) {
   Plan p;
   p.R = R;
@@ -112,6 +126,18 @@ Plan make_plan(const mbt_model* m, int R, int mbs) {
   attn_plan(R, (int)m->h.n_kv_heads, mbs, m->num_sms, &p.attn_bps, &p.attn_nsplit);
   const int nb0 = std::min(R, 8);
   const int H = (int)m->h.hidden, Q = (int)(m->h.n_q_heads * m->h.head_dim), F = (int)m->h.ffn;
+  const int QKV = (int)((m->h.n_q_heads + 2 * m->h.n_kv_heads) * m->h.head_dim);
+  const int L = (int)m->h.n_layers;
+  p.use_tc = m->tc_ok && R >= 16 && R <= 128;
+  if (p.use_tc) {
+    p.rp = (R + 7) / 8 * 8;
+    p.ns_qkv = tc_ksplit(m, EPI_PARTIAL, QKV, H);
+    p.ns_o = tc_ksplit(m, EPI_PARTIAL, H, Q);
+    p.ns_down = tc_ksplit(m, EPI_PARTIAL, H, F);
+    p.g_lm = tc_tiles(EPI_ARGMAX, (int)m->h.vocab);
+    p.kernels = 1 + 7 * L + 3;
+    return p;
+  }
   p.ns_qkv = 1;                                          // norm prologue: whole rows per CTA
   p.ns_o = gemv_plan(EPI_PARTIAL, m->wtype, nb0, H, Q, m->num_sms, 0).nsplit;
   p.ns_down = gemv_plan(EPI_PARTIAL, m->wtype, nb0, H, F, m->num_sms, 0).nsplit;
@@ -119,7 +145,7 @@ Plan make_plan(const mbt_model* m, int R, int mbs) {
   p.g_lm = gemv_plan(EPI_ARGMAX, m->wtype, std::min(nb0, mn), (int)m->h.vocab, H, m->num_sms, 0, PRO_NORM).grid;
   const int c8 = (R + 7) / 8;
   const int cn = (R + mn - 1) / mn;                      // chunks of the norm-prologue projections
-  p.kernels = 1 + (int)m->h.n_layers * (2 * cn + 2 * c8 + 1) + cn + 1;
+  p.kernels = 1 + L * (2 * cn + 2 * c8 + 1) + cn + 1;
   return p;
 }
 
@@ -167,6 +193,10 @@ int ensure_ws(mbt_model* m, int R, int mbs) {
   const size_t o_a = take((size_t)cap * F * 4);
   const size_t o_lp = take((size_t)g_lm * cap * sizeof(ArgmaxPart));
   const size_t o_tk = take((size_t)cap * m->h.n_kv_heads * 4);
+  const int rp_cap = (cap + 7) / 8 * 8;
+  const size_t b_xhl = (size_t)2 * rp_cap * H * 2, b_ohl = (size_t)2 * rp_cap * Q * 2;
+  const size_t b_ahl = (size_t)2 * rp_cap * F * 2;
+  const size_t o_xhl = take(b_xhl), o_ohl = take(b_ohl), o_ahl = take(b_ahl);
   void* mem = nullptr;
   if (cudaMalloc(&mem, off) != cudaSuccess) { cudaGetLastError(); return MBT_ERR_OOM; }
   char* base = (char*)mem;
@@ -179,8 +209,11 @@ int ensure_ws(mbt_model* m, int R, int mbs) {
   w.act = (float*)(base + o_a);
   w.lm_part = (ArgmaxPart*)(base + o_lp);
   w.tickets = (int*)(base + o_tk);
-  // attention tickets start at zero; every launch leaves them at zero
-  if (cudaMemset(w.tickets, 0, (size_t)cap * m->h.n_kv_heads * 4) != cudaSuccess) return MBT_ERR_CUDA;
+  w.rp_cap = rp_cap;
+  w.x_hl = (bf16*)(base + o_xhl); w.o_hl = (bf16*)(base + o_ohl); w.act_hl = (bf16*)(base + o_ahl);
+  // attention tickets start at zero and every launch leaves them at zero; the
+  // high/low activation rows start at zero so padding rows never hold NaN bits
+  if (cudaMemset(mem, 0, off) != cudaSuccess) return MBT_ERR_CUDA;
   return MBT_OK;
 }
 
@@ -225,6 +258,66 @@ cudaError_t gemv_rows(const mbt_model* m, int epi, const NormIn* nin, const void
   return cudaSuccess;
 }
 
+// Layers, final norm and LM head at batch 16..128 on the tensor cores: each
+// projection reads BF16 high/low activation rows written by its producer
+// (residual add + RMSNorm, attention, the gate/up GEMM's SwiGLU epilogue).
+int run_layers_tc(mbt_model* m, mbt_kv* kv, const Plan& p, const int* pos, const int* bt, int bt_stride,
+                  const int* sl, int* next_ids, float* logits, cudaStream_t s) {
+  const Workspace& w = m->ws;
+  const int R = p.R, Rp = p.rp;
+  const int H = (int)m->h.hidden, d = (int)m->h.head_dim;
+  const int nq = (int)m->h.n_q_heads, nkv = (int)m->h.n_kv_heads;
+  const int Q = nq * d, F = (int)m->h.ffn, V = (int)m->h.vocab;
+  const int QKV = (nq + 2 * nkv) * d;
+  const size_t half = kv_layer_half_bytes(m, kv->num_blocks);
+  const long long rh = (long long)R * H;
+  TmaMap xh, xq, xf;
+  MBT_CUDA(tc_make_map(&xh, w.x_hl, 2 * Rp, H, 2 * Rp));
+  MBT_CUDA(tc_make_map(&xq, w.o_hl, 2 * Rp, Q, 2 * Rp));
+  MBT_CUDA(tc_make_map(&xf, w.act_hl, 2 * Rp, F, 2 * Rp));
+  auto norm = [&](const float* delta, int n_delta, const bf16* gamma) {
+    AddNormArgs an{R, H, w.r, delta, n_delta, rh, gamma, m->h.eps, nullptr, w.x_hl, Rp};
+    return launch_add_rmsnorm(an, s);
+  };
+  auto partial = [&](const TmaMap& wm, const TmaMap& xm, const float* sc, int N, int K, float* out, int ks) {
+    TcArgs a = {};
+    a.N = N; a.K = K; a.R = R; a.Rp = Rp; a.scale = sc;
+    a.out = out; a.split_stride = (long long)R * N; a.ldo = N; a.err = m->err;
+    return tc_launch(EPI_PARTIAL, &wm, &xm, a, ks, s);
+  };
+  for (int l = 0; l < (int)m->h.n_layers; ++l) {
+    const Layer& L = m->layers[l];
+    const TmaMap* wm = &m->wmaps[(size_t)l * 4];
+    char* kbase = (char*)kv->pool + 2 * half * (size_t)l;
+    MBT_CUDA(norm(l ? w.delta2 : nullptr, l ? p.ns_down : 0, L.g_attn));
+    MBT_CUDA(partial(wm[0], xh, L.s_qkv, QKV, H, w.qkv, p.ns_qkv));
+    AttnArgs at = {};
+    at.B = R; at.nq = nq; at.nkv = nkv; at.d = d;
+    at.qkv = w.qkv; at.qkv_nsplit = p.ns_qkv; at.qkv_split_stride = (long long)R * QKV; at.ld_qkv = QKV;
+    at.positions = pos; at.rope = m->rope; at.max_pos = (int)m->h.max_pos;
+    at.kpool = kbase; at.vpool = kbase + half; at.kv_fp8 = m->kv8;
+    at.k_scale = kv->k_scale[l]; at.v_scale = kv->v_scale[l];
+    at.bt = bt; at.bt_stride = bt_stride; at.seq_lens = sl; at.num_blocks = kv->num_blocks;
+    at.bps = p.attn_bps; at.nsplit = p.attn_nsplit;
+    at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = nullptr; at.tickets = w.tickets; at.err = m->err;
+    at.out_hl = w.o_hl; at.rp_hl = Rp;
+    MBT_CUDA(launch_attention(at, s));
+    MBT_CUDA(partial(wm[1], xq, L.s_o, H, Q, w.delta, p.ns_o));
+    MBT_CUDA(norm(w.delta, p.ns_o, L.g_ffn));
+    TcArgs g = {};
+    g.N = F; g.K = H; g.R = R; g.Rp = Rp; g.scale = L.s_gu; g.act_hl = w.act_hl; g.ld_act = F; g.err = m->err;
+    MBT_CUDA(tc_launch(EPI_SWIGLU, &wm[2], &xh, g, 1, s));
+    MBT_CUDA(partial(wm[3], xf, L.s_down, H, F, w.delta2, p.ns_down));
+  }
+  MBT_CUDA(norm(w.delta2, p.ns_down, m->g_final));
+  TcArgs a = {};
+  a.N = V; a.K = H; a.R = R; a.Rp = Rp; a.scale = m->s_lm; a.logits = logits; a.ldl = V;
+  a.part = w.lm_part; a.part_ld = R; a.err = m->err;
+  MBT_CUDA(tc_launch(EPI_ARGMAX, &m->wmaps[(size_t)m->h.n_layers * 4], &xh, a, 1, s));
+  MBT_CUDA(launch_argmax_reduce(R, w.lm_part, R, p.g_lm, next_ids, m->err, s));
+  return MBT_OK;
+}
+
 // The decode step over R rows whose inputs are already in device memory.
 // Per layer: QKV projection with the RMSNorm prologue, attention with RoPE +
 // KV write fused in, O projection, gate/up projection with the RMSNorm
@@ -245,6 +338,7 @@ int run_step(mbt_model* m, mbt_kv* kv, const Plan& p, const int* tok, const int*
 
   EmbedNormArgs en{R, H, V, tok, m->embed, w.r, m->layers[0].g_attn, m->h.eps, nullptr, m->err};
   MBT_CUDA(launch_embed_rmsnorm(en, s));
+  if (p.use_tc) return run_layers_tc(m, kv, p, pos, bt, bt_stride, sl, next_ids, logits, s);
   for (int l = 0; l < (int)m->h.n_layers; ++l) {
     const Layer& L = m->layers[l];
     char* kbase = (char*)kv->pool + 2 * half * (size_t)l;
@@ -462,6 +556,23 @@ int model_create(const void* blob, size_t bytes, int blob_is_device, void* strea
     L.w_down = at(MBT_T_W_DOWN, l); L.s_down = (const float*)at(MBT_T_S_DOWN, l);
     L.g_attn = (const bf16*)at(MBT_T_G_ATTN, l); L.g_ffn = (const bf16*)at(MBT_T_G_FFN, l);
   }
+  // tensor maps for the tensor-core path (BF16 weights; 64-row boxes)
+  if (m->wtype == W_BF16 && tc_init() == cudaSuccess) {
+    const int Hh = (int)h.hidden, Qd = (int)(h.n_q_heads * h.head_dim), Ff = (int)h.ffn;
+    const int QKVr = (int)((h.n_q_heads + 2 * h.n_kv_heads) * h.head_dim);
+    m->wmaps.resize((size_t)h.n_layers * 4 + 1);
+    bool ok = true;
+    for (int l = 0; l < (int)h.n_layers && ok; ++l) {
+      const Layer& L = m->layers[l];
+      ok = tc_make_map(&m->wmaps[l * 4 + 0], L.w_qkv, QKVr, Hh, 64) == cudaSuccess &&
+           tc_make_map(&m->wmaps[l * 4 + 1], L.w_o, Hh, Qd, 64) == cudaSuccess &&
+           tc_make_map(&m->wmaps[l * 4 + 2], L.w_gu, 2 * Ff, Hh, 64) == cudaSuccess &&
+           tc_make_map(&m->wmaps[l * 4 + 3], L.w_down, Hh, Ff, 64) == cudaSuccess;
+    }
+    ok = ok && tc_make_map(&m->wmaps[(size_t)h.n_layers * 4], m->lm, (int)h.vocab, Hh, 64) == cudaSuccess;
+    m->tc_ok = ok;
+  }
+  cudaGetLastError();
   *out = m;
   return MBT_OK;
 }

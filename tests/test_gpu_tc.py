@@ -1,0 +1,106 @@
+"""Tensor-core (tcgen05) projection through the C ABI (op_gemm_tc) against the
+oracle, and whole steps that run on it (batch 16..128, BF16 weights).
+
+The activations enter as BF16 high/low pairs (x = hi + lo with |x - hi - lo| <=
+2^-18 |x|), the MMAs accumulate in fp32, so the bound of the CUDA-core GEMV
+tests applies: |gpu - exact| <= 2e-5 * sum_k |w_k x_k| + 1e-7."""
+import numpy as np
+import pytest
+import torch
+
+from memory_bound_transformer_gb300 import capi
+from oracle.decode import OracleKV, decode_weight, silu
+from synth import ONE_B, ModelConfig, gen_tensor
+from tests.helpers import SMALL, oracle_weights
+from tests.test_gpu_step import Case, _run
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL_REL, TOL_ABS = 2e-5, 1e-7
+
+
+def _weights(rows, K, seed):
+    cfg = ModelConfig("op", 1, K, 1, 1, 64, 16, rows)
+    t = gen_tensor(cfg, seed, "lm_head", -1, device=DEV)
+    return t, {"w": t["w"].view(torch.int16).cpu().numpy().view(np.uint16)}
+
+
+def _x(B, K, seed, scale=1.0):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    return (torch.randn((B, K), generator=g) * scale).to(DEV)
+
+
+@pytest.mark.parametrize("B", [1, 16, 24, 64, 128])
+@pytest.mark.parametrize("N,K,ks", [(1000, 1040, 1), (1000, 1040, 3), (6144, 4096, 3), (200, 64, 1)])
+def test_tc_partial(cuda_lib, B, N, K, ks):
+    t, raw = _weights(N, K, seed=N + K)
+    x = _x(B, K, seed=B)
+    out = torch.full((ks, B, N), float("nan"), device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    capi.op_gemm_tc(capi.EPI_PARTIAL, t["w"], None, N, K, x, B, ks, out=out, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    got = out.double().sum(0).cpu().numpy()
+    W = decode_weight(raw)
+    xv = x.double().cpu().numpy()
+    ref = xv @ W.T
+    bound = TOL_REL * (np.abs(xv) @ np.abs(W).T) + TOL_ABS
+    assert np.all(np.abs(got - ref) <= bound)
+
+
+@pytest.mark.parametrize("B", [16, 40, 64])
+def test_tc_swiglu(cuda_lib, B):
+    F, K = 700, 512
+    t, raw = _weights(2 * F, K, seed=7)
+    x = _x(B, K, seed=3, scale=3.0)
+    act = torch.full((B, F), float("nan"), device=DEV)
+    capi.op_gemm_tc(capi.EPI_SWIGLU, t["w"], None, F, K, x, B, act=act)
+    torch.cuda.synchronize()
+    W = decode_weight(raw)
+    xv = x.double().cpu().numpy()
+    gu = xv @ W.T
+    bg = TOL_REL * (np.abs(xv) @ np.abs(W).T) + TOL_ABS
+    g, u = gu[:, :F], gu[:, F:]
+    ref = silu(g) * u
+    got = act.double().cpu().numpy()
+    # fp32 error of g and u, fp32 silu, and the high/low BF16 storage (2^-17)
+    bound = 1e-5 * np.abs(ref) + 1.1 * np.abs(u) * bg[:, :F] + np.abs(silu(g)) * bg[:, F:] + 1e-30
+    assert np.all(np.abs(got - ref) <= bound)
+
+
+@pytest.mark.parametrize("B", [16, 64])
+def test_tc_argmax(cuda_lib, B):
+    V, K = 3001, 512
+    t, raw = _weights(V, K, seed=11)
+    x = _x(B, K, seed=21, scale=2.0)
+    logits = torch.zeros((B, V), device=DEV)
+    ids = torch.full((B,), -1, dtype=torch.int32, device=DEV)
+    capi.op_gemm_tc(capi.EPI_ARGMAX, t["w"], None, V, K, x, B, logits=logits, next_ids=ids)
+    torch.cuda.synchronize()
+    lg = logits.double().cpu().numpy()
+    gid = ids.cpu().numpy()
+    assert np.array_equal(gid, np.argmax(lg, axis=1))
+    W = decode_weight(raw)
+    xv = x.double().cpu().numpy()
+    ref = xv @ W.T
+    bound = TOL_REL * (np.abs(xv) @ np.abs(W).T) + TOL_ABS
+    assert np.all(np.abs(lg - ref) <= bound)
+
+
+@pytest.mark.parametrize("B", [16, 24, 40])
+def test_small_model_tensor_core_step(cuda_lib, B):
+    cfg = SMALL
+    rng = np.random.default_rng(B)
+    case = Case(cfg, 55 + B, B, rng.integers(0, 200, size=B), 2, ladder=[8, 16, 24, 40], graph=True)
+    assert case.eng.stats(B)[1]
+    okv = OracleKV(case.pool0.copy(), np.ones(cfg.n_layers), np.ones(cfg.n_layers))
+    _run(case, oracle_weights(case.model), okv, 2)
+
+
+def test_1b_batch64(cuda_lib):
+    """1B-class decoder at batch 64 on the tensor cores, graph replay."""
+    cfg = ONE_B
+    rng = np.random.default_rng(64)
+    case = Case(cfg, 1236, 64, rng.integers(100, 600, size=64), 1, ladder=[64], graph=True)
+    okv = OracleKV(case.pool0.copy(), np.ones(cfg.n_layers), np.ones(cfg.n_layers))
+    _run(case, oracle_weights(case.model), okv, 1)
