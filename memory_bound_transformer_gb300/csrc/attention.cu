@@ -22,7 +22,6 @@ namespace mbt {
 
 constexpr int kAttnThreads = 128;
 constexpr int kAttnTile = 64;      // tokens per shared-memory tile (4 blocks)
-constexpr int kMaxGroup = 16;      // query heads per KV head
 
 __device__ __forceinline__ void cp_async16(void* s, const void* g) {
   const unsigned sa = (unsigned)__cvta_generic_to_shared(s);
@@ -35,25 +34,21 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 template <int D, int KV8>
 struct AttnShape {
   static constexpr int ESZ = KV8 ? 1 : 2;
-  static constexpr int ROWB = D * ESZ;               // bytes of one token's K (or V) for one head
-  static constexpr int NCH = ROWB / 16;              // 16-byte chunks per row
-  static constexpr int EPC = 16 / ESZ;               // elements per chunk
-  static constexpr int SWZ = NCH >= 8 ? 7 : NCH - 1; // XOR swizzle of K chunks (bank spread)
-  static constexpr int DC = D / 4;                   // 4-element output chunks per head
-  static constexpr int HL = kAttnThreads / DC;       // head lanes in the PV phase
-  static constexpr int HPT_PV = (kMaxGroup + HL - 1) / HL;
-  static constexpr int HPT_QK = kMaxGroup / 2;
-  static constexpr size_t SMEM = (size_t)kMaxGroup * D * 4 + 4 * (size_t)kAttnTile * ROWB +
-                                 (size_t)kMaxGroup * kAttnTile * 4 + 3 * kMaxGroup * 4;
+  static constexpr int ROWB = D * ESZ;               // bytes of one token's K (or V) for one head in the cache
+  static constexpr int NCH = ROWB / 16;              // 16-byte chunks per cache row
+  static constexpr int BROWB = D * 2;                // bytes per token row of a BF16 compute tile
+  static constexpr int BNCH = BROWB / 16;            // 16-byte chunks per BF16 row (8 or 16)
+  static constexpr int KSTEPS = D / 16;              // MMA k-steps over d for Q K^T
+  static constexpr int DT = D / 8;                   // 8-wide d tiles of the output
+  static constexpr size_t Q_BYTES = (size_t)16 * D * 4;
+  static constexpr size_t T_BYTES = (size_t)kAttnTile * BROWB;
+  static constexpr size_t R_BYTES = (size_t)kAttnTile * ROWB;
+  static constexpr size_t SMEM = Q_BYTES + 4 * T_BYTES + (KV8 ? 4 * R_BYTES : 0);
 };
 
+// 16 e4m3 codes -> 16 floats, exactly.
 template <int KV8>
 __device__ __forceinline__ void chunk_to_float(const uint4& c, float* f);
-template <>
-__device__ __forceinline__ void chunk_to_float<0>(const uint4& c, float* f) {
-  f[0] = bf16_lo(c.x); f[1] = bf16_hi(c.x); f[2] = bf16_lo(c.y); f[3] = bf16_hi(c.y);
-  f[4] = bf16_lo(c.z); f[5] = bf16_hi(c.z); f[6] = bf16_lo(c.w); f[7] = bf16_hi(c.w);
-}
 template <>
 __device__ __forceinline__ void chunk_to_float<1>(const uint4& c, float* f) {
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
@@ -64,20 +59,50 @@ __device__ __forceinline__ void chunk_to_float<1>(const uint4& c, float* f) {
   }
 }
 
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return a | (b << 16);
+}
+// x = hi + lo: the BF16 high part and the BF16 rounding of the remainder.
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+  hi = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+  lo = pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+// D += A (16x16 BF16, row) * B (16x8 BF16, col), fp32 accumulate.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // One split of one (row, KV head): stream its KV blocks once for all query
 // heads of the group and leave (unnormalised o, running max m, sum l) per head.
+// The group's query heads are the 16 rows of the MMA tiles (padded with zero
+// rows); each warp takes 16 tokens of every 64-token tile: S = Q K^T and
+// O += P V on the tensor cores with Q and P split into BF16 high + low parts
+// (fp32-level accuracy), the online softmax in registers, and the four warps'
+// states merged at the end.
 template <int D, int KV8>
 __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, int b, int h, int sp,
                                        int G, size_t head0, int seq, int blk0, int blk1) {
   using S = AttnShape<D, KV8>;
-  float* qs = reinterpret_cast<float*>(smem);                        // [group][D]
-  unsigned char* kt = smem + (size_t)kMaxGroup * D * 4;               // [2][tile][ROWB] swizzled
-  unsigned char* vt = kt + 2 * (size_t)kAttnTile * S::ROWB;           // [2][tile][ROWB]
-  float* sc = reinterpret_cast<float*>(vt + 2 * (size_t)kAttnTile * S::ROWB);   // [group][tile]
-  float* st_m = sc + kMaxGroup * kAttnTile;
-  float* st_l = st_m + kMaxGroup;
-  float* st_a = st_l + kMaxGroup;
+  float* qs = reinterpret_cast<float*>(smem);                        // [16][D], rows >= G are zero
+  unsigned char* kbf = smem + S::Q_BYTES;                             // [2][tile][BROWB] BF16, swizzled
+  unsigned char* vbf = kbf + 2 * S::T_BYTES;
+  unsigned char* raw = vbf + 2 * S::T_BYTES;                          // e4m3 caches: [2][K|V][tile][ROWB]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t4 = lane & 3;
 
   // queries of the group, pre-scaled into the log2 domain with the K dequant scale
   const float qscale = 1.4426950408889634f / sqrtf((float)D) * a.k_scale;
@@ -90,20 +115,20 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
     const float* src = a.qkv + (size_t)b * a.ld_qkv + (size_t)h * G * D;
     const float2* cs = a.rope + (size_t)pos * half;
     for (int e = tid; e < G * half; e += kAttnThreads) {
-      const int g = e / half, i = e - g * half;
+      const int gg = e / half, i = e - gg * half;
       float x1 = 0.f, x2 = 0.f;
       for (int s2 = 0; s2 < a.qkv_nsplit; ++s2) {
-        x1 += src[(size_t)s2 * a.qkv_split_stride + g * D + i];
-        x2 += src[(size_t)s2 * a.qkv_split_stride + g * D + i + half];
+        x1 += src[(size_t)s2 * a.qkv_split_stride + gg * D + i];
+        x2 += src[(size_t)s2 * a.qkv_split_stride + gg * D + i + half];
       }
       const float2 t = cs[i];
-      qs[g * D + i] = (x1 * t.x - x2 * t.y) * qscale;
-      qs[g * D + i + half] = (x2 * t.x + x1 * t.y) * qscale;
+      qs[gg * D + i] = (x1 * t.x - x2 * t.y) * qscale;
+      qs[gg * D + i + half] = (x2 * t.x + x1 * t.y) * qscale;
     }
   } else {
     for (int i = tid; i < G * D; i += kAttnThreads) qs[i] = a.q[head0 * D + i] * qscale;
   }
-  if (tid < G) { st_m[tid] = -INFINITY; st_l[tid] = 0.f; }
+  for (int i = G * D + tid; i < 16 * D; i += kAttnThreads) qs[i] = 0.f;
 
   const unsigned char* kpool = reinterpret_cast<const unsigned char*>(a.kpool);
   const unsigned char* vpool = reinterpret_cast<const unsigned char*>(a.vpool);
@@ -115,8 +140,8 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
   auto load_tile = [&](int t, int buf) {
     const int tok0 = tok_begin + t * kAttnTile;
     const int rows = min(kAttnTile, tok_end_blk - tok0);
-    unsigned char* kd = kt + (size_t)buf * kAttnTile * S::ROWB;
-    unsigned char* vd = vt + (size_t)buf * kAttnTile * S::ROWB;
+    unsigned char* kd = KV8 ? raw + (size_t)buf * 2 * S::R_BYTES : kbf + (size_t)buf * S::T_BYTES;
+    unsigned char* vd = KV8 ? kd + S::R_BYTES : vbf + (size_t)buf * S::T_BYTES;
     for (int i = tid; i < rows * S::NCH; i += kAttnThreads) {
       const int row = i / S::NCH, ch = i - row * S::NCH;
       const int tok = tok0 + row;
@@ -126,20 +151,31 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
         blk = a.num_blocks;
       }
       const size_t off = (((size_t)blk * a.nkv + h) * kBlockTokens + (tok % kBlockTokens)) * S::ROWB + ch * 16;
-      cp_async16(kd + row * S::ROWB + ((ch ^ (row & S::SWZ)) * 16), kpool + off);
-      cp_async16(vd + row * S::ROWB + ch * 16, vpool + off);
+      const int sch = KV8 ? ch : (ch ^ (row & 7));                   // BF16 tiles are swizzled in place
+      cp_async16(kd + row * S::ROWB + sch * 16, kpool + off);
+      cp_async16(vd + row * S::ROWB + sch * 16, vpool + off);
     }
     cp_async_commit();
   };
 
-  float o[S::HPT_PV][4];
-#pragma unroll
-  for (int j = 0; j < S::HPT_PV; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[j][e] = 0.f;
-  const int dc = tid % S::DC, hl = tid / S::DC;
-
   load_tile(0, 0);
+  __syncthreads();                                                    // qs complete
+
+  // Q fragments (A operand, rows = query heads, k = d), high and low parts
+  uint32_t qh[S::KSTEPS][4], ql[S::KSTEPS][4];
+#pragma unroll
+  for (int kk = 0; kk < S::KSTEPS; ++kk)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int row = g + (r & 1) * 8, col = 16 * kk + 2 * t4 + (r >> 1) * 8;
+      split_bf16(qs[row * D + col], qs[row * D + col + 1], qh[kk][r], ql[kk][r]);
+    }
+
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;          // rows g and g + 8
+  float o[S::DT][4];
+#pragma unroll
+  for (int i = 0; i < S::DT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
   for (int t = 0; t < ntiles; ++t) {
     const int buf = t & 1;
     if (t + 1 < ntiles) { load_tile(t + 1, buf ^ 1); cp_async_wait<1>(); }
@@ -147,101 +183,148 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
     __syncthreads();
     const int tok0 = tok_begin + t * kAttnTile;
     const int nvalid = min(kAttnTile, min(seq, tok_end_blk) - tok0);   // this split's tokens only
-
-    // scores: thread = (token, head parity)
-    {
-      const int tt = tid & (kAttnTile - 1), hp = tid >> 6;
-      float s[S::HPT_QK];
-#pragma unroll
-      for (int j = 0; j < S::HPT_QK; ++j) s[j] = 0.f;
-      const unsigned char* krow = kt + (size_t)buf * kAttnTile * S::ROWB + tt * S::ROWB;
-#pragma unroll 4
-      for (int ch = 0; ch < S::NCH; ++ch) {
-        const uint4 kc = *reinterpret_cast<const uint4*>(krow + ((ch ^ (tt & S::SWZ)) * 16));
-        float kf[S::EPC];
-        chunk_to_float<KV8>(kc, kf);
-#pragma unroll
-        for (int j = 0; j < S::HPT_QK; ++j) {
-          const int g = hp + 2 * j;
-          if (g < G) {
-            const float* qg = qs + g * D + ch * S::EPC;
-#pragma unroll
-            for (int e = 0; e < S::EPC; ++e) s[j] = fmaf(qg[e], kf[e], s[j]);
-          }
+    unsigned char* kt = kbf + (size_t)buf * S::T_BYTES;
+    unsigned char* vt = vbf + (size_t)buf * S::T_BYTES;
+    if (KV8) {
+      // widen the e4m3 tile to BF16 (exact), swizzled; rows past the context are zero
+      const unsigned char* rk = raw + (size_t)buf * 2 * S::R_BYTES;
+      for (int i = tid; i < 2 * kAttnTile * S::NCH; i += kAttnThreads) {
+        const int which = i / (kAttnTile * S::NCH), j = i - which * kAttnTile * S::NCH;
+        const int row = j / S::NCH, ch = j - row * S::NCH;
+        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+        if (row < nvalid) {
+          const uint4 c = *reinterpret_cast<const uint4*>(rk + which * S::R_BYTES + row * S::ROWB + ch * 16);
+          float f[16];
+          chunk_to_float<1>(c, f);
+          lo = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+          hi = make_uint4(pack_bf16(f[8], f[9]), pack_bf16(f[10], f[11]), pack_bf16(f[12], f[13]), pack_bf16(f[14], f[15]));
         }
+        unsigned char* dst = (which ? vt : kt) + row * S::BROWB;
+        *reinterpret_cast<uint4*>(dst + (((2 * ch) ^ (row & 7)) * 16)) = lo;
+        *reinterpret_cast<uint4*>(dst + (((2 * ch + 1) ^ (row & 7)) * 16)) = hi;
       }
-#pragma unroll
-      for (int j = 0; j < S::HPT_QK; ++j) {
-        const int g = hp + 2 * j;
-        if (g < G) sc[g * kAttnTile + tt] = tt < nvalid ? s[j] : -INFINITY;
+      __syncthreads();
+    } else if (nvalid < kAttnTile) {
+      // rows past the context hold whatever the pool had: zero V so that P = 0 stays 0
+      for (int i = tid; i < (kAttnTile - nvalid) * S::BNCH; i += kAttnThreads) {
+        const int row = nvalid + i / S::BNCH, ch = i % S::BNCH;
+        *reinterpret_cast<uint4*>(vt + row * S::BROWB + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
+      __syncthreads();
     }
-    __syncthreads();
 
-    // online softmax statistics, one warp per head
-    for (int g = warp; g < G; g += kAttnThreads / 32) {
-      const float v0 = sc[g * kAttnTile + lane], v1 = sc[g * kAttnTile + lane + 32];
-      const float mx = warp_max(fmaxf(v0, v1));
-      const float m_old = st_m[g];
-      const float m_new = fmaxf(m_old, mx);
-      const float p0 = exp2f(v0 - m_new), p1 = exp2f(v1 - m_new);
-      sc[g * kAttnTile + lane] = p0;
-      sc[g * kAttnTile + lane + 32] = p1;
-      const float ps = warp_sum(p0 + p1);
-      if (lane == 0) {
-        const float al = exp2f(m_old - m_new);
-        st_a[g] = al;
-        st_l[g] = st_l[g] * al + ps;
-        st_m[g] = m_new;
-      }
-    }
-    __syncthreads();
-
-    // o <- o * alpha + P V: thread = (4-element chunk of d, head lane)
-    {
+    const int n0 = 16 * warp;                                         // this warp's tokens in the tile
+    if (n0 < nvalid) {
+      const uint32_t kbase = (uint32_t)__cvta_generic_to_shared(kt);
+      const uint32_t vbase = (uint32_t)__cvta_generic_to_shared(vt);
+      const int lm = lane >> 3, lr = lane & 7;
+      // S = Q K^T over 16 tokens (two 8-token n-tiles)
+      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int krow = n0 + (lm >> 1) * 8 + lr;
 #pragma unroll
-      for (int j = 0; j < S::HPT_PV; ++j) {
-        const int g = hl + S::HL * j;
-        if (g < G) {
-          const float al = st_a[g];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o[j][e] *= al;
+        for (int kk = 0; kk < S::KSTEPS; ++kk) {
+          uint32_t kf[4];
+          const int ch = 2 * kk + (lm & 1);
+          ldsm_x4(kbase + krow * S::BROWB + ((ch ^ (krow & 7)) * 16), kf);
+          mma16816(sacc[0], qh[kk], kf[0], kf[1]);
+          mma16816(sacc[0], ql[kk], kf[0], kf[1]);
+          mma16816(sacc[1], qh[kk], kf[2], kf[3]);
+          mma16816(sacc[1], ql[kk], kf[2], kf[3]);
         }
       }
-      const unsigned char* vb = vt + (size_t)buf * kAttnTile * S::ROWB + dc * 4 * S::ESZ;
-      for (int tt = 0; tt < nvalid; ++tt) {
-        float vf[4];
-        if (KV8) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(vb + tt * S::ROWB);
-          const float2 x = e4m3x2_to_float2(w), y = e4m3x2_to_float2(w >> 16);
-          vf[0] = x.x; vf[1] = x.y; vf[2] = y.x; vf[3] = y.y;
-        } else {
-          const uint2 w = *reinterpret_cast<const uint2*>(vb + tt * S::ROWB);
-          vf[0] = bf16_lo(w.x); vf[1] = bf16_hi(w.x); vf[2] = bf16_lo(w.y); vf[3] = bf16_hi(w.y);
-        }
+      // mask, online softmax per query-head row (quad of lanes holds a row)
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < S::HPT_PV; ++j) {
-          const int g = hl + S::HL * j;
-          if (g < G) {
-            const float p = sc[g * kAttnTile + tt];
+      for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[j][e] = fmaf(p, vf[e], o[j][e]);
-          }
+        for (int c = 0; c < 4; ++c) {
+          const int tok = n0 + 8 * j + 2 * t4 + (c & 1);
+          if (tok >= nvalid) sacc[j][c] = -INFINITY;
+          if (c < 2) mx0 = fmaxf(mx0, sacc[j][c]); else mx1 = fmaxf(mx1, sacc[j][c]);
         }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float p = exp2f(sacc[j][c] - (c < 2 ? mu0 : mu1));
+          sacc[j][c] = p;
+          if (c < 2) ps0 += p; else ps1 += p;
+        }
+      ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
+      ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
+      ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
+      ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
+      l0 = l0 * al0 + ps0;
+      l1 = l1 * al1 + ps1;
+      m0 = mn0;
+      m1 = mn1;
+#pragma unroll
+      for (int i = 0; i < S::DT; ++i) { o[i][0] *= al0; o[i][1] *= al0; o[i][2] *= al1; o[i][3] *= al1; }
+      // P as the A operand (rows = heads, k = the 16 tokens), high and low parts
+      uint32_t ph[4], pl[4];
+      split_bf16(sacc[0][0], sacc[0][1], ph[0], pl[0]);
+      split_bf16(sacc[0][2], sacc[0][3], ph[1], pl[1]);
+      split_bf16(sacc[1][0], sacc[1][1], ph[2], pl[2]);
+      split_bf16(sacc[1][2], sacc[1][3], ph[3], pl[3]);
+      // O += P V (V fragments transposed out of the swizzled tile)
+      const int vrow = n0 + (lm & 1) * 8 + lr;
+#pragma unroll
+      for (int dp = 0; dp < S::DT / 2; ++dp) {
+        uint32_t vf[4];
+        const int ch = 2 * dp + (lm >> 1);
+        ldsm_x4_t(vbase + vrow * S::BROWB + ((ch ^ (vrow & 7)) * 16), vf);
+        mma16816(o[2 * dp], ph, vf[0], vf[1]);
+        mma16816(o[2 * dp], pl, vf[0], vf[1]);
+        mma16816(o[2 * dp + 1], ph, vf[2], vf[3]);
+        mma16816(o[2 * dp + 1], pl, vf[2], vf[3]);
       }
     }
     __syncthreads();
   }
 
-#pragma unroll
-  for (int j = 0; j < S::HPT_PV; ++j) {
-    const int g = hl + S::HL * j;
-    if (g < G) {
-      float4 v = make_float4(o[j][0], o[j][1], o[j][2], o[j][3]);
-      *reinterpret_cast<float4*>(a.part_o + ((head0 + g) * a.nsplit + sp) * D + dc * 4) = v;
-    }
+  // merge the four warps' (m, l, o) per head row and write this split's partial
+  float* sm_m = reinterpret_cast<float*>(kbf);                        // [4][16]
+  float* sm_l = sm_m + 4 * 16;
+  float* sm_o = sm_l + 4 * 16;                                        // [4][16][D]
+  if (t4 == 0) {
+    sm_m[warp * 16 + g] = m0; sm_m[warp * 16 + g + 8] = m1;
+    sm_l[warp * 16 + g] = l0; sm_l[warp * 16 + g + 8] = l1;
   }
-  if (tid < G) a.part_ml[(head0 + tid) * a.nsplit + sp] = make_float2(st_m[tid], st_l[tid]);
+#pragma unroll
+  for (int i = 0; i < S::DT; ++i) {
+    const int d0 = 8 * i + 2 * t4;
+    sm_o[(warp * 16 + g) * D + d0] = o[i][0];
+    sm_o[(warp * 16 + g) * D + d0 + 1] = o[i][1];
+    sm_o[(warp * 16 + g + 8) * D + d0] = o[i][2];
+    sm_o[(warp * 16 + g + 8) * D + d0 + 1] = o[i][3];
+  }
+  __syncthreads();
+  for (int e = tid; e < G * D; e += kAttnThreads) {
+    const int hr = e / D, d = e - hr * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) if (sm_l[w * 16 + hr] > 0.f) M = fmaxf(M, sm_m[w * 16 + hr]);
+    float L = 0.f, acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      if (sm_l[w * 16 + hr] > 0.f) {
+        const float sc = exp2f(sm_m[w * 16 + hr] - M);
+        L += sm_l[w * 16 + hr] * sc;
+        acc += sm_o[(w * 16 + hr) * D + d] * sc;
+      }
+    }
+    a.part_o[((head0 + hr) * a.nsplit + sp) * D + d] = acc;
+    if (d == 0) a.part_ml[(head0 + hr) * a.nsplit + sp] = make_float2(L > 0.f ? M : -INFINITY, L);
+  }
 }
 
 // Merge the splits of the group's G query heads: rescale each partial to the
