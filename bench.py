@@ -40,7 +40,7 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the gate/up GEMV
 # (8B shape, batch 1) from the ncu capture summarised in
 # profiles/gemv_swiglu_8b_b1.md; None until that capture matches this kernel.
-GEMV_TRAFFIC_BYTES = None
+GEMV_TRAFFIC_BYTES = 237759488      # 234.93 MB read + 2.82 MB written (first captured launch)
 
 
 def parse():
