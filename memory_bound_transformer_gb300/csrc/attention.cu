@@ -471,9 +471,11 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_split_kernel(const AttnA
 
 
 void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nsplit) {
-  // Enough CTAs to cover the SMs, but at least two 64-token tiles per split so
-  // that the double buffer overlaps loads with math and the merge stays short.
-  const int target = num_sms;
+  // About four CTAs per SM so that rows with long contexts do not form the
+  // tail (contexts in one batch differ by up to 8x), but at least two 64-token
+  // tiles per split so that the double buffer overlaps loads with math and
+  // the merge stays short.
+  const int target = 4 * num_sms;
   const int pairs = B * nkv;
   int want = (target + pairs - 1) / pairs;
   if (want < 1) want = 1;

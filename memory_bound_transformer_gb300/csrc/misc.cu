@@ -149,8 +149,10 @@ __global__ void __launch_bounds__(1024) add_rmsnorm_kernel(const AddNormArgs a) 
     norm_store(v, ss, a.H, a.gamma, a.eps, a.y + (size_t)b * a.H, scratch);
 }
 
+// One float4 per thread where the row allows it, so a CTA has the whole row
+// (and its split-K partials) in flight at once.
 static int norm_threads(int H) {
-  int t = (H / 4 + kNormMaxV - 1) / kNormMaxV;
+  int t = H / 4;
   t = ((t + 31) / 32) * 32;
   if (t < 128) t = 128;
   if (t > 1024) t = 1024;

@@ -113,7 +113,7 @@ size_t kv_layer_half_bytes(const mbt_model* m, int num_blocks) {
 
 int tc_ksplit(const mbt_model* m, int epi, int N, int K) {
   const int tiles = tc_tiles(epi, N);
-  int ks = m->num_sms / tiles;
+  int ks = 2 * m->num_sms / tiles;             // two CTAs per SM
   const int chunks = (K + 63) / 64;
   if (ks > chunks / 4) ks = chunks / 4;        // at least 4 stages of K per split
   return ks < 1 ? 1 : ks;
@@ -165,7 +165,7 @@ int ensure_ws(mbt_model* m, int R, int mbs) {
     Plan p = make_plan(m, r, mbs_cap);
     // attn_plan never uses more splits than this, whatever the table width
     const int pairs = r * (int)m->h.n_kv_heads;
-    const int split_bound = std::max(1, (2 * m->num_sms + pairs - 1) / pairs);
+    const int split_bound = std::max(1, (4 * m->num_sms + pairs - 1) / pairs);
     pml = std::max(pml, (size_t)r * m->h.n_q_heads * split_bound);
     ns_qkv = std::max(ns_qkv, p.ns_qkv);
     ns_delta = std::max({ns_delta, p.ns_o, p.ns_down});

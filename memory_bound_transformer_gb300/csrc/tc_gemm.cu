@@ -11,7 +11,7 @@
 //     along N, so one MMA with N = 2 * rows keeps near-fp32 accuracy while the
 //     weights are read once;
 //   * TMA moves 128-byte-swizzled K-major tiles of both operands into a
-//     4-stage shared-memory ring; one thread issues the TMA copies, one thread
+//     3-stage shared-memory ring (two CTAs per SM); one thread issues the TMA copies, one thread
 //     issues the MMAs into a TMEM accumulator, mbarriers hand stages back and
 //     forth (every wait is bounded: on a timeout the kernel flags the error
 //     word, frees its TMEM and returns);
@@ -28,7 +28,7 @@ namespace mbt {
 constexpr int kTcThreads = 128;
 constexpr int kTcBM = 128;              // weight rows per tile (MMA M)
 constexpr int kTcBK = 64;               // K elements per stage: one 128-byte swizzle row of BF16
-constexpr int kTcStages = 4;
+constexpr int kTcStages = 3;            // 3 x 32 KB at 64 rows: two CTAs fit an SM
 constexpr long long kTcWaitCycles = 4000000000LL;   // about 2 s at GB300 clocks
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -104,7 +104,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
 }
 
 template <int EPI>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const TcArgs a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
