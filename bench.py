@@ -55,8 +55,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kernel-timing", action="store_true")
     ap.add_argument("--ladder", default=None, help="comma-separated graph ladder (default: the workload's)")
-    ap.add_argument("--kernel-only", action="store_true",
-                    help="time only the dominant kernel (gate/up GEMV) over 4 layers' matrices; for profiling")
+    ap.add_argument("--context", default=None,
+                    help="LO,HI: per-sequence context range instead of the workload's (context sweeps)")
+    ap.add_argument("--kernel-only", nargs="?", const="gemv", default=None, choices=["gemv", "attention"],
+                    help="time one kernel alone for profiling: the gate/up GEMV over 4 layers' matrices, "
+                         "or one layer's paged attention at the workload's contexts")
     return ap.parse_args()
 
 
@@ -115,9 +118,10 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def build_case(wl, B, steps_total, device="cuda"):
+def build_case(wl, B, steps_total, device="cuda", context=None):
     cfg = wl.model
-    ctx = random_contexts(B, wl.context[0], wl.context[1], wl.seed + 2000)
+    lo, hi = context or wl.context
+    ctx = random_contexts(B, lo, hi, wl.seed + 2000)
     cap = ctx + steps_total + 1
     nb = int(sum(-(-int(c) // 16) for c in cap)) + 1
     tables = seeded_block_tables(cap, 16, nb, wl.seed + 3000)
@@ -131,6 +135,19 @@ def build_case(wl, B, steps_total, device="cuda"):
     eng.pool().copy_(pool.view(torch.uint8).reshape(-1))
     del pool
     return cfg, ctx, tables, nb, eng
+
+
+def job_rate(local_ms: float, local_tokens: int, world: int, device=None):
+    """Whole-job throughput of N replicas: the tokens of all ranks over the
+    slowest rank's time (replicas share nothing, so the job ends with the last
+    one). Returns (tokens/s, max ms, total tokens); collective only for N > 1."""
+    if world == 1:
+        return local_tokens / (local_ms / 1e3), local_ms, local_tokens
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    n = torch.tensor([float(local_tokens)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(n, op=torch.distributed.ReduceOp.SUM)
+    return n.item() / (t.item() / 1e3), t.item(), int(n.item())
 
 
 def timed_steps(eng, cfg, ctx, tables, B, K, W, dev, world, clocks_on):
@@ -166,14 +183,10 @@ def timed_steps(eng, cfg, ctx, tables, B, K, W, dev, world, clocks_on):
         torch.distributed.barrier()
     ck = clocks.stop() if clocks else None
     per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(K)]
-    total_ms = ev[0].elapsed_time(ev[K])
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    rate, total_ms, _ = job_rate(ev[0].elapsed_time(ev[K]), B * K, world, dev)
     byte_steps = [ledger.step_bytes(cfg, ctx[:B] + W + t + 1) for t in range(K)]
     kps, graph = eng.stats(B)
-    return dict(B=B, total_ms=total_ms, per_step=per_step, avg_bytes=float(np.mean(byte_steps)),
+    return dict(B=B, total_ms=total_ms, rate=rate, per_step=per_step, avg_bytes=float(np.mean(byte_steps)),
                 clocks=ck, kernels_per_step=kps, uses_graph=graph)
 
 
@@ -183,7 +196,8 @@ def time_native(args, rank, world):
     Bmax = max(batches)
     K, W = args.steps, args.warmup
     dev = torch.device("cuda", torch.cuda.current_device())
-    cfg, ctx, tables, nb, eng = build_case(wl, Bmax, K + W + (0 if args.no_e2e else K + 2))
+    context = tuple(int(v) for v in args.context.split(",")) if args.context else None
+    cfg, ctx, tables, nb, eng = build_case(wl, Bmax, K + W + (0 if args.no_e2e else K + 2), context=context)
     mbs = tables.shape[1]
     ladder = [int(x) for x in args.ladder.split(",")] if args.ladder else list(wl.ladder)
     if Bmax > max(ladder):
@@ -191,6 +205,12 @@ def time_native(args, rank, world):
     eng.capture(ladder=ladder, max_blocks_per_seq=mbs)
     runs = [timed_steps(eng, cfg, ctx, tables, B, K, W, dev, world, clocks_on=(i == 0))
             for i, B in enumerate(batches)]
+    # launch-tax ablation ("CUDA graphs & kernel fusion", "Direct answer":
+    # T_eager ~ T_compute + N tau, T_graph ~ T_compute + tau): the same step,
+    # same kernels, launched one by one from the host
+    eng.set_eager(True)
+    eager = timed_steps(eng, cfg, ctx, tables, batches[0], K, W, dev, world, clocks_on=False)
+    eng.set_eager(False)
     # dominant kernel of the batch-1 step: the fused gate/up + SwiGLU GEMV
     # (largest matrix of the layer), timed on its own stream over all layers'
     # matrices (each larger than L2)
@@ -199,7 +219,7 @@ def time_native(args, rank, world):
     bt0 = torch.tensor(tables[:B0], device=dev)
     e2e = None if args.no_e2e else time_e2e(eng, cfg, ctx[:B0] + W + K, bt0, B0, K, dev, tables[:B0])
     eng.close()
-    return dict(cfg=cfg, K=K, W=W, runs=runs, kern=kern, e2e=e2e, ctx=ctx, wl=wl)
+    return dict(cfg=cfg, K=K, W=W, runs=runs, kern=kern, e2e=e2e, ctx=ctx, wl=wl, eager=eager)
 
 
 def time_gemv_swiglu(cfg, wl, B, dev, reps=3, layers=None):
@@ -235,6 +255,38 @@ def time_gemv_swiglu(cfg, wl, B, dev, reps=3, layers=None):
     del mats
     torch.cuda.empty_cache()
     return {"ms": ms, "bytes": nbytes, "launches": n}
+
+
+def time_attention(wl, B, dev, reps=10):
+    """One layer's paged attention at batch B over the workload's contexts (a
+    one-layer cache of random values), timed with CUDA events on its stream."""
+    cfg = wl.model
+    lo, hi = wl.context
+    ctx = random_contexts(B, lo, hi, wl.seed + 2000)
+    nb = int(sum(-(-int(c) // 16) for c in ctx)) + 1
+    tables = seeded_block_tables(ctx, 16, nb, wl.seed + 3000)
+    tables[tables < 0] = nb
+    one = cfg.replace(n_layers=1)
+    pool = random_kv_pool(one, nb, wl.seed + 4000, device=dev).view(torch.uint8).reshape(2, -1)
+    q = torch.randn((B, cfg.n_q_heads, cfg.head_dim), device=dev)
+    out = torch.empty((B, cfg.n_q_heads * cfg.head_dim), device=dev)
+    bt = torch.tensor(tables, device=dev)
+    sl = torch.tensor(ctx, device=dev)
+    kvd = capi.DTYPE_E4M3 if cfg.kv_dtype == "fp8" else capi.DTYPE_BF16
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            capi.op_paged_attention(q, cfg.n_kv_heads, pool[0], pool[1], kvd, 1.0, 1.0, bt, sl, nb, out, stream=s)
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(reps):
+            capi.op_paged_attention(q, cfg.n_kv_heads, pool[0], pool[1], kvd, 1.0, 1.0, bt, sl, nb, out, stream=s)
+        e1.record(s)
+        s.synchronize()
+    k = 1 if cfg.kv_dtype == "fp8" else 2
+    nbytes = int(sum(int(c) for c in ctx)) * 2 * cfg.n_kv_heads * cfg.head_dim * k
+    return {"ms": e0.elapsed_time(e1) / reps, "bytes": nbytes, "launches": reps}
 
 
 def time_e2e(eng, cfg, ctx0, bt, B, K, dev, tables):
@@ -345,12 +397,18 @@ def main():
         capi.load()
         wl = WORKLOADS[args.workload]
         B = args.batch or 1
-        k = time_gemv_swiglu(wl.model, wl, B, torch.device("cuda", local), reps=1, layers=4)
+        dev = torch.device("cuda", local)
         peak, src = peaks()
+        if args.kernel_only == "attention":
+            k = time_attention(wl, B, dev)
+            name = "paged attention (split-K, tensor-core QK/PV, merge)"
+        else:
+            k = time_gemv_swiglu(wl.model, wl, B, dev, reps=1, layers=4)
+            name = "gate/up GEMV with SwiGLU epilogue"
         gbs = k["bytes"] / (k["ms"] / 1e3) / 1e9
-        print(json.dumps({"kernel": "gate/up GEMV with SwiGLU epilogue", "workload": wl.key, "batch": B,
-                          "launches": k["launches"], "avg_ms": round(k["ms"], 5), "bytes": k["bytes"],
-                          "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "peak_source": src}))
+        print(json.dumps({"kernel": name, "workload": wl.key, "batch": B, "launches": k["launches"],
+                          "avg_ms": round(k["ms"], 5), "bytes": k["bytes"], "achieved_gbs": round(gbs, 1),
+                          "frac": round(gbs / peak, 4), "peak_source": src}))
         return
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
@@ -365,7 +423,7 @@ def main():
         step_ms = run["total_ms"] / K
         gbs = run["avg_bytes"] / (step_ms * 1e-3) / 1e9
         ps = sorted(run["per_step"])
-        return {"batch": run["B"], "value": round(world * run["B"] * K / (run["total_ms"] / 1e3), 2),
+        return {"batch": run["B"], "value": round(run["rate"], 2),
                 "unit": "tokens/s", "ms_per_step": round(step_ms, 4),
                 "latency_ms": {"p50": round(ps[len(ps) // 2], 4),
                                "p99": round(ps[min(len(ps) - 1, int(0.99 * len(ps)))], 4)},
@@ -397,6 +455,11 @@ def main():
     }
     for run in r["runs"][1:]:
         line["batch%d" % run["B"]] = summary(run)
+    ge, ee = r["runs"][0]["total_ms"] / K, r["eager"]["total_ms"] / K
+    n_k = r["eager"]["kernels_per_step"]
+    line["launch_tax"] = {"batch": head["batch"], "graph_ms": round(ge, 4), "eager_ms": round(ee, 4),
+                          "eager_kernels_per_step": n_k, "tau_us": round((ee - ge) / max(n_k - 1, 1) * 1e3, 3),
+                          "speedup": round(ee / ge, 4)}
     if r["runs"][0]["clocks"]:
         line["clocks"] = r["runs"][0]["clocks"]
     if r["e2e"]:

@@ -22,6 +22,7 @@ namespace mbt {
 
 constexpr int kAttnThreads = 128;
 constexpr int kAttnTile = 64;      // tokens per shared-memory tile (4 blocks)
+constexpr int kMaxSplitBlocks = 512;   // KV blocks one split may cover (8192 tokens)
 
 __device__ __forceinline__ void cp_async16(void* s, const void* g) {
   const unsigned sa = (unsigned)__cvta_generic_to_shared(s);
@@ -132,7 +133,17 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
 
   const unsigned char* kpool = reinterpret_cast<const unsigned char*>(a.kpool);
   const unsigned char* vpool = reinterpret_cast<const unsigned char*>(a.vpool);
+  // this split's block ids, staged once in shared memory (validated here)
+  __shared__ int sblk[kMaxSplitBlocks];
   const int* bt = a.bt + (size_t)b * a.bt_stride;
+  for (int j = tid; j < blk1 - blk0; j += kAttnThreads) {
+    int blk = bt[blk0 + j];
+    if (blk < 0 || blk > a.num_blocks) {
+      set_err(a.err, MBT_DEV_BLOCK_RANGE);
+      blk = a.num_blocks;
+    }
+    sblk[j] = blk;
+  }
   const int tok_begin = blk0 * kBlockTokens;
   const int tok_end_blk = blk1 * kBlockTokens;                       // whole blocks loaded
   const int ntiles = (tok_end_blk - tok_begin + kAttnTile - 1) / kAttnTile;
@@ -145,11 +156,7 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
     for (int i = tid; i < rows * S::NCH; i += kAttnThreads) {
       const int row = i / S::NCH, ch = i - row * S::NCH;
       const int tok = tok0 + row;
-      int blk = bt[tok / kBlockTokens];
-      if (blk < 0 || blk > a.num_blocks) {
-        set_err(a.err, MBT_DEV_BLOCK_RANGE);
-        blk = a.num_blocks;
-      }
+      const int blk = sblk[tok / kBlockTokens - blk0];
       const size_t off = (((size_t)blk * a.nkv + h) * kBlockTokens + (tok % kBlockTokens)) * S::ROWB + ch * 16;
       const int sch = KV8 ? ch : (ch ^ (row & 7));                   // BF16 tiles are swizzled in place
       cp_async16(kd + row * S::ROWB + sch * 16, kpool + off);
@@ -158,8 +165,8 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
     cp_async_commit();
   };
 
+  __syncthreads();                                                    // qs and block ids complete
   load_tile(0, 0);
-  __syncthreads();                                                    // qs complete
 
   // Q fragments (A operand, rows = query heads, k = d), high and low parts
   uint32_t qh[S::KSTEPS][4], ql[S::KSTEPS][4];
@@ -420,7 +427,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_split_kernel(const AttnA
   if (seq >= 1 && seq <= a.bt_stride * kBlockTokens) {
     const int nb_all = (seq + kBlockTokens - 1) / kBlockTokens;
     const int j = sp * a.bps + (tid >> 1);
-    if ((tid >> 1) < a.bps && j < nb_all) {
+    // only the first two tiles: at large batches all CTAs' splits together
+    // exceed L2 and a deeper prefetch would be evicted before use
+    const int pf = min(a.bps, 2 * kAttnTile / kBlockTokens);
+    if ((tid >> 1) < pf && j < nb_all) {
       const int blk = a.bt[(size_t)b * a.bt_stride + j];
       if (blk >= 0 && blk <= a.num_blocks) {
         const size_t off = ((size_t)blk * a.nkv + h) * kBlockTokens * S::ROWB;
@@ -483,6 +493,7 @@ void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nspli
   const int min_per = 2 * kAttnTile / kBlockTokens;
   if (per < min_per) per = min_per;
   if (per > max_blocks) per = max_blocks;
+  if (per > kMaxSplitBlocks) per = kMaxSplitBlocks;
   if (per < 1) per = 1;
   *bps = per;
   *nsplit = (max_blocks + per - 1) / per;

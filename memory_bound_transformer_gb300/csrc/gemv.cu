@@ -140,29 +140,42 @@ gemv_kernel(const GemvArgs a) {
     // fusion") done by every CTA into its own x tile; CTA 0 stores the new residual.
     const int k4n = a.K / 4;
     const bool store_r = (c == 0 && split == 0);
+    constexpr int PV = 8;                        // float4 per thread in flight per pass
     float ss[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       ss[b] = 0.f;
-      if (b < a.nb) {
-        const float4* __restrict__ r4 = reinterpret_cast<const float4*>(a.r_in + (size_t)b * a.K);
-        const float4* __restrict__ d4 = reinterpret_cast<const float4*>(a.delta + (size_t)b * a.K);
-        float4* __restrict__ o4 = reinterpret_cast<float4*>(a.r_out + (size_t)b * a.K);
-        for (int k4 = tid; k4 < k4n; k4 += kGemvThreads) {
-          float4 x = r4[k4];
-          for (int sidx = 0; sidx < a.n_delta; ++sidx) {
-            const float4 t = d4[(size_t)sidx * (a.delta_stride / 4) + k4];
-            x.x += t.x; x.y += t.y; x.z += t.z; x.w += t.w;
-          }
-          if (store_r) o4[k4] = x;
-          ss[b] += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
-          const int v = k4 / QN, q = k4 - v * QN;
-          xs[(b * QN + q) * nvec + v] = x;
+      const bool live = b < a.nb;
+      const float4* __restrict__ r4 = reinterpret_cast<const float4*>(a.r_in + (size_t)b * a.K);
+      const float4* __restrict__ d4 = reinterpret_cast<const float4*>(a.delta + (size_t)b * a.K);
+      float4* __restrict__ o4 = reinterpret_cast<float4*>(a.r_out + (size_t)b * a.K);
+      for (int base = 0; base < k4n; base += PV * kGemvThreads) {
+        // all loads of the pass first (one round trip), then the sums
+        float4 v[PV];
+#pragma unroll
+        for (int j = 0; j < PV; ++j) {
+          const int k4 = base + tid + j * kGemvThreads;
+          v[j] = (live && k4 < k4n) ? r4[k4] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-      } else {
-        for (int k4 = tid; k4 < k4n; k4 += kGemvThreads) {
-          const int v = k4 / QN, q = k4 - v * QN;
-          xs[(b * QN + q) * nvec + v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sidx = 0; sidx < a.n_delta; ++sidx) {
+          float4 t[PV];
+#pragma unroll
+          for (int j = 0; j < PV; ++j) {
+            const int k4 = base + tid + j * kGemvThreads;
+            t[j] = (live && k4 < k4n) ? d4[(size_t)sidx * (a.delta_stride / 4) + k4] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int j = 0; j < PV; ++j) { v[j].x += t[j].x; v[j].y += t[j].y; v[j].z += t[j].z; v[j].w += t[j].w; }
+        }
+#pragma unroll
+        for (int j = 0; j < PV; ++j) {
+          const int k4 = base + tid + j * kGemvThreads;
+          if (k4 < k4n) {
+            if (store_r && live) o4[k4] = v[j];
+            ss[b] += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+            const int vv = k4 / QN, q = k4 - vv * QN;
+            xs[(b * QN + q) * nvec + vv] = v[j];
+          }
         }
       }
       ss[b] = warp_sum(ss[b]);
@@ -181,6 +194,7 @@ gemv_kernel(const GemvArgs a) {
       inv[b] = 1.0f / sqrtf(t / (float)a.K + a.eps);
     }
     const uint2* g2 = reinterpret_cast<const uint2*>(a.gamma);
+#pragma unroll 8
     for (int k4 = tid; k4 < k4n; k4 += kGemvThreads) {
       const uint2 g = g2[k4];
       const float g0 = bf16_lo(g.x), g1 = bf16_hi(g.x), gg2 = bf16_lo(g.y), g3 = bf16_hi(g.y);

@@ -165,7 +165,8 @@ int ensure_ws(mbt_model* m, int R, int mbs) {
     Plan p = make_plan(m, r, mbs_cap);
     // attn_plan never uses more splits than this, whatever the table width
     const int pairs = r * (int)m->h.n_kv_heads;
-    const int split_bound = std::max(1, (4 * m->num_sms + pairs - 1) / pairs);
+    // attn_plan never uses more splits than this, whatever the table width up to mbs_cap
+    const int split_bound = std::max({1, (4 * m->num_sms + pairs - 1) / pairs, (mbs_cap + 511) / 512});
     pml = std::max(pml, (size_t)r * m->h.n_q_heads * split_bound);
     ns_qkv = std::max(ns_qkv, p.ns_qkv);
     ns_delta = std::max({ns_delta, p.ns_o, p.ns_down});

@@ -19,8 +19,8 @@ from memory_bound_transformer_gb300 import capi
 from memory_bound_transformer_gb300.engine import Engine
 from oracle.decode import OracleKV, decode_step
 from oracle.numerics import bf16_decode, e4m3_decode
-from synth import (EIGHT_B, ONE_B, TINY, SynthModel, random_kv_pool, random_tokens,
-                   seeded_block_tables)
+from synth import (EIGHT_B, ONE_B, SEVENTY_B_FP8, TINY, SynthModel, raw_numpy, random_kv_pool,
+                   random_tokens, seeded_block_tables)
 from tests.helpers import SMALL, SMALL_D128, SMALL_FP8, SMALL_G5, kv_numpy, oracle_weights
 
 pytestmark = pytest.mark.gpu
@@ -192,17 +192,27 @@ def test_1b_workload(cuda_lib):
     _run(case, oracle_weights(case.model), okv, 2)
 
 
-def test_8b_full_size_batch1(cuda_lib):
-    """8B-class decoder, batch 1, one step at a 300-token context."""
-    cfg = EIGHT_B
-    case = Case(cfg, 1237, 1, [300], 1, cache_weights=False, ladder=[1], graph=True)
+def _full_size(cfg, seed, ctx):
+    case = Case(cfg, seed, 1, [ctx], 1, cache_weights=False, ladder=[1], graph=True)
     okv = OracleKV(case.pool0.copy(), np.ones(cfg.n_layers), np.ones(cfg.n_layers))
-    model = SynthModel(cfg, 1237, device=DEV, cache=False)
+    model = SynthModel(cfg, seed, device=DEV, cache=False)
 
     def W(name, layer):
-        from synth import raw_numpy
         return {k: raw_numpy(v) for k, v in model.get(name, layer).items()}
     _run(case, W, okv, 1)
+
+
+def test_8b_full_size_batch1(cuda_lib):
+    """8B-class decoder, batch 1, one step at a 300-token context."""
+    _full_size(EIGHT_B, 1237, 300)
+
+
+@pytest.mark.slow
+def test_70b_fp8_full_size_batch1(cuda_lib):
+    """70B-class decoder, FP8-e4m3 weights with per-channel scales and an FP8
+    cache, batch 1, one step at a 2048-token context (the oracle streams the
+    ~70 GB of e4m3 weights through float64 layer by layer)."""
+    _full_size(SEVENTY_B_FP8, 1239, 2048)
 
 
 def test_host_detected_errors(cuda_lib):
