@@ -20,6 +20,9 @@
 
 namespace mbt {
 
+#ifndef MBT_ATTN_MINB
+#define MBT_ATTN_MINB 3
+#endif
 constexpr int kAttnThreads = 128;
 constexpr int kAttnTile = 64;      // tokens per shared-memory tile (4 blocks)
 constexpr int kMaxSplitBlocks = 512;   // KV blocks one split may cover (8192 tokens)
@@ -40,11 +43,14 @@ struct AttnShape {
   static constexpr int BROWB = D * 2;                // bytes per token row of a BF16 compute tile
   static constexpr int BNCH = BROWB / 16;            // 16-byte chunks per BF16 row (8 or 16)
   static constexpr int KSTEPS = D / 16;              // MMA k-steps over d for Q K^T
-  static constexpr int DT = D / 8;                   // 8-wide d tiles of the output
+  static constexpr int MT = D / 16;                  // 16-row d tiles of O^T
   static constexpr size_t Q_BYTES = (size_t)16 * D * 4;
   static constexpr size_t T_BYTES = (size_t)kAttnTile * BROWB;
   static constexpr size_t R_BYTES = (size_t)kAttnTile * ROWB;
-  static constexpr size_t SMEM = Q_BYTES + 4 * T_BYTES + (KV8 ? 4 * R_BYTES : 0);
+  // BF16 caches: K and V tiles double-buffered in place. e4m3 caches: the raw
+  // tiles are double-buffered and widened into one BF16 K and V tile.
+  static constexpr int NBUF = KV8 ? 1 : 2;
+  static constexpr size_t SMEM = Q_BYTES + 2 * NBUF * T_BYTES + (KV8 ? 4 * R_BYTES : 0);
 };
 
 // 16 e4m3 codes -> 16 floats, exactly.
@@ -81,55 +87,83 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
 }
 // D += A (16x16 BF16, row) * B (16x8 BF16, col), fp32 accumulate.
+// Transpose of an 8x8 BF16 matrix held one row pair per lane (mma fragment layout).
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
                : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Fused "RoPE + KV-cache write" ("Kernels, Fusion & CUDA Graphs", "Fix 1:
+// kernel fusion"): rotate the new token's key for KV head h and store it and its
+// value at block bt[p / 16], slot p % 16, rounded to the cache format. Thread
+// i < D handles element i and returns its two codes (for a copy in shared memory).
+template <int D, int KV8>
+__device__ __forceinline__ void write_new_kv(const AttnArgs& a, int b, int h, int pos, int blk,
+                                             uint32_t& kcode, uint32_t& vcode) {
+  static_assert(D <= kAttnThreads, "one element per thread");
+  const int half = D / 2;
+  const float* src = a.qkv + (size_t)b * a.ld_qkv;
+  const int kcol = (a.nq + h) * D, vcol = (a.nq + a.nkv + h) * D;
+  const float2* cs = a.rope + (size_t)pos * half;
+  const size_t base = (((size_t)blk * a.nkv + h) * kBlockTokens + pos % kBlockTokens) * D;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) {
+    float k1 = 0.f, k2 = 0.f, v = 0.f;
+    const int ip = i < half ? i : i - half;
+    for (int s2 = 0; s2 < a.qkv_nsplit; ++s2) {
+      const float* p = src + (size_t)s2 * a.qkv_split_stride;
+      k1 += p[kcol + ip];
+      k2 += p[kcol + ip + half];
+      v += p[vcol + i];
+    }
+    const float2 t = cs[ip];
+    const float k = i < half ? k1 * t.x - k2 * t.y : k2 * t.x + k1 * t.y;
+    const float ks = __fdiv_rn(k, a.k_scale), vs = __fdiv_rn(v, a.v_scale);
+    if (KV8) {
+      kcode = f32_to_e4m3(ks);
+      vcode = f32_to_e4m3(vs);
+      reinterpret_cast<uint8_t*>(const_cast<void*>(a.kpool))[base + i] = (uint8_t)kcode;
+      reinterpret_cast<uint8_t*>(const_cast<void*>(a.vpool))[base + i] = (uint8_t)vcode;
+    } else {
+      kcode = f32_to_bf16_bits(ks);
+      vcode = f32_to_bf16_bits(vs);
+      reinterpret_cast<uint16_t*>(const_cast<void*>(a.kpool))[base + i] = (uint16_t)kcode;
+      reinterpret_cast<uint16_t*>(const_cast<void*>(a.vpool))[base + i] = (uint16_t)vcode;
+    }
+  }
+}
+
 // One split of one (row, KV head): stream its KV blocks once for all query
 // heads of the group and leave (unnormalised o, running max m, sum l) per head.
-// The group's query heads are the 16 rows of the MMA tiles (padded with zero
-// rows); each warp takes 16 tokens of every 64-token tile: S = Q K^T and
-// O += P V on the tensor cores with Q and P split into BF16 high + low parts
-// (fp32-level accuracy), the online softmax in registers, and the four warps'
-// states merged at the end.
-template <int D, int KV8>
+// Each warp takes 16 tokens of every 64-token tile; the group's query heads
+// are the N dimension of the MMA tiles (8 per n-tile, zero-padded):
+// S^T = K Q^T and O^T += V^T P^T on the tensor cores with Q and P split into
+// BF16 high + low parts (fp32-level accuracy), the online softmax in
+// registers, and the four warps' states merged at the end.
+//
+// The cached context does not depend on the previous kernel (only this
+// kernel writes this layer's cache, and a step starts after the previous one
+// has finished), so the block ids and the first two tiles are requested
+// before the wait on the QKV projection. The new token's row, which this CTA
+// writes after the wait, is patched into a tile already in shared memory
+// (tiles loaded later read it from the cache).
+template <int D, int KV8, int NT>
 __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, int b, int h, int sp,
-                                       int G, size_t head0, int seq, int blk0, int blk1) {
+                                       int G, size_t head0, int seq, int blk0, int blk1, bool writer,
+                                       int pos, int wblk) {
   using S = AttnShape<D, KV8>;
   float* qs = reinterpret_cast<float*>(smem);                        // [16][D], rows >= G are zero
-  unsigned char* kbf = smem + S::Q_BYTES;                             // [2][tile][BROWB] BF16, swizzled
-  unsigned char* vbf = kbf + 2 * S::T_BYTES;
-  unsigned char* raw = vbf + 2 * S::T_BYTES;                          // e4m3 caches: [2][K|V][tile][ROWB]
+  unsigned char* kbf = smem + S::Q_BYTES;                             // [NBUF][tile][BROWB] BF16, swizzled
+  unsigned char* vbf = kbf + S::NBUF * S::T_BYTES;
+  unsigned char* raw = vbf + S::NBUF * S::T_BYTES;                    // e4m3 caches: [2][K|V][tile][ROWB]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t4 = lane & 3;
-
-  // queries of the group, pre-scaled into the log2 domain with the K dequant scale
-  const float qscale = 1.4426950408889634f / sqrtf((float)D) * a.k_scale;
-  if (a.qkv) {
-    // RoPE (rotate-half: element i pairs with i + D/2) straight from the QKV
-    // projection's partial sums
-    const int half = D / 2;
-    int pos = a.positions[b];
-    if (pos < 0 || pos >= a.max_pos) pos = 0;
-    const float* src = a.qkv + (size_t)b * a.ld_qkv + (size_t)h * G * D;
-    const float2* cs = a.rope + (size_t)pos * half;
-    for (int e = tid; e < G * half; e += kAttnThreads) {
-      const int gg = e / half, i = e - gg * half;
-      float x1 = 0.f, x2 = 0.f;
-      for (int s2 = 0; s2 < a.qkv_nsplit; ++s2) {
-        x1 += src[(size_t)s2 * a.qkv_split_stride + gg * D + i];
-        x2 += src[(size_t)s2 * a.qkv_split_stride + gg * D + i + half];
-      }
-      const float2 t = cs[i];
-      qs[gg * D + i] = (x1 * t.x - x2 * t.y) * qscale;
-      qs[gg * D + i + half] = (x2 * t.x + x1 * t.y) * qscale;
-    }
-  } else {
-    for (int i = tid; i < G * D; i += kAttnThreads) qs[i] = a.q[head0 * D + i] * qscale;
-  }
-  for (int i = G * D + tid; i < 16 * D; i += kAttnThreads) qs[i] = 0.f;
 
   const unsigned char* kpool = reinterpret_cast<const unsigned char*>(a.kpool);
   const unsigned char* vpool = reinterpret_cast<const unsigned char*>(a.vpool);
@@ -147,6 +181,8 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
   const int tok_begin = blk0 * kBlockTokens;
   const int tok_end_blk = blk1 * kBlockTokens;                       // whole blocks loaded
   const int ntiles = (tok_end_blk - tok_begin + kAttnTile - 1) / kAttnTile;
+  // tile of this split that holds the new token (written below), else -1
+  const int tnew = (writer && pos >= tok_begin && pos < tok_end_blk) ? (pos - tok_begin) / kAttnTile : -1;
 
   auto load_tile = [&](int t, int buf) {
     const int tok0 = tok_begin + t * kAttnTile;
@@ -165,33 +201,106 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
     cp_async_commit();
   };
 
-  __syncthreads();                                                    // qs and block ids complete
-  load_tile(0, 0);
-
-  // Q fragments (A operand, rows = query heads, k = d), high and low parts
-  uint32_t qh[S::KSTEPS][4], ql[S::KSTEPS][4];
-#pragma unroll
-  for (int kk = 0; kk < S::KSTEPS; ++kk)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int row = g + (r & 1) * 8, col = 16 * kk + 2 * t4 + (r >> 1) * 8;
-      split_bf16(qs[row * D + col], qs[row * D + col + 1], qh[kk][r], ql[kk][r]);
+  __syncthreads();                                                    // block ids complete
+  for (int t = 0; t < 2 && t < ntiles; ++t) load_tile(t, t);
+  // the next two tiles towards L2
+  if (ntiles > 2) {
+    const int j = 2 * kAttnTile / kBlockTokens + (tid >> 1);
+    if ((tid >> 1) < 2 * kAttnTile / kBlockTokens && j < blk1 - blk0) {
+      const size_t off = ((size_t)sblk[j] * a.nkv + h) * kBlockTokens * S::ROWB;
+      prefetch_l2((const unsigned char*)((tid & 1) ? a.vpool : a.kpool) + off, kBlockTokens * S::ROWB);
     }
+  }
 
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;          // rows g and g + 8
-  float o[S::DT][4];
+  pdl_wait();
+
+  if (writer) {
+    // the new token's K (rotated) and V go into the cache, and into the tile
+    // already requested when it is one of the first two
+    uint32_t kc = 0, vc = 0;
+    write_new_kv<D, KV8>(a, b, h, pos, wblk, kc, vc);
+    if (tnew == 0 || tnew == 1) {
+      cp_async_wait<0>();
+      __syncthreads();                                                // the tile's copies have landed
+      const int r = pos - (tok_begin + tnew * kAttnTile);
+      if (tid < D) {
+        if (KV8) {
+          unsigned char* rk = raw + (size_t)tnew * 2 * S::R_BYTES + (size_t)r * S::ROWB + tid;
+          rk[0] = (unsigned char)kc;
+          rk[S::R_BYTES] = (unsigned char)vc;
+        } else {
+          const size_t off = (size_t)tnew * S::T_BYTES + (size_t)r * S::BROWB +
+                             (size_t)(((tid >> 3) ^ (r & 7)) * 16 + (tid & 7) * 2);
+          *reinterpret_cast<uint16_t*>(kbf + off) = (uint16_t)kc;
+          *reinterpret_cast<uint16_t*>(vbf + off) = (uint16_t)vc;
+        }
+      }
+    }
+  }
+
+  // queries of the group, pre-scaled into the log2 domain with the K dequant scale
+  const float qscale = 1.4426950408889634f / sqrtf((float)D) * a.k_scale;
+  if (a.qkv) {
+    // RoPE (rotate-half: element i pairs with i + D/2) straight from the QKV
+    // projection's partial sums
+    const int half = D / 2;
+    int qpos = a.positions[b];
+    if (qpos < 0 || qpos >= a.max_pos) qpos = 0;
+    const float* src = a.qkv + (size_t)b * a.ld_qkv + (size_t)h * G * D;
+    const float2* cs = a.rope + (size_t)qpos * half;
+    for (int e = tid; e < G * half; e += kAttnThreads) {
+      const int gg = e / half, i = e - gg * half;
+      float x1 = 0.f, x2 = 0.f;
+      for (int s2 = 0; s2 < a.qkv_nsplit; ++s2) {
+        x1 += src[(size_t)s2 * a.qkv_split_stride + gg * D + i];
+        x2 += src[(size_t)s2 * a.qkv_split_stride + gg * D + i + half];
+      }
+      const float2 t = cs[i];
+      qs[gg * D + i] = (x1 * t.x - x2 * t.y) * qscale;
+      qs[gg * D + i + half] = (x2 * t.x + x1 * t.y) * qscale;
+    }
+  } else {
+    for (int i = tid; i < G * D; i += kAttnThreads) qs[i] = a.q[head0 * D + i] * qscale;
+  }
+  for (int i = G * D + tid; i < 16 * D; i += kAttnThreads) qs[i] = 0.f;
+  __syncthreads();                                                    // qs complete
+
+  // Q^T fragments (B operand: k = d, n = query head), high and low parts, in
+  // NT n-tiles of 8 heads (heads >= G are the zero rows of qs)
+  uint32_t qh[NT][S::KSTEPS][2], ql[NT][S::KSTEPS][2];
 #pragma unroll
-  for (int i = 0; i < S::DT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int kk = 0; kk < S::KSTEPS; ++kk)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int head = nt * 8 + g, col = 16 * kk + 2 * t4 + r * 8;
+        split_bf16(qs[head * D + col], qs[head * D + col + 1], qh[nt][kk][r], ql[nt][kk][r]);
+      }
+
+  // softmax state of this thread's two heads per n-tile (nt*8 + 2*t4, +1),
+  // the same in every lane of a column group
+  float mst[NT][2], lst[NT][2];
+  float o[NT][S::MT][4];                                              // O^T: 16 d x 8 heads per m-tile
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    mst[nt][0] = mst[nt][1] = -INFINITY;
+    lst[nt][0] = lst[nt][1] = 0.f;
+#pragma unroll
+    for (int i = 0; i < S::MT; ++i) o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
+  }
 
   for (int t = 0; t < ntiles; ++t) {
     const int buf = t & 1;
-    if (t + 1 < ntiles) { load_tile(t + 1, buf ^ 1); cp_async_wait<1>(); }
+    // tiles 0 and 1 were requested up front; from tile 1 on, the tile after
+    // next goes into the buffer the previous tile has left
+    if (t >= 1 && t + 1 < ntiles) { load_tile(t + 1, buf ^ 1); cp_async_wait<1>(); }
     else cp_async_wait<0>();
     __syncthreads();
     const int tok0 = tok_begin + t * kAttnTile;
     const int nvalid = min(kAttnTile, min(seq, tok_end_blk) - tok0);   // this split's tokens only
-    unsigned char* kt = kbf + (size_t)buf * S::T_BYTES;
-    unsigned char* vt = vbf + (size_t)buf * S::T_BYTES;
+    unsigned char* kt = kbf + (size_t)(KV8 ? 0 : buf) * S::T_BYTES;
+    unsigned char* vt = vbf + (size_t)(KV8 ? 0 : buf) * S::T_BYTES;
     if (KV8) {
       // widen the e4m3 tile to BF16 (exact), swizzled; rows past the context are zero
       const unsigned char* rk = raw + (size_t)buf * 2 * S::R_BYTES;
@@ -225,94 +334,102 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
       const uint32_t kbase = (uint32_t)__cvta_generic_to_shared(kt);
       const uint32_t vbase = (uint32_t)__cvta_generic_to_shared(vt);
       const int lm = lane >> 3, lr = lane & 7;
-      // S = Q K^T over 16 tokens (two 8-token n-tiles)
-      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // S^T [16 tokens x 8 heads] = K Q^T: K rows are the A operand
+      float st[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) st[nt][0] = st[nt][1] = st[nt][2] = st[nt][3] = 0.f;
       {
-        const int krow = n0 + (lm >> 1) * 8 + lr;
+        const int krow = n0 + (lm & 1) * 8 + lr;
 #pragma unroll
         for (int kk = 0; kk < S::KSTEPS; ++kk) {
           uint32_t kf[4];
-          const int ch = 2 * kk + (lm & 1);
+          const int ch = 2 * kk + (lm >> 1);
           ldsm_x4(kbase + krow * S::BROWB + ((ch ^ (krow & 7)) * 16), kf);
-          mma16816(sacc[0], qh[kk], kf[0], kf[1]);
-          mma16816(sacc[0], ql[kk], kf[0], kf[1]);
-          mma16816(sacc[1], qh[kk], kf[2], kf[3]);
-          mma16816(sacc[1], ql[kk], kf[2], kf[3]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma16816(st[nt], kf, qh[nt][kk][0], qh[nt][kk][1]);
+            mma16816(st[nt], kf, ql[nt][kk][0], ql[nt][kk][1]);
+          }
         }
       }
-      // mask, online softmax per query-head row (quad of lanes holds a row)
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+      const bool v0 = n0 + g < nvalid, v1 = n0 + g + 8 < nvalid;     // tokens of c0/c1 and c2/c3
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
+      for (int nt = 0; nt < NT; ++nt) {
+        if (!v0) { st[nt][0] = -INFINITY; st[nt][1] = -INFINITY; }
+        if (!v1) { st[nt][2] = -INFINITY; st[nt][3] = -INFINITY; }
+        // online softmax per head: the 16 tokens of a column sit in the 8 lanes of one t4
+        float mx[2] = {fmaxf(st[nt][0], st[nt][2]), fmaxf(st[nt][1], st[nt][3])};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int tok = n0 + 8 * j + 2 * t4 + (c & 1);
-          if (tok >= nvalid) sacc[j][c] = -INFINITY;
-          if (c < 2) mx0 = fmaxf(mx0, sacc[j][c]); else mx1 = fmaxf(mx1, sacc[j][c]);
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], off));
+        float al[2], ps[2];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const float mn = fmaxf(mst[nt][c], mx[c]);
+          const float mu = mn == -INFINITY ? 0.f : mn;
+          al[c] = exp2f(mst[nt][c] - mu);
+          const float pa = exp2f(st[nt][c] - mu), pb = exp2f(st[nt][c + 2] - mu);
+          st[nt][c] = pa;
+          st[nt][c + 2] = pb;
+          ps[c] = pa + pb;
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) ps[c] += __shfl_xor_sync(0xffffffffu, ps[c], off);
+          lst[nt][c] = lst[nt][c] * al[c] + ps[c];
+          mst[nt][c] = mn;
         }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
-      float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float p = exp2f(sacc[j][c] - (c < 2 ? mu0 : mu1));
-          sacc[j][c] = p;
-          if (c < 2) ps0 += p; else ps1 += p;
+        for (int i = 0; i < S::MT; ++i) {
+          o[nt][i][0] *= al[0]; o[nt][i][1] *= al[1]; o[nt][i][2] *= al[0]; o[nt][i][3] *= al[1];
         }
-      ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
-      ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
-      ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
-      ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
-      l0 = l0 * al0 + ps0;
-      l1 = l1 * al1 + ps1;
-      m0 = mn0;
-      m1 = mn1;
+      }
+      // P^T as the B operand (k = tokens, n = heads): transpose the 8x8 BF16
+      // halves of the S^T accumulator in registers; high and low parts
+      uint32_t ph[NT][2], pl[NT][2];
 #pragma unroll
-      for (int i = 0; i < S::DT; ++i) { o[i][0] *= al0; o[i][1] *= al0; o[i][2] *= al1; o[i][3] *= al1; }
-      // P as the A operand (rows = heads, k = the 16 tokens), high and low parts
-      uint32_t ph[4], pl[4];
-      split_bf16(sacc[0][0], sacc[0][1], ph[0], pl[0]);
-      split_bf16(sacc[0][2], sacc[0][3], ph[1], pl[1]);
-      split_bf16(sacc[1][0], sacc[1][1], ph[2], pl[2]);
-      split_bf16(sacc[1][2], sacc[1][3], ph[3], pl[3]);
-      // O += P V (V fragments transposed out of the swizzled tile)
-      const int vrow = n0 + (lm & 1) * 8 + lr;
+      for (int nt = 0; nt < NT; ++nt) {
+        uint32_t h0, l0, h1, l1;
+        split_bf16(st[nt][0], st[nt][1], h0, l0);
+        split_bf16(st[nt][2], st[nt][3], h1, l1);
+        ph[nt][0] = movm_t(h0); ph[nt][1] = movm_t(h1);
+        pl[nt][0] = movm_t(l0); pl[nt][1] = movm_t(l1);
+      }
+      // O^T [16 d x 8 heads] += V^T P^T: V^T fragments read transposed from the tile
+      const int vrow = n0 + (lm >> 1) * 8 + lr;
 #pragma unroll
-      for (int dp = 0; dp < S::DT / 2; ++dp) {
+      for (int mt = 0; mt < S::MT; ++mt) {
         uint32_t vf[4];
-        const int ch = 2 * dp + (lm >> 1);
+        const int ch = 2 * mt + (lm & 1);
         ldsm_x4_t(vbase + vrow * S::BROWB + ((ch ^ (vrow & 7)) * 16), vf);
-        mma16816(o[2 * dp], ph, vf[0], vf[1]);
-        mma16816(o[2 * dp], pl, vf[0], vf[1]);
-        mma16816(o[2 * dp + 1], ph, vf[2], vf[3]);
-        mma16816(o[2 * dp + 1], pl, vf[2], vf[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma16816(o[nt][mt], vf, ph[nt][0], ph[nt][1]);
+          mma16816(o[nt][mt], vf, pl[nt][0], pl[nt][1]);
+        }
       }
     }
     __syncthreads();
   }
 
-  // merge the four warps' (m, l, o) per head row and write this split's partial
+  // merge the four warps' (m, l, o) per head and write this split's partial
   float* sm_m = reinterpret_cast<float*>(kbf);                        // [4][16]
   float* sm_l = sm_m + 4 * 16;
   float* sm_o = sm_l + 4 * 16;                                        // [4][16][D]
-  if (t4 == 0) {
-    sm_m[warp * 16 + g] = m0; sm_m[warp * 16 + g + 8] = m1;
-    sm_l[warp * 16 + g] = l0; sm_l[warp * 16 + g + 8] = l1;
-  }
 #pragma unroll
-  for (int i = 0; i < S::DT; ++i) {
-    const int d0 = 8 * i + 2 * t4;
-    sm_o[(warp * 16 + g) * D + d0] = o[i][0];
-    sm_o[(warp * 16 + g) * D + d0 + 1] = o[i][1];
-    sm_o[(warp * 16 + g + 8) * D + d0] = o[i][2];
-    sm_o[(warp * 16 + g + 8) * D + d0 + 1] = o[i][3];
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h0 = nt * 8 + 2 * t4;
+    if (g == 0) {
+      sm_m[warp * 16 + h0] = mst[nt][0]; sm_m[warp * 16 + h0 + 1] = mst[nt][1];
+      sm_l[warp * 16 + h0] = lst[nt][0]; sm_l[warp * 16 + h0 + 1] = lst[nt][1];
+    }
+#pragma unroll
+    for (int i = 0; i < S::MT; ++i) {
+      const int d0 = 16 * i + g;
+      sm_o[(warp * 16 + h0) * D + d0] = o[nt][i][0];
+      sm_o[(warp * 16 + h0 + 1) * D + d0] = o[nt][i][1];
+      sm_o[(warp * 16 + h0) * D + d0 + 8] = o[nt][i][2];
+      sm_o[(warp * 16 + h0 + 1) * D + d0 + 8] = o[nt][i][3];
+    }
   }
   __syncthreads();
   for (int e = tid; e < G * D; e += kAttnThreads) {
@@ -336,11 +453,34 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
 
 // Merge the splits of the group's G query heads: rescale each partial to the
 // common maximum, sum, divide by the total softmax mass, apply the V scale.
-// One warp per head finds the maximum and the mass; every thread then sums one
-// output element over the splits with several loads in flight.
-__device__ __forceinline__ void merge_splits(const AttnArgs& a, float* wsm, int G, size_t head0, int D) {
+// The group's partials are pulled into shared memory in chunks of splits with
+// one round of cp.async each (one L2 round trip per chunk instead of one per
+// element a thread sums); one warp per head finds the maximum and the mass
+// while the first chunk is in flight. Splits without tokens left part_o
+// unwritten: their weight is 0 and they are skipped.
+constexpr int kMergeMaxE = 16;     // G * D <= 16 * 128
+__device__ __forceinline__ void merge_splits(const AttnArgs& a, unsigned char* smem, size_t smem_bytes, int G,
+                                             size_t head0, int D) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ns = a.nsplit;
+  float* wsm = reinterpret_cast<float*>(smem);                      // [G][ns] weights
+  const size_t w_bytes = ((size_t)G * ns * 4 + 15) & ~(size_t)15;
+  // running sums over chunks when the partials do not fit in one
+  const bool one = w_bytes + (size_t)G * ns * D * 4 <= smem_bytes;
+  float* run = reinterpret_cast<float*>(smem + w_bytes);            // [G * D] (chunked only)
+  float* so = one ? run : run + G * D;                               // [G][chunk][D]
+  const size_t avail = smem_bytes - (size_t)((unsigned char*)so - smem);
+  const int chunk = one ? ns : max(1, (int)(avail / ((size_t)G * D * 4)));
+  auto stage = [&](int s0, int sc) {
+    const int per_g = sc * D / 4;                                    // float4 per head in this chunk
+    for (int g = 0; g < G; ++g) {
+      const float* src = a.part_o + ((head0 + g) * ns + s0) * D;
+      float* dst = so + (size_t)g * sc * D;
+      for (int j = tid; j < per_g; j += kAttnThreads) cp_async16(dst + 4 * j, src + 4 * j);
+    }
+    cp_async_commit();
+  };
+  stage(0, min(chunk, ns));
   for (int g = warp; g < G; g += kAttnThreads / 32) {
     const float2* ml = a.part_ml + (head0 + g) * ns;
     float M = -INFINITY;
@@ -352,116 +492,87 @@ __device__ __forceinline__ void merge_splits(const AttnArgs& a, float* wsm, int 
     const float inv = L > 0.f ? a.v_scale / L : 0.f;
     for (int s = lane; s < ns; s += 32) wsm[g * ns + s] = ml[s].y > 0.f ? exp2f(ml[s].x - M) * inv : 0.f;
   }
-  __syncthreads();
-  for (int e = tid; e < G * D; e += kAttnThreads) {
-    const int g = e / D, d = e - g * D;
-    const float* po = a.part_o + (head0 + g) * ns * D + d;
-    const float* wg = wsm + g * ns;
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-    int s = 0;
-    for (; s + 4 <= ns; s += 4) {
-      const float w0 = wg[s], w1 = wg[s + 1], w2 = wg[s + 2], w3 = wg[s + 3];
-      if (w0 != 0.f) acc0 += w0 * po[(size_t)s * D];
-      if (w1 != 0.f) acc1 += w1 * po[(size_t)(s + 1) * D];
-      if (w2 != 0.f) acc2 += w2 * po[(size_t)(s + 2) * D];
-      if (w3 != 0.f) acc3 += w3 * po[(size_t)(s + 3) * D];
+  for (int s0 = 0; s0 < ns; s0 += chunk) {
+    const int sc = min(chunk, ns - s0);
+    const bool last = s0 + chunk >= ns;
+    cp_async_wait<0>();
+    __syncthreads();                                                 // chunk (and, first time, weights) ready
+    for (int e = tid; e < G * D; e += kAttnThreads) {
+      const int g = e / D, d = e - g * D;
+      const float* po = so + (size_t)g * sc * D + d;
+      const float* wg = wsm + g * ns + s0;
+      float acc0 = s0 ? run[e] : 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+      int s = 0;
+      for (; s + 4 <= sc; s += 4) {
+        const float w0 = wg[s], w1 = wg[s + 1], w2 = wg[s + 2], w3 = wg[s + 3];
+        if (w0 != 0.f) acc0 += w0 * po[(size_t)s * D];
+        if (w1 != 0.f) acc1 += w1 * po[(size_t)(s + 1) * D];
+        if (w2 != 0.f) acc2 += w2 * po[(size_t)(s + 2) * D];
+        if (w3 != 0.f) acc3 += w3 * po[(size_t)(s + 3) * D];
+      }
+      for (; s < sc; ++s) if (wg[s] != 0.f) acc0 += wg[s] * po[(size_t)s * D];
+      const float o = (acc0 + acc1) + (acc2 + acc3);
+      if (!last) { run[e] = o; continue; }
+      const size_t oi = (head0 + g) * D + d;
+      if (a.out) a.out[oi] = o;
+      if (a.out_hl) {                              // high/low BF16 rows for the tensor-core GEMM
+        const size_t row = oi / ((size_t)a.nq * D), col = oi % ((size_t)a.nq * D);
+        const bf16 h = __float2bfloat16_rn(o);
+        a.out_hl[row * a.nq * D + col] = h;
+        a.out_hl[(a.rp_hl + row) * a.nq * D + col] = __float2bfloat16_rn(o - __bfloat162float(h));
+      }
     }
-    for (; s < ns; ++s) if (wg[s] != 0.f) acc0 += wg[s] * po[(size_t)s * D];
-    const float o = (acc0 + acc1) + (acc2 + acc3);
-    const size_t oi = (head0 + g) * D + d;
-    if (a.out) a.out[oi] = o;
-    if (a.out_hl) {                                // high/low BF16 rows for the tensor-core GEMM
-      const size_t row = oi / ((size_t)a.nq * D), col = oi % ((size_t)a.nq * D);
-      const bf16 h = __float2bfloat16_rn(o);
-      a.out_hl[row * a.nq * D + col] = h;
-      a.out_hl[(a.rp_hl + row) * a.nq * D + col] = __float2bfloat16_rn(o - __bfloat162float(h));
-    }
-  }
-}
-
-// Fused "RoPE + KV-cache write" ("Kernels, Fusion & CUDA Graphs", "Fix 1:
-// kernel fusion"): rotate the new token's key for KV head h and store it and its
-// value at block bt[p / 16], slot p % 16, rounded to the cache format.
-template <int D, int KV8>
-__device__ __forceinline__ void write_new_kv(const AttnArgs& a, int b, int h, int pos, int blk) {
-  const int half = D / 2;
-  const float* src = a.qkv + (size_t)b * a.ld_qkv;
-  const int kcol = (a.nq + h) * D, vcol = (a.nq + a.nkv + h) * D;
-  const float2* cs = a.rope + (size_t)pos * half;
-  const size_t base = (((size_t)blk * a.nkv + h) * kBlockTokens + pos % kBlockTokens) * D;
-  for (int i = threadIdx.x; i < D; i += blockDim.x) {
-    float k1 = 0.f, k2 = 0.f, v = 0.f;
-    const int ip = i < half ? i : i - half;
-    for (int s2 = 0; s2 < a.qkv_nsplit; ++s2) {
-      const float* p = src + (size_t)s2 * a.qkv_split_stride;
-      k1 += p[kcol + ip];
-      k2 += p[kcol + ip + half];
-      v += p[vcol + i];
-    }
-    const float2 t = cs[ip];
-    const float k = i < half ? k1 * t.x - k2 * t.y : k2 * t.x + k1 * t.y;
-    const float ks = __fdiv_rn(k, a.k_scale), vs = __fdiv_rn(v, a.v_scale);
-    if (KV8) {
-      reinterpret_cast<uint8_t*>(const_cast<void*>(a.kpool))[base + i] = f32_to_e4m3(ks);
-      reinterpret_cast<uint8_t*>(const_cast<void*>(a.vpool))[base + i] = f32_to_e4m3(vs);
-    } else {
-      reinterpret_cast<uint16_t*>(const_cast<void*>(a.kpool))[base + i] = f32_to_bf16_bits(ks);
-      reinterpret_cast<uint16_t*>(const_cast<void*>(a.vpool))[base + i] = f32_to_bf16_bits(vs);
+    if (!last) {
+      __syncthreads();                                               // chunk consumed
+      stage(s0 + chunk, min(chunk, ns - s0 - chunk));
     }
   }
 }
 
-template <int D, int KV8>
-__global__ void __launch_bounds__(kAttnThreads, 2) attn_split_kernel(const AttnArgs a) {
+template <int D, int KV8, int NT>
+__global__ void __launch_bounds__(kAttnThreads, MBT_ATTN_MINB) attn_split_kernel(const AttnArgs a) {
   using S = AttnShape<D, KV8>;
   extern __shared__ __align__(16) unsigned char smem[];
   const int sp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int G = a.nq / a.nkv;
   const int tid = threadIdx.x;
   const size_t head0 = (size_t)b * a.nq + (size_t)h * G;             // first query head of the group
+  // step inputs (lengths, positions, block tables) are staged before the
+  // step's first kernel starts, so they may be read before the wait
   const int seq = a.seq_lens[b];
   pdl_launch_dependents();
 
-  // The cached context is not produced by the previous kernel: pull this
-  // split's K and V blocks into L2 before waiting for it.
-  if (seq >= 1 && seq <= a.bt_stride * kBlockTokens) {
-    const int nb_all = (seq + kBlockTokens - 1) / kBlockTokens;
-    const int j = sp * a.bps + (tid >> 1);
-    // only the first two tiles: at large batches all CTAs' splits together
-    // exceed L2 and a deeper prefetch would be evicted before use
-    const int pf = min(a.bps, 2 * kAttnTile / kBlockTokens);
-    if ((tid >> 1) < pf && j < nb_all) {
-      const int blk = a.bt[(size_t)b * a.bt_stride + j];
-      if (blk >= 0 && blk <= a.num_blocks) {
-        const size_t off = ((size_t)blk * a.nkv + h) * kBlockTokens * S::ROWB;
-        prefetch_l2((const unsigned char*)((tid & 1) ? a.vpool : a.kpool) + off, kBlockTokens * S::ROWB);
-      }
-    }
-  }
-  pdl_wait();
-
-  if (a.qkv) {
-    // the split holding the new token's block writes its K and V first
-    int pos = a.positions[b];
-    const bool pos_ok = pos >= 0 && pos < a.max_pos;
-    if (!pos_ok && tid == 0 && sp == 0 && h == 0) set_err(a.err, MBT_DEV_POS_RANGE);
-    const int jb = pos_ok ? pos / kBlockTokens : -1;
-    if (pos_ok && jb < a.bt_stride && sp == jb / a.bps) {
-      const int blk = a.bt[(size_t)b * a.bt_stride + jb];
-      if (blk >= 0 && blk <= a.num_blocks) write_new_kv<D, KV8>(a, b, h, pos, blk);
-      else if (tid == 0) set_err(a.err, MBT_DEV_BLOCK_RANGE);
-    } else if (pos_ok && jb >= a.bt_stride && tid == 0 && sp == 0) {
-      set_err(a.err, MBT_DEV_BLOCK_RANGE);
-    }
-    __syncthreads();
-  }
   const bool seq_ok = seq >= 1 && seq <= a.bt_stride * kBlockTokens;
   if (!seq_ok && tid == 0 && sp == 0 && h == 0) set_err(a.err, MBT_DEV_SEQLEN_RANGE);
   const int nblk = seq_ok ? (seq + kBlockTokens - 1) / kBlockTokens : 0;
   const int blk0 = sp * a.bps;
   const int blk1 = min(nblk, blk0 + a.bps);
-  if (blk0 < nblk) attend<D, KV8>(a, smem, b, h, sp, G, head0, seq, blk0, blk1);
-  else if (tid < G) a.part_ml[(head0 + tid) * a.nsplit + sp] = make_float2(-INFINITY, 0.f);
+
+  // the split holding the new token's block writes its K and V
+  bool writer = false;
+  int pos = 0, wblk = 0;
+  if (a.qkv) {
+    pos = a.positions[b];
+    const bool pos_ok = pos >= 0 && pos < a.max_pos;
+    if (!pos_ok && tid == 0 && sp == 0 && h == 0) set_err(a.err, MBT_DEV_POS_RANGE);
+    const int jb = pos_ok ? pos / kBlockTokens : -1;
+    if (pos_ok && jb < a.bt_stride && sp == jb / a.bps) {
+      wblk = a.bt[(size_t)b * a.bt_stride + jb];
+      writer = wblk >= 0 && wblk <= a.num_blocks;
+      if (!writer && tid == 0) set_err(a.err, MBT_DEV_BLOCK_RANGE);
+    } else if (pos_ok && jb >= a.bt_stride && tid == 0 && sp == 0) {
+      set_err(a.err, MBT_DEV_BLOCK_RANGE);
+    }
+  }
+
+  if (blk0 < nblk) {
+    attend<D, KV8, NT>(a, smem, b, h, sp, G, head0, seq, blk0, blk1, writer, pos, wblk);
+  } else {
+    pdl_wait();
+    uint32_t kc, vc;
+    if (writer) write_new_kv<D, KV8>(a, b, h, pos, wblk, kc, vc);
+    if (tid < G) a.part_ml[(head0 + tid) * a.nsplit + sp] = make_float2(-INFINITY, 0.f);
+  }
 
   // ticket: the last CTA of this (row, KV head) merges the splits
   __shared__ int last;
@@ -474,7 +585,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_split_kernel(const AttnA
   __syncthreads();
   if (!last) return;
   __threadfence();
-  merge_splits(a, reinterpret_cast<float*>(smem), G, head0, D);
+  merge_splits(a, smem, S::SMEM, G, head0, D);
   if (tid == 0) a.tickets[(size_t)b * a.nkv + h] = 0;     // ready for the next launch
 }
 
@@ -500,35 +611,44 @@ void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nspli
 }
 
 namespace {
+template <int D, int KV8, int NT>
+void* attn_fn() { return (void*)attn_split_kernel<D, KV8, NT>; }
 template <int D, int KV8>
-void* attn_fn() { return (void*)attn_split_kernel<D, KV8>; }
-void* attn_pick(int d, int kv8, size_t* smem) {
+void* attn_fn_nt(int nt) { return nt == 2 ? attn_fn<D, KV8, 2>() : attn_fn<D, KV8, 1>(); }
+// query heads per KV head: up to 8 in one n-tile of the MMA, up to 16 in two
+void* attn_pick(int d, int kv8, int nt, size_t* smem) {
   if (d == 64) {
     *smem = kv8 ? AttnShape<64, 1>::SMEM : AttnShape<64, 0>::SMEM;
-    return kv8 ? attn_fn<64, 1>() : attn_fn<64, 0>();
+    return kv8 ? attn_fn_nt<64, 1>(nt) : attn_fn_nt<64, 0>(nt);
   }
   *smem = kv8 ? AttnShape<128, 1>::SMEM : AttnShape<128, 0>::SMEM;
-  return kv8 ? attn_fn<128, 1>() : attn_fn<128, 0>();
+  return kv8 ? attn_fn_nt<128, 1>(nt) : attn_fn_nt<128, 0>(nt);
 }
 }  // namespace
 
 cudaError_t attn_init() {
   for (int d : {64, 128})
-    for (int kv8 = 0; kv8 < 2; ++kv8) {
-      size_t sm;
-      void* fn = attn_pick(d, kv8, &sm);
-      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      if (e != cudaSuccess) return e;
-    }
+    for (int kv8 = 0; kv8 < 2; ++kv8)
+      for (int nt = 1; nt <= 2; ++nt) {
+        size_t sm;
+        void* fn = attn_pick(d, kv8, nt, &sm);
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        if (e != cudaSuccess) return e;
+      }
   return cudaSuccess;
 }
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
   size_t sm;
-  void* fn = attn_pick(a.d, a.kv_fp8, &sm);
+  void* fn = attn_pick(a.d, a.kv_fp8, (a.nq / a.nkv) > 8 ? 2 : 1, &sm);
+  // the merge needs the group's weights and at least one split of partials in shared memory
+  const int G = a.nq / a.nkv;
+  const size_t w_bytes = ((size_t)G * a.nsplit * 4 + 15) & ~(size_t)15;
+  if (G * a.d > kMergeMaxE * kAttnThreads || w_bytes + (size_t)2 * G * a.d * 4 > sm) return cudaErrorInvalidValue;
   AttnArgs args = a;
   void* params[] = {&args};
-  return launch_pdl(fn, dim3(a.nsplit, a.nkv, a.B), dim3(kAttnThreads), sm, s, params);
+  return launch_pdl(fn, dim3(a.nsplit, a.nkv, a.B), dim3(kAttnThreads), sm, s, params,
+                    a.carveout > 0 ? a.carveout : -1);
 }
 
 }  // namespace mbt

@@ -103,19 +103,39 @@ gemv_kernel(const GemvArgs a) {
   const size_t row_bytes = (size_t)a.K * (WT == W_BF16 ? 2 : 1);
   const unsigned char* Wb = reinterpret_cast<const unsigned char*>(a.W) + (size_t)v0 * 16;
 
+  // Static part of the schedule: the CTA's contiguous range of rows, or with a
+  // work queue its first static_groups groups (the rest is claimed later).
+  int rb = r_begin, re = r_end;
+  int* const sched = a.sched ? a.sched + split : nullptr;
+  const int dyn0 = a.sched ? G * a.static_groups * CH : a.N;
+  if (sched) {
+    rb = min(a.N, c * a.static_groups * CH);
+    re = min(a.N, rb + a.static_groups * CH);
+  }
+
   // The weights do not depend on the previous kernel: pull this CTA's first
   // rows (all of them when prefetch_bytes says so) into L2 while it drains.
-  if (r_begin < r_end) {
+  if (rb < re) {
     const size_t seg = (size_t)nvec * 16;                       // this split's bytes of a row
     const size_t budget = a.prefetch_bytes ? a.prefetch_bytes : 65536;
-    const int rows = (EPI == EPI_SWIGLU ? 2 : 1) * (r_end - r_begin);
+    const int rows = (EPI == EPI_SWIGLU ? 2 : 1) * (re - rb);
     const int n_pf = (int)min((size_t)rows, max((size_t)1, budget / seg));
     for (int i = tid; i < n_pf; i += kGemvThreads) {
-      const int ch = r_begin + (EPI == EPI_SWIGLU ? i / 2 : i);
+      const int ch = rb + (EPI == EPI_SWIGLU ? i / 2 : i);
       const int wr = (EPI == EPI_SWIGLU && (i & 1)) ? a.N + ch : ch;
       const unsigned char* rp = Wb + (size_t)wr * row_bytes;
       for (size_t o = 0; o < seg; o += 65536)
         prefetch_l2(rp + o, (uint32_t)min(seg - o, (size_t)65536));
+    }
+  }
+  // the norm's gain is a weight too: into registers before the wait
+  constexpr int kGammaPre = 8;
+  uint2 gpre[kGammaPre];
+  if (PRO == PRO_NORM) {
+#pragma unroll
+    for (int j = 0; j < kGammaPre; ++j) {
+      const int k4 = tid + j * kGemvThreads;
+      gpre[j] = k4 < a.K / 4 ? reinterpret_cast<const uint2*>(a.gamma)[k4] : make_uint2(0u, 0u);
     }
   }
   pdl_wait();
@@ -126,13 +146,31 @@ gemv_kernel(const GemvArgs a) {
   float* red = reinterpret_cast<float*>(smem + (size_t)NB * xrow * 16);   // [2][warps][32]
   float* fin = red + 2 * kGemvWarps * 32;                                  // [M]
   if (PRO == PRO_X) {
+    // coalesced float4 reads of this split's slice of each row, XU in flight
+    // per thread, scattered into the [q][v] layout of the tile
     const float* xb = a.x + (size_t)v0 * EPV;
-    for (int i = tid; i < NB * xrow; i += kGemvThreads) {
-      const int b = i / xrow, j = i - b * xrow;          // j = q * nvec + v
-      const int q = j / nvec, v = j - q * nvec;
-      float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (b < a.nb) val = *reinterpret_cast<const float4*>(xb + (size_t)b * a.ldx + (size_t)v * EPV + q * 4);
-      xs[i] = val;
+    constexpr int XU = 8;
+    const int k4n = xrow;                                // float4 per row in this split
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const bool live = b < a.nb;
+      const float4* __restrict__ x4 = reinterpret_cast<const float4*>(xb + (size_t)b * a.ldx);
+      for (int base = 0; base < k4n; base += XU * kGemvThreads) {
+        float4 val[XU];
+#pragma unroll
+        for (int j = 0; j < XU; ++j) {
+          const int k4 = base + tid + j * kGemvThreads;
+          val[j] = (live && k4 < k4n) ? x4[k4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < XU; ++j) {
+          const int k4 = base + tid + j * kGemvThreads;
+          if (k4 < k4n) {
+            const int vv = k4 / QN, q = k4 - vv * QN;
+            xs[(b * QN + q) * nvec + vv] = val[j];
+          }
+        }
+      }
     }
   } else {
     // RMSNorm prologue (nsplit == 1): x = (r_in + sum_s delta_s) / rms * gamma.
@@ -196,7 +234,8 @@ gemv_kernel(const GemvArgs a) {
     const uint2* g2 = reinterpret_cast<const uint2*>(a.gamma);
 #pragma unroll 8
     for (int k4 = tid; k4 < k4n; k4 += kGemvThreads) {
-      const uint2 g = g2[k4];
+      const int j = (k4 - tid) / kGemvThreads;
+      const uint2 g = j < kGammaPre ? gpre[j] : g2[k4];
       const float g0 = bf16_lo(g.x), g1 = bf16_hi(g.x), gg2 = bf16_lo(g.y), g3 = bf16_hi(g.y);
       const int v = k4 / QN, q = k4 - v * QN;
 #pragma unroll
@@ -212,13 +251,24 @@ gemv_kernel(const GemvArgs a) {
   float best_v = -INFINITY;
   int best_i = 0x7fffffff;
   int buf = 0;
+  // Work-queue tail: CTAs stream at unequal rates (a fixed split left the
+  // last CTA of a batch-1 gate/up projection ~60% behind the median), so
+  // after the static part each CTA claims one group at a time. Thread 0 claims
+  // the next group when it starts the last group of its current range, so
+  // the atomic's round trip hides behind that group's loads; groups are
+  // claimed in increasing order, so every CTA still sees its rows ascending.
+  __shared__ int s_next;
+  int claim = 0;
+  if (sched && tid == 0 && rb >= re) claim = atomicAdd(sched, 1);
 
-  for (int r0 = r_begin; r0 < r_end; r0 += CH, buf ^= 1) {
+  for (;;) {
+  for (int r0 = rb; r0 < re; r0 += CH, buf ^= 1) {
+    if (sched && tid == 0 && r0 + CH >= re) claim = atomicAdd(sched, 1);
     const unsigned char* rowp[RG];
 #pragma unroll
     for (int i = 0; i < RG; ++i) {
       int ch = r0 + (i % CH);
-      ch = ch < r_end ? ch : r_end - 1;
+      ch = ch < re ? ch : re - 1;
       const int wr = (EPI == EPI_SWIGLU && i >= CH) ? a.N + ch : ch;
       rowp[i] = Wb + (size_t)wr * row_bytes;
     }
@@ -276,7 +326,7 @@ gemv_kernel(const GemvArgs a) {
         float t = 0.f;
 #pragma unroll
         for (int w2 = 0; w2 < kGemvWarps; ++w2) t += rb[w2 * 32 + tid];
-        if (ch < r_end && b < a.nb) {
+        if (ch < re && b < a.nb) {
           if (WT == W_E4M3) t *= a.scale[ch];
           a.out[(size_t)split * a.split_stride + (size_t)b * a.ldo + ch] = t;
         }
@@ -290,7 +340,7 @@ gemv_kernel(const GemvArgs a) {
           g += rb[w2 * 32 + tid];
           u += rb[w2 * 32 + tid + CH * NB];
         }
-        if (ch < r_end && b < a.nb) {
+        if (ch < re && b < a.nb) {
           if (WT == W_E4M3) { g *= a.scale[ch]; u *= a.scale[a.N + ch]; }
           a.act[(size_t)b * a.lda + ch] = g / (1.f + expf(-g)) * u;
         }
@@ -301,16 +351,16 @@ gemv_kernel(const GemvArgs a) {
         float t = 0.f;
 #pragma unroll
         for (int w2 = 0; w2 < kGemvWarps; ++w2) t += rb[w2 * 32 + tid];
-        if (WT == W_E4M3 && ch < r_end) t *= a.scale[ch];
+        if (WT == W_E4M3 && ch < re) t *= a.scale[ch];
         fin[tid] = t;
-        if (ch < r_end && b < a.nb && a.logits) a.logits[(size_t)b * a.ldl + ch] = t;
+        if (ch < re && b < a.nb && a.logits) a.logits[(size_t)b * a.ldl + ch] = t;
       }
       __syncthreads();
       if (tid < NB) {
 #pragma unroll
         for (int i = 0; i < RG; ++i) {
           const int ch = r0 + i;
-          if (ch < r_end) {
+          if (ch < re) {
             const float t = fin[i * NB + tid];
             if (t > best_v) { best_v = t; best_i = ch; }          // rows ascend: first max kept
             else if (!(t == t)) set_err(a.err, MBT_DEV_NONFINITE);
@@ -318,6 +368,15 @@ gemv_kernel(const GemvArgs a) {
         }
       }
     }
+  }
+  if (!sched) break;
+  // every thread has read the previous s_next: the range above held at least
+  // one group (with its barrier), or this is the first claim
+  if (tid == 0) s_next = claim;
+  __syncthreads();
+  rb = dyn0 + s_next * CH;
+  re = min(a.N, rb + CH);
+  if (rb >= re) break;
   }
   if (EPI == EPI_ARGMAX && tid < NB && tid < a.nb) {
     ArgmaxPart p; p.v = best_v; p.i = best_i;
@@ -329,8 +388,12 @@ gemv_kernel(const GemvArgs a) {
 // host side
 
 namespace {
-constexpr size_t kXsBudgetShared = 96 * 1024;    // x tile that still lets 2 CTAs share an SM
+constexpr size_t kXsBudgetShared = kStreamSmemPerCta - 3 * 1024;   // x tile that still lets 2 CTAs share an SM
 constexpr size_t kXsMax = 216 * 1024;            // largest x tile (1 CTA per SM)
+// work queue: share of each CTA's groups assigned up front, and the fewest
+// groups per CTA for which the queue is used at all
+constexpr double kStaticShare = 0.5;
+constexpr int kMinGroupsPerCta = 4;
 
 int nb_template(int nb) { return nb <= 1 ? 1 : nb <= 2 ? 2 : nb <= 4 ? 4 : 8; }
 
@@ -395,21 +458,32 @@ GemvLaunch gemv_plan(int epi, int wtype, int nb, int N, int K, int num_sms, int 
   g.nsplit = ns;
   const size_t nvec_max = (size_t)(nvec_all + ns - 1) / ns;
   g.smem = (size_t)g.nb_tmpl * nvec_max * 16 * (epv / 4) + 2 * kGemvWarps * 32 * 4 + 32 * 4;
-  const int per_sm = (g.nb_tmpl < 8 && g.smem <= 110 * 1024) ? 2 : 1;
+  const int per_sm = (g.nb_tmpl < 8 && g.smem <= kStreamSmemPerCta) ? 2 : 1;
   int grid = num_sms * per_sm / ns;
   if (grid < 1) grid = 1;
   const int rg = rows_per_group(g.nb_tmpl, epi);
+  g.group_rows = rg;
   const int max_grid = (N + rg - 1) / rg;
   if (grid > max_grid) grid = max_grid;
   g.grid = grid;
   return g;
 }
 
+int gemv_queue_static_groups(const GemvLaunch& g, int N) {
+  // only where a CTA's share spans several groups: one group of a long row
+  // is a sizeable part of the launch, and claiming it late is the tail
+  const int ng = (N + g.group_rows - 1) / g.group_rows;
+  if (ng < kMinGroupsPerCta * g.grid) return -1;
+  return (int)(kStaticShare * ng / g.grid);
+}
+
 cudaError_t gemv_launch(int epi, int pro, const GemvArgs& a, const GemvLaunch& g, cudaStream_t s) {
   void* fn = pick(g.nb_tmpl, a.wtype, epi, pro);
   GemvArgs args = a;
   void* params[] = {&args};
-  return launch_pdl(fn, dim3(g.grid, g.nsplit), dim3(kGemvThreads), g.smem, s, params);
+  // 1 CTA per SM only when the x tile needs more than the batch-1 carveout
+  return launch_pdl(fn, dim3(g.grid, g.nsplit), dim3(kGemvThreads), g.smem, s, params,
+                    g.smem <= kStreamSmemPerCta ? kStreamCarveout : -1);
 }
 
 cudaError_t gemv_init() {
@@ -418,9 +492,13 @@ cudaError_t gemv_init() {
     for (int wt = 0; wt < 2; ++wt)
       for (int epi = 0; epi < 3; ++epi)
         for (int pro = 0; pro < 2; ++pro) {
-          const int lim = 227 * 1024;
-          cudaError_t e = cudaFuncSetAttribute(pick(nbs[i], wt, epi, pro),
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+          // 227 KB per CTA in all, static shared memory included
+          const void* fn = pick(nbs[i], wt, epi, pro);
+          cudaFuncAttributes fa;
+          cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+          if (e != cudaSuccess) return e;
+          const int lim = 227 * 1024 - (int)fa.sharedSizeBytes;
+          e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
           if (e != cudaSuccess) return e;
         }
   return cudaSuccess;

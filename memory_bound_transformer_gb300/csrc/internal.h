@@ -14,11 +14,38 @@ enum Prologue { PRO_X = 0, PRO_NORM = 1 };
 
 // Launch with the programmatic-stream-serialization attribute (PDL) so that the
 // kernel's independent prologue overlaps the previous kernel's tail.
-cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args);
+// Launch with programmatic dependent launch allowed (pdl = true) or as an
+// ordinary stream-ordered launch; carveout >= 0 sets the shared-memory share
+// of the unified L1 (percent) for this launch.
+cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args,
+                      bool pdl, int carveout);
+inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args,
+                              int carveout = -1) {
+  return launch_ex(fn, grid, block, smem, s, args, true, carveout);
+}
 
 struct ArgmaxPart { float v; int i; };
 
 // y = W x for up to 8 batch rows (weight-streaming GEMV, CUDA cores).
+// Shared-memory share of the unified L1 (percent) for every kernel of the
+// CUDA-core (batch 1..15) step. Two things pull on it: the weight stream
+// keeps ~128 KB of loads in flight per SM and those land in L1, so the
+// share must stay well below the maximum; and neighbouring kernels overlap
+// on an SM under programmatic dependent launch only if they ask for the same
+// split (otherwise an SM drains before it takes the next kernel's CTAs).
+// 44% = 100 KB: two GEMV CTAs with up to 46 KB of x tile each, or a BF16
+// attention CTA next to a batch-1 GEMV CTA (measured on the 8B batch-1 step:
+// 44% 2.84 ms, 58% 2.89 ms, 72% 2.94 ms, 86-100% 3.45 ms).
+#ifndef MBT_SMEM_CARVEOUT
+#define MBT_SMEM_CARVEOUT 44
+#endif
+#ifndef MBT_STREAM_SMEM_KB
+#define MBT_STREAM_SMEM_KB 48
+#endif
+constexpr int kStreamCarveout = MBT_SMEM_CARVEOUT;
+// largest dynamic shared memory of a GEMV CTA that runs two per SM under it
+constexpr size_t kStreamSmemPerCta = (size_t)MBT_STREAM_SMEM_KB * 1024;
+
 struct GemvArgs {
   const void* W;            // [rows][K] row-major, BF16 or e4m3 codes
   const float* scale;       // per-row scale for e4m3 weights, else null
@@ -44,9 +71,19 @@ struct GemvArgs {
   // previous kernel (0 = default 64 KB); a kernel that follows a latency-bound
   // one (attention) prefetches its whole slice
   uint32_t prefetch_bytes;
+  // Work queue for the tail (null: every CTA takes one fixed contiguous range
+  // of rows). Otherwise CTA c first takes row groups [c*static_groups,
+  // (c+1)*static_groups) and then claims the groups from grid*static_groups on,
+  // one at a time, from the counter sched[split] (zero at launch, left at the
+  // number of groups claimed + the number of CTAs).
+  int* sched; int static_groups;
 };
 
-struct GemvLaunch { int nb_tmpl; int nsplit; int grid; size_t smem; };
+struct GemvLaunch { int nb_tmpl; int nsplit; int grid; size_t smem; int group_rows; };
+
+// Static groups per CTA when this launch should take the work-queue tail
+// (GemvArgs::sched, one zeroed counter per K split), else -1.
+int gemv_queue_static_groups(const GemvLaunch& g, int N);
 
 // Launch geometry for a GEMV of this shape (deterministic: the same inputs give
 // the same geometry, so eager runs and graph replays do the same arithmetic).
@@ -82,6 +119,8 @@ cudaError_t tc_from_hl(const bf16* hl, int B, int Rp, int N, float* out, cudaStr
 struct EmbedNormArgs {
   int B, H, vocab; const int* tokens; const bf16* embed;
   float* r; const bf16* gamma; float eps; float* y; uint32_t* err;
+  int* zero; int n_zero;    // the step's GEMV work-queue counters, cleared here
+  int carveout;             // launch carveout (percent); 0 (zero-initialised) = the default
 };
 cudaError_t launch_embed_rmsnorm(const EmbedNormArgs& a, cudaStream_t s);
 
@@ -121,6 +160,7 @@ struct AttnArgs {
   int bps; int nsplit;      // KV blocks per split, splits per (row, kv head)
   float* part_o; float2* part_ml; float* out; int* tickets; uint32_t* err;
   bf16* out_hl; int rp_hl;  // optional: output also as BF16 high/low rows [2 * rp_hl][nq * d]
+  int carveout;             // launch carveout (percent); 0 (zero-initialised) = the default
 };
 void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nsplit);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
@@ -128,7 +168,7 @@ cudaError_t attn_init();
 
 // next_ids[b] = index of the best of part[0..G)[b]
 cudaError_t launch_argmax_reduce(int B, const ArgmaxPart* part, int part_ld, int G,
-                                 int* next_ids, uint32_t* err, cudaStream_t s);
+                                 int* next_ids, uint32_t* err, cudaStream_t s, int carveout = -1);
 
 // Copy B caller rows into the graph's static buffers and fill pad rows [B, R).
 struct StageArgs {

@@ -9,17 +9,27 @@ namespace mbt {
 constexpr int kRowThreads = 256;
 constexpr int kNormMaxV = 8;        // float4 per thread: H <= 8 * 4 * 1024
 
-cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args) {
+cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args,
+                      bool pdl, int carveout) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (carveout >= 0) {
+    attr[n].id = cudaLaunchAttributePreferredSharedMemoryCarveout;
+    attr[n].val.sharedMemCarveout = (unsigned)carveout;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = n;
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
@@ -55,6 +65,10 @@ __global__ void __launch_bounds__(1024) embed_rmsnorm_kernel(const EmbedNormArgs
   const int b = blockIdx.x;
   pdl_launch_dependents();
   pdl_wait();
+  // every kernel of the previous step has finished (each waited on its
+  // predecessor), and this step's projections start after this kernel
+  if (b == 0)
+    for (int i = threadIdx.x; i < a.n_zero; i += blockDim.x) a.zero[i] = 0;
   int tok = a.tokens[b];
   if (tok < 0 || tok >= a.vocab) {
     if (threadIdx.x == 0) set_err(a.err, MBT_DEV_TOKEN_RANGE);
@@ -161,9 +175,14 @@ static int norm_threads(int H) {
 
 cudaError_t launch_embed_rmsnorm(const EmbedNormArgs& a, cudaStream_t s) {
   if (a.H % 4 || a.H > 4 * kNormMaxV * 1024) return cudaErrorInvalidValue;
+  // An ordinary launch: the step's first kernel starts only once everything
+  // before it on the stream (the previous step included) has finished, which
+  // is what lets later kernels of the step read the step inputs and the KV
+  // cache before their programmatic wait.
   EmbedNormArgs args = a;
   void* p[] = {&args};
-  return launch_pdl((const void*)embed_rmsnorm_kernel, dim3(a.B), dim3(norm_threads(a.H)), 0, s, p);
+  return launch_ex((const void*)embed_rmsnorm_kernel, dim3(a.B), dim3(norm_threads(a.H)), 0, s, p, false,
+                   a.carveout > 0 ? a.carveout : -1);
 }
 
 cudaError_t launch_add_rmsnorm(const AddNormArgs& a, cudaStream_t s) {
@@ -295,10 +314,10 @@ __global__ void __launch_bounds__(kRowThreads) argmax_reduce_kernel(
 }
 
 cudaError_t launch_argmax_reduce(int B, const ArgmaxPart* part, int part_ld, int G,
-                                 int* next_ids, uint32_t* err, cudaStream_t s) {
+                                 int* next_ids, uint32_t* err, cudaStream_t s, int carveout) {
   (void)err;
   void* p[] = {&part, &part_ld, &G, &next_ids};
-  return launch_pdl((const void*)argmax_reduce_kernel, dim3(B), dim3(kRowThreads), 0, s, p);
+  return launch_pdl((const void*)argmax_reduce_kernel, dim3(B), dim3(kRowThreads), 0, s, p, carveout);
 }
 
 // ---------------------------------------------------------------------------

@@ -70,6 +70,17 @@ int op_gemv(int epi, int w_dtype, const void* W, const float* scales, int N, int
       cudaMallocAsync((void**)&part, (size_t)g0.grid * B * sizeof(ArgmaxPart), s) != cudaSuccess)
     return MBT_ERR_OOM;
   const int step = gemv_max_rows(epi, K);
+  // work-queue counters, one per launch and K split, zeroed
+  const int nlaunch = (B + step - 1) / step;
+  int* sched = nullptr;
+  if (gemv_queue_static_groups(g0, N) >= 0) {
+    const size_t bytes = (size_t)nlaunch * g0.nsplit * sizeof(int);
+    if (cudaMallocAsync((void**)&sched, bytes, s) != cudaSuccess) {
+      if (part) cudaFreeAsync(part, s);
+      return MBT_ERR_OOM;
+    }
+    if (cudaMemsetAsync(sched, 0, bytes, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  }
   for (int b0 = 0; b0 < B && rc == MBT_OK; b0 += step) {
     const int nb = std::min(step, B - b0);
     GemvLaunch g = gemv_plan(epi, wt, nb, N, K, nsm, epi == EPI_PARTIAL ? g0.nsplit : 0);
@@ -82,12 +93,18 @@ int op_gemv(int epi, int w_dtype, const void* W, const float* scales, int N, int
     a.logits = logits ? logits + (size_t)b0 * N : nullptr; a.ldl = N;
     a.part = part ? part + b0 : nullptr; a.part_ld = B;
     a.err = err;
+    const int sg = gemv_queue_static_groups(g, N);
+    if (sched && sg >= 0) {
+      a.sched = sched + (size_t)(b0 / step) * g0.nsplit;
+      a.static_groups = sg;
+    }
     if (gemv_launch(epi, PRO_X, a, g, s) != cudaSuccess) rc = MBT_ERR_CUDA;
   }
   if (rc == MBT_OK && epi == EPI_ARGMAX &&
       launch_argmax_reduce(B, part, B, g0.grid, next_ids, err, s) != cudaSuccess)
     rc = MBT_ERR_CUDA;
   if (part) cudaFreeAsync(part, s);
+  if (sched) cudaFreeAsync(sched, s);
   return rc;
 }
 

@@ -20,6 +20,9 @@ using namespace mbt;
 
 namespace {
 
+// GEMV work-queue counters per step (one per launch and K split)
+constexpr int kSchedCap = 8192;
+
 struct Layer {
   const void* w_qkv; const float* s_qkv;
   const void* w_o; const float* s_o;
@@ -51,6 +54,7 @@ struct Workspace {
   float* delta = nullptr; float* delta2 = nullptr;   // O and down partials [splits][cap][H]
   float* act = nullptr; ArgmaxPart* lm_part = nullptr;
   int* tickets = nullptr;
+  int* sched = nullptr;                              // GEMV work-queue counters, zeroed each step
   int rp_cap = 0;                                    // tensor-core path: BF16 high/low rows
   bf16* x_hl = nullptr; bf16* o_hl = nullptr; bf16* act_hl = nullptr;
 };
@@ -194,6 +198,7 @@ int ensure_ws(mbt_model* m, int R, int mbs) {
   const size_t o_a = take((size_t)cap * F * 4);
   const size_t o_lp = take((size_t)g_lm * cap * sizeof(ArgmaxPart));
   const size_t o_tk = take((size_t)cap * m->h.n_kv_heads * 4);
+  const size_t o_sc = take((size_t)kSchedCap * 4);
   const int rp_cap = (cap + 7) / 8 * 8;
   const size_t b_xhl = (size_t)2 * rp_cap * H * 2, b_ohl = (size_t)2 * rp_cap * Q * 2;
   const size_t b_ahl = (size_t)2 * rp_cap * F * 2;
@@ -210,6 +215,7 @@ int ensure_ws(mbt_model* m, int R, int mbs) {
   w.act = (float*)(base + o_a);
   w.lm_part = (ArgmaxPart*)(base + o_lp);
   w.tickets = (int*)(base + o_tk);
+  w.sched = (int*)(base + o_sc);
   w.rp_cap = rp_cap;
   w.x_hl = (bf16*)(base + o_xhl); w.o_hl = (bf16*)(base + o_ohl); w.act_hl = (bf16*)(base + o_ahl);
   // attention tickets start at zero and every launch leaves them at zero; the
@@ -229,7 +235,8 @@ struct NormIn {
 cudaError_t gemv_rows(const mbt_model* m, int epi, const NormIn* nin, const void* W, const float* sc,
                       int N, int K, const float* x, int R, int nsplit, int grid_fixed, float* out,
                       long long split_stride, int ldo, float* act, int lda, float* logits,
-                      ArgmaxPart* part, int part_ld, cudaStream_t s, uint32_t prefetch = 0) {
+                      ArgmaxPart* part, int part_ld, cudaStream_t s, uint32_t prefetch = 0,
+                      int* sched_used = nullptr) {
   const int pro = nin ? PRO_NORM : PRO_X;
   const int step = gemv_max_rows(epi, K, pro);
   for (int b0 = 0; b0 < R; b0 += step) {
@@ -253,6 +260,14 @@ cudaError_t gemv_rows(const mbt_model* m, int epi, const NormIn* nin, const void
     a.part = part ? part + b0 : nullptr; a.part_ld = part_ld;
     a.err = m->err;
     a.prefetch_bytes = prefetch;
+    // work-queue tail: a fixed share of each CTA's rows, the rest claimed one
+    // group at a time (kernels that prefetch their whole slice keep it fixed)
+    const int sg = gemv_queue_static_groups(g, N);
+    if (sched_used && prefetch != 0xffffffffu && sg >= 0 && *sched_used + g.nsplit <= kSchedCap) {
+      a.sched = m->ws.sched + *sched_used;
+      a.static_groups = sg;
+      *sched_used += g.nsplit;
+    }
     cudaError_t e = gemv_launch(epi, pro, a, g, s);
     if (e != cudaSuccess) return e;
   }
@@ -337,16 +352,18 @@ int run_step(mbt_model* m, mbt_kv* kv, const Plan& p, const int* tok, const int*
   const size_t half = kv_layer_half_bytes(m, kv->num_blocks);
   const long long rh = (long long)R * H;
 
-  EmbedNormArgs en{R, H, V, tok, m->embed, w.r, m->layers[0].g_attn, m->h.eps, nullptr, m->err};
+  EmbedNormArgs en{R, H, V, tok, m->embed, w.r, m->layers[0].g_attn, m->h.eps, nullptr, m->err,
+                   w.sched, kSchedCap, p.use_tc ? 0 : kStreamCarveout};
   MBT_CUDA(launch_embed_rmsnorm(en, s));
   if (p.use_tc) return run_layers_tc(m, kv, p, pos, bt, bt_stride, sl, next_ids, logits, s);
+  int sq = 0;                                        // work-queue counters taken so far
   for (int l = 0; l < (int)m->h.n_layers; ++l) {
     const Layer& L = m->layers[l];
     char* kbase = (char*)kv->pool + 2 * half * (size_t)l;
     // RMSNorm prologue + fused QKV projection
     NormIn n1{w.r, l ? w.delta2 : nullptr, l ? p.ns_down : 0, L.g_attn, w.r2};
     MBT_CUDA(gemv_rows(m, EPI_PARTIAL, &n1, L.w_qkv, L.s_qkv, QKV, H, nullptr, R, 1, 0, w.qkv,
-                       (long long)R * QKV, QKV, nullptr, 0, nullptr, nullptr, 0, s));
+                       (long long)R * QKV, QKV, nullptr, 0, nullptr, nullptr, 0, s, 0, &sq));
     // RoPE + paged KV write + split-K attention + merge
     AttnArgs at = {};
     at.B = R; at.q = nullptr; at.nq = nq; at.nkv = nkv; at.d = d;
@@ -357,6 +374,7 @@ int run_step(mbt_model* m, mbt_kv* kv, const Plan& p, const int* tok, const int*
     at.bt = bt; at.bt_stride = bt_stride; at.seq_lens = sl; at.num_blocks = kv->num_blocks;
     at.bps = p.attn_bps; at.nsplit = p.attn_nsplit;
     at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = w.o; at.tickets = w.tickets; at.err = m->err;
+    at.carveout = kStreamCarveout;
     MBT_CUDA(launch_attention(at, s));
     // O projection (residual partials); it starts during attention, whose
     // batch-1 form leaves HBM idle, so it prefetches all of its weights
@@ -365,17 +383,17 @@ int run_step(mbt_model* m, mbt_kv* kv, const Plan& p, const int* tok, const int*
     // RMSNorm prologue + gate/up projection + SwiGLU epilogue
     NormIn n2{w.r2, w.delta, p.ns_o, L.g_ffn, w.r};
     MBT_CUDA(gemv_rows(m, EPI_SWIGLU, &n2, L.w_gu, L.s_gu, F, H, nullptr, R, 1, 0, nullptr, 0, 0,
-                       w.act, F, nullptr, nullptr, 0, s));
+                       w.act, F, nullptr, nullptr, 0, s, 0, &sq));
     // down projection (residual partials)
     MBT_CUDA(gemv_rows(m, EPI_PARTIAL, nullptr, L.w_down, L.s_down, H, F, w.act, R, p.ns_down, 0,
-                       w.delta2, rh, H, nullptr, 0, nullptr, nullptr, 0, s));
+                       w.delta2, rh, H, nullptr, 0, nullptr, nullptr, 0, s, 0, &sq));
   }
   // final RMSNorm prologue + LM head with the arg-max epilogue, then the
   // cross-CTA reduction
   NormIn nf{w.r, w.delta2, p.ns_down, m->g_final, w.r2};
   MBT_CUDA(gemv_rows(m, EPI_ARGMAX, &nf, m->lm, m->s_lm, V, H, nullptr, R, 1, p.g_lm, nullptr, 0, 0,
-                     nullptr, 0, logits, w.lm_part, R, s));
-  MBT_CUDA(launch_argmax_reduce(R, w.lm_part, R, p.g_lm, next_ids, m->err, s));
+                     nullptr, 0, logits, w.lm_part, R, s, 0, &sq));
+  MBT_CUDA(launch_argmax_reduce(R, w.lm_part, R, p.g_lm, next_ids, m->err, s, kStreamCarveout));
   return MBT_OK;
 }
 

@@ -128,6 +128,45 @@ def test_gemv_argmax(cuda_lib, wt, B):
     assert torch.equal(ids, ids2)
 
 
+@pytest.mark.parametrize("wt", ["bf16", "fp8"])
+@pytest.mark.parametrize("B", [1, 3])
+def test_gemv_work_queue_every_row(cuda_lib, wt, B):
+    """Projections tall enough for the work-queue tail (every CTA owns several
+    8-row groups, half of them claimed at run time): every output row of the
+    three epilogues against the oracle, and the same ids with and without
+    logits (rows reach a CTA out of order across CTAs)."""
+    K = 256
+    N = 16384
+    t, raw = _weights(wt, N, K, seed=101 + B)
+    x = _f32_rand((B, K), seed=31 + B, scale=2.0).to(DEV)
+    W = decode_weight(raw)
+    xv = x.double().cpu().numpy()
+    ref = xv @ W.T
+    bound = TOL_REL * (np.abs(xv) @ np.abs(W).T) + TOL_ABS
+    ns = capi.op_gemv_nsplit(capi.EPI_PARTIAL, _dtype(wt), B, N, K)
+    out = torch.full((ns, B, N), float("nan"), device=DEV)
+    capi.op_gemv(capi.EPI_PARTIAL, _dtype(wt), t["w"], t.get("s"), N, K, x, B, out=out)
+    assert np.all(np.abs(out.sum(0).double().cpu().numpy() - ref) <= bound)
+    # SwiGLU over the same rows read as [gate; up]
+    F = N // 2
+    act = torch.full((B, F), float("nan"), device=DEV)
+    capi.op_gemv(capi.EPI_SWIGLU, _dtype(wt), t["w"], t.get("s"), F, K, x, B, act=act)
+    g, u = ref[:, :F], ref[:, F:]
+    want = silu(g) * u
+    b_act = 1e-6 * np.abs(want) + 1.1 * np.abs(u) * bound[:, :F] + np.abs(silu(g)) * bound[:, F:] + 1e-30
+    assert np.all(np.abs(act.double().cpu().numpy() - want) <= b_act)
+    # arg-max over all rows
+    logits = torch.zeros((B, N), device=DEV)
+    ids = torch.full((B,), -1, dtype=torch.int32, device=DEV)
+    capi.op_gemv(capi.EPI_ARGMAX, _dtype(wt), t["w"], t.get("s"), N, K, x, B, logits=logits, next_ids=ids)
+    lg = logits.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(lg - ref) <= bound)
+    assert np.array_equal(ids.cpu().numpy(), np.argmax(lg, axis=1))
+    ids2 = torch.full((B,), -1, dtype=torch.int32, device=DEV)
+    capi.op_gemv(capi.EPI_ARGMAX, _dtype(wt), t["w"], t.get("s"), N, K, x, B, next_ids=ids2)
+    assert torch.equal(ids, ids2)
+
+
 @pytest.mark.parametrize("wt,N,K,B", [("bf16", 28672, 4096, 1), ("bf16", 4096, 14336, 8),
                                       ("fp8", 8192, 28672, 8), ("fp8", 57344, 8192, 1),
                                       ("bf16", 128256, 4096, 1)])

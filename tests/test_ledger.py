@@ -1,49 +1,56 @@
 """Host logic: the byte/FLOP ledger against the numbers the pages print.
 
-"GPU Inference Internals": machine balance 989e12 / 3.35e12 ~ 295 and
-1979e12 / 3.35e12 ~ 590 ("The Hardware Ledger"); 2 x 70e9 = 140 GFLOP, intensity
-2, 3.35 TB/s / 70 GB ~ 48 tokens/s, crossover of 2B/b_w with 295 at B ~ 295
-("Roofline: Why Decode Is Memory-Bound"); 2 x 80 x 8 x 128 x 2 ~ 320 KB per
-token and ~40 GB at 128K tokens ("The KV-Cache Ledger"); the naive 8192^2 BF16
-score matrix ~ 134 MB ("Kernels: FlashAttention and the Memory Hierarchy").
-"CUDA graphs & kernel fusion", "Code": 5.5 GiB -> 5.9 / 8.1 / 5.9 ms, 1.36x and
-14.2 GiB -> 15.2 / 17.4 / 15.3 ms, 1.14x."""
+The printed values live in tests/golden/ledger_printed.json, each with the page
+title and section it comes from: machine balance ("GPU Inference Internals",
+"The Hardware Ledger"), the 70B FP8 roofline example ("Roofline: Why Decode Is
+Memory-Bound"), KV bytes per token ("The KV-Cache Ledger"), the naive score
+matrix ("Kernels: FlashAttention and the Memory Hierarchy") and the launch-tax
+step model's printed output ("CUDA graphs & kernel fusion", "Code")."""
+import json
+import os
+
 import pytest
 
 from memory_bound_transformer_gb300 import ledger
 from synth import EIGHT_B, SEVENTY_B_FP8, ONE_B
 
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "ledger_printed.json")))
 
-def test_machine_balance():
-    assert round(ledger.machine_balance(989e12, 3.35e12)) == 295
-    assert round(ledger.machine_balance(1979e12, 3.35e12)) == 591     # printed as "~590"
-    assert abs(ledger.machine_balance(1979e12, 3.35e12) - 590) < 1.5
+
+@pytest.mark.parametrize("case", GOLD["machine_balance"], ids=lambda c: str(c["printed"]))
+def test_machine_balance(case):
+    got = ledger.machine_balance(case["peak_flops"], case["hbm_bytes_per_s"])
+    assert abs(got - case["printed"]) <= case["tol"]
 
 
 def test_roofline_70b_example():
-    assert 2 * 70e9 == 140e9
-    assert 140e9 / 70e9 == 2
-    assert round(ledger.single_stream_ceiling(3.35e12, 70e9)) == 48
-    # 2B / b_w reaches 295 FLOP/B near B = 295 for BF16 (b_w = 2) ...
+    c = GOLD["roofline_70b_fp8"]
+    assert 2 * c["params"] == c["flops"]
+    assert c["flops"] / c["weight_bytes"] == c["intensity"]
+    assert round(ledger.single_stream_ceiling(c["hbm_bytes_per_s"], c["weight_bytes"])) == c["tokens_per_s"]
+    # 2B / b_w reaches the BF16 balance (295) near B = 295 with b_w = 2 ...
     assert abs(ledger.weight_intensity(295, 2) - 295) < 1e-9
-    # ... and for FP8 (b_w = 1, balance 590) at the same B
+    # ... and twice that for FP8 (b_w = 1) at the same B
     assert abs(ledger.weight_intensity(295, 1) - 590) < 1e-9
 
 
 def test_kv_ledger():
-    per_tok = ledger.kv_bytes_per_token(80, 8, 128, 2)
-    assert per_tok == 327680
-    assert round(per_tok / 1024) == 320
-    assert abs(per_tok * 128 * 1024 / 2 ** 30 - 40) < 1e-9          # 40 GiB at 128K tokens
-    assert abs(8192 ** 2 * 2 / 1e6 - 134) < 0.3
+    c = GOLD["kv_per_token"]
+    per_tok = ledger.kv_bytes_per_token(c["layers"], c["kv_heads"], c["head_dim"], c["bytes_per_elem"])
+    assert per_tok == 2 * 80 * 8 * 128 * 2
+    assert round(per_tok / 1024) == c["printed_kb"]
+    assert abs(per_tok * 128 * 1024 / 2 ** 30 - c["gib_at_128k"]) < 1e-9
+    n = GOLD["naive_score_matrix"]
+    assert abs(n["tokens"] ** 2 * n["bytes_per_elem"] / 1e6 - n["printed_mb"]) < 0.3
 
 
-@pytest.mark.parametrize("gib,printed", [(5.5, (5.9, 8.1, 5.9, 1.36)), (14.2, (15.2, 17.4, 15.3, 1.14))])
-def test_launch_tax_printed_outputs(gib, printed):
-    c, e, g, s = ledger.launch_tax(gib)
-    assert (round(c, 1), round(e, 1), round(g, 1), round(s, 2)) == printed
+@pytest.mark.parametrize("case", GOLD["launch_tax"], ids=lambda c: str(c["gib"]))
+def test_launch_tax_printed_outputs(case):
+    c, e, g, s = ledger.launch_tax(case["gib"])
+    assert (round(c, 1), round(e, 1), round(g, 1), round(s, 2)) == \
+        (case["compute_ms"], case["eager_ms"], case["graph_ms"], case["speedup"])
     # the remark that the tax is ~36 % of a 6 ms step and ~14 % of a 15 ms step
-    assert round((e - c) / c, 2) in ((0.36,) if gib == 5.5 else (0.14,))
+    assert round((e - c) / c, 2) == case["tax_frac"]
 
 
 def test_step_ledger_configs():
