@@ -40,7 +40,7 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the gate/up GEMV
 # (8B shape, batch 1) from the ncu capture summarised in
 # profiles/gemv_swiglu_8b_b1.md; None until that capture matches this kernel.
-GEMV_TRAFFIC_BYTES = 237759488      # 234.93 MB read + 2.82 MB written (first captured launch)
+GEMV_TRAFFIC_BYTES = 238168320      # 234.93 MB read + 3.24 MB written (first captured launch)
 
 
 def parse():
@@ -233,18 +233,22 @@ def time_gemv_swiglu(cfg, wl, B, dev, reps=3, layers=None):
     x = torch.randn((B, cfg.hidden), device=dev)
     act = torch.empty((B, cfg.ffn), device=dev)
     wdt = capi.DTYPE_E4M3 if cfg.weight_dtype == "fp8" else capi.DTYPE_BF16
+    # the work-queue counters stay zeroed between launches: no memset between them
+    sched = torch.zeros(max(1, capi.op_gemv_sched_ints(capi.EPI_SWIGLU, wdt, B, cfg.ffn, cfg.hidden)),
+                        dtype=torch.int32, device=dev)
     s = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(s):
         for m in mats[:2]:
-            capi.op_gemv(capi.EPI_SWIGLU, wdt, m["w"], m.get("s"), cfg.ffn, cfg.hidden, x, B, act=act, stream=s)
+            capi.op_gemv_ex(capi.EPI_SWIGLU, wdt, m["w"], m.get("s"), cfg.ffn, cfg.hidden, x, B, sched, act=act,
+                            stream=s)
         s.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
         n = 0
         for _ in range(reps):
             for m in mats:
-                capi.op_gemv(capi.EPI_SWIGLU, wdt, m["w"], m.get("s"), cfg.ffn, cfg.hidden, x, B, act=act,
-                             stream=s)
+                capi.op_gemv_ex(capi.EPI_SWIGLU, wdt, m["w"], m.get("s"), cfg.ffn, cfg.hidden, x, B, sched,
+                                act=act, stream=s)
                 n += 1
         e1.record(s)
         s.synchronize()

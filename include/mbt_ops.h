@@ -59,6 +59,23 @@ int op_gemv(int epi, int w_dtype, const void* W, const float* scales, int N, int
             const float* x, int B, int force_nsplit, float* out, float* act,
             float* logits, int32_t* next_ids, int* nsplit_used, uint32_t* err, void* stream);
 
+/* op_gemv_sched_ints: ints of work-queue counters op_gemv_ex may use for this
+ * shape (the projections split their tail into row groups claimed at run
+ * time from one counter per launch and K split). */
+int op_gemv_sched_ints(int epi, int w_dtype, int B, int N, int K);
+
+/* op_gemv_ex: op_gemv with caller-owned work-queue counters: sched_ints
+ * (device, op_gemv_sched_ints(...) ints) must be zero when the call is issued
+ * and is zero again when it completes, so one array serves any number of
+ * calls issued in order on one stream (not calls that run concurrently).
+ * NULL: the counters are allocated and zeroed per call, as op_gemv does. The
+ * pages have no counterpart: it exists so that back-to-back launches (timing
+ * one projection, for one) carry no memset between them. */
+int op_gemv_ex(int epi, int w_dtype, const void* W, const float* scales, int N, int K,
+               const float* x, int B, int force_nsplit, float* out, float* act,
+               float* logits, int32_t* next_ids, int* nsplit_used, int* sched_ints, uint32_t* err,
+               void* stream);
+
 /* op_gemm_tc: the tensor-core (tcgen05) projection the decode step uses at
  * batch 16..128 with BF16 weights: W [rows][K] BF16 (K a multiple of 16,
  * >= 64), x [B][K] fp32 with 1 <= B <= 128, split internally into BF16

@@ -47,6 +47,8 @@ SIGNATURES = {
     "op_add_rmsnorm": (_I, [_I, _I, _P, _P, _I, _P, _F, _P, _P]),
     "op_gemv_nsplit": (_I, [_I, _I, _I, _I, _I]),
     "op_gemv": (_I, [_I, _I, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _P, ctypes.POINTER(_I), _P, _P]),
+    "op_gemv_sched_ints": (_I, [_I, _I, _I, _I, _I]),
+    "op_gemv_ex": (_I, [_I, _I, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _P, ctypes.POINTER(_I), _P, _P, _P]),
     "op_gemm_tc": (_I, [_I, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P]),
     "op_rope_kv_write": (_I, [_I, _P, _I, _I, _I, _P, _P, _I, _I, _F, _P, _P, _I, _I, _F, _F, _P, _P, _P]),
     "op_paged_attention": (_I, [_I, _P, _I, _I, _I, _P, _P, _I, _F, _F, _P, _I, _P, _I, _P, _P, _P]),
@@ -226,6 +228,21 @@ def op_gemv(epi, w_dtype, W, scales, N, K, x, B, force_nsplit=0, out=None, act=N
     _check("op_gemv", load().op_gemv(epi, w_dtype, _ptr(W), _ptr(scales), N, K, _ptr(x), B, force_nsplit,
                                      _ptr(out), _ptr(act), _ptr(logits), _ptr(next_ids),
                                      ctypes.byref(used), _ptr(err), _stream(stream)))
+    return used.value
+
+
+def op_gemv_sched_ints(epi: int, w_dtype: int, B: int, N: int, K: int) -> int:
+    return load().op_gemv_sched_ints(epi, w_dtype, B, N, K)
+
+
+def op_gemv_ex(epi, w_dtype, W, scales, N, K, x, B, sched, force_nsplit=0, out=None, act=None, logits=None,
+               next_ids=None, err=None, stream=None) -> int:
+    """op_gemv with caller-owned work-queue counters (zeroed int32 device
+    tensor of op_gemv_sched_ints(...) elements; left zeroed)."""
+    used = ctypes.c_int()
+    _check("op_gemv_ex", load().op_gemv_ex(epi, w_dtype, _ptr(W), _ptr(scales), N, K, _ptr(x), B, force_nsplit,
+                                           _ptr(out), _ptr(act), _ptr(logits), _ptr(next_ids),
+                                           ctypes.byref(used), _ptr(sched), _ptr(err), _stream(stream)))
     return used.value
 
 

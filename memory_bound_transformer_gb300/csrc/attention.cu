@@ -48,23 +48,10 @@ struct AttnShape {
   static constexpr size_t T_BYTES = (size_t)kAttnTile * BROWB;
   static constexpr size_t R_BYTES = (size_t)kAttnTile * ROWB;
   // BF16 caches: K and V tiles double-buffered in place. e4m3 caches: the raw
-  // tiles are double-buffered and widened into one BF16 K and V tile.
+  // tiles are double-buffered and widened into one FP16 K and V tile.
   static constexpr int NBUF = KV8 ? 1 : 2;
   static constexpr size_t SMEM = Q_BYTES + 2 * NBUF * T_BYTES + (KV8 ? 4 * R_BYTES : 0);
 };
-
-// 16 e4m3 codes -> 16 floats, exactly.
-template <int KV8>
-__device__ __forceinline__ void chunk_to_float(const uint4& c, float* f);
-template <>
-__device__ __forceinline__ void chunk_to_float<1>(const uint4& c, float* f) {
-  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float2 a = e4m3x2_to_float2(w[i]), b = e4m3x2_to_float2(w[i] >> 16);
-    f[4 * i] = a.x; f[4 * i + 1] = a.y; f[4 * i + 2] = b.x; f[4 * i + 3] = b.y;
-  }
-}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
@@ -86,19 +73,44 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
 }
-// D += A (16x16 BF16, row) * B (16x8 BF16, col), fp32 accumulate.
-// Transpose of an 8x8 BF16 matrix held one row pair per lane (mma fragment layout).
+// Transpose of an 8x8 16-bit matrix held one row pair per lane (mma fragment layout).
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
 }
 
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+// x = hi + lo in FP16 (used with e4m3 caches, whose codes widen to FP16 exactly)
+__device__ __forceinline__ void split_f16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+  hi = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+  const __half l0 = __float2half_rn(x0 - __half2float(h0)), l1 = __float2half_rn(x1 - __half2float(h1));
+  lo = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
 }
+// two e4m3 codes (low byte first) -> FP16x2 bits, exactly
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+template <int F16>
+__device__ __forceinline__ void split_hl(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  if (F16) split_f16(x0, x1, hi, lo);
+  else split_bf16(x0, x1, hi, lo);
+}
+
+// D += A (16x16, row) * B (16x8, col), fp32 accumulate; BF16 or FP16 operands.
+template <int F16>
+__device__ __forceinline__ void mma_t(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if (F16)
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  else
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 
 // Fused "RoPE + KV-cache write" ("Kernels, Fusion & CUDA Graphs", "Fix 1:
 // kernel fusion"): rotate the new token's key for KV head h and store it and its
@@ -239,7 +251,10 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
   }
 
   // queries of the group, pre-scaled into the log2 domain with the K dequant scale
-  const float qscale = 1.4426950408889634f / sqrtf((float)D) * a.k_scale;
+  // (e4m3 caches: Q is split in FP16, so the K scale is applied to the fp32
+  // scores instead, keeping Q's range independent of it)
+  const float qscale = 1.4426950408889634f / sqrtf((float)D) * (KV8 ? 1.f : a.k_scale);
+  const float sscale = KV8 ? a.k_scale : 1.f;
   if (a.qkv) {
     // RoPE (rotate-half: element i pairs with i + D/2) straight from the QKV
     // projection's partial sums
@@ -248,16 +263,31 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
     if (qpos < 0 || qpos >= a.max_pos) qpos = 0;
     const float* src = a.qkv + (size_t)b * a.ld_qkv + (size_t)h * G * D;
     const float2* cs = a.rope + (size_t)qpos * half;
-    for (int e = tid; e < G * half; e += kAttnThreads) {
-      const int gg = e / half, i = e - gg * half;
-      float x1 = 0.f, x2 = 0.f;
-      for (int s2 = 0; s2 < a.qkv_nsplit; ++s2) {
-        x1 += src[(size_t)s2 * a.qkv_split_stride + gg * D + i];
-        x2 += src[(size_t)s2 * a.qkv_split_stride + gg * D + i + half];
+    // every load of the thread's elements first (one round trip), then the rotation
+    constexpr int QE = 16 * (D / 2) / kAttnThreads;               // elements per thread at G <= 16
+    float x1[QE], x2[QE];
+    float2 tc[QE];
+#pragma unroll
+    for (int j = 0; j < QE; ++j) {
+      const int e = tid + j * kAttnThreads;
+      x1[j] = 0.f; x2[j] = 0.f; tc[j] = make_float2(0.f, 0.f);
+      if (e < G * half) {
+        const int gg = e / half, i = e - gg * half;
+        for (int s2 = 0; s2 < a.qkv_nsplit; ++s2) {
+          x1[j] += src[(size_t)s2 * a.qkv_split_stride + gg * D + i];
+          x2[j] += src[(size_t)s2 * a.qkv_split_stride + gg * D + i + half];
+        }
+        tc[j] = cs[i];
       }
-      const float2 t = cs[i];
-      qs[gg * D + i] = (x1 * t.x - x2 * t.y) * qscale;
-      qs[gg * D + i + half] = (x2 * t.x + x1 * t.y) * qscale;
+    }
+#pragma unroll
+    for (int j = 0; j < QE; ++j) {
+      const int e = tid + j * kAttnThreads;
+      if (e < G * half) {
+        const int gg = e / half, i = e - gg * half;
+        qs[gg * D + i] = (x1[j] * tc[j].x - x2[j] * tc[j].y) * qscale;
+        qs[gg * D + i + half] = (x2[j] * tc[j].x + x1[j] * tc[j].y) * qscale;
+      }
     }
   } else {
     for (int i = tid; i < G * D; i += kAttnThreads) qs[i] = a.q[head0 * D + i] * qscale;
@@ -275,7 +305,7 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int head = nt * 8 + g, col = 16 * kk + 2 * t4 + r * 8;
-        split_bf16(qs[head * D + col], qs[head * D + col + 1], qh[nt][kk][r], ql[nt][kk][r]);
+        split_hl<KV8>(qs[head * D + col], qs[head * D + col + 1], qh[nt][kk][r], ql[nt][kk][r]);
       }
 
   // softmax state of this thread's two heads per n-tile (nt*8 + 2*t4, +1),
@@ -302,7 +332,8 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
     unsigned char* kt = kbf + (size_t)(KV8 ? 0 : buf) * S::T_BYTES;
     unsigned char* vt = vbf + (size_t)(KV8 ? 0 : buf) * S::T_BYTES;
     if (KV8) {
-      // widen the e4m3 tile to BF16 (exact), swizzled; rows past the context are zero
+      // widen the e4m3 tile to FP16 (exact, one conversion per two codes),
+      // swizzled; rows past the context are zero
       const unsigned char* rk = raw + (size_t)buf * 2 * S::R_BYTES;
       for (int i = tid; i < 2 * kAttnTile * S::NCH; i += kAttnThreads) {
         const int which = i / (kAttnTile * S::NCH), j = i - which * kAttnTile * S::NCH;
@@ -310,10 +341,8 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
         uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
         if (row < nvalid) {
           const uint4 c = *reinterpret_cast<const uint4*>(rk + which * S::R_BYTES + row * S::ROWB + ch * 16);
-          float f[16];
-          chunk_to_float<1>(c, f);
-          lo = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
-          hi = make_uint4(pack_bf16(f[8], f[9]), pack_bf16(f[10], f[11]), pack_bf16(f[12], f[13]), pack_bf16(f[14], f[15]));
+          lo = make_uint4(e4m3x2_to_h2(c.x), e4m3x2_to_h2(c.x >> 16), e4m3x2_to_h2(c.y), e4m3x2_to_h2(c.y >> 16));
+          hi = make_uint4(e4m3x2_to_h2(c.z), e4m3x2_to_h2(c.z >> 16), e4m3x2_to_h2(c.w), e4m3x2_to_h2(c.w >> 16));
         }
         unsigned char* dst = (which ? vt : kt) + row * S::BROWB;
         *reinterpret_cast<uint4*>(dst + (((2 * ch) ^ (row & 7)) * 16)) = lo;
@@ -347,14 +376,15 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
           ldsm_x4(kbase + krow * S::BROWB + ((ch ^ (krow & 7)) * 16), kf);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            mma16816(st[nt], kf, qh[nt][kk][0], qh[nt][kk][1]);
-            mma16816(st[nt], kf, ql[nt][kk][0], ql[nt][kk][1]);
+            mma_t<KV8>(st[nt], kf, qh[nt][kk][0], qh[nt][kk][1]);
+            mma_t<KV8>(st[nt], kf, ql[nt][kk][0], ql[nt][kk][1]);
           }
         }
       }
       const bool v0 = n0 + g < nvalid, v1 = n0 + g + 8 < nvalid;     // tokens of c0/c1 and c2/c3
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
+        if (KV8) { st[nt][0] *= sscale; st[nt][1] *= sscale; st[nt][2] *= sscale; st[nt][3] *= sscale; }
         if (!v0) { st[nt][0] = -INFINITY; st[nt][1] = -INFINITY; }
         if (!v1) { st[nt][2] = -INFINITY; st[nt][3] = -INFINITY; }
         // online softmax per head: the 16 tokens of a column sit in the 8 lanes of one t4
@@ -389,8 +419,8 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         uint32_t h0, l0, h1, l1;
-        split_bf16(st[nt][0], st[nt][1], h0, l0);
-        split_bf16(st[nt][2], st[nt][3], h1, l1);
+        split_hl<KV8>(st[nt][0], st[nt][1], h0, l0);
+        split_hl<KV8>(st[nt][2], st[nt][3], h1, l1);
         ph[nt][0] = movm_t(h0); ph[nt][1] = movm_t(h1);
         pl[nt][0] = movm_t(l0); pl[nt][1] = movm_t(l1);
       }
@@ -403,8 +433,8 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
         ldsm_x4_t(vbase + vrow * S::BROWB + ((ch ^ (vrow & 7)) * 16), vf);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          mma16816(o[nt][mt], vf, ph[nt][0], ph[nt][1]);
-          mma16816(o[nt][mt], vf, pl[nt][0], pl[nt][1]);
+          mma_t<KV8>(o[nt][mt], vf, ph[nt][0], ph[nt][1]);
+          mma_t<KV8>(o[nt][mt], vf, pl[nt][0], pl[nt][1]);
         }
       }
     }
@@ -453,24 +483,25 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
 
 // Merge the splits of the group's G query heads: rescale each partial to the
 // common maximum, sum, divide by the total softmax mass, apply the V scale.
-// The group's partials are pulled into shared memory in chunks of splits with
-// one round of cp.async each (one L2 round trip per chunk instead of one per
-// element a thread sums); one warp per head finds the maximum and the mass
-// while the first chunk is in flight. Splits without tokens left part_o
-// unwritten: their weight is 0 and they are skipped.
+// Only the first na splits hold tokens (the others have zero mass). Their
+// partials are pulled into shared memory with one round of cp.async per
+// chunk (one L2 round trip instead of one per element a thread sums) while
+// the (max, mass) pairs are read alongside; the weights then come from shared
+// memory, one warp per head.
 constexpr int kMergeMaxE = 16;     // G * D <= 16 * 128
 __device__ __forceinline__ void merge_splits(const AttnArgs& a, unsigned char* smem, size_t smem_bytes, int G,
-                                             size_t head0, int D) {
+                                             size_t head0, int D, int na) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ns = a.nsplit;
-  float* wsm = reinterpret_cast<float*>(smem);                      // [G][ns] weights
-  const size_t w_bytes = ((size_t)G * ns * 4 + 15) & ~(size_t)15;
+  const int ns = a.nsplit;                                           // stride of the partials
+  float2* sml = reinterpret_cast<float2*>(smem);                     // [G][na] (max, mass)
+  float* wsm = reinterpret_cast<float*>(smem + (((size_t)G * na * 8 + 15) & ~(size_t)15));   // [G][na] weights
+  const size_t w_bytes = (((size_t)G * na * 8 + 15) & ~(size_t)15) + (((size_t)G * na * 4 + 15) & ~(size_t)15);
   // running sums over chunks when the partials do not fit in one
-  const bool one = w_bytes + (size_t)G * ns * D * 4 <= smem_bytes;
+  const bool one = w_bytes + (size_t)G * na * D * 4 <= smem_bytes;
   float* run = reinterpret_cast<float*>(smem + w_bytes);            // [G * D] (chunked only)
   float* so = one ? run : run + G * D;                               // [G][chunk][D]
   const size_t avail = smem_bytes - (size_t)((unsigned char*)so - smem);
-  const int chunk = one ? ns : max(1, (int)(avail / ((size_t)G * D * 4)));
+  const int chunk = one ? na : max(1, (int)(avail / ((size_t)G * D * 4)));
   auto stage = [&](int s0, int sc) {
     const int per_g = sc * D / 4;                                    // float4 per head in this chunk
     for (int g = 0; g < G; ++g) {
@@ -480,27 +511,32 @@ __device__ __forceinline__ void merge_splits(const AttnArgs& a, unsigned char* s
     }
     cp_async_commit();
   };
-  stage(0, min(chunk, ns));
+  stage(0, min(chunk, na));
+  for (int i = tid; i < G * na; i += kAttnThreads) {
+    const int g = i / na, sidx = i - g * na;
+    sml[i] = a.part_ml[(head0 + g) * ns + sidx];
+  }
+  __syncthreads();                                                   // (max, mass) pairs staged
   for (int g = warp; g < G; g += kAttnThreads / 32) {
-    const float2* ml = a.part_ml + (head0 + g) * ns;
+    const float2* ml = sml + g * na;
     float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) if (ml[s].y > 0.f) M = fmaxf(M, ml[s].x);
+    for (int s = lane; s < na; s += 32) if (ml[s].y > 0.f) M = fmaxf(M, ml[s].x);
     M = warp_max(M);
     float L = 0.f;
-    for (int s = lane; s < ns; s += 32) if (ml[s].y > 0.f) L += exp2f(ml[s].x - M) * ml[s].y;
+    for (int s = lane; s < na; s += 32) if (ml[s].y > 0.f) L += exp2f(ml[s].x - M) * ml[s].y;
     L = warp_sum(L);
     const float inv = L > 0.f ? a.v_scale / L : 0.f;
-    for (int s = lane; s < ns; s += 32) wsm[g * ns + s] = ml[s].y > 0.f ? exp2f(ml[s].x - M) * inv : 0.f;
+    for (int s = lane; s < na; s += 32) wsm[g * na + s] = ml[s].y > 0.f ? exp2f(ml[s].x - M) * inv : 0.f;
   }
-  for (int s0 = 0; s0 < ns; s0 += chunk) {
-    const int sc = min(chunk, ns - s0);
-    const bool last = s0 + chunk >= ns;
+  for (int s0 = 0; s0 < na; s0 += chunk) {
+    const int sc = min(chunk, na - s0);
+    const bool last = s0 + chunk >= na;
     cp_async_wait<0>();
     __syncthreads();                                                 // chunk (and, first time, weights) ready
     for (int e = tid; e < G * D; e += kAttnThreads) {
       const int g = e / D, d = e - g * D;
       const float* po = so + (size_t)g * sc * D + d;
-      const float* wg = wsm + g * ns + s0;
+      const float* wg = wsm + g * na + s0;
       float acc0 = s0 ? run[e] : 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
       int s = 0;
       for (; s + 4 <= sc; s += 4) {
@@ -510,7 +546,7 @@ __device__ __forceinline__ void merge_splits(const AttnArgs& a, unsigned char* s
         if (w2 != 0.f) acc2 += w2 * po[(size_t)(s + 2) * D];
         if (w3 != 0.f) acc3 += w3 * po[(size_t)(s + 3) * D];
       }
-      for (; s < sc; ++s) if (wg[s] != 0.f) acc0 += wg[s] * po[(size_t)s * D];
+    for (; s < sc; ++s) if (wg[s] != 0.f) acc0 += wg[s] * po[(size_t)s * D];
       const float o = (acc0 + acc1) + (acc2 + acc3);
       if (!last) { run[e] = o; continue; }
       const size_t oi = (head0 + g) * D + d;
@@ -524,7 +560,7 @@ __device__ __forceinline__ void merge_splits(const AttnArgs& a, unsigned char* s
     }
     if (!last) {
       __syncthreads();                                               // chunk consumed
-      stage(s0 + chunk, min(chunk, ns - s0 - chunk));
+      stage(s0 + chunk, min(chunk, na - s0 - chunk));
     }
   }
 }
@@ -585,7 +621,9 @@ __global__ void __launch_bounds__(kAttnThreads, MBT_ATTN_MINB) attn_split_kernel
   __syncthreads();
   if (!last) return;
   __threadfence();
-  merge_splits(a, smem, S::SMEM, G, head0, D);
+  // splits past the last one with tokens hold nothing to merge
+  const int na = max(1, min(a.nsplit, (nblk + a.bps - 1) / a.bps));
+  merge_splits(a, smem, S::SMEM, G, head0, D, na);
   if (tid == 0) a.tickets[(size_t)b * a.nkv + h] = 0;     // ready for the next launch
 }
 
@@ -638,12 +676,18 @@ cudaError_t attn_init() {
   return cudaSuccess;
 }
 
+size_t attn_smem_bytes(int d, int kv8, int G) {
+  size_t sm;
+  attn_pick(d, kv8, G > 8 ? 2 : 1, &sm);
+  return sm + sizeof(int) * kMaxSplitBlocks + 16;     // + the staged block ids and the ticket flag
+}
+
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
   size_t sm;
   void* fn = attn_pick(a.d, a.kv_fp8, (a.nq / a.nkv) > 8 ? 2 : 1, &sm);
   // the merge needs the group's weights and at least one split of partials in shared memory
   const int G = a.nq / a.nkv;
-  const size_t w_bytes = ((size_t)G * a.nsplit * 4 + 15) & ~(size_t)15;
+  const size_t w_bytes = (((size_t)G * a.nsplit * 8 + 15) & ~(size_t)15) + (((size_t)G * a.nsplit * 4 + 15) & ~(size_t)15);
   if (G * a.d > kMergeMaxE * kAttnThreads || w_bytes + (size_t)2 * G * a.d * 4 > sm) return cudaErrorInvalidValue;
   AttnArgs args = a;
   void* params[] = {&args};

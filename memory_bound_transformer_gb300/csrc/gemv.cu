@@ -30,6 +30,10 @@ template <> struct GemvShape<4> { static constexpr int RG = 4, U = 2, MINB = 2; 
 template <> struct GemvShape<8> { static constexpr int RG = 4, U = 2, MINB = 1; };
 
 constexpr int kGemvThreads = 256;
+#ifndef MBT_GEMV_PREFETCH_KB
+#define MBT_GEMV_PREFETCH_KB 64
+#endif
+constexpr int kGemvPrefetchKB = MBT_GEMV_PREFETCH_KB;   // default L2 prefetch per CTA before the PDL wait
 constexpr int kGemvWarps = kGemvThreads / 32;
 
 // Reduce M per-lane values over the warp with a transpose: each step halves the
@@ -117,7 +121,7 @@ gemv_kernel(const GemvArgs a) {
   // rows (all of them when prefetch_bytes says so) into L2 while it drains.
   if (rb < re) {
     const size_t seg = (size_t)nvec * 16;                       // this split's bytes of a row
-    const size_t budget = a.prefetch_bytes ? a.prefetch_bytes : 65536;
+    const size_t budget = a.prefetch_bytes ? a.prefetch_bytes : (size_t)kGemvPrefetchKB * 1024;
     const int rows = (EPI == EPI_SWIGLU ? 2 : 1) * (re - rb);
     const int n_pf = (int)min((size_t)rows, max((size_t)1, budget / seg));
     for (int i = tid; i < n_pf; i += kGemvThreads) {
@@ -376,7 +380,14 @@ gemv_kernel(const GemvArgs a) {
   __syncthreads();
   rb = dyn0 + s_next * CH;
   re = min(a.N, rb + CH);
-  if (rb >= re) break;
+  if (rb >= re) {
+    // Every CTA ends with one claim past the last group, so the counter
+    // takes n_dyn + grid claims in all; whoever holds the very last one is
+    // the last to touch it and leaves it at zero for the next launch.
+    const int n_dyn = dyn0 < a.N ? (a.N - dyn0 + CH - 1) / CH : 0;
+    if (tid == 0 && s_next == n_dyn + G - 1) atomicExch(sched, 0);
+    break;
+  }
   }
   if (EPI == EPI_ARGMAX && tid < NB && tid < a.nb) {
     ArgmaxPart p; p.v = best_v; p.i = best_i;
@@ -388,7 +399,6 @@ gemv_kernel(const GemvArgs a) {
 // host side
 
 namespace {
-constexpr size_t kXsBudgetShared = kStreamSmemPerCta - 3 * 1024;   // x tile that still lets 2 CTAs share an SM
 constexpr size_t kXsMax = 216 * 1024;            // largest x tile (1 CTA per SM)
 // work queue: share of each CTA's groups assigned up front, and the fewest
 // groups per CTA for which the queue is used at all
@@ -442,13 +452,15 @@ int gemv_max_rows(int epi, int K, int pro) {
   return 1;
 }
 
-GemvLaunch gemv_plan(int epi, int wtype, int nb, int N, int K, int num_sms, int force_nsplit, int pro) {
+GemvLaunch gemv_plan(int epi, int wtype, int nb, int N, int K, int num_sms, int force_nsplit, int pro,
+                     const StreamCfg& sc) {
   GemvLaunch g;
+  const size_t xs_budget = sc.cta_smem - 3 * 1024;     // x tile that still lets 2 CTAs share an SM
   g.nb_tmpl = nb_template(nb);
   const int epv = wtype == W_BF16 ? 8 : 16;
   const int nvec_all = K / epv;
   const size_t xs_full = (size_t)g.nb_tmpl * K * 4;
-  int ns = (int)((xs_full + kXsBudgetShared - 1) / kXsBudgetShared);
+  int ns = (int)((xs_full + xs_budget - 1) / xs_budget);
   if (g.nb_tmpl == 8) ns = (int)((xs_full + kXsMax - 1) / kXsMax);
   if (epi != EPI_PARTIAL) ns = 1;
   if (force_nsplit > 0) ns = force_nsplit;
@@ -458,7 +470,9 @@ GemvLaunch gemv_plan(int epi, int wtype, int nb, int N, int K, int num_sms, int 
   g.nsplit = ns;
   const size_t nvec_max = (size_t)(nvec_all + ns - 1) / ns;
   g.smem = (size_t)g.nb_tmpl * nvec_max * 16 * (epv / 4) + 2 * kGemvWarps * 32 * 4 + 32 * 4;
-  const int per_sm = (g.nb_tmpl < 8 && g.smem <= kStreamSmemPerCta) ? 2 : 1;
+  const int per_sm = (g.nb_tmpl < 8 && g.smem <= sc.cta_smem) ? 2 : 1;
+  // 1 CTA per SM only when the x tile needs more than the step's split
+  g.carveout = per_sm == 2 ? sc.carveout : -1;
   int grid = num_sms * per_sm / ns;
   if (grid < 1) grid = 1;
   const int rg = rows_per_group(g.nb_tmpl, epi);
@@ -467,6 +481,23 @@ GemvLaunch gemv_plan(int epi, int wtype, int nb, int N, int K, int num_sms, int 
   if (grid > max_grid) grid = max_grid;
   g.grid = grid;
   return g;
+}
+
+StreamCfg stream_config(size_t attn_bytes, int o_k) {
+  const size_t kb = 1024;
+  const size_t gemv1 = (size_t)o_k * 4 + 2 * kGemvWarps * 32 * 4 + 32 * 4;   // batch-1 O-projection CTA
+  const size_t need = attn_bytes + gemv1 + 2 * kb;                             // + 1 KB reserved per CTA
+  const int cfgs[5] = {100, 132, 164, 196, 228};
+  StreamCfg c;
+  for (int kbs : cfgs) {
+    if ((size_t)kbs * kb >= need || kbs == 228) {
+      c.carveout = (kbs * 100 + 114) / 228;                                    // nearest percent
+      c.cta_smem = ((size_t)kbs * kb - 2 * kb) / 2;
+      if (c.cta_smem > kXsMax) c.cta_smem = kXsMax;
+      break;
+    }
+  }
+  return c;
 }
 
 int gemv_queue_static_groups(const GemvLaunch& g, int N) {
@@ -481,9 +512,7 @@ cudaError_t gemv_launch(int epi, int pro, const GemvArgs& a, const GemvLaunch& g
   void* fn = pick(g.nb_tmpl, a.wtype, epi, pro);
   GemvArgs args = a;
   void* params[] = {&args};
-  // 1 CTA per SM only when the x tile needs more than the batch-1 carveout
-  return launch_pdl(fn, dim3(g.grid, g.nsplit), dim3(kGemvThreads), g.smem, s, params,
-                    g.smem <= kStreamSmemPerCta ? kStreamCarveout : -1);
+  return launch_pdl(fn, dim3(g.grid, g.nsplit), dim3(kGemvThreads), g.smem, s, params, g.carveout);
 }
 
 cudaError_t gemv_init() {

@@ -33,9 +33,10 @@ struct ArgmaxPart { float v; int i; };
 // share must stay well below the maximum; and neighbouring kernels overlap
 // on an SM under programmatic dependent launch only if they ask for the same
 // split (otherwise an SM drains before it takes the next kernel's CTAs).
-// 44% = 100 KB: two GEMV CTAs with up to 46 KB of x tile each, or a BF16
-// attention CTA next to a batch-1 GEMV CTA (measured on the 8B batch-1 step:
-// 44% 2.84 ms, 58% 2.89 ms, 72% 2.94 ms, 86-100% 3.45 ms).
+// The model picks the smallest split that holds an attention CTA next to
+// the O projection's GEMV CTA (stream_config); 44% = 100 KB suits an 8B-class
+// model (measured on its batch-1 step: 44% 2.84 ms, 58% 2.89 ms, 72% 2.94 ms,
+// 86-100% 3.45 ms) and is the default of the kernel-level entry points.
 #ifndef MBT_SMEM_CARVEOUT
 #define MBT_SMEM_CARVEOUT 44
 #endif
@@ -45,6 +46,15 @@ struct ArgmaxPart { float v; int i; };
 constexpr int kStreamCarveout = MBT_SMEM_CARVEOUT;
 // largest dynamic shared memory of a GEMV CTA that runs two per SM under it
 constexpr size_t kStreamSmemPerCta = (size_t)MBT_STREAM_SMEM_KB * 1024;
+// Carveout (percent) and per-CTA GEMV shared-memory budget of one step.
+struct StreamCfg {
+  int carveout = kStreamCarveout;
+  size_t cta_smem = kStreamSmemPerCta;
+};
+// The smallest supported split (100, 132, 164, 196 or 228 KB) that holds an
+// attention CTA (attn_bytes, static + dynamic) next to a GEMV CTA whose x tile
+// is o_k fp32 values, and the GEMV budget that lets two of those share an SM.
+StreamCfg stream_config(size_t attn_bytes, int o_k);
 
 struct GemvArgs {
   const void* W;            // [rows][K] row-major, BF16 or e4m3 codes
@@ -74,12 +84,12 @@ struct GemvArgs {
   // Work queue for the tail (null: every CTA takes one fixed contiguous range
   // of rows). Otherwise CTA c first takes row groups [c*static_groups,
   // (c+1)*static_groups) and then claims the groups from grid*static_groups on,
-  // one at a time, from the counter sched[split] (zero at launch, left at the
-  // number of groups claimed + the number of CTAs).
+  // one at a time, from the counter sched[split] (zero at launch; the CTA
+  // that makes the last claim sets it back to zero).
   int* sched; int static_groups;
 };
 
-struct GemvLaunch { int nb_tmpl; int nsplit; int grid; size_t smem; int group_rows; };
+struct GemvLaunch { int nb_tmpl; int nsplit; int grid; size_t smem; int group_rows; int carveout; };
 
 // Static groups per CTA when this launch should take the work-queue tail
 // (GemvArgs::sched, one zeroed counter per K split), else -1.
@@ -88,7 +98,7 @@ int gemv_queue_static_groups(const GemvLaunch& g, int N);
 // Launch geometry for a GEMV of this shape (deterministic: the same inputs give
 // the same geometry, so eager runs and graph replays do the same arithmetic).
 GemvLaunch gemv_plan(int epi, int wtype, int nb, int N, int K, int num_sms, int force_nsplit,
-                     int pro = PRO_X);
+                     int pro = PRO_X, const StreamCfg& sc = StreamCfg());
 // Most batch rows one launch may take for this epilogue and prologue (the fp32
 // x tile must fit in shared memory when K cannot be split).
 int gemv_max_rows(int epi, int K, int pro = PRO_X);
@@ -165,6 +175,7 @@ struct AttnArgs {
 void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nsplit);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
 cudaError_t attn_init();
+size_t attn_smem_bytes(int d, int kv8, int G);   // static + dynamic shared memory of one attention CTA
 
 // next_ids[b] = index of the best of part[0..G)[b]
 cudaError_t launch_argmax_reduce(int B, const ArgmaxPart* part, int part_ld, int G,

@@ -52,6 +52,22 @@ int op_gemv_nsplit(int epi, int w_dtype, int B, int N, int K) {
 int op_gemv(int epi, int w_dtype, const void* W, const float* scales, int N, int K,
             const float* x, int B, int force_nsplit, float* out, float* act,
             float* logits, int32_t* next_ids, int* nsplit_used, uint32_t* err, void* stream) {
+  return op_gemv_ex(epi, w_dtype, W, scales, N, K, x, B, force_nsplit, out, act, logits, next_ids,
+                    nsplit_used, nullptr, err, stream);
+}
+
+int op_gemv_sched_ints(int epi, int w_dtype, int B, int N, int K) {
+  const int n = sm_count();
+  if (n <= 0 || B < 1 || N < 1 || K < 16) return 0;
+  const int step = gemv_max_rows(epi, K);
+  const GemvLaunch g = gemv_plan(epi, w_dtype == MBT_DTYPE_E4M3 ? W_E4M3 : W_BF16, std::min(B, step), N, K, n, 0);
+  return ((B + step - 1) / step) * g.nsplit;
+}
+
+int op_gemv_ex(int epi, int w_dtype, const void* W, const float* scales, int N, int K,
+               const float* x, int B, int force_nsplit, float* out, float* act,
+               float* logits, int32_t* next_ids, int* nsplit_used, int* sched_ints, uint32_t* err,
+               void* stream) {
   if (epi < 0 || epi > 2 || (w_dtype != MBT_DTYPE_BF16 && w_dtype != MBT_DTYPE_E4M3)) return MBT_ERR_BAD_ARG;
   if (!W || !x || B < 1 || N < 1 || K < 16 || K % 16) return MBT_ERR_BAD_ARG;
   if (w_dtype == MBT_DTYPE_E4M3 && !scales) return MBT_ERR_BAD_ARG;
@@ -70,15 +86,18 @@ int op_gemv(int epi, int w_dtype, const void* W, const float* scales, int N, int
       cudaMallocAsync((void**)&part, (size_t)g0.grid * B * sizeof(ArgmaxPart), s) != cudaSuccess)
     return MBT_ERR_OOM;
   const int step = gemv_max_rows(epi, K);
-  // work-queue counters, one per launch and K split, zeroed
+  // work-queue counters, one per launch and K split, zero at launch (the
+  // kernel leaves them at zero): the caller's, or allocated and zeroed here
   const int nlaunch = (B + step - 1) / step;
-  int* sched = nullptr;
-  if (gemv_queue_static_groups(g0, N) >= 0) {
+  int* sched = sched_ints;
+  bool own = false;
+  if (!sched && gemv_queue_static_groups(g0, N) >= 0) {
     const size_t bytes = (size_t)nlaunch * g0.nsplit * sizeof(int);
     if (cudaMallocAsync((void**)&sched, bytes, s) != cudaSuccess) {
       if (part) cudaFreeAsync(part, s);
       return MBT_ERR_OOM;
     }
+    own = true;
     if (cudaMemsetAsync(sched, 0, bytes, s) != cudaSuccess) rc = MBT_ERR_CUDA;
   }
   for (int b0 = 0; b0 < B && rc == MBT_OK; b0 += step) {
@@ -104,7 +123,7 @@ int op_gemv(int epi, int w_dtype, const void* W, const float* scales, int N, int
       launch_argmax_reduce(B, part, B, g0.grid, next_ids, err, s) != cudaSuccess)
     rc = MBT_ERR_CUDA;
   if (part) cudaFreeAsync(part, s);
-  if (sched) cudaFreeAsync(sched, s);
+  if (own) cudaFreeAsync(sched, s);
   return rc;
 }
 

@@ -23,6 +23,8 @@ namespace {
 // GEMV work-queue counters per step (one per launch and K split)
 constexpr int kSchedCap = 8192;
 
+
+
 struct Layer {
   const void* w_qkv; const float* s_qkv;
   const void* w_o; const float* s_o;
@@ -71,6 +73,7 @@ struct mbt_model {
   mbt_blob_header h;
   int device = 0, num_sms = 0;
   int wtype = W_BF16, kv8 = 0;
+  StreamCfg stream;                 // L1 split and GEMV shared-memory budget of the batch 1..15 step
   void* wmem = nullptr;
   size_t wbytes = 0;
   const bf16* embed = nullptr; const bf16* g_final = nullptr;
@@ -143,10 +146,12 @@ Plan make_plan(const mbt_model* m, int R, int mbs) {
     return p;
   }
   p.ns_qkv = 1;                                          // norm prologue: whole rows per CTA
-  p.ns_o = gemv_plan(EPI_PARTIAL, m->wtype, nb0, H, Q, m->num_sms, 0).nsplit;
-  p.ns_down = gemv_plan(EPI_PARTIAL, m->wtype, nb0, H, F, m->num_sms, 0).nsplit;
+  p.ns_o = gemv_plan(EPI_PARTIAL, m->wtype, nb0, H, Q, m->num_sms, 0, PRO_X, m->stream).nsplit;
+  p.ns_down = gemv_plan(EPI_PARTIAL, m->wtype, nb0, H, F, m->num_sms, 0, PRO_X, m->stream).nsplit;
   const int mn = gemv_max_rows(EPI_ARGMAX, H, PRO_NORM);
-  p.g_lm = gemv_plan(EPI_ARGMAX, m->wtype, std::min(nb0, mn), (int)m->h.vocab, H, m->num_sms, 0, PRO_NORM).grid;
+  p.g_lm = gemv_plan(EPI_ARGMAX, m->wtype, std::min(nb0, mn), (int)m->h.vocab, H, m->num_sms, 0, PRO_NORM,
+                     m->stream).grid;
+
   const int c8 = (R + 7) / 8;
   const int cn = (R + mn - 1) / mn;                      // chunks of the norm-prologue projections
   p.kernels = 1 + L * (2 * cn + 2 * c8 + 1) + cn + 1;
@@ -241,7 +246,7 @@ cudaError_t gemv_rows(const mbt_model* m, int epi, const NormIn* nin, const void
   const int step = gemv_max_rows(epi, K, pro);
   for (int b0 = 0; b0 < R; b0 += step) {
     const int nb = std::min(step, R - b0);
-    GemvLaunch g = gemv_plan(epi, m->wtype, nb, N, K, m->num_sms, epi == EPI_PARTIAL ? nsplit : 0, pro);
+    GemvLaunch g = gemv_plan(epi, m->wtype, nb, N, K, m->num_sms, epi == EPI_PARTIAL ? nsplit : 0, pro, m->stream);
     if (grid_fixed > 0) g.grid = grid_fixed;
     GemvArgs a;
     memset(&a, 0, sizeof(a));
@@ -353,7 +358,7 @@ int run_step(mbt_model* m, mbt_kv* kv, const Plan& p, const int* tok, const int*
   const long long rh = (long long)R * H;
 
   EmbedNormArgs en{R, H, V, tok, m->embed, w.r, m->layers[0].g_attn, m->h.eps, nullptr, m->err,
-                   w.sched, kSchedCap, p.use_tc ? 0 : kStreamCarveout};
+                   w.sched, kSchedCap, p.use_tc ? 0 : m->stream.carveout};
   MBT_CUDA(launch_embed_rmsnorm(en, s));
   if (p.use_tc) return run_layers_tc(m, kv, p, pos, bt, bt_stride, sl, next_ids, logits, s);
   int sq = 0;                                        // work-queue counters taken so far
@@ -374,10 +379,10 @@ int run_step(mbt_model* m, mbt_kv* kv, const Plan& p, const int* tok, const int*
     at.bt = bt; at.bt_stride = bt_stride; at.seq_lens = sl; at.num_blocks = kv->num_blocks;
     at.bps = p.attn_bps; at.nsplit = p.attn_nsplit;
     at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = w.o; at.tickets = w.tickets; at.err = m->err;
-    at.carveout = kStreamCarveout;
+    at.carveout = m->stream.carveout;
     MBT_CUDA(launch_attention(at, s));
     // O projection (residual partials); it starts during attention, whose
-    // batch-1 form leaves HBM idle, so it prefetches all of its weights
+    // batch-1 form leaves HBM idle, so it prefetches all of its weights and
     MBT_CUDA(gemv_rows(m, EPI_PARTIAL, nullptr, L.w_o, L.s_o, H, Q, w.o, R, p.ns_o, 0, w.delta,
                        rh, H, nullptr, 0, nullptr, nullptr, 0, s, 0xffffffffu));
     // RMSNorm prologue + gate/up projection + SwiGLU epilogue
@@ -393,7 +398,7 @@ int run_step(mbt_model* m, mbt_kv* kv, const Plan& p, const int* tok, const int*
   NormIn nf{w.r, w.delta2, p.ns_down, m->g_final, w.r2};
   MBT_CUDA(gemv_rows(m, EPI_ARGMAX, &nf, m->lm, m->s_lm, V, H, nullptr, R, 1, p.g_lm, nullptr, 0, 0,
                      nullptr, 0, logits, w.lm_part, R, s, 0, &sq));
-  MBT_CUDA(launch_argmax_reduce(R, w.lm_part, R, p.g_lm, next_ids, m->err, s, kStreamCarveout));
+  MBT_CUDA(launch_argmax_reduce(R, w.lm_part, R, p.g_lm, next_ids, m->err, s, m->stream.carveout));
   return MBT_OK;
 }
 
@@ -527,6 +532,8 @@ int model_create(const void* blob, size_t bytes, int blob_is_device, void* strea
   m->num_sms = prop.multiProcessorCount;
   m->wtype = fp8 ? W_E4M3 : W_BF16;
   m->kv8 = h.kv_dtype == MBT_DTYPE_E4M3;
+  m->stream = stream_config(attn_smem_bytes((int)h.head_dim, m->kv8, (int)(h.n_q_heads / h.n_kv_heads)),
+                            (int)(h.n_q_heads * h.head_dim));
   int rc = MBT_OK;
   if (gemv_init() != cudaSuccess || attn_init() != cudaSuccess) rc = MBT_ERR_CUDA;
   if (rc == MBT_OK && cudaMalloc(&m->wmem, total) != cudaSuccess) { cudaGetLastError(); rc = MBT_ERR_OOM; }

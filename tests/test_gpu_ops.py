@@ -165,6 +165,17 @@ def test_gemv_work_queue_every_row(cuda_lib, wt, B):
     ids2 = torch.full((B,), -1, dtype=torch.int32, device=DEV)
     capi.op_gemv(capi.EPI_ARGMAX, _dtype(wt), t["w"], t.get("s"), N, K, x, B, next_ids=ids2)
     assert torch.equal(ids, ids2)
+    # caller-owned counters: three launches in a row on one zeroed array give
+    # the same bits as op_gemv, and the array is zero again afterwards
+    n_int = capi.op_gemv_sched_ints(capi.EPI_PARTIAL, _dtype(wt), B, N, K)
+    assert n_int >= 1
+    sched = torch.zeros(n_int, dtype=torch.int32, device=DEV)
+    for _ in range(3):
+        out2 = torch.full_like(out, float("nan"))
+        capi.op_gemv_ex(capi.EPI_PARTIAL, _dtype(wt), t["w"], t.get("s"), N, K, x, B, sched, out=out2)
+        torch.cuda.synchronize()
+        assert torch.equal(out2, out)
+        assert int(sched.abs().sum().item()) == 0
 
 
 @pytest.mark.parametrize("wt,N,K,B", [("bf16", 28672, 4096, 1), ("bf16", 4096, 14336, 8),
