@@ -89,6 +89,16 @@ int op_gemm_tc(int epi, const void* W, const float* scales, int N, int K, const 
                int ksplit, float* out, float* act, float* logits, int32_t* next_ids, uint32_t* err,
                void* stream);
 
+/* op_gemm_tc_e4m3: as op_gemm_tc for e4m3 weights W [rows][K] (codes) with
+ * fp32 per-row scales (required): the codes are widened to FP16 in shared
+ * memory, x is split into FP16 high/low rows, the scale is applied in the
+ * epilogue ("Kernel Fusion for Large-Scale LLM Inference", section 11, FP8
+ * weights and "Epilogue and dequant fusion"). K a multiple of 16, >= 64;
+ * 1 <= B <= 128. */
+int op_gemm_tc_e4m3(int epi, const void* W, const float* scales, int N, int K, const float* x, int B,
+                    int ksplit, float* out, float* act, float* logits, int32_t* next_ids, uint32_t* err,
+                    void* stream);
+
 /* op_rope_kv_write: rotate q and k of qkv [B][(nq + 2 nkv) d] (fp32; q heads,
  * then k heads, then v heads) at positions[b] with the rotate-half pairing
  * (element i with i + d/2, angle p * theta^(-2i/d)), write rotated q to q_out

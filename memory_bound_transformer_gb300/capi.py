@@ -50,6 +50,7 @@ SIGNATURES = {
     "op_gemv_sched_ints": (_I, [_I, _I, _I, _I, _I]),
     "op_gemv_ex": (_I, [_I, _I, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _P, ctypes.POINTER(_I), _P, _P, _P]),
     "op_gemm_tc": (_I, [_I, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "op_gemm_tc_e4m3": (_I, [_I, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P]),
     "op_rope_kv_write": (_I, [_I, _P, _I, _I, _I, _P, _P, _I, _I, _F, _P, _P, _I, _I, _F, _F, _P, _P, _P]),
     "op_paged_attention": (_I, [_I, _P, _I, _I, _I, _P, _P, _I, _F, _F, _P, _I, _P, _I, _P, _P, _P]),
     "op_paged_attention_noalloc": (_I, [_I, _P, _I, _I, _I, _P, _P, _I, _F, _F, _P, _I, _P, _I, _P, _P, _P]),
@@ -244,6 +245,13 @@ def op_gemv_ex(epi, w_dtype, W, scales, N, K, x, B, sched, force_nsplit=0, out=N
                                            _ptr(out), _ptr(act), _ptr(logits), _ptr(next_ids),
                                            ctypes.byref(used), _ptr(sched), _ptr(err), _stream(stream)))
     return used.value
+
+
+def op_gemm_tc_e4m3(epi, W, scales, N, K, x, B, ksplit=1, out=None, act=None, logits=None, next_ids=None,
+                    err=None, stream=None) -> None:
+    _check("op_gemm_tc_e4m3", load().op_gemm_tc_e4m3(epi, _ptr(W), _ptr(scales), N, K, _ptr(x), B, ksplit,
+                                                     _ptr(out), _ptr(act), _ptr(logits), _ptr(next_ids),
+                                                     _ptr(err), _stream(stream)))
 
 
 def op_gemm_tc(epi, W, scales, N, K, x, B, ksplit=1, out=None, act=None, logits=None, next_ids=None,

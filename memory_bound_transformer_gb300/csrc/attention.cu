@@ -87,11 +87,6 @@ __device__ __forceinline__ void split_f16(float x0, float x1, uint32_t& hi, uint
   const __half l0 = __float2half_rn(x0 - __half2float(h0)), l1 = __float2half_rn(x1 - __half2float(h1));
   lo = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
 }
-// two e4m3 codes (low byte first) -> FP16x2 bits, exactly
-__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
-}
 template <int F16>
 __device__ __forceinline__ void split_hl(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   if (F16) split_f16(x0, x1, hi, lo);
@@ -341,8 +336,10 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
         uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
         if (row < nvalid) {
           const uint4 c = *reinterpret_cast<const uint4*>(rk + which * S::R_BYTES + row * S::ROWB + ch * 16);
-          lo = make_uint4(e4m3x2_to_h2(c.x), e4m3x2_to_h2(c.x >> 16), e4m3x2_to_h2(c.y), e4m3x2_to_h2(c.y >> 16));
-          hi = make_uint4(e4m3x2_to_h2(c.z), e4m3x2_to_h2(c.z >> 16), e4m3x2_to_h2(c.w), e4m3x2_to_h2(c.w >> 16));
+          lo = make_uint4(e4m3x2_to_h2bits(c.x), e4m3x2_to_h2bits(c.x >> 16), e4m3x2_to_h2bits(c.y),
+                          e4m3x2_to_h2bits(c.y >> 16));
+          hi = make_uint4(e4m3x2_to_h2bits(c.z), e4m3x2_to_h2bits(c.z >> 16), e4m3x2_to_h2bits(c.w),
+                          e4m3x2_to_h2bits(c.w >> 16));
         }
         unsigned char* dst = (which ? vt : kt) + row * S::BROWB;
         *reinterpret_cast<uint4*>(dst + (((2 * ch) ^ (row & 7)) * 16)) = lo;
@@ -551,11 +548,14 @@ __device__ __forceinline__ void merge_splits(const AttnArgs& a, unsigned char* s
       if (!last) { run[e] = o; continue; }
       const size_t oi = (head0 + g) * D + d;
       if (a.out) a.out[oi] = o;
-      if (a.out_hl) {                              // high/low BF16 rows for the tensor-core GEMM
+      if (a.out_hl) {                              // high/low 16-bit rows for the tensor-core GEMM
         const size_t row = oi / ((size_t)a.nq * D), col = oi % ((size_t)a.nq * D);
-        const bf16 h = __float2bfloat16_rn(o);
-        a.out_hl[row * a.nq * D + col] = h;
-        a.out_hl[(a.rp_hl + row) * a.nq * D + col] = __float2bfloat16_rn(o - __bfloat162float(h));
+        uint16_t* hl = reinterpret_cast<uint16_t*>(a.out_hl);
+        const float hv = a.hl_f16 ? __half2float(__float2half_rn(o)) : __bfloat162float(__float2bfloat16_rn(o));
+        hl[row * a.nq * D + col] = a.hl_f16 ? __half_as_ushort(__float2half_rn(o))
+                                            : __bfloat16_as_ushort(__float2bfloat16_rn(o));
+        hl[(a.rp_hl + row) * a.nq * D + col] = a.hl_f16 ? __half_as_ushort(__float2half_rn(o - hv))
+                                                         : __bfloat16_as_ushort(__float2bfloat16_rn(o - hv));
       }
     }
     if (!last) {

@@ -60,6 +60,25 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
   return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
 
+// Two e4m3 codes (low byte first) -> FP16x2 bits, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_h2bits(uint32_t two_codes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// x = hi + lo in the 16-bit format the next tensor-core projection reads.
+__device__ __forceinline__ void store_hl16(uint16_t* hi_at, uint16_t* lo_at, float x, int f16) {
+  if (f16) {
+    const __half h = __float2half_rn(x);
+    *hi_at = __half_as_ushort(h);
+    *lo_at = __half_as_ushort(__float2half_rn(x - __half2float(h)));
+  } else {
+    const bf16 h = __float2bfloat16_rn(x);
+    *hi_at = __bfloat16_as_ushort(h);
+    *lo_at = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+  }
+}
+
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }

@@ -114,16 +114,23 @@ struct TcArgs {
   const float* scale;         // per-row weight scale or null
   float* out; long long split_stride; int ldo;       // EPI_PARTIAL: out[split][b][n]
   bf16* act_hl; int ld_act;                            // EPI_SWIGLU: [2 * Rp][ld_act] hi/lo rows
+  int hl_f16;                                          // act_hl rows as FP16 (e4m3 weights), else BF16
   float* logits; int ldl; ArgmaxPart* part; int part_ld;   // EPI_ARGMAX
   uint32_t* err;
 };
 cudaError_t tc_init();
 cudaError_t tc_make_map(void* map, const void* base, int rows, int K, int box_rows);
 cudaError_t tc_launch(int epi, const void* mapW, const void* mapX, const TcArgs& a, int ksplit, cudaStream_t s);
+// e4m3 weights: [rows][K] codes, 64-code x 64-row boxes without swizzle; the
+// activations as FP16 high/low rows (map from tc_make_map)
+cudaError_t tc_make_map_u8(void* map, const void* base, int rows, int K);
+cudaError_t tc8_init();
+cudaError_t tc8_launch(int epi, const void* mapW, const void* mapX, const TcArgs& a, int ksplit, cudaStream_t s);
+size_t tc8_smem(int Rp);
 int tc_tiles(int epi, int N);
 size_t tc_smem(int Rp);
-cudaError_t tc_to_hl(const float* x, int B, int Rp, int K, bf16* hl, cudaStream_t s);
-cudaError_t tc_from_hl(const bf16* hl, int B, int Rp, int N, float* out, cudaStream_t s);
+cudaError_t tc_to_hl(const float* x, int B, int Rp, int K, bf16* hl, cudaStream_t s, int f16 = 0);
+cudaError_t tc_from_hl(const bf16* hl, int B, int Rp, int N, float* out, cudaStream_t s, int f16 = 0);
 
 // r <- E[token] (fp32); y <- rmsnorm(r) * gamma (fp32)
 struct EmbedNormArgs {
@@ -141,6 +148,7 @@ struct AddNormArgs {
   int B, H; float* r; const float* delta; int n_delta; long long delta_stride;
   const bf16* gamma; float eps; float* y;
   bf16* y_hl; int rp;
+  int hl_f16;               // y_hl rows as FP16 (for e4m3 weights) rather than BF16
 };
 cudaError_t launch_add_rmsnorm(const AddNormArgs& a, cudaStream_t s);
 
@@ -169,7 +177,8 @@ struct AttnArgs {
   const int* bt; int bt_stride; const int* seq_lens; int num_blocks;
   int bps; int nsplit;      // KV blocks per split, splits per (row, kv head)
   float* part_o; float2* part_ml; float* out; int* tickets; uint32_t* err;
-  bf16* out_hl; int rp_hl;  // optional: output also as BF16 high/low rows [2 * rp_hl][nq * d]
+  bf16* out_hl; int rp_hl;  // optional: output also as 16-bit high/low rows [2 * rp_hl][nq * d]
+  int hl_f16;               // out_hl as FP16 (for e4m3 weights) rather than BF16
   int carveout;             // launch carveout (percent); 0 (zero-initialised) = the default
 };
 void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nsplit);

@@ -95,10 +95,11 @@ __global__ void __launch_bounds__(1024) embed_rmsnorm_kernel(const EmbedNormArgs
 // "Residual add + RMSNorm ... doing both in one pass" ("Kernels, Fusion & CUDA
 // Graphs", "Fix 1: kernel fusion"). The projection before it left its output
 // as split-K partial sums; they are added here too, in a fixed order.
-// y as BF16 high/low rows (y = hi + lo to ~2^-17) for the tensor-core GEMM.
+// y as 16-bit high/low rows (BF16: y = hi + lo to ~2^-17; FP16 for e4m3
+// weights) for the tensor-core GEMM.
 __device__ __forceinline__ void norm_store_hl(const float4 (&v)[kNormMaxV], float ss, int H,
-                                             const bf16* __restrict__ gamma, float eps, bf16* hi_row,
-                                             bf16* lo_row, float* scratch) {
+                                             const bf16* __restrict__ gamma, float eps, uint16_t* hi_row,
+                                             uint16_t* lo_row, float* scratch, int f16) {
   const float tot = block_sum(ss, scratch);
   const float inv = 1.0f / sqrtf(tot / (float)H + eps);
   const int nv = H / 4;
@@ -111,11 +112,7 @@ __device__ __forceinline__ void norm_store_hl(const float4 (&v)[kNormMaxV], floa
       const float o[4] = {v[j].x * inv * bf16_lo(g.x), v[j].y * inv * bf16_hi(g.x),
                           v[j].z * inv * bf16_lo(g.y), v[j].w * inv * bf16_hi(g.y)};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const bf16 h = __float2bfloat16_rn(o[e]);
-        hi_row[4 * i + e] = h;
-        lo_row[4 * i + e] = __float2bfloat16_rn(o[e] - __bfloat162float(h));
-      }
+      for (int e = 0; e < 4; ++e) store_hl16(hi_row + 4 * i + e, lo_row + 4 * i + e, o[e], f16);
     }
   }
 }
@@ -157,8 +154,10 @@ __global__ void __launch_bounds__(1024) add_rmsnorm_kernel(const AddNormArgs a) 
     const int i = threadIdx.x + j * blockDim.x;
     if (i < nv) r[i] = v[j];
   }
-  if (a.y_hl)
-    norm_store_hl(v, ss, a.H, a.gamma, a.eps, a.y_hl + (size_t)b * a.H, a.y_hl + (size_t)(a.rp + b) * a.H, scratch);
+  if (a.y_hl) {
+    uint16_t* hl = reinterpret_cast<uint16_t*>(a.y_hl);
+    norm_store_hl(v, ss, a.H, a.gamma, a.eps, hl + (size_t)b * a.H, hl + (size_t)(a.rp + b) * a.H, scratch, a.hl_f16);
+  }
   else
     norm_store(v, ss, a.H, a.gamma, a.eps, a.y + (size_t)b * a.H, scratch);
 }

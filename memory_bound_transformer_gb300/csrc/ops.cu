@@ -127,16 +127,20 @@ int op_gemv_ex(int epi, int w_dtype, const void* W, const float* scales, int N, 
   return rc;
 }
 
-int op_gemm_tc(int epi, const void* W, const float* scales, int N, int K, const float* x, int B,
-               int ksplit, float* out, float* act, float* logits, int32_t* next_ids, uint32_t* err,
-               void* stream) {
+namespace {
+// Shared body of the BF16 (f8 = 0) and e4m3 (f8 = 1) tensor-core entry points.
+int gemm_tc_impl(int f8, int epi, const void* W, const float* scales, int N, int K, const float* x, int B,
+                 int ksplit, float* out, float* act, float* logits, int32_t* next_ids, uint32_t* err,
+                 void* stream) {
+  if (f8 && !scales) return MBT_ERR_BAD_ARG;
   if (epi < 0 || epi > 2 || !W || !x || B < 1 || B > 128 || N < 1 || K < 64 || K % 16) return MBT_ERR_BAD_ARG;
   if ((epi == EPI_PARTIAL && !out) || (epi == EPI_SWIGLU && !act) || (epi == EPI_ARGMAX && !next_ids))
     return MBT_ERR_BAD_ARG;
   if (epi != EPI_PARTIAL) ksplit = 1;
   if (ksplit < 1) ksplit = 1;
   {
-    const cudaError_t e = tc_init();
+    cudaError_t e = tc_init();
+    if (e == cudaSuccess && f8) e = tc8_init();
     if (e == cudaErrorNotSupported) return MBT_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return MBT_ERR_CUDA;
   }
@@ -154,20 +158,35 @@ int op_gemm_tc(int epi, const void* W, const float* scales, int N, int K, const 
   bf16* ahl = (bf16*)(scratch + ((b_x + 255) & ~(size_t)255));
   ArgmaxPart* part = (ArgmaxPart*)((char*)ahl + ((b_a + 255) & ~(size_t)255));
   TmaMap wm, xm;
-  if (tc_make_map(&wm, W, wrows, K, 64) != cudaSuccess || tc_make_map(&xm, xhl, 2 * Rp, K, 2 * Rp) != cudaSuccess)
-    rc = MBT_ERR_BAD_ARG;
-  if (rc == MBT_OK && tc_to_hl(x, B, Rp, K, xhl, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  const cudaError_t me = f8 ? tc_make_map_u8(&wm, W, wrows, K) : tc_make_map(&wm, W, wrows, K, 64);
+  if (me != cudaSuccess || tc_make_map(&xm, xhl, 2 * Rp, K, 2 * Rp) != cudaSuccess) rc = MBT_ERR_BAD_ARG;
+  if (rc == MBT_OK && tc_to_hl(x, B, Rp, K, xhl, s, f8) != cudaSuccess) rc = MBT_ERR_CUDA;
   TcArgs a = {};
   a.N = N; a.K = K; a.R = B; a.Rp = Rp; a.scale = scales;
   a.out = out; a.split_stride = (long long)B * N; a.ldo = N;
-  a.act_hl = ahl; a.ld_act = N;
+  a.act_hl = ahl; a.ld_act = N; a.hl_f16 = f8;
   a.logits = logits; a.ldl = N; a.part = part; a.part_ld = B; a.err = err;
-  if (rc == MBT_OK && tc_launch(epi, &wm, &xm, a, ksplit, s) != cudaSuccess) rc = MBT_ERR_CUDA;
-  if (rc == MBT_OK && epi == EPI_SWIGLU && tc_from_hl(ahl, B, Rp, N, act, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+  if (rc == MBT_OK &&
+      (f8 ? tc8_launch(epi, &wm, &xm, a, ksplit, s) : tc_launch(epi, &wm, &xm, a, ksplit, s)) != cudaSuccess)
+    rc = MBT_ERR_CUDA;
+  if (rc == MBT_OK && epi == EPI_SWIGLU && tc_from_hl(ahl, B, Rp, N, act, s, f8) != cudaSuccess) rc = MBT_ERR_CUDA;
   if (rc == MBT_OK && epi == EPI_ARGMAX && launch_argmax_reduce(B, part, B, tiles, next_ids, err, s) != cudaSuccess)
     rc = MBT_ERR_CUDA;
   cudaFreeAsync(scratch, s);
   return rc;
+}
+}  // namespace
+
+int op_gemm_tc(int epi, const void* W, const float* scales, int N, int K, const float* x, int B,
+               int ksplit, float* out, float* act, float* logits, int32_t* next_ids, uint32_t* err,
+               void* stream) {
+  return gemm_tc_impl(0, epi, W, scales, N, K, x, B, ksplit, out, act, logits, next_ids, err, stream);
+}
+
+int op_gemm_tc_e4m3(int epi, const void* W, const float* scales, int N, int K, const float* x, int B,
+                    int ksplit, float* out, float* act, float* logits, int32_t* next_ids, uint32_t* err,
+                    void* stream) {
+  return gemm_tc_impl(1, epi, W, scales, N, K, x, B, ksplit, out, act, logits, next_ids, err, stream);
 }
 
 int op_rope_kv_write(int B, const float* qkv, int nq, int nkv, int d, const int32_t* positions,

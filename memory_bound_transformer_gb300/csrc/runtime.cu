@@ -120,7 +120,8 @@ size_t kv_layer_half_bytes(const mbt_model* m, int num_blocks) {
 
 int tc_ksplit(const mbt_model* m, int epi, int N, int K) {
   const int tiles = tc_tiles(epi, N);
-  int ks = 2 * m->num_sms / tiles;             // two CTAs per SM
+  // two CTAs per SM (BF16), one (e4m3: its deeper copy ring fills the SM)
+  int ks = (m->wtype == W_E4M3 ? 1 : 2) * m->num_sms / tiles;
   const int chunks = (K + 63) / 64;
   if (ks > chunks / 4) ks = chunks / 4;        // at least 4 stages of K per split
   return ks < 1 ? 1 : ks;
@@ -296,15 +297,20 @@ int run_layers_tc(mbt_model* m, mbt_kv* kv, const Plan& p, const int* pos, const
   MBT_CUDA(tc_make_map(&xh, w.x_hl, 2 * Rp, H, 2 * Rp));
   MBT_CUDA(tc_make_map(&xq, w.o_hl, 2 * Rp, Q, 2 * Rp));
   MBT_CUDA(tc_make_map(&xf, w.act_hl, 2 * Rp, F, 2 * Rp));
+  // e4m3 weights: FP16 activations and the widening kernel; BF16 otherwise
+  const int f16 = m->wtype == W_E4M3;
+  auto gemm = [&](int epi, const void* wm, const void* xm, const TcArgs& a, int ks) {
+    return f16 ? tc8_launch(epi, wm, xm, a, ks, s) : tc_launch(epi, wm, xm, a, ks, s);
+  };
   auto norm = [&](const float* delta, int n_delta, const bf16* gamma) {
-    AddNormArgs an{R, H, w.r, delta, n_delta, rh, gamma, m->h.eps, nullptr, w.x_hl, Rp};
+    AddNormArgs an{R, H, w.r, delta, n_delta, rh, gamma, m->h.eps, nullptr, w.x_hl, Rp, f16};
     return launch_add_rmsnorm(an, s);
   };
   auto partial = [&](const TmaMap& wm, const TmaMap& xm, const float* sc, int N, int K, float* out, int ks) {
     TcArgs a = {};
     a.N = N; a.K = K; a.R = R; a.Rp = Rp; a.scale = sc;
     a.out = out; a.split_stride = (long long)R * N; a.ldo = N; a.err = m->err;
-    return tc_launch(EPI_PARTIAL, &wm, &xm, a, ks, s);
+    return gemm(EPI_PARTIAL, &wm, &xm, a, ks);
   };
   for (int l = 0; l < (int)m->h.n_layers; ++l) {
     const Layer& L = m->layers[l];
@@ -321,20 +327,21 @@ int run_layers_tc(mbt_model* m, mbt_kv* kv, const Plan& p, const int* pos, const
     at.bt = bt; at.bt_stride = bt_stride; at.seq_lens = sl; at.num_blocks = kv->num_blocks;
     at.bps = p.attn_bps; at.nsplit = p.attn_nsplit;
     at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = nullptr; at.tickets = w.tickets; at.err = m->err;
-    at.out_hl = w.o_hl; at.rp_hl = Rp;
+    at.out_hl = w.o_hl; at.rp_hl = Rp; at.hl_f16 = f16;
     MBT_CUDA(launch_attention(at, s));
     MBT_CUDA(partial(wm[1], xq, L.s_o, H, Q, w.delta, p.ns_o));
     MBT_CUDA(norm(w.delta, p.ns_o, L.g_ffn));
     TcArgs g = {};
     g.N = F; g.K = H; g.R = R; g.Rp = Rp; g.scale = L.s_gu; g.act_hl = w.act_hl; g.ld_act = F; g.err = m->err;
-    MBT_CUDA(tc_launch(EPI_SWIGLU, &wm[2], &xh, g, 1, s));
+    g.hl_f16 = f16;
+    MBT_CUDA(gemm(EPI_SWIGLU, &wm[2], &xh, g, 1));
     MBT_CUDA(partial(wm[3], xf, L.s_down, H, F, w.delta2, p.ns_down));
   }
   MBT_CUDA(norm(w.delta2, p.ns_down, m->g_final));
   TcArgs a = {};
   a.N = V; a.K = H; a.R = R; a.Rp = Rp; a.scale = m->s_lm; a.logits = logits; a.ldl = V;
   a.part = w.lm_part; a.part_ld = R; a.err = m->err;
-  MBT_CUDA(tc_launch(EPI_ARGMAX, &m->wmaps[(size_t)m->h.n_layers * 4], &xh, a, 1, s));
+  MBT_CUDA(gemm(EPI_ARGMAX, &m->wmaps[(size_t)m->h.n_layers * 4], &xh, a, 1));
   MBT_CUDA(launch_argmax_reduce(R, w.lm_part, R, p.g_lm, next_ids, m->err, s));
   return MBT_OK;
 }
@@ -582,20 +589,23 @@ int model_create(const void* blob, size_t bytes, int blob_is_device, void* strea
     L.w_down = at(MBT_T_W_DOWN, l); L.s_down = (const float*)at(MBT_T_S_DOWN, l);
     L.g_attn = (const bf16*)at(MBT_T_G_ATTN, l); L.g_ffn = (const bf16*)at(MBT_T_G_FFN, l);
   }
-  // tensor maps for the tensor-core path (BF16 weights; 64-row boxes)
-  if (m->wtype == W_BF16 && tc_init() == cudaSuccess) {
+  // tensor maps for the tensor-core path (64-row boxes: BF16 tiles swizzled
+  // for the MMA, e4m3 tiles plain for the widening warps)
+  if (tc_init() == cudaSuccess && (m->wtype == W_BF16 || tc8_init() == cudaSuccess)) {
     const int Hh = (int)h.hidden, Qd = (int)(h.n_q_heads * h.head_dim), Ff = (int)h.ffn;
     const int QKVr = (int)((h.n_q_heads + 2 * h.n_kv_heads) * h.head_dim);
+    auto mk = [&](TmaMap* map, const void* base, int rows, int K) {
+      return (m->wtype == W_E4M3 ? tc_make_map_u8(map, base, rows, K) : tc_make_map(map, base, rows, K, 64)) ==
+             cudaSuccess;
+    };
     m->wmaps.resize((size_t)h.n_layers * 4 + 1);
     bool ok = true;
     for (int l = 0; l < (int)h.n_layers && ok; ++l) {
       const Layer& L = m->layers[l];
-      ok = tc_make_map(&m->wmaps[l * 4 + 0], L.w_qkv, QKVr, Hh, 64) == cudaSuccess &&
-           tc_make_map(&m->wmaps[l * 4 + 1], L.w_o, Hh, Qd, 64) == cudaSuccess &&
-           tc_make_map(&m->wmaps[l * 4 + 2], L.w_gu, 2 * Ff, Hh, 64) == cudaSuccess &&
-           tc_make_map(&m->wmaps[l * 4 + 3], L.w_down, Hh, Ff, 64) == cudaSuccess;
+      ok = mk(&m->wmaps[l * 4 + 0], L.w_qkv, QKVr, Hh) && mk(&m->wmaps[l * 4 + 1], L.w_o, Hh, Qd) &&
+           mk(&m->wmaps[l * 4 + 2], L.w_gu, 2 * Ff, Hh) && mk(&m->wmaps[l * 4 + 3], L.w_down, Hh, Ff);
     }
-    ok = ok && tc_make_map(&m->wmaps[(size_t)h.n_layers * 4], m->lm, (int)h.vocab, Hh, 64) == cudaSuccess;
+    ok = ok && mk(&m->wmaps[(size_t)h.n_layers * 4], m->lm, (int)h.vocab, Hh);
     m->tc_ok = ok;
   }
   cudaGetLastError();

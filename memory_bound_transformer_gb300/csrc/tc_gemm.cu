@@ -18,91 +18,12 @@
 //   * epilogues read TMEM with tcgen05.ld: split-K partial sums, SwiGLU over a
 //     tile of 64 gate + 64 up rows (written back as hi/lo BF16 for the down
 //     projection), or a per-tile arg-max for the LM head.
-#include <cuda.h>
-
-#include "common.cuh"
-#include "internal.h"
+#include "tcgen05.cuh"
 
 namespace mbt {
 
 constexpr int kTcThreads = 128;
-constexpr int kTcBM = 128;              // weight rows per tile (MMA M)
-constexpr int kTcBK = 64;               // K elements per stage: one 128-byte swizzle row of BF16
 constexpr int kTcStages = 3;            // 3 x 32 KB at 64 rows: two CTAs fit an SM
-constexpr long long kTcWaitCycles = 4000000000LL;   // about 2 s at GB300 clocks
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t n) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(n) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok) : "r"(smem_u32(b)), "r"(parity) : "memory");
-  return ok != 0;
-}
-// Wait for a phase; false once the time limit has passed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
-  if (mbar_try(b, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try(b, parity))
-    if (clock64() - t0 > kTcWaitCycles) return false;
-  return true;
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)) : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major tile of 128-byte rows, 128-byte
-// swizzle, 8-row (1024-byte) atoms stacked along M/N.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFF);        // start address
-  d |= (uint64_t)1 << 16;                         // leading byte offset (unused here), 16 B
-  d |= (uint64_t)(1024 >> 4) << 32;               // stride byte offset: one 8-row atom
-  d |= (uint64_t)1 << 46;                         // descriptor version
-  d |= (uint64_t)2 << 61;                         // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: BF16 A and B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-      ::"r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 8 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 template <int EPI>
 __global__ void __launch_bounds__(kTcThreads, 2)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const TcArgs a) {
@@ -175,7 +96,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   } else if (warp == 1 && lane == 0) {
     pdl_wait();
     // MMA issuer: 4 MMAs of K = 16 per 64-element stage
-    const uint32_t idesc = idesc_bf16(kTcBM, NM);
+    const uint32_t idesc = idesc_16(kTcBM, NM, 0);
     bool ok = true;
     for (int i = 0; i < nk; ++i) {
       const int s = i % kTcStages;
@@ -186,7 +107,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
       const uint64_t bd = sw128_desc(smem_u32(sB + s * b_bytes));
 #pragma unroll
       for (int kk = 0; kk < kTcBK / 16; ++kk)
-        umma_bf16(tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        umma_kf16(tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (i > 0 || kk > 0) ? 1u : 0u);
       umma_commit(&empty[s]);
     }
     if (ok) umma_commit(&done);
@@ -204,98 +125,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   __syncthreads();
   const bool have = have_s != 0;
   tc_fence_after();
-  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-  const int row = warp * 32 + lane;
   if (!have) {
     if (tid == 0 && (abort_flag || nk > 0)) set_err(a.err, MBT_DEV_WAIT_LIMIT);
-  } else if (EPI == EPI_PARTIAL) {
-    const int n = tile * kTcBM + row;
-    const float sc = (a.scale && n < a.N) ? a.scale[n] : 1.f;
-    for (int c0 = 0; c0 < Rp; c0 += 8) {
-      float hi[8], lo[8];
-      tmem_ld8(lane_base + c0, hi);
-      tmem_ld8(lane_base + Rp + c0, lo);
-      if (n < a.N) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (c0 + j < a.R)
-            a.out[(size_t)split * a.split_stride + (size_t)(c0 + j) * a.ldo + n] = (hi[j] + lo[j]) * sc;
-      }
-    }
-  } else if (EPI == EPI_SWIGLU) {
-    // lanes 0..63: gate rows, 64..127: up rows of channels tile*64 + (row % 64)
-    float* ex = reinterpret_cast<float*>(sA);      // [64][Rp] up values (the stage ring is free now)
-    const int j = tile * 64 + (row & 63);
-    const bool ch_ok = j < a.N;
-    if (warp >= 2) {
-      const float su = (a.scale && ch_ok) ? a.scale[a.N + j] : 1.f;
-      for (int c0 = 0; c0 < Rp; c0 += 8) {
-        float hi[8], lo[8];
-        tmem_ld8(lane_base + c0, hi);
-        tmem_ld8(lane_base + Rp + c0, lo);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) ex[(row - 64) * Rp + c0 + q] = (hi[q] + lo[q]) * su;
-      }
-    }
-    __syncthreads();
-    if (warp < 2) {
-      const float sg = (a.scale && ch_ok) ? a.scale[j] : 1.f;
-      for (int c0 = 0; c0 < Rp; c0 += 8) {
-        float hi[8], lo[8];
-        tmem_ld8(lane_base + c0, hi);
-        tmem_ld8(lane_base + Rp + c0, lo);
-        if (ch_ok) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int b = c0 + q;
-            const float g = (hi[q] + lo[q]) * sg;
-            const float u = ex[row * Rp + b];
-            const float act = b < a.R ? g / (1.f + expf(-g)) * u : 0.f;
-            const bf16 h = __float2bfloat16_rn(act);
-            a.act_hl[(size_t)b * a.ld_act + j] = h;
-            a.act_hl[(size_t)(Rp + b) * a.ld_act + j] = __float2bfloat16_rn(act - __bfloat162float(h));
-          }
-        }
-      }
-    }
-  } else {  // EPI_ARGMAX
-    float* bv = reinterpret_cast<float*>(sA);        // [4 warps][Rp]
-    int* bi = reinterpret_cast<int*>(sA + 4 * Rp * 4);
-    const int n = tile * kTcBM + row;
-    const float sc = (a.scale && n < a.N) ? a.scale[n] : 1.f;
-    for (int c0 = 0; c0 < Rp; c0 += 8) {
-      float hi[8], lo[8];
-      tmem_ld8(lane_base + c0, hi);
-      tmem_ld8(lane_base + Rp + c0, lo);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int b = c0 + q;
-        float v = n < a.N ? (hi[q] + lo[q]) * sc : -INFINITY;
-        if (!(v == v)) { set_err(a.err, MBT_DEV_NONFINITE); v = -INFINITY; }
-        if (n < a.N && b < a.R && a.logits) a.logits[(size_t)b * a.ldl + n] = v;
-        int idx = n;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-          if (ov > v || (ov == v && oi < idx)) { v = ov; idx = oi; }
-        }
-        if (lane == 0) { bv[warp * Rp + b] = v; bi[warp * Rp + b] = idx; }
-      }
-    }
-    __syncthreads();
-    for (int b = tid; b < a.R; b += kTcThreads) {
-      float v = bv[b];
-      int idx = bi[b];
-      for (int w2 = 1; w2 < 4; ++w2) {
-        const float ov = bv[w2 * Rp + b];
-        const int oi = bi[w2 * Rp + b];
-        if (ov > v || (ov == v && oi < idx)) { v = ov; idx = oi; }
-      }
-      ArgmaxPart p;
-      p.v = v; p.i = idx;
-      a.part[(size_t)tile * a.part_ld + b] = p;
-    }
+  } else {
+    tc_epilogue<EPI>(a, tmem, warp, lane, tid, tile, split, sA, 1);     // the stage ring is free now
   }
 
   // teardown: no TMA or MMA of this CTA is still in flight once `done` fired;
@@ -311,30 +144,32 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   }
 }
 
-// fp32 rows -> BF16 high/low rows [2 * Rp][K] (rows B..Rp-1 zero).
-__global__ void to_hl_kernel(const float* x, int B, int Rp, int K, bf16* hl) {
+// fp32 rows -> 16-bit (BF16, or FP16 when f16) high/low rows [2 * Rp][K] (rows B..Rp-1 zero).
+__global__ void to_hl_kernel(const float* x, int B, int Rp, int K, uint16_t* hl, int f16) {
   const int b = blockIdx.x;
   for (int k = threadIdx.x; k < K; k += blockDim.x) {
     const float v = b < B ? x[(size_t)b * K + k] : 0.f;
-    const bf16 h = __float2bfloat16_rn(v);
-    hl[(size_t)b * K + k] = h;
-    hl[(size_t)(Rp + b) * K + k] = __float2bfloat16_rn(v - __bfloat162float(h));
+    store_hl16(hl + (size_t)b * K + k, hl + (size_t)(Rp + b) * K + k, v, f16);
   }
 }
 
-// act[b][j] = hi + lo of the SwiGLU epilogue's high/low rows.
-__global__ void from_hl_kernel(const bf16* hl, int B, int Rp, int N, float* out) {
-  const int b = blockIdx.x;
-  for (int j = threadIdx.x; j < N; j += blockDim.x)
-    out[(size_t)b * N + j] = __bfloat162float(hl[(size_t)b * N + j]) + __bfloat162float(hl[(size_t)(Rp + b) * N + j]);
+__device__ __forceinline__ float hl16_to_f32(uint16_t u, int f16) {
+  return f16 ? __half2float(__ushort_as_half(u)) : __uint_as_float((uint32_t)u << 16);
 }
 
-cudaError_t tc_to_hl(const float* x, int B, int Rp, int K, bf16* hl, cudaStream_t s) {
-  to_hl_kernel<<<Rp, 256, 0, s>>>(x, B, Rp, K, hl);
+// act[b][j] = hi + lo of the SwiGLU epilogue's high/low rows.
+__global__ void from_hl_kernel(const uint16_t* hl, int B, int Rp, int N, float* out, int f16) {
+  const int b = blockIdx.x;
+  for (int j = threadIdx.x; j < N; j += blockDim.x)
+    out[(size_t)b * N + j] = hl16_to_f32(hl[(size_t)b * N + j], f16) + hl16_to_f32(hl[(size_t)(Rp + b) * N + j], f16);
+}
+
+cudaError_t tc_to_hl(const float* x, int B, int Rp, int K, bf16* hl, cudaStream_t s, int f16) {
+  to_hl_kernel<<<Rp, 256, 0, s>>>(x, B, Rp, K, reinterpret_cast<uint16_t*>(hl), f16);
   return cudaGetLastError();
 }
-cudaError_t tc_from_hl(const bf16* hl, int B, int Rp, int N, float* out, cudaStream_t s) {
-  from_hl_kernel<<<B, 256, 0, s>>>(hl, B, Rp, N, out);
+cudaError_t tc_from_hl(const bf16* hl, int B, int Rp, int N, float* out, cudaStream_t s, int f16) {
+  from_hl_kernel<<<B, 256, 0, s>>>(reinterpret_cast<const uint16_t*>(hl), B, Rp, N, out, f16);
   return cudaGetLastError();
 }
 
@@ -383,6 +218,21 @@ cudaError_t tc_make_map(void* map, const void* base, int rows, int K, int box_ro
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode((CUtensorMap*)map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// 2-D tensor map over e4m3 codes [rows][K] (K contiguous), box of 64 codes x
+// 64 rows, no swizzle (the widening warps read it), zero fill out of bounds.
+cudaError_t tc_make_map_u8(void* map, const void* base, int rows, int K) {
+  if (!g_encode) return cudaErrorNotSupported;
+  if (((uintptr_t)base & 15) || K % 16) return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K};
+  const cuuint32_t box[2] = {(cuuint32_t)kTcBK, 64u};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode((CUtensorMap*)map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

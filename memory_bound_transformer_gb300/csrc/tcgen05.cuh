@@ -1,0 +1,205 @@
+// tcgen05 building blocks shared by the BF16 and the e4m3 skinny GEMMs:
+// mbarriers (every wait bounded), TMA tile loads, shared-memory and
+// instruction descriptors, the MMA and commit, TMEM loads, and the epilogues
+// that read the fp32 accumulator out of TMEM.
+#pragma once
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mbt {
+
+constexpr int kTcBM = 128;              // weight rows per tile (MMA M)
+constexpr int kTcBK = 64;               // K elements per stage: one 128-byte swizzle row of 16-bit values
+constexpr long long kTcWaitCycles = 4000000000LL;   // about 2 s at GB300 clocks
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(smem_u32(b)), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Wait for a phase; false once the time limit has passed.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+  if (mbar_try(b, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try(b, parity))
+    if (clock64() - t0 > kTcWaitCycles) return false;
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major tile of 128-byte rows, 128-byte
+// swizzle, 8-row (1024-byte) atoms stacked along M/N.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);        // start address
+  d |= (uint64_t)1 << 16;                         // leading byte offset (unused here), 16 B
+  d |= (uint64_t)(1024 >> 4) << 32;               // stride byte offset: one 8-row atom
+  d |= (uint64_t)1 << 46;                         // descriptor version
+  d |= (uint64_t)2 << 61;                         // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 D, A and B both BF16 (f16 = 0) or
+// both FP16 (f16 = 1), both K-major.
+__host__ __device__ constexpr uint32_t idesc_16(int M, int N, int f16) {
+  return (1u << 4) | (f16 ? 0u : (1u << 7) | (1u << 10)) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_kf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+      ::"r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 8 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+// Generic-proxy writes to shared memory made visible to the tensor core (async proxy).
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Barrier among `n` threads (a multiple of 32) under id `id` (1..15).
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Epilogue of one 128-row tile, run by four warps whose TMEM lane quarters are
+// q = 0..3 (lane `lane` of quarter q holds weight row q*32 + lane): split-K
+// partials, SwiGLU over 64 gate + 64 up rows (written as 16-bit high/low rows
+// for the down projection), or the tile's arg-max per batch row. `scratch`
+// (free shared memory, >= 64 * Rp * 4 bytes) and barrier `bar` of the 128
+// epilogue threads are the epilogue's own. `et` = the thread's index among them.
+template <int EPI>
+__device__ __forceinline__ void tc_epilogue(const TcArgs& a, uint32_t tmem, int q, int lane, int et, int tile,
+                                            int split, unsigned char* scratch, int bar) {
+  const int Rp = a.Rp;
+  const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+  const int row = q * 32 + lane;
+  if (EPI == EPI_PARTIAL) {
+    const int n = tile * kTcBM + row;
+    const float sc = (a.scale && n < a.N) ? a.scale[n] : 1.f;
+    for (int c0 = 0; c0 < Rp; c0 += 8) {
+      float hi[8], lo[8];
+      tmem_ld8(lane_base + c0, hi);
+      tmem_ld8(lane_base + Rp + c0, lo);
+      if (n < a.N) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (c0 + j < a.R)
+            a.out[(size_t)split * a.split_stride + (size_t)(c0 + j) * a.ldo + n] = (hi[j] + lo[j]) * sc;
+      }
+    }
+  } else if (EPI == EPI_SWIGLU) {
+    // lanes 0..63: gate rows, 64..127: up rows of channels tile*64 + (row % 64)
+    float* ex = reinterpret_cast<float*>(scratch);   // [64][Rp] up values
+    const int j = tile * 64 + (row & 63);
+    const bool ch_ok = j < a.N;
+    uint16_t* act = reinterpret_cast<uint16_t*>(a.act_hl);
+    if (q >= 2) {
+      const float su = (a.scale && ch_ok) ? a.scale[a.N + j] : 1.f;
+      for (int c0 = 0; c0 < Rp; c0 += 8) {
+        float hi[8], lo[8];
+        tmem_ld8(lane_base + c0, hi);
+        tmem_ld8(lane_base + Rp + c0, lo);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ex[(row - 64) * Rp + c0 + k] = (hi[k] + lo[k]) * su;
+      }
+    }
+    named_bar(bar, 128);
+    if (q < 2) {
+      const float sg = (a.scale && ch_ok) ? a.scale[j] : 1.f;
+      for (int c0 = 0; c0 < Rp; c0 += 8) {
+        float hi[8], lo[8];
+        tmem_ld8(lane_base + c0, hi);
+        tmem_ld8(lane_base + Rp + c0, lo);
+        if (ch_ok) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int b = c0 + k;
+            const float g = (hi[k] + lo[k]) * sg;
+            const float u = ex[row * Rp + b];
+            const float v = b < a.R ? g / (1.f + expf(-g)) * u : 0.f;
+            store_hl16(act + (size_t)b * a.ld_act + j, act + (size_t)(Rp + b) * a.ld_act + j, v, a.hl_f16);
+          }
+        }
+      }
+    }
+  } else {  // EPI_ARGMAX
+    float* bv = reinterpret_cast<float*>(scratch);   // [4 quarters][Rp]
+    int* bi = reinterpret_cast<int*>(scratch + 4 * Rp * 4);
+    const int n = tile * kTcBM + row;
+    const float sc = (a.scale && n < a.N) ? a.scale[n] : 1.f;
+    for (int c0 = 0; c0 < Rp; c0 += 8) {
+      float hi[8], lo[8];
+      tmem_ld8(lane_base + c0, hi);
+      tmem_ld8(lane_base + Rp + c0, lo);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int b = c0 + k;
+        float v = n < a.N ? (hi[k] + lo[k]) * sc : -INFINITY;
+        if (!(v == v)) { set_err(a.err, MBT_DEV_NONFINITE); v = -INFINITY; }
+        if (n < a.N && b < a.R && a.logits) a.logits[(size_t)b * a.ldl + n] = v;
+        int idx = n;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+          if (ov > v || (ov == v && oi < idx)) { v = ov; idx = oi; }
+        }
+        if (lane == 0) { bv[q * Rp + b] = v; bi[q * Rp + b] = idx; }
+      }
+    }
+    named_bar(bar, 128);
+    for (int b = et; b < a.R; b += 128) {
+      float v = bv[b];
+      int idx = bi[b];
+      for (int w2 = 1; w2 < 4; ++w2) {
+        const float ov = bv[w2 * Rp + b];
+        const int oi = bi[w2 * Rp + b];
+        if (ov > v || (ov == v && oi < idx)) { v = ov; idx = oi; }
+      }
+      ArgmaxPart p;
+      p.v = v; p.i = idx;
+      a.part[(size_t)tile * a.part_ld + b] = p;
+    }
+  }
+}
+
+}  // namespace mbt

@@ -1,5 +1,6 @@
-"""Tensor-core (tcgen05) projection through the C ABI (op_gemm_tc) against the
-oracle, and whole steps that run on it (batch 16..128, BF16 weights).
+"""Tensor-core (tcgen05) projections through the C ABI (op_gemm_tc for BF16
+weights, op_gemm_tc_e4m3 for e4m3 weights widened to FP16 in shared memory)
+against the oracle, and whole steps that run on them (batch 16..128).
 
 The activations enter as BF16 high/low pairs (x = hi + lo with |x - hi - lo| <=
 2^-18 |x|), the MMAs accumulate in fp32, so the bound of the CUDA-core GEMV
@@ -11,7 +12,7 @@ import torch
 from memory_bound_transformer_gb300 import capi
 from oracle.decode import OracleKV, decode_weight, silu
 from synth import ONE_B, ModelConfig, gen_tensor
-from tests.helpers import SMALL, oracle_weights
+from tests.helpers import SMALL, SMALL_FP8, oracle_weights
 from tests.test_gpu_step import Case, _run
 
 pytestmark = pytest.mark.gpu
@@ -23,6 +24,12 @@ def _weights(rows, K, seed):
     cfg = ModelConfig("op", 1, K, 1, 1, 64, 16, rows)
     t = gen_tensor(cfg, seed, "lm_head", -1, device=DEV)
     return t, {"w": t["w"].view(torch.int16).cpu().numpy().view(np.uint16)}
+
+
+def _weights8(rows, K, seed):
+    cfg = ModelConfig("op", 1, K, 1, 1, 64, 16, rows, weight_dtype="fp8")
+    t = gen_tensor(cfg, seed, "lm_head", -1, device=DEV)
+    return t, {"w": t["w"].cpu().numpy(), "s": t["s"].cpu().numpy()}
 
 
 def _x(B, K, seed, scale=1.0):
@@ -104,3 +111,71 @@ def test_1b_batch64(cuda_lib):
     case = Case(cfg, 1236, 64, rng.integers(100, 600, size=64), 1, ladder=[64], graph=True)
     okv = OracleKV(case.pool0.copy(), np.ones(cfg.n_layers), np.ones(cfg.n_layers))
     _run(case, oracle_weights(case.model), okv, 1)
+
+
+@pytest.mark.parametrize("B", [16, 24, 64, 128])
+@pytest.mark.parametrize("N,K,ks", [(1000, 1040, 1), (1000, 1040, 3), (6144, 4096, 3), (200, 64, 1)])
+def test_tc8_partial(cuda_lib, B, N, K, ks):
+    t, raw = _weights8(N, K, seed=N + K + 1)
+    x = _x(B, K, seed=B + 1)
+    out = torch.full((ks, B, N), float("nan"), device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    capi.op_gemm_tc_e4m3(capi.EPI_PARTIAL, t["w"], t["s"], N, K, x, B, ks, out=out, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    got = out.double().sum(0).cpu().numpy()
+    W = decode_weight(raw)
+    xv = x.double().cpu().numpy()
+    ref = xv @ W.T
+    bound = TOL_REL * (np.abs(xv) @ np.abs(W).T) + TOL_ABS
+    assert np.all(np.abs(got - ref) <= bound)
+
+
+@pytest.mark.parametrize("B", [16, 40, 64])
+def test_tc8_swiglu(cuda_lib, B):
+    F, K = 700, 512
+    t, raw = _weights8(2 * F, K, seed=8)
+    x = _x(B, K, seed=4, scale=3.0)
+    act = torch.full((B, F), float("nan"), device=DEV)
+    capi.op_gemm_tc_e4m3(capi.EPI_SWIGLU, t["w"], t["s"], F, K, x, B, act=act)
+    torch.cuda.synchronize()
+    W = decode_weight(raw)
+    xv = x.double().cpu().numpy()
+    gu = xv @ W.T
+    bg = TOL_REL * (np.abs(xv) @ np.abs(W).T) + TOL_ABS
+    g, u = gu[:, :F], gu[:, F:]
+    ref = silu(g) * u
+    got = act.double().cpu().numpy()
+    # as the BF16 test; the act rows are stored as FP16 high/low parts (2^-21)
+    bound = 1e-5 * np.abs(ref) + 1.1 * np.abs(u) * bg[:, :F] + np.abs(silu(g)) * bg[:, F:] + 1e-30
+    assert np.all(np.abs(got - ref) <= bound)
+
+
+@pytest.mark.parametrize("B", [16, 64])
+def test_tc8_argmax(cuda_lib, B):
+    V, K = 3001, 512
+    t, raw = _weights8(V, K, seed=12)
+    x = _x(B, K, seed=22, scale=2.0)
+    logits = torch.zeros((B, V), device=DEV)
+    ids = torch.full((B,), -1, dtype=torch.int32, device=DEV)
+    capi.op_gemm_tc_e4m3(capi.EPI_ARGMAX, t["w"], t["s"], V, K, x, B, logits=logits, next_ids=ids)
+    torch.cuda.synchronize()
+    lg = logits.double().cpu().numpy()
+    assert np.array_equal(ids.cpu().numpy(), np.argmax(lg, axis=1))
+    W = decode_weight(raw)
+    xv = x.double().cpu().numpy()
+    ref = xv @ W.T
+    bound = TOL_REL * (np.abs(xv) @ np.abs(W).T) + TOL_ABS
+    assert np.all(np.abs(lg - ref) <= bound)
+
+
+@pytest.mark.parametrize("B", [16, 24, 40])
+def test_small_fp8_model_tensor_core_step(cuda_lib, B):
+    """e4m3 weights and cache at batch 16..40: the step runs the widening
+    tensor-core GEMM (FP16 activations) and FP16 attention."""
+    cfg = SMALL_FP8
+    rng = np.random.default_rng(B + 7)
+    case = Case(cfg, 65 + B, B, rng.integers(0, 200, size=B), 2, ladder=[8, 16, 24, 40], graph=True)
+    assert case.eng.stats(B)[1]
+    okv = OracleKV(case.pool0.copy(), np.ones(cfg.n_layers), np.ones(cfg.n_layers))
+    _run(case, oracle_weights(case.model), okv, 2)
