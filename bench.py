@@ -57,7 +57,7 @@ def parse():
     ap.add_argument("--ladder", default=None, help="comma-separated graph ladder (default: the workload's)")
     ap.add_argument("--context", default=None,
                     help="LO,HI: per-sequence context range instead of the workload's (context sweeps)")
-    ap.add_argument("--kernel-only", nargs="?", const="gemv", default=None, choices=["gemv", "attention"],
+    ap.add_argument("--kernel-only", nargs="?", const="gemv", default=None, choices=["gemv", "attention", "tc"],
                     help="time one kernel alone for profiling: the gate/up GEMV over 4 layers' matrices, "
                          "or one layer's paged attention at the workload's contexts")
     return ap.parse_args()
@@ -261,6 +261,40 @@ def time_gemv_swiglu(cfg, wl, B, dev, reps=3, layers=None):
     return {"ms": ms, "bytes": nbytes, "launches": n}
 
 
+def time_tc_swiglu(cfg, wl, B, dev, reps=3, layers=4):
+    """Average duration of the tensor-core gate/up projection with the SwiGLU
+    epilogue (the e4m3 widening kernel for FP8 weights) at batch B over a few
+    layers' matrices, CUDA events on its stream. Includes the entry point's
+    fp32 -> high/low row split and act readback kernels (small next to it)."""
+    model = SynthModel(cfg, wl.seed + 17, device=dev, cache=False)
+    mats = [model.get("w_gu", l) for l in range(min(cfg.n_layers, layers))]
+    x = torch.randn((B, cfg.hidden), device=dev)
+    act = torch.empty((B, cfg.ffn), device=dev)
+    fp8 = cfg.weight_dtype == "fp8"
+    fn = capi.op_gemm_tc_e4m3 if fp8 else capi.op_gemm_tc
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        for m in mats[:2]:
+            fn(capi.EPI_SWIGLU, m["w"], m.get("s"), cfg.ffn, cfg.hidden, x, B, act=act, stream=s)
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        n = 0
+        for _ in range(reps):
+            for m in mats:
+                fn(capi.EPI_SWIGLU, m["w"], m.get("s"), cfg.ffn, cfg.hidden, x, B, act=act, stream=s)
+                n += 1
+        e1.record(s)
+        s.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    w = 1 if fp8 else 2
+    nbytes = 2 * cfg.ffn * cfg.hidden * w + (2 * cfg.ffn * 4 if fp8 else 0) + B * cfg.hidden * 4 + B * cfg.ffn * 4
+    flops = 2 * B * 2 * cfg.ffn * cfg.hidden
+    del mats
+    torch.cuda.empty_cache()
+    return {"ms": ms, "bytes": nbytes, "flops": flops, "launches": n}
+
+
 def time_attention(wl, B, dev, reps=10):
     """One layer's paged attention at batch B over the workload's contexts (a
     one-layer cache of random values), timed with CUDA events on its stream."""
@@ -406,13 +440,20 @@ def main():
         if args.kernel_only == "attention":
             k = time_attention(wl, B, dev)
             name = "paged attention (split-K, tensor-core QK/PV, merge)"
+        elif args.kernel_only == "tc":
+            k = time_tc_swiglu(wl.model, wl, args.batch or 64, dev)
+            B = args.batch or 64
+            name = "tensor-core gate/up with SwiGLU epilogue (" + wl.model.weight_dtype + " weights)"
         else:
             k = time_gemv_swiglu(wl.model, wl, B, dev, reps=1, layers=4)
             name = "gate/up GEMV with SwiGLU epilogue"
         gbs = k["bytes"] / (k["ms"] / 1e3) / 1e9
-        print(json.dumps({"kernel": name, "workload": wl.key, "batch": B, "launches": k["launches"],
-                          "avg_ms": round(k["ms"], 5), "bytes": k["bytes"], "achieved_gbs": round(gbs, 1),
-                          "frac": round(gbs / peak, 4), "peak_source": src}))
+        line = {"kernel": name, "workload": wl.key, "batch": B, "launches": k["launches"],
+                "avg_ms": round(k["ms"], 5), "bytes": k["bytes"], "achieved_gbs": round(gbs, 1),
+                "frac": round(gbs / peak, 4), "peak_source": src}
+        if "flops" in k:
+            line["achieved_tflops"] = round(k["flops"] / (k["ms"] / 1e3) / 1e12, 1)
+        print(json.dumps(line))
         return
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))

@@ -208,11 +208,17 @@ def random_kv_pool(cfg: ModelConfig, num_blocks: int, seed: int, device="cpu",
     FP8 caches hold e4m3 codes of N(0, std²) (per-layer scale 1.0). Returned as
     int16 (bf16 bits) or uint8 (e4m3 codes).
     """
-    shape = (cfg.n_layers, 2, num_blocks + 1, cfg.n_kv_heads, cfg.block_size, cfg.head_dim)
-    x = std * _randn(shape, _tensor_seed(seed, "kv", 0), device)
-    if cfg.kv_dtype == "fp8":
-        return x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
-    return x.to(torch.bfloat16).view(torch.int16)
+    shape = (2, num_blocks + 1, cfg.n_kv_heads, cfg.block_size, cfg.head_dim)
+    fp8 = cfg.kv_dtype == "fp8"
+    out = torch.empty((cfg.n_layers,) + shape, dtype=torch.uint8 if fp8 else torch.int16, device=device)
+    for layer in range(cfg.n_layers):          # one layer at a time: no full-size fp32 temporary
+        x = std * _randn(shape, _tensor_seed(seed, "kv", layer), device)
+        if fp8:
+            out[layer] = x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        else:
+            out[layer] = x.to(torch.bfloat16).view(torch.int16)
+        del x
+    return out
 
 
 def seeded_block_tables(seq_capacity: Sequence[int], block_size: int, num_blocks: int,
