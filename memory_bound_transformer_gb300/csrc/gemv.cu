@@ -182,7 +182,8 @@ gemv_kernel(const GemvArgs a) {
     // fusion") done by every CTA into its own x tile; CTA 0 stores the new residual.
     const int k4n = a.K / 4;
     const bool store_r = (c == 0 && split == 0);
-    constexpr int PV = 8;                        // float4 per thread in flight per pass
+    constexpr int PV = 4;                        // float4 of r per thread per pass
+    constexpr int ND = 3;                        // partials loaded with r in the same round trip
     float ss[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
@@ -191,23 +192,35 @@ gemv_kernel(const GemvArgs a) {
       const float4* __restrict__ r4 = reinterpret_cast<const float4*>(a.r_in + (size_t)b * a.K);
       const float4* __restrict__ d4 = reinterpret_cast<const float4*>(a.delta + (size_t)b * a.K);
       float4* __restrict__ o4 = reinterpret_cast<float4*>(a.r_out + (size_t)b * a.K);
+      const size_t dst4 = (size_t)(a.delta_stride / 4);
       for (int base = 0; base < k4n; base += PV * kGemvThreads) {
-        // all loads of the pass first (one round trip), then the sums
-        float4 v[PV];
+        // the loads of r and of the first ND partials first (one round trip),
+        // then the sums in the fixed order r + d0 + d1 + ...
+        float4 v[PV], t[ND][PV];
 #pragma unroll
         for (int j = 0; j < PV; ++j) {
           const int k4 = base + tid + j * kGemvThreads;
-          v[j] = (live && k4 < k4n) ? r4[k4] : make_float4(0.f, 0.f, 0.f, 0.f);
+          const bool in = live && k4 < k4n;
+          v[j] = in ? r4[k4] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int sd = 0; sd < ND; ++sd)
+            t[sd][j] = (in && sd < a.n_delta) ? d4[sd * dst4 + k4] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        for (int sidx = 0; sidx < a.n_delta; ++sidx) {
-          float4 t[PV];
+#pragma unroll
+        for (int sd = 0; sd < ND; ++sd)
+          if (sd < a.n_delta) {
+#pragma unroll
+            for (int j = 0; j < PV; ++j) {
+              v[j].x += t[sd][j].x; v[j].y += t[sd][j].y; v[j].z += t[sd][j].z; v[j].w += t[sd][j].w;
+            }
+          }
+        for (int sidx = ND; sidx < a.n_delta; ++sidx) {
 #pragma unroll
           for (int j = 0; j < PV; ++j) {
             const int k4 = base + tid + j * kGemvThreads;
-            t[j] = (live && k4 < k4n) ? d4[(size_t)sidx * (a.delta_stride / 4) + k4] : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 u = (live && k4 < k4n) ? d4[sidx * dst4 + k4] : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[j].x += u.x; v[j].y += u.y; v[j].z += u.z; v[j].w += u.w;
           }
-#pragma unroll
-          for (int j = 0; j < PV; ++j) { v[j].x += t[j].x; v[j].y += t[j].y; v[j].z += t[j].z; v[j].w += t[j].w; }
         }
 #pragma unroll
         for (int j = 0; j < PV; ++j) {

@@ -23,7 +23,10 @@
 namespace mbt {
 
 constexpr int kTcThreads = 128;
-constexpr int kTcStages = 3;            // 3 x 32 KB at 64 rows: two CTAs fit an SM
+#ifndef MBT_TC_STAGES
+#define MBT_TC_STAGES 3
+#endif
+constexpr int kTcStages = MBT_TC_STAGES;   // 3 x 32 KB at 64 rows: two CTAs fit an SM
 template <int EPI>
 __global__ void __launch_bounds__(kTcThreads, 2)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const TcArgs a) {

@@ -13,7 +13,7 @@
 //                        (8 KB each: the bytes in flight that keep HBM busy);
 //   warp 1 (one thread): the MMAs and their commits;
 //   warp 2 (one thread): TMA copies of the activation tiles (3 stages);
-//   warps 3-6:           widen each raw tile into a 2-stage ring of FP16
+//   warps 3-6:           widen each raw tile into a 4-stage ring of FP16
 //                        tiles in the 128-byte-swizzled K-major layout the
 //                        MMA reads, then run the epilogue.
 // Every wait is bounded (about 2 s): on a timeout the kernel flags
@@ -23,10 +23,19 @@
 
 namespace mbt {
 
+#ifndef MBT_F8_RAW
+#define MBT_F8_RAW 8
+#endif
+#ifndef MBT_F8_HALF
+#define MBT_F8_HALF 4
+#endif
+#ifndef MBT_F8_BST
+#define MBT_F8_BST 3
+#endif
 constexpr int kF8Threads = 224;
-constexpr int kF8Raw = 8;                         // raw e4m3 stages
-constexpr int kF8Half = 2;                        // FP16 A stages
-constexpr int kF8B = 3;                           // activation stages
+constexpr int kF8Raw = MBT_F8_RAW;                // raw e4m3 stages
+constexpr int kF8Half = MBT_F8_HALF;              // FP16 A stages
+constexpr int kF8B = MBT_F8_BST;                  // activation stages
 constexpr uint32_t kF8RawBytes = kTcBM * kTcBK;   // 128 rows x 64 codes
 constexpr uint32_t kF8HalfBytes = kTcBM * 128;    // 128 rows x 64 FP16
 
