@@ -13,9 +13,9 @@
 //                        (8 KB each: the bytes in flight that keep HBM busy);
 //   warp 1 (one thread): the MMAs and their commits;
 //   warp 2 (one thread): TMA copies of the activation tiles (3 stages);
-//   warps 3-6:           widen each raw tile into a 4-stage ring of FP16
+//   warps 3-10:          widen each raw tile into a 4-stage ring of FP16
 //                        tiles in the 128-byte-swizzled K-major layout the
-//                        MMA reads, then run the epilogue.
+//                        MMA reads; warps 3-6 then run the epilogue.
 // Every wait is bounded (about 2 s): on a timeout the kernel flags
 // MBT_DEV_WAIT_LIMIT, waits (bounded) for the copies it issued, frees its TMEM
 // and returns.
@@ -32,7 +32,12 @@ namespace mbt {
 #ifndef MBT_F8_BST
 #define MBT_F8_BST 3
 #endif
-constexpr int kF8Threads = 224;
+#ifndef MBT_F8_CONV_WARPS
+#define MBT_F8_CONV_WARPS 8
+#endif
+constexpr int kF8Conv = MBT_F8_CONV_WARPS * 32;   // widening threads (warps 3..); the first 128 run the epilogue
+constexpr int kF8Threads = 96 + kF8Conv;
+constexpr int kF8Items = kTcBM * 4 / kF8Conv;     // (row, 16 codes) items per widening thread per stage
 constexpr int kF8Raw = MBT_F8_RAW;                // raw e4m3 stages
 constexpr int kF8Half = MBT_F8_HALF;              // FP16 A stages
 constexpr int kF8B = MBT_F8_BST;                  // activation stages
@@ -69,8 +74,8 @@ tc_gemm_f8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant
 
   pdl_launch_dependents();
   if (tid == 0) {
-    for (int s = 0; s < kF8Raw; ++s) { mbar_init(&raw_full[s], 1); mbar_init(&raw_empty[s], 128); }
-    for (int s = 0; s < kF8Half; ++s) { mbar_init(&half_full[s], 128); mbar_init(&half_empty[s], 1); }
+    for (int s = 0; s < kF8Raw; ++s) { mbar_init(&raw_full[s], 1); mbar_init(&raw_empty[s], kF8Conv); }
+    for (int s = 0; s < kF8Half; ++s) { mbar_init(&half_full[s], kF8Conv); mbar_init(&half_empty[s], 1); }
     for (int s = 0; s < kF8B; ++s) { mbar_init(&b_full[s], 1); mbar_init(&b_empty[s], 1); }
     mbar_init(&done, 1);
     abort_flag = 0;
@@ -161,8 +166,8 @@ tc_gemm_f8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant
       const unsigned char* src = sR + r * kF8RawBytes;
       unsigned char* dst = sH + h * kF8HalfBytes;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int item = ct + 128 * j, row = item >> 2, c = item & 3;
+      for (int j = 0; j < kF8Items; ++j) {
+        const int item = ct + kF8Conv * j, row = item >> 2, c = item & 3;
         const uint4 w = *reinterpret_cast<const uint4*>(src + row * kTcBK + c * 16);
         uint4 lo, hi;
         lo.x = e4m3x2_to_h2bits(w.x); lo.y = e4m3x2_to_h2bits(w.x >> 16);
@@ -189,7 +194,7 @@ tc_gemm_f8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant
   if (tid == 0) have_s = done_ok && !abort_flag && nk > 0;
   __syncthreads();
   tc_fence_after();
-  if (warp >= 3) {
+  if (warp >= 3 && warp < 7) {
     if (!have_s) {
       if (tid == 96 && (abort_flag || nk > 0)) set_err(a.err, MBT_DEV_WAIT_LIMIT);
     } else {
