@@ -179,3 +179,25 @@ def test_small_fp8_model_tensor_core_step(cuda_lib, B):
     assert case.eng.stats(B)[1]
     okv = OracleKV(case.pool0.copy(), np.ones(cfg.n_layers), np.ones(cfg.n_layers))
     _run(case, oracle_weights(case.model), okv, 2)
+
+
+@pytest.mark.parametrize("N,K,B,ks", [(57344, 8192, 64, 1), (8192, 28672, 64, 2), (27648 * 2, 5120, 32, 1)])
+def test_tc8_full_size_sampled(cuda_lib, N, K, B, ks):
+    """Full model-size e4m3 projections on the tensor cores (70B gate/up and
+    down at batch 64, 32B gate/up at batch 32): 64 sampled output rows, the
+    last row included, checked one by one by the oracle."""
+    t, _ = _weights8(N, K, seed=N ^ K)
+    x = _x(B, K, seed=9)
+    out = torch.zeros((ks, B, N), device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    capi.op_gemm_tc_e4m3(capi.EPI_PARTIAL, t["w"], t["s"], N, K, x, B, ks, out=out, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    got = out.sum(0).double().cpu().numpy()
+    rows = np.sort(np.random.default_rng(N).choice(N, 64, replace=False))
+    rows[-1] = N - 1
+    W = decode_weight({"w": t["w"][rows].cpu().numpy(), "s": t["s"][rows].cpu().numpy()})
+    xv = x.double().cpu().numpy()
+    ref = xv @ W.T
+    bound = TOL_REL * (np.abs(xv) @ np.abs(W).T) + TOL_ABS
+    assert np.all(np.abs(got[:, rows] - ref) <= bound)
