@@ -128,6 +128,10 @@ cudaError_t tc8_init();
 cudaError_t tc8_launch(int epi, const void* mapW, const void* mapX, const TcArgs& a, int ksplit, cudaStream_t s);
 size_t tc8_smem(int Rp);
 int tc_tiles(int epi, int N);
+#ifndef MBT_TC_TP
+#define MBT_TC_TP 1
+#endif
+constexpr int kTcTP = MBT_TC_TP;        // BF16 GEMM: weight tiles per CTA sharing each activation tile
 size_t tc_smem(int Rp);
 cudaError_t tc_to_hl(const float* x, int B, int Rp, int K, bf16* hl, cudaStream_t s, int f16 = 0);
 cudaError_t tc_from_hl(const bf16* hl, int B, int Rp, int N, float* out, cudaStream_t s, int f16 = 0);

@@ -119,9 +119,9 @@ size_t kv_layer_half_bytes(const mbt_model* m, int num_blocks) {
 }
 
 int tc_ksplit(const mbt_model* m, int epi, int N, int K) {
-  const int tiles = tc_tiles(epi, N);
-  // two CTAs per SM (BF16), one (e4m3: its deeper copy ring fills the SM)
-  int ks = (m->wtype == W_E4M3 ? 1 : 2) * m->num_sms / tiles;
+  const int tiles = m->wtype == W_E4M3 ? tc_tiles(epi, N) : (tc_tiles(epi, N) + kTcTP - 1) / kTcTP;
+  // two CTAs per SM (BF16, one tile each), one (e4m3: its deeper copy ring fills the SM)
+  int ks = (m->wtype == W_E4M3 || kTcTP > 1 ? 1 : 2) * m->num_sms / tiles;
   const int chunks = (K + 63) / 64;
   if (ks > chunks / 4) ks = chunks / 4;        // at least 4 stages of K per split
   return ks < 1 ? 1 : ks;

@@ -28,7 +28,7 @@ constexpr int kTcThreads = 128;
 #endif
 constexpr int kTcStages = MBT_TC_STAGES;   // 3 x 32 KB at 64 rows: two CTAs fit an SM
 template <int EPI>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(kTcThreads, kTcTP == 1 ? 2 : 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const TcArgs a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -38,17 +38,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   __shared__ int have_s, issued_s, consumed_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tile = blockIdx.x, split = blockIdx.y;
+  // kTcTP weight tiles per CTA share every activation tile
+  const int tile0 = blockIdx.x * kTcTP, split = blockIdx.y;
+  const int ntiles = EPI == EPI_SWIGLU ? (a.N + 63) / 64 : (a.N + kTcBM - 1) / kTcBM;
   const int Rp = a.Rp, NM = 2 * Rp;                // MMA N: hi rows then lo rows
-  const uint32_t a_bytes = kTcBM * 128, b_bytes = (uint32_t)NM * 128;
+  const uint32_t at_bytes = kTcBM * 128, a_bytes = kTcTP * at_bytes, b_bytes = (uint32_t)NM * 128;
   unsigned char* sA = smem;
   unsigned char* sB = smem + kTcStages * a_bytes;
   const int nk_all = (a.K + kTcBK - 1) / kTcBK;
   const int kc0 = (int)((long long)nk_all * split / gridDim.y);
   const int nk = (int)((long long)nk_all * (split + 1) / gridDim.y) - kc0;
-  // weight rows of the tile's two 64-row halves (SwiGLU: gate half, up half)
-  const int rowA0 = EPI == EPI_SWIGLU ? tile * 64 : tile * kTcBM;
-  const int rowA1 = EPI == EPI_SWIGLU ? a.N + tile * 64 : tile * kTcBM + 64;
+  // weight rows of each tile's two 64-row halves (SwiGLU: gate half, up half)
+  auto rowA0 = [&](int t) { return EPI == EPI_SWIGLU ? t * 64 : t * kTcBM; };
+  auto rowA1 = [&](int t) { return EPI == EPI_SWIGLU ? a.N + t * 64 : t * kTcBM + 64; };
 
   pdl_launch_dependents();
   if (tid == 0) {
@@ -61,7 +63,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
   }
-  const uint32_t tcols = NM <= 32 ? 32 : NM <= 64 ? 64 : NM <= 128 ? 128 : 256;
+  const int ncols = kTcTP * NM;
+  const uint32_t tcols = ncols <= 32 ? 32 : ncols <= 64 ? 64 : ncols <= 128 ? 128 : ncols <= 256 ? 256 : 512;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  ::"r"(smem_u32(&tmem_slot)), "r"(tcols) : "memory");
@@ -79,8 +82,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     for (int i = 0; i < pre; ++i) {
       mbar_arrive_tx(&full[i], a_bytes + b_bytes);
       const int kx = (kc0 + i) * kTcBK;
-      tma_load_2d(sA + i * a_bytes, &tmW, kx, rowA0, &full[i]);
-      tma_load_2d(sA + i * a_bytes + 64 * 128, &tmW, kx, rowA1, &full[i]);
+      for (int j = 0; j < kTcTP; ++j) {
+        tma_load_2d(sA + i * a_bytes + j * at_bytes, &tmW, kx, rowA0(tile0 + j), &full[i]);
+        tma_load_2d(sA + i * a_bytes + j * at_bytes + 64 * 128, &tmW, kx, rowA1(tile0 + j), &full[i]);
+      }
     }
     pdl_wait();
     for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * b_bytes, &tmX, (kc0 + i) * kTcBK, 0, &full[i]);
@@ -90,8 +95,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
       if (abort_flag || !mbar_wait(&empty[s], ((i / kTcStages) - 1) & 1)) { abort_flag = 1; break; }
       mbar_arrive_tx(&full[s], a_bytes + b_bytes);
       const int kx = (kc0 + i) * kTcBK;
-      tma_load_2d(sA + s * a_bytes, &tmW, kx, rowA0, &full[s]);
-      tma_load_2d(sA + s * a_bytes + 64 * 128, &tmW, kx, rowA1, &full[s]);
+      for (int j = 0; j < kTcTP; ++j) {
+        tma_load_2d(sA + s * a_bytes + j * at_bytes, &tmW, kx, rowA0(tile0 + j), &full[s]);
+        tma_load_2d(sA + s * a_bytes + j * at_bytes + 64 * 128, &tmW, kx, rowA1(tile0 + j), &full[s]);
+      }
       tma_load_2d(sB + s * b_bytes, &tmX, kx, 0, &full[s]);
       issued = i + 1;
     }
@@ -106,11 +113,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
       if (abort_flag || !mbar_wait(&full[s], (i / kTcStages) & 1)) { abort_flag = 1; ok = false; break; }
       consumed_s = i + 1;
       tc_fence_after();
-      const uint64_t ad = sw128_desc(smem_u32(sA + s * a_bytes));
       const uint64_t bd = sw128_desc(smem_u32(sB + s * b_bytes));
 #pragma unroll
-      for (int kk = 0; kk < kTcBK / 16; ++kk)
-        umma_kf16(tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+      for (int j = 0; j < kTcTP; ++j) {
+        const uint64_t ad = sw128_desc(smem_u32(sA + s * a_bytes + j * at_bytes));
+#pragma unroll
+        for (int kk = 0; kk < kTcBK / 16; ++kk)
+          umma_kf16(tmem + (uint32_t)(j * NM), ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
+                    (i > 0 || kk > 0) ? 1u : 0u);
+      }
       umma_commit(&empty[s]);
     }
     if (ok) umma_commit(&done);
@@ -131,7 +142,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   if (!have) {
     if (tid == 0 && (abort_flag || nk > 0)) set_err(a.err, MBT_DEV_WAIT_LIMIT);
   } else {
-    tc_epilogue<EPI>(a, tmem, warp, lane, tid, tile, split, sA, 1);     // the stage ring is free now
+    for (int j = 0; j < kTcTP && tile0 + j < ntiles; ++j) {
+      if (j) named_bar(1, kTcThreads);                                   // the scratch is reused
+      tc_epilogue<EPI>(a, tmem + (uint32_t)(j * NM), warp, lane, tid, tile0 + j, split, sA, 1);   // ring free
+    }
   }
 
   // teardown: no TMA or MMA of this CTA is still in flight once `done` fired;
@@ -240,7 +254,7 @@ cudaError_t tc_make_map_u8(void* map, const void* base, int rows, int K) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-size_t tc_smem(int Rp) { return 1024 + (size_t)kTcStages * (kTcBM * 128 + (size_t)2 * Rp * 128); }
+size_t tc_smem(int Rp) { return 1024 + (size_t)kTcStages * (kTcTP * kTcBM * 128 + (size_t)2 * Rp * 128); }
 
 int tc_tiles(int epi, int N) { return epi == EPI_SWIGLU ? (N + 63) / 64 : (N + kTcBM - 1) / kTcBM; }
 
@@ -248,7 +262,8 @@ cudaError_t tc_launch(int epi, const void* mapW, const void* mapX, const TcArgs&
   CUtensorMap w = *(const CUtensorMap*)mapW, x = *(const CUtensorMap*)mapX;
   TcArgs args = a;
   void* params[] = {&w, &x, &args};
-  return launch_pdl(tc_pick(epi), dim3(tc_tiles(epi, a.N), ksplit), dim3(kTcThreads), tc_smem(a.Rp), s, params);
+  return launch_pdl(tc_pick(epi), dim3((tc_tiles(epi, a.N) + kTcTP - 1) / kTcTP, ksplit), dim3(kTcThreads),
+                    tc_smem(a.Rp), s, params);
 }
 
 }  // namespace mbt
