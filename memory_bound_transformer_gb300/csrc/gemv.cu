@@ -1,4 +1,4 @@
-// Weight-streaming GEMV for decode at batch 1..8 (CUDA cores).
+// Weight-streaming GEMV for decode at batch 1..15 (CUDA cores; up to 8 rows per launch).
 //
 // Decode "is effectively a matrix-vector product: it reads enormous weight
 // matrices to compute a single token's worth of output" ("Kernel Fusion for
@@ -11,6 +11,9 @@
 //     logits by ~5e-2) sit in shared memory for the whole CTA;
 //   * rows are split over CTAs in equal contiguous ranges (the grid is a
 //     multiple of the SM count), so every SM streams the same number of bytes;
+//     where every CTA owns several 8-row groups, half of each range is fixed
+//     and the rest is claimed group by group from an atomic counter, because
+//     CTAs do not stream at equal rates and the slowest one sets the time;
 //   * FP8-e4m3 weights are converted in registers and the per-output-channel
 //     scale is applied once to the finished dot product, which is exact
 //     reassociation ("Epilogue and dequant fusion", same section 11);
