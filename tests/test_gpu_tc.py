@@ -201,3 +201,13 @@ def test_tc8_full_size_sampled(cuda_lib, N, K, B, ks):
     ref = xv @ W.T
     bound = TOL_REL * (np.abs(xv) @ np.abs(W).T) + TOL_ABS
     assert np.all(np.abs(got[:, rows] - ref) <= bound)
+
+
+def test_small_fp8_model_batch64(cuda_lib):
+    """e4m3 weights and cache at batch 64 (FP16 high/low rows, N = 128 per MMA), graph replay."""
+    cfg = SMALL_FP8
+    rng = np.random.default_rng(640)
+    case = Case(cfg, 640, 64, rng.integers(0, 200, size=64), 1, ladder=[64], graph=True)
+    assert case.eng.stats(64)[1]
+    okv = OracleKV(case.pool0.copy(), np.ones(cfg.n_layers), np.ones(cfg.n_layers))
+    _run(case, oracle_weights(case.model), okv, 1)
