@@ -64,3 +64,25 @@ def test_blob_layout_matches_header():
     ents = [mblob.ENTRY.unpack(bytes(b[off + 48 * i: off + 48 * (i + 1)].numpy())) for i in range(n)]
     assert all(e[6] % 256 == 0 and e[6] + e[7] <= b.numel() for e in ents)
     assert {(e[0], e[1]) for e in ents} >= {(0, -1), (12, -1), (2, 0), (7, 0)}
+
+
+def test_argument_checks_before_any_device_call(lib):
+    """Entry points reject malformed arguments with a status code before they
+    touch the device (these run on a machine without a GPU)."""
+    capi._lib = None
+    l = capi.load()
+    BAD = -1
+    # op_gemv: unknown epilogue, unknown weight type, K not a multiple of 16
+    assert l.op_gemv(7, 0, None, None, 8, 16, None, 1, 0, None, None, None, None, None, None, None) == BAD
+    assert l.op_gemv(0, 9, None, None, 8, 16, None, 1, 0, None, None, None, None, None, None, None) == BAD
+    assert l.op_gemv(0, 0, 1, None, 8, 17, 1, 1, 0, 1, None, None, None, None, None, None) == BAD
+    # e4m3 weights need their per-row scales
+    assert l.op_gemv(0, 1, 1, None, 8, 16, 1, 1, 0, 1, None, None, None, None, None, None) == BAD
+    assert l.op_gemm_tc_e4m3(0, 1, None, 8, 64, 1, 16, 1, 1, None, None, None, None, None) == BAD
+    # tensor-core entry points: batch above 128, K below 64
+    assert l.op_gemm_tc(0, 1, None, 8, 64, 1, 129, 1, 1, None, None, None, None, None) == BAD
+    assert l.op_gemm_tc(0, 1, None, 8, 32, 1, 16, 1, 1, None, None, None, None, None) == BAD
+    # the step: a missing model or kv handle, and B <= 0
+    assert l.model_create(None, 0, 0, None, None) == BAD
+    assert l.kv_alloc(None, 4, None, None) == BAD
+    assert l.model_capture(None, None, None, 0, 0, None) == BAD
