@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--ladder", default=None, help="comma-separated graph ladder (default: the workload's)")
     ap.add_argument("--context", default=None,
                     help="LO,HI: per-sequence context range instead of the workload's (context sweeps)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="batch sweep over the graph ladder: one JSON line per batch (tok/s, step p50/p99, GB/s)")
     ap.add_argument("--kernel-only", nargs="?", const="gemv", default=None, choices=["gemv", "attention", "tc"],
                     help="time one kernel alone for profiling: the gate/up GEMV over 4 layers' matrices, "
                          "or one layer's paged attention at the workload's contexts")
@@ -220,6 +222,30 @@ def time_native(args, rank, world):
     e2e = None if args.no_e2e else time_e2e(eng, cfg, ctx[:B0] + W + K, bt0, B0, K, dev, tables[:B0])
     eng.close()
     return dict(cfg=cfg, K=K, W=W, runs=runs, kern=kern, e2e=e2e, ctx=ctx, wl=wl, eager=eager)
+
+
+def batch_sweep(args):
+    """Tokens/s against step latency across the graph ladder ("GPU Inference
+    Internals", "Batching Economics": the weight bytes are shared by the batch,
+    the KV bytes grow with it), one graph per rung, same contexts."""
+    wl = WORKLOADS[args.workload]
+    ladder = [int(x) for x in args.ladder.split(",")] if args.ladder else list(wl.ladder)
+    K, W = args.steps, args.warmup
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cfg, ctx, tables, nb, eng = build_case(wl, max(ladder), K + W)
+    eng.capture(ladder=ladder, max_blocks_per_seq=tables.shape[1])
+    peak, src = peaks()
+    for B in ladder:
+        r = timed_steps(eng, cfg, ctx, tables, B, K, W, dev, 1, clocks_on=False)
+        ps = np.array(r["per_step"])
+        gbs = r["avg_bytes"] / (np.mean(ps) / 1e3) / 1e9
+        print(json.dumps({"sweep": wl.key, "batch": B, "tokens_per_s": round(r["rate"], 2),
+                          "step_ms_p50": round(float(np.percentile(ps, 50)), 4),
+                          "step_ms_p99": round(float(np.percentile(ps, 99)), 4),
+                          "bytes_per_step": int(r["avg_bytes"]), "achieved_gbs": round(gbs, 1),
+                          "frac_of_peak": round(gbs / peak, 4), "peak_source": src,
+                          "kernels_per_step": r["kernels_per_step"], "graph": r["uses_graph"]}), flush=True)
+    eng.close()
 
 
 def time_gemv_swiglu(cfg, wl, B, dev, reps=3, layers=None):
@@ -431,6 +457,10 @@ def main():
             return
         return main_reference(args)
     torch.cuda.set_device(local)
+    if args.sweep:
+        capi.load()
+        batch_sweep(args)
+        return
     if args.kernel_only:
         capi.load()
         wl = WORKLOADS[args.workload]

@@ -416,6 +416,7 @@ gemv_kernel(const GemvArgs a) {
 
 namespace {
 constexpr size_t kXsMax = 216 * 1024;            // largest x tile (1 CTA per SM)
+constexpr size_t kXsTwoPerSm = 110 * 1024;       // largest CTA footprint two of which share an SM
 // work queue: share of each CTA's groups assigned up front, and the fewest
 // groups per CTA for which the queue is used at all
 constexpr double kStaticShare = 0.5;
@@ -486,9 +487,13 @@ GemvLaunch gemv_plan(int epi, int wtype, int nb, int N, int K, int num_sms, int 
   g.nsplit = ns;
   const size_t nvec_max = (size_t)(nvec_all + ns - 1) / ns;
   g.smem = (size_t)g.nb_tmpl * nvec_max * 16 * (epv / 4) + 2 * kGemvWarps * 32 * 4 + 32 * 4;
-  const int per_sm = (g.nb_tmpl < 8 && g.smem <= sc.cta_smem) ? 2 : 1;
-  // 1 CTA per SM only when the x tile needs more than the step's split
-  g.carveout = per_sm == 2 ? sc.carveout : -1;
+  // Two CTAs per SM under the step's L1 split when the x tile fits its budget;
+  // a larger tile (4 rows of a norm-prologue projection, whose K cannot be
+  // split) still runs two per SM, with the driver's default split for that
+  // launch; only 8-row tiles run one per SM.
+  const bool fits = g.smem <= sc.cta_smem;
+  const int per_sm = (g.nb_tmpl < 8 && (fits || g.smem <= kXsTwoPerSm)) ? 2 : 1;
+  g.carveout = fits && per_sm == 2 ? sc.carveout : -1;
   int grid = num_sms * per_sm / ns;
   if (grid < 1) grid = 1;
   const int rg = rows_per_group(g.nb_tmpl, epi);
