@@ -105,9 +105,11 @@ int gemv_max_rows(int epi, int K, int pro = PRO_X);
 cudaError_t gemv_launch(int epi, int pro, const GemvArgs& a, const GemvLaunch& g, cudaStream_t s);
 cudaError_t gemv_init();   // raise dynamic shared-memory limits (once per process)
 
-// Tensor-core skinny GEMM (batch 16..128, BF16 weights): y = W x with x given
-// as [2 * Rp][K] BF16 rows (rows 0..Rp-1 the high parts, Rp..2Rp-1 the low
-// parts of the fp32 activations). Tensor maps are opaque 128-byte blobs.
+// Tensor-core skinny GEMMs (batch 16..128): y = W x with x given as
+// [2 * Rp][K] 16-bit rows (rows 0..Rp-1 the high parts, Rp..2Rp-1 the low
+// parts of the fp32 activations; BF16 for BF16 weights, FP16 for e4m3 weights,
+// whose codes are widened to FP16 in shared memory). Tensor maps are opaque
+// 128-byte blobs.
 struct TmaMap { alignas(64) unsigned char bytes[128]; };
 struct TcArgs {
   int N, K, R, Rp;            // output channels (SWIGLU: ffn), K, live rows, padded rows (multiple of 8)
