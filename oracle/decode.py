@@ -36,6 +36,8 @@ lowest index wins an exact arg-max tie.
 from __future__ import annotations
 
 import dataclasses
+import os
+from concurrent.futures import ThreadPoolExecutor
 from typing import Callable, Dict, Optional
 
 import numpy as np
@@ -104,16 +106,35 @@ def decode_weight(t: Dict[str, np.ndarray], rows: Optional[slice] = None) -> np.
     raise TypeError(f"unsupported weight storage {w.dtype}")
 
 
-def matmul(t: Dict[str, np.ndarray], x: np.ndarray, chunk_bytes: int = 1 << 28) -> np.ndarray:
+_THREADS = max(1, os.cpu_count() or 1)
+
+
+def matmul(t: Dict[str, np.ndarray], x: np.ndarray, chunk_bytes: int = 1 << 24) -> np.ndarray:
     """y[b, n] = sum_k W[n, k] x[b, k] in float64 (W decoded row chunk by row chunk
-    so that large matrices never exist whole in float64)."""
+    so that large matrices never exist whole in float64).
+
+    Each output element is one float64 dot product over k; the pages fix no
+    summation order. For a few input rows (decode batches) the row chunks are
+    independent and run on a thread pool, each decoded and multiplied with
+    NumPy's own loops (einsum, no BLAS, so the threads do not oversubscribe the
+    cores); larger inputs use one BLAS product per chunk."""
     n, k = t["w"].shape
     x = np.atleast_2d(np.asarray(x, dtype=np.float64))
     out = np.empty((x.shape[0], n), dtype=np.float64)
     step = max(1, chunk_bytes // (8 * k))
-    for r0 in range(0, n, step):
+    starts = range(0, n, step)
+    if x.shape[0] > 16 or _THREADS == 1 or len(starts) == 1:
+        for r0 in starts:
+            r1 = min(n, r0 + step)
+            out[:, r0:r1] = x @ decode_weight(t, slice(r0, r1)).T
+        return out
+
+    def chunk(r0):
         r1 = min(n, r0 + step)
-        out[:, r0:r1] = x @ decode_weight(t, slice(r0, r1)).T
+        out[:, r0:r1] = np.einsum("bk,nk->bn", x, decode_weight(t, slice(r0, r1)))
+
+    with ThreadPoolExecutor(min(_THREADS, len(starts))) as ex:
+        list(ex.map(chunk, starts))
     return out
 
 
