@@ -21,12 +21,23 @@ pins live in tests/test_oracle_*.py):
 * decode.paged_attention: brute-force softmax over a contiguous cache written
   as plain Python loops, shuffled block tables, S in {1, 15, 16, 17, 33},
   GQA groups 1, 2, 5, 8; S = 1 gives V_0; q = 0 gives the mean of V.
+* decode.prefill: the same logits and cache as feeding the prompt to
+  decode_step one token at a time (the definition), on tiny models, from
+  position 0 and from a later start.
 * decode.decode_step: a scalar pure-Python brute-force step on a tiny model;
   closed forms with zeroed projections (logits = W_lm . norm(E[tok]));
   shift invariance of the whole step under a common position offset; the
   per-token multiply-add count within 1 % of 2 x matmul params + attention,
   within 10 % of 2 x all params.
 
+* sampling.philox4x32_10: the generator's published known-answer vectors
+  (tests/golden/philox4x32_10_kat.json); sampling.uniforms: values strictly
+  inside (0, 1) on the 2^-24 grid, moments and a chi-square test of
+  uniformity; sampling.sample: Gumbel-max frequencies against softmax
+  probabilities (chi-square), arg-max at top_k = 1, at a vanishing temperature
+  and at a tiny top_p, draws inside the top-k set; sampling.keep_set: the
+  top-p set is the minimal most-probable prefix.
+
 No function is "parity unpinned".
 """
-from . import numerics, decode  # noqa: F401
+from . import numerics, decode, sampling  # noqa: F401

@@ -45,7 +45,7 @@ import numpy as np
 from .numerics import bf16_decode, e4m3_decode, round_bf16, round_e4m3
 
 __all__ = ["rmsnorm", "rope", "silu", "swiglu", "decode_weight", "matmul",
-           "OracleKV", "paged_attention", "decode_step", "StepResult"]
+           "OracleKV", "paged_attention", "decode_step", "StepResult", "prefill"]
 
 
 # ---------------------------------------------------------------------------
@@ -300,3 +300,22 @@ def decode_step(weights: WeightSource, cfg, kv: OracleKV, tokens, positions, blo
     mm += 2 * B * cfg.vocab * H
     ids = np.argmax(logits, axis=1)                           # first maximum on ties
     return StepResult(logits, ids, mm + at, mm, at)
+
+
+def prefill(weights: WeightSource, cfg, kv: OracleKV, tokens, start_pos: int, block_table) -> StepResult:
+    """Ingest the prompt tokens of one sequence at positions start_pos,
+    start_pos + 1, ... ("GPU Inference Internals", "Roofline: Why Decode Is
+    Memory-Bound": prefill runs the whole prompt through the model at once;
+    what it computes is the same as feeding the prompt one token at a time).
+
+    Every prompt token is one row of a decode step over the sequence's block
+    table, at its own position and attending over position + 1 tokens. Within
+    each layer decode_step takes the rows in order and writes a row's K and V
+    before that row attends, so row i sees exactly the prompt positions up to
+    its own: causal attention. The last row's logits and arg-max are the
+    prompt's next token; `kv` holds every prompt token's K and V."""
+    tokens = np.asarray(tokens, dtype=np.int64)
+    n = len(tokens)
+    pos = int(start_pos) + np.arange(n, dtype=np.int64)
+    tables = np.repeat(np.asarray(block_table, dtype=np.int64)[None, :], n, axis=0)
+    return decode_step(weights, cfg, kv, tokens, pos, tables, pos + 1)

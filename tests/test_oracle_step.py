@@ -6,13 +6,15 @@
   identity on the residual stream, so logits = W_lm . RMSNorm(E[tok]) * g_final.
 * Relative position: keys stored at positions j + t and a query at m + t give
   the same attention output as j and m ("RoFormer"), up to the cache rounding.
+* Prefill: ingesting a prompt at once gives the logits and cache of feeding
+  it one token at a time.
 * FLOPs: "A transformer forward pass performs roughly 2 x P FLOPs per token"
   ("GPU Inference Internals", "Roofline: Why Decode Is Memory-Bound").
 """
 import numpy as np
 import pytest
 
-from oracle.decode import OracleKV, decode_step, paged_attention, rmsnorm, rope
+from oracle.decode import OracleKV, decode_step, paged_attention, prefill, rmsnorm, rope
 from oracle.numerics import bf16_decode, round_bf16
 from synth import ONE_B, tensor_shape, SynthModel
 from tests import bruteforce as bf
@@ -107,3 +109,40 @@ def test_flops_about_twice_params():
     assert abs(res.flops - (2 * p_matmul + attn)) <= 0.01 * res.flops
     assert abs(res.flops / (2 * p_total) - 1) <= 0.10
     assert res.attn_flops == attn
+
+
+@pytest.mark.parametrize("cfg", [MICRO, MICRO_FP8], ids=lambda c: c.name)
+@pytest.mark.parametrize("start,n", [(0, 1), (0, 19), (23, 9)])
+def test_prefill_equals_token_by_token(cfg, start, n):
+    """Prefill of n tokens from `start` = n decode steps of one token each
+    (positions start, start + 1, ...): same last-token logits, same cache."""
+    model = SynthModel(cfg, seed=31)
+    W = oracle_weights(model)
+    nblk = -(-(start + n) // 16) + 1
+    table = np.random.default_rng(4).permutation(nblk + 2)[:nblk].astype(np.int32)
+    from synth import random_kv_pool
+    raw = kv_numpy(random_kv_pool(cfg, nblk + 2, seed=8))
+    ks = np.array([0.75, 1.5]) if cfg.kv_dtype == "fp8" else np.ones(2)
+    toks = np.random.default_rng(5).integers(0, cfg.vocab, size=n).astype(np.int32)
+    a = OracleKV(raw.copy(), ks, ks[::-1].copy())
+    res = prefill(W, cfg, a, toks, start, table)
+    b = OracleKV(raw.copy(), ks, ks[::-1].copy())
+    for i in range(n):
+        r1 = decode_step(W, cfg, b, toks[i:i + 1], [start + i], table[None, :], [start + i + 1])
+    np.testing.assert_allclose(res.logits[-1], r1.logits[0], rtol=1e-9, atol=1e-12)
+    # the two runs round the same values to the cache format; their fp64
+    # inputs differ only in summation order, so codes agree except (rarely)
+    # at a rounding boundary, where they are neighbours
+    dec = (lambda r: bf16_decode(r)) if cfg.kv_dtype == "bf16" else None
+    if dec is None:
+        from oracle.numerics import e4m3_decode as dec
+    diff = a.raw != b.raw
+    assert diff.sum() <= 2
+    if diff.any():
+        ga, gb = dec(a.raw[diff]), dec(b.raw[diff])
+        assert np.all(np.abs(ga - gb) <= 0.13 * np.maximum(np.abs(ga), np.abs(gb)))
+    # slots outside the prompt's positions are untouched
+    untouched = np.ones(raw.shape[2:5], bool)
+    for p in range(start, start + n):
+        untouched[table[p // 16], :, p % 16] = False
+    assert np.array_equal(a.raw[:, :, untouched], raw[:, :, untouched])
