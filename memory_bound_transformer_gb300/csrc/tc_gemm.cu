@@ -240,7 +240,9 @@ cudaError_t tc_make_map(void* map, const void* base, int rows, int K, int box_ro
 }
 
 // 2-D tensor map over e4m3 codes [rows][K] (K contiguous), box of 64 codes x
-// 64 rows, no swizzle (the widening warps read it), zero fill out of bounds.
+// 64 rows, 64-byte swizzle (16-byte chunk c of row r lands at chunk
+// c ^ ((r / 2) % 4), so the widening threads, one row each, read shared memory
+// without bank conflicts), zero fill out of bounds.
 cudaError_t tc_make_map_u8(void* map, const void* base, int rows, int K) {
   if (!g_encode) return cudaErrorNotSupported;
   if (((uintptr_t)base & 15) || K % 16) return cudaErrorInvalidValue;
@@ -249,7 +251,7 @@ cudaError_t tc_make_map_u8(void* map, const void* base, int rows, int K) {
   const cuuint32_t box[2] = {(cuuint32_t)kTcBK, 64u};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode((CUtensorMap*)map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

@@ -69,6 +69,14 @@ __device__ __forceinline__ void umma_kf16(uint32_t tmem_d, uint64_t a, uint64_t 
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
       ::"r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
+// The same MMA with A read from tensor memory: M = 128 rows in lanes 0..127,
+// two 16-bit K elements per 32-bit column (the lower K index in the low half).
+__device__ __forceinline__ void umma_kf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                                 uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+      ::"r"(tmem_d), "r"(tmem_a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                ::"r"(smem_u32(bar)) : "memory");
@@ -87,6 +95,13 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 consecutive 32-bit columns of this thread's TMEM lane from registers
+// (the warp covers the 32 lanes of its quarter); then wait for the stores.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+               ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]) : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
@@ -108,13 +123,13 @@ __device__ __forceinline__ void named_bar(int id, int n) {
 // epilogue threads are the epilogue's own. `et` = the thread's index among them.
 template <int EPI>
 __device__ __forceinline__ void tc_epilogue(const TcArgs& a, uint32_t tmem, int q, int lane, int et, int tile,
-                                            int split, unsigned char* scratch, int bar) {
+                                            int split, unsigned char* scratch, int bar, float mul = 1.f) {
   const int Rp = a.Rp;
   const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
   const int row = q * 32 + lane;
   if (EPI == EPI_PARTIAL) {
     const int n = tile * kTcBM + row;
-    const float sc = (a.scale && n < a.N) ? a.scale[n] : 1.f;
+    const float sc = ((a.scale && n < a.N) ? a.scale[n] : 1.f) * mul;
     for (int c0 = 0; c0 < Rp; c0 += 8) {
       float hi[8], lo[8];
       tmem_ld8(lane_base + c0, hi);
@@ -133,7 +148,7 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& a, uint32_t tmem, int 
     const bool ch_ok = j < a.N;
     uint16_t* act = reinterpret_cast<uint16_t*>(a.act_hl);
     if (q >= 2) {
-      const float su = (a.scale && ch_ok) ? a.scale[a.N + j] : 1.f;
+      const float su = ((a.scale && ch_ok) ? a.scale[a.N + j] : 1.f) * mul;
       for (int c0 = 0; c0 < Rp; c0 += 8) {
         float hi[8], lo[8];
         tmem_ld8(lane_base + c0, hi);
@@ -144,7 +159,7 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& a, uint32_t tmem, int 
     }
     named_bar(bar, 128);
     if (q < 2) {
-      const float sg = (a.scale && ch_ok) ? a.scale[j] : 1.f;
+      const float sg = ((a.scale && ch_ok) ? a.scale[j] : 1.f) * mul;
       for (int c0 = 0; c0 < Rp; c0 += 8) {
         float hi[8], lo[8];
         tmem_ld8(lane_base + c0, hi);
@@ -165,7 +180,7 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& a, uint32_t tmem, int 
     float* bv = reinterpret_cast<float*>(scratch);   // [4 quarters][Rp]
     int* bi = reinterpret_cast<int*>(scratch + 4 * Rp * 4);
     const int n = tile * kTcBM + row;
-    const float sc = (a.scale && n < a.N) ? a.scale[n] : 1.f;
+    const float sc = ((a.scale && n < a.N) ? a.scale[n] : 1.f) * mul;
     for (int c0 = 0; c0 < Rp; c0 += 8) {
       float hi[8], lo[8];
       tmem_ld8(lane_base + c0, hi);
