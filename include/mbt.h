@@ -169,7 +169,9 @@ int kv_set_scales(mbt_kv* kv, const float* k_scales, const float* v_scales);
  * eagerly first (warm-up) on `stream` and synchronises it. After capture
  * decode_step pads a batch of B rows to the smallest captured size >= B and
  * replays its graph; B above the largest size, another kv, or a block table
- * the graph cannot address runs eagerly.
+ * wider than max_blocks_per_seq entries (bt_stride) runs eagerly. An eager
+ * step never invalidates the graphs: when it needs more workspace than they
+ * were captured with, it uses a separate one.
  * Errors: MBT_ERR_BAD_ARG, MBT_ERR_OOM, MBT_ERR_CUDA. */
 int model_capture(mbt_model* m, mbt_kv* kv, const int* ladder, int n,
                   int max_blocks_per_seq, void* stream);
@@ -184,8 +186,10 @@ int model_set_eager(mbt_model* m, int eager);
  *                            block block_tables[b][p / 16], slot p % 16
  *   block_tables[B][bt_stride] int32 physical block ids of each sequence
  *   seq_lens[B]       int32  tokens attended over, the new one included
- *                            (normally positions[b] + 1); with graphs it must
- *                            not exceed max_blocks_per_seq * 16
+ *                            (normally positions[b] + 1); at most
+ *                            bt_stride * 16: a row beyond its table is
+ *                            flagged MBT_DEV_SEQLEN_RANGE and attends over
+ *                            nothing, on the graph and the eager path alike
  *   next_ids[B]       int32  out: arg-max of the logits (lowest id on ties)
  *   logits_or_null    float  out: [B][vocab] fp32 logits, or NULL
  * Asynchronous on `stream`. Returns MBT_ERR_BATCH for B <= 0, MBT_ERR_BAD_ARG
@@ -195,6 +199,29 @@ int decode_step(mbt_model* m, mbt_kv* kv, int B, const int32_t* token_ids,
                 const int32_t* positions, const int32_t* block_tables, int bt_stride,
                 const int32_t* seq_lens, int32_t* next_ids, float* logits_or_null,
                 void* stream);
+
+/* prefill: ingest the prompt tokens[0..n) of one sequence, at positions
+ * start_pos .. start_pos + n - 1, in passes of up to 128 tokens through the
+ * whole layer stack ("GPU Inference Internals", "Roofline: Why Decode Is
+ * Memory-Bound": prefill works on the whole prompt at once, 2 x params x n
+ * FLOPs, compute-bound; "Kernel Fusion for Large-Scale LLM Inference",
+ * section 12: time to first token). Each prompt token's K and V are written
+ * where decode_step would write them (block block_table[p / 16], slot p % 16)
+ * with the same rounding, each token attends causally over positions 0..p
+ * (positions before start_pos must already be in the cache), and the arg-max
+ * of the last token's logits goes to next_id. Projections run on the tensor
+ * cores for passes of 16 tokens or more.
+ *   tokens[n]            int32 device
+ *   block_table[bt_len]  int32 device: the sequence's blocks; bt_len * 16 >= start_pos + n
+ *   next_id[1]           int32 device, out
+ *   logits_or_null       float device [vocab], out: the last token's logits, or NULL
+ * Runs eagerly (no graph) and asynchronously on `stream`; captured graphs stay
+ * valid. Errors: MBT_ERR_BATCH (n < 1), MBT_ERR_BAD_ARG (a null pointer,
+ * start_pos < 0, start_pos + n beyond max_pos or beyond the table, a kv of
+ * another model), MBT_ERR_OOM, MBT_ERR_CUDA. Device-detected range errors go
+ * to the error word. */
+int prefill(mbt_model* m, mbt_kv* kv, int n, const int32_t* tokens, int start_pos,
+            const int32_t* block_table, int bt_len, int32_t* next_id, float* logits_or_null, void* stream);
 
 /* model_poll_errors: synchronise `stream`, return the device error word in
  * *bits (host) and clear it. */

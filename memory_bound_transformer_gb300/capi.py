@@ -39,6 +39,7 @@ SIGNATURES = {
     "model_capture": (_I, [_P, _P, _P, _I, _I, _P]),
     "model_set_eager": (_I, [_P, _I]),
     "decode_step": (_I, [_P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P]),
+    "prefill": (_I, [_P, _P, _I, _P, _I, _P, _I, _P, _P, _P]),
     "model_poll_errors": (_I, [_P, _P, ctypes.POINTER(_U)]),
     "model_stats": (_I, [_P, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "status_string": (ctypes.c_char_p, [_I]),
@@ -49,6 +50,8 @@ SIGNATURES = {
     "op_gemv": (_I, [_I, _I, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _P, ctypes.POINTER(_I), _P, _P]),
     "op_gemv_sched_ints": (_I, [_I, _I, _I, _I, _I]),
     "op_gemv_ex": (_I, [_I, _I, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _P, ctypes.POINTER(_I), _P, _P, _P]),
+    "op_gemv_norm_sched_ints": (_I, [_I, _I, _I, _I, _I]),
+    "op_gemv_norm": (_I, [_I, _I, _P, _P, _I, _I, _P, _P, _I, _P, _F, _P, _I, _P, _P, _P, _P, _P, _P, _P]),
     "op_gemm_tc": (_I, [_I, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P]),
     "op_gemm_tc_e4m3": (_I, [_I, _P, _P, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P]),
     "op_rope_kv_write": (_I, [_I, _P, _I, _I, _I, _P, _P, _I, _I, _F, _P, _P, _I, _I, _F, _F, _P, _P, _P]),
@@ -186,6 +189,22 @@ def decode_step_raw(model: int, kv: int, B: int, tok, pos, bt, bt_stride: int, s
                               _ptr(next_ids), _ptr(logits), _stream(stream))
 
 
+def prefill(model: int, kv: int, tokens: torch.Tensor, start_pos: int, block_table: torch.Tensor,
+            next_id: torch.Tensor, logits: Optional[torch.Tensor] = None, stream=None) -> None:
+    """tokens [n] int32, block_table [bt_len] int32, next_id [1] int32 (device);
+    logits [vocab] fp32 or None."""
+    _require_cuda(tokens, block_table, next_id, logits)
+    _check("prefill", load().prefill(model, kv, tokens.numel(), _ptr(tokens), int(start_pos), _ptr(block_table),
+                                     block_table.numel(), _ptr(next_id), _ptr(logits), _stream(stream)))
+
+
+def prefill_raw(model: int, kv: int, n: int, tokens, start_pos: int, block_table, bt_len: int, next_id,
+                logits=None, stream=None) -> int:
+    """Pointer-level call; returns the status code instead of raising."""
+    return load().prefill(model, kv, n, _ptr(tokens), start_pos, _ptr(block_table), bt_len, _ptr(next_id),
+                          _ptr(logits), _stream(stream))
+
+
 def model_poll_errors(model: int, stream=None) -> int:
     bits = ctypes.c_uint32()
     _check("model_poll_errors", load().model_poll_errors(model, _stream(stream), ctypes.byref(bits)))
@@ -245,6 +264,22 @@ def op_gemv_ex(epi, w_dtype, W, scales, N, K, x, B, sched, force_nsplit=0, out=N
                                            _ptr(out), _ptr(act), _ptr(logits), _ptr(next_ids),
                                            ctypes.byref(used), _ptr(sched), _ptr(err), _stream(stream)))
     return used.value
+
+
+def op_gemv_norm_sched_ints(epi: int, w_dtype: int, B: int, N: int, K: int) -> int:
+    return load().op_gemv_norm_sched_ints(epi, w_dtype, B, N, K)
+
+
+def op_gemv_norm(epi, w_dtype, W, scales, N, K, r_in, delta, gamma, eps, r_out, sched=None, out=None, act=None,
+                 logits=None, next_ids=None, err=None, stream=None) -> None:
+    """The norm-prologue projection: r_in, r_out [B][K] fp32, delta [n][B][K]
+    fp32 or None, gamma [K] BF16 (int16 bits or bfloat16)."""
+    B = r_in.shape[0]
+    n = 0 if delta is None else delta.shape[0]
+    _check("op_gemv_norm", load().op_gemv_norm(epi, w_dtype, _ptr(W), _ptr(scales), N, K, _ptr(r_in), _ptr(delta),
+                                               n, _ptr(gamma), eps, _ptr(r_out), B, _ptr(out), _ptr(act),
+                                               _ptr(logits), _ptr(next_ids), _ptr(sched), _ptr(err),
+                                               _stream(stream)))
 
 
 def op_gemm_tc_e4m3(epi, W, scales, N, K, x, B, ksplit=1, out=None, act=None, logits=None, next_ids=None,

@@ -691,8 +691,8 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
   if (G * a.d > kMergeMaxE * kAttnThreads || w_bytes + (size_t)2 * G * a.d * 4 > sm) return cudaErrorInvalidValue;
   AttnArgs args = a;
   void* params[] = {&args};
-  return launch_pdl(fn, dim3(a.nsplit, a.nkv, a.B), dim3(kAttnThreads), sm, s, params,
-                    a.carveout > 0 ? a.carveout : -1);
+  return launch_ex(fn, dim3(a.nsplit, a.nkv, a.B), dim3(kAttnThreads), sm, s, params, !a.no_pdl,
+                   a.carveout > 0 ? a.carveout : -1);
 }
 
 }  // namespace mbt

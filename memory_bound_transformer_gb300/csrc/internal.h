@@ -123,8 +123,8 @@ struct TcArgs {
 cudaError_t tc_init();
 cudaError_t tc_make_map(void* map, const void* base, int rows, int K, int box_rows);
 cudaError_t tc_launch(int epi, const void* mapW, const void* mapX, const TcArgs& a, int ksplit, cudaStream_t s);
-// e4m3 weights: [rows][K] codes, 64-code x 64-row boxes without swizzle; the
-// activations as FP16 high/low rows (map from tc_make_map)
+// e4m3 weights: [rows][K] codes, 64-code x 64-row boxes with 64-byte swizzle;
+// the activations as FP16 high/low rows (map from tc_make_map)
 cudaError_t tc_make_map_u8(void* map, const void* base, int rows, int K);
 cudaError_t tc8_init();
 cudaError_t tc8_launch(int epi, const void* mapW, const void* mapX, const TcArgs& a, int ksplit, cudaStream_t s);
@@ -186,6 +186,7 @@ struct AttnArgs {
   bf16* out_hl; int rp_hl;  // optional: output also as 16-bit high/low rows [2 * rp_hl][nq * d]
   int hl_f16;               // out_hl as FP16 (for e4m3 weights) rather than BF16
   int carveout;             // launch carveout (percent); 0 (zero-initialised) = the default
+  int no_pdl;               // ordinary launch: the previous kernel wrote this layer's cache
 };
 void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nsplit);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
@@ -197,10 +198,24 @@ cudaError_t launch_argmax_reduce(int B, const ArgmaxPart* part, int part_ld, int
                                  int* next_ids, uint32_t* err, cudaStream_t s, int carveout = -1);
 
 // Copy B caller rows into the graph's static buffers and fill pad rows [B, R).
+// Live rows keep the caller's table width: entries from bt_stride on are
+// written as -1 (an invalid id), and a row whose seq_len needs more than
+// bt_stride blocks gets seq_len 0 and MBT_DEV_SEQLEN_RANGE in err, so the
+// graph treats it as the eager path does (no attention, error bit set).
 struct StageArgs {
   int B, R; const int* tok; const int* pos; const int* bt; int bt_stride; const int* sl;
   int* s_tok; int* s_pos; int* s_bt; int s_stride; int* s_sl; int null_block;
+  uint32_t* err;
 };
 cudaError_t launch_stage_inputs(const StageArgs& a, cudaStream_t s);
+
+// Rows of one prefill pass: R consecutive prompt tokens of one sequence from
+// position p0 on (token, position, seq_len = position + 1, and the
+// sequence's block table repeated per row).
+struct PrefillStageArgs {
+  int R; const int* tokens; int p0; const int* bt; int bt_len;
+  int* s_tok; int* s_pos; int* s_sl; int* s_bt;
+};
+cudaError_t launch_stage_prefill(const PrefillStageArgs& a, cudaStream_t s);
 
 }  // namespace mbt

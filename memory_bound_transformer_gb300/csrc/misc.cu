@@ -323,7 +323,11 @@ cudaError_t launch_argmax_reduce(int B, const ArgmaxPart* part, int part_ld, int
 // Static input buffers for graph replay ("copies inputs into the graph's static
 // buffers", "Kernels, Fusion & CUDA Graphs", "Fix 2: CUDA graphs"): rows [B, R)
 // become padding rows (token 0, position 0, one token of context in the null
-// block) whose only write is to the null block.
+// block) whose only write is to the null block. A live row's table keeps the
+// caller's width: the graph's wider static table is filled with -1 past it
+// (never the null block, which would make the graph attend over padding), and
+// a seq_len the caller's table cannot hold becomes 0 (flagged), which the
+// attention kernel treats exactly as the eager path treats the original.
 
 __global__ void stage_inputs_kernel(const StageArgs a) {
   const int b = blockIdx.x;
@@ -331,17 +335,40 @@ __global__ void stage_inputs_kernel(const StageArgs a) {
   if (threadIdx.x == 0) {
     a.s_tok[b] = live ? a.tok[b] : 0;
     a.s_pos[b] = live ? a.pos[b] : 0;
-    a.s_sl[b] = live ? a.sl[b] : 1;
+    int sl = 1;
+    if (live) {
+      sl = a.sl[b];
+      if (sl > a.bt_stride * kBlockTokens) {
+        set_err(a.err, MBT_DEV_SEQLEN_RANGE);
+        sl = 0;
+      }
+    }
+    a.s_sl[b] = sl;
   }
   for (int j = threadIdx.x; j < a.s_stride; j += blockDim.x) {
     int v = a.null_block;
-    if (live && j < a.bt_stride) v = a.bt[(size_t)b * a.bt_stride + j];
+    if (live) v = j < a.bt_stride ? a.bt[(size_t)b * a.bt_stride + j] : -1;
     a.s_bt[(size_t)b * a.s_stride + j] = v;
   }
 }
 
 cudaError_t launch_stage_inputs(const StageArgs& a, cudaStream_t s) {
   stage_inputs_kernel<<<a.R, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+__global__ void stage_prefill_kernel(const PrefillStageArgs a) {
+  const int b = blockIdx.x;
+  if (threadIdx.x == 0) {
+    a.s_tok[b] = a.tokens[b];
+    a.s_pos[b] = a.p0 + b;
+    a.s_sl[b] = a.p0 + b + 1;
+  }
+  for (int j = threadIdx.x; j < a.bt_len; j += blockDim.x) a.s_bt[(size_t)b * a.bt_len + j] = a.bt[j];
+}
+
+cudaError_t launch_stage_prefill(const PrefillStageArgs& a, cudaStream_t s) {
+  stage_prefill_kernel<<<a.R, 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 

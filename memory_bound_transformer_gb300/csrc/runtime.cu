@@ -22,6 +22,18 @@ namespace {
 
 // GEMV work-queue counters per step (one per launch and K split)
 constexpr int kSchedCap = 8192;
+// Fewest rows that run on the tensor cores (below: the CUDA-core GEMV). The
+// CUDA-core GEMV re-reads the weights for every 8 rows and keeps 8 rows x 32
+// accumulators per thread at one CTA per SM; measured on the 8B-class BF16
+// step (ms per step at 1 / 2 / 3 / 4 / 8 rows): CUDA cores 2.94 / 3.56 / 5.00
+// / 5.16 / 9.07 against tensor cores - / 3.52 / 3.46 / 3.47 / 3.63, so every
+// batch from 2 rows on runs on the tensor cores.
+#ifndef MBT_TC_MIN_ROWS
+#define MBT_TC_MIN_ROWS 2
+#endif
+constexpr int kTcMinRows = MBT_TC_MIN_ROWS;
+// Prompt tokens per prefill pass (rows of one pass through the layers).
+constexpr int kPrefillChunk = 128;
 
 
 
@@ -59,6 +71,9 @@ struct Workspace {
   int* sched = nullptr;                              // GEMV work-queue counters, zeroed each step
   int rp_cap = 0;                                    // tensor-core path: BF16 high/low rows
   bf16* x_hl = nullptr; bf16* o_hl = nullptr; bf16* act_hl = nullptr;
+  float* q = nullptr;                                // prefill: rotated queries [cap][nq * d]
+  int* pf_tok = nullptr; int* pf_pos = nullptr; int* pf_sl = nullptr;   // prefill rows [cap]
+  int* pf_bt = nullptr;                              // prefill block tables [cap][mbs_cap]
 };
 
 struct Graph {
@@ -83,7 +98,8 @@ struct mbt_model {
   bool tc_ok = false;
   float2* rope = nullptr;
   uint32_t* err = nullptr;
-  Workspace ws;
+  Workspace ws;                     // bound to the captured graphs (their kernels hold its addresses)
+  Workspace ws_eager;               // eager steps the graph-bound workspace is too small for
   // graphs
   std::vector<Graph> graphs;
   mbt_kv* graph_kv = nullptr;
@@ -136,7 +152,7 @@ Plan make_plan(const mbt_model* m, int R, int mbs) {
   const int H = (int)m->h.hidden, Q = (int)(m->h.n_q_heads * m->h.head_dim), F = (int)m->h.ffn;
   const int QKV = (int)((m->h.n_q_heads + 2 * m->h.n_kv_heads) * m->h.head_dim);
   const int L = (int)m->h.n_layers;
-  p.use_tc = m->tc_ok && R >= 16 && R <= 128;
+  p.use_tc = m->tc_ok && R >= kTcMinRows && R <= 128;
   if (p.use_tc) {
     p.rp = (R + 7) / 8 * 8;
     p.ns_qkv = tc_ksplit(m, EPI_PARTIAL, QKV, H);
@@ -164,35 +180,54 @@ void free_ws(Workspace& w) {
   w = Workspace();
 }
 
-// Grow the workspace to serve R rows with block tables of mbs entries.
-int ensure_ws(mbt_model* m, int R, int mbs) {
-  Workspace& w = m->ws;
-  int cap = std::max(R, w.cap);
-  int mbs_cap = std::max(mbs, w.mbs_cap);
-  size_t po = 0, pml = 0;
-  int ns_qkv = 1, ns_delta = 1, g_lm = 1;
-  for (int r = 1; r <= cap; ++r) {
-    Plan p = make_plan(m, r, mbs_cap);
-    // attn_plan never uses more splits than this, whatever the table width
+// Capacities a workspace needs to serve R rows with block tables of mbs entries.
+struct WsNeed {
+  int cap, mbs_cap, ns_qkv, ns_delta, g_lm;
+  size_t po, pml;
+};
+
+WsNeed ws_need(const mbt_model* m, const Workspace& w, int R, int mbs) {
+  WsNeed n;
+  n.cap = std::max(R, w.cap);
+  n.mbs_cap = std::max(mbs, w.mbs_cap);
+  n.ns_qkv = 1; n.ns_delta = 1; n.g_lm = 1;
+  n.pml = 0;
+  for (int r = 1; r <= n.cap; ++r) {
+    Plan p = make_plan(m, r, n.mbs_cap);
     const int pairs = r * (int)m->h.n_kv_heads;
     // attn_plan never uses more splits than this, whatever the table width up to mbs_cap
-    const int split_bound = std::max({1, (4 * m->num_sms + pairs - 1) / pairs, (mbs_cap + 511) / 512});
-    pml = std::max(pml, (size_t)r * m->h.n_q_heads * split_bound);
-    ns_qkv = std::max(ns_qkv, p.ns_qkv);
-    ns_delta = std::max({ns_delta, p.ns_o, p.ns_down});
-    g_lm = std::max(g_lm, p.g_lm);
+    const int split_bound = std::max({1, (4 * m->num_sms + pairs - 1) / pairs, (n.mbs_cap + 511) / 512});
+    n.pml = std::max(n.pml, (size_t)r * m->h.n_q_heads * split_bound);
+    n.ns_qkv = std::max(n.ns_qkv, p.ns_qkv);
+    n.ns_delta = std::max({n.ns_delta, p.ns_o, p.ns_down});
+    n.g_lm = std::max(n.g_lm, p.g_lm);
   }
-  po = pml * m->h.head_dim;
-  if (w.mem && cap <= w.cap && po <= w.part_o_elems && ns_qkv <= w.ns_qkv_cap &&
-      ns_delta <= w.ns_delta_cap && g_lm <= w.g_lm_cap)
-    return MBT_OK;
-  // growing invalidates captured graphs (they hold the old addresses)
+  n.po = n.pml * m->h.head_dim;
+  return n;
+}
+
+bool ws_covers(const Workspace& w, const WsNeed& n) {
+  return w.mem && n.cap <= w.cap && n.mbs_cap <= w.mbs_cap && n.po <= w.part_o_elems &&
+         n.ns_qkv <= w.ns_qkv_cap && n.ns_delta <= w.ns_delta_cap && n.g_lm <= w.g_lm_cap;
+}
+
+// Grow workspace `w` to serve R rows with block tables of mbs entries. Growing
+// the graph-bound workspace invalidates the captured graphs (they hold its old
+// addresses), so callers grow it only while no graph exists (capture, or eager
+// mode before any capture); eager steps beside live graphs use m->ws_eager.
+int ensure_ws(mbt_model* m, Workspace& w, int R, int mbs) {
+  const WsNeed n = ws_need(m, w, R, mbs);
+  if (ws_covers(w, n)) return MBT_OK;
   if (cudaDeviceSynchronize() != cudaSuccess) return MBT_ERR_CUDA;
-  for (auto& g : m->graphs)
-    for (auto& e : g.exec) if (e) cudaGraphExecDestroy(e);
-  m->graphs.clear();
-  m->graph_kv = nullptr;
+  if (&w == &m->ws) {
+    for (auto& g : m->graphs)
+      for (auto& e : g.exec) if (e) cudaGraphExecDestroy(e);
+    m->graphs.clear();
+    m->graph_kv = nullptr;
+  }
   free_ws(w);
+  const int cap = n.cap, mbs_cap = n.mbs_cap, ns_qkv = n.ns_qkv, ns_delta = n.ns_delta, g_lm = n.g_lm;
+  const size_t po = n.po, pml = n.pml;
   const size_t H = m->h.hidden, Q = (size_t)m->h.n_q_heads * m->h.head_dim, F = m->h.ffn;
   const size_t QKV = (size_t)(m->h.n_q_heads + 2 * m->h.n_kv_heads) * m->h.head_dim;
   size_t off = 0;
@@ -209,6 +244,8 @@ int ensure_ws(mbt_model* m, int R, int mbs) {
   const size_t b_xhl = (size_t)2 * rp_cap * H * 2, b_ohl = (size_t)2 * rp_cap * Q * 2;
   const size_t b_ahl = (size_t)2 * rp_cap * F * 2;
   const size_t o_xhl = take(b_xhl), o_ohl = take(b_ohl), o_ahl = take(b_ahl);
+  const size_t o_q = take((size_t)cap * Q * 4);
+  const size_t o_pf = take((size_t)cap * 3 * 4), o_pfbt = take((size_t)cap * mbs_cap * 4);
   void* mem = nullptr;
   if (cudaMalloc(&mem, off) != cudaSuccess) { cudaGetLastError(); return MBT_ERR_OOM; }
   char* base = (char*)mem;
@@ -224,6 +261,9 @@ int ensure_ws(mbt_model* m, int R, int mbs) {
   w.sched = (int*)(base + o_sc);
   w.rp_cap = rp_cap;
   w.x_hl = (bf16*)(base + o_xhl); w.o_hl = (bf16*)(base + o_ohl); w.act_hl = (bf16*)(base + o_ahl);
+  w.q = (float*)(base + o_q);
+  w.pf_tok = (int*)(base + o_pf); w.pf_pos = w.pf_tok + cap; w.pf_sl = w.pf_pos + cap;
+  w.pf_bt = (int*)(base + o_pfbt);
   // attention tickets start at zero and every launch leaves them at zero; the
   // high/low activation rows start at zero so padding rows never hold NaN bits
   if (cudaMemset(mem, 0, off) != cudaSuccess) return MBT_ERR_CUDA;
@@ -238,7 +278,7 @@ struct NormIn {
 
 // One GEMV over R rows, issued in chunks of at most 8 rows (fewer when the
 // fp32 x tile of an unsplittable launch would not fit in shared memory).
-cudaError_t gemv_rows(const mbt_model* m, int epi, const NormIn* nin, const void* W, const float* sc,
+cudaError_t gemv_rows(const mbt_model* m, const Workspace& ws, int epi, const NormIn* nin, const void* W, const float* sc,
                       int N, int K, const float* x, int R, int nsplit, int grid_fixed, float* out,
                       long long split_stride, int ldo, float* act, int lda, float* logits,
                       ArgmaxPart* part, int part_ld, cudaStream_t s, uint32_t prefetch = 0,
@@ -270,7 +310,7 @@ cudaError_t gemv_rows(const mbt_model* m, int epi, const NormIn* nin, const void
     // group at a time (kernels that prefetch their whole slice keep it fixed)
     const int sg = gemv_queue_static_groups(g, N);
     if (sched_used && prefetch != 0xffffffffu && sg >= 0 && *sched_used + g.nsplit <= kSchedCap) {
-      a.sched = m->ws.sched + *sched_used;
+      a.sched = ws.sched + *sched_used;
       a.static_groups = sg;
       *sched_used += g.nsplit;
     }
@@ -280,12 +320,49 @@ cudaError_t gemv_rows(const mbt_model* m, int epi, const NormIn* nin, const void
   return cudaSuccess;
 }
 
+// Prefill form of the attention step: the chunk's rows are consecutive
+// tokens of one sequence, so every row's K and V must be in the cache before
+// any row attends (row i reads rows < i of the same chunk). RoPE + KV write
+// runs as its own kernel over all rows (queries rotated into w.q), then the
+// attention kernel reads the queries and the cache, writing nothing; it is an
+// ordinary launch, so its early cache reads see the writes just made.
+cudaError_t prefill_rope_kv(const mbt_model* m, const Workspace& w, const mbt_kv* kv, int l, int R, int ns_qkv,
+                            const int* pos, const int* bt, int bt_stride, cudaStream_t s) {
+  const int d = (int)m->h.head_dim, nq = (int)m->h.n_q_heads, nkv = (int)m->h.n_kv_heads;
+  const int QKV = (nq + 2 * nkv) * d;
+  const size_t half = kv_layer_half_bytes(m, kv->num_blocks);
+  char* kbase = (char*)kv->pool + 2 * half * (size_t)l;
+  RopeKvArgs rk = {};
+  rk.B = R; rk.qkv = w.qkv; rk.nsplit = ns_qkv; rk.split_stride = (long long)R * QKV; rk.ld_qkv = QKV;
+  rk.nq = nq; rk.nkv = nkv; rk.d = d; rk.positions = pos; rk.bt = bt; rk.bt_stride = bt_stride;
+  rk.max_pos = (int)m->h.max_pos; rk.rope = m->rope; rk.q_out = w.q;
+  rk.kpool = kbase; rk.vpool = kbase + half; rk.num_blocks = kv->num_blocks;
+  rk.kv_fp8 = m->kv8; rk.k_scale = kv->k_scale[l]; rk.v_scale = kv->v_scale[l]; rk.err = m->err;
+  return launch_rope_kv_write(rk, s);
+}
+
+// Prefill tail: final norm and LM head for the chunk's last row only (the
+// sequence's next token); the residual of that row plus the down projection's
+// pending partials, normalised into w.r2, then the arg-max GEMV.
+int lm_head_last_row(mbt_model* m, const Workspace& w, const Plan& p, int* next_ids, float* logits, cudaStream_t s) {
+  const int R = p.R, H = (int)m->h.hidden, V = (int)m->h.vocab;
+  const size_t last = (size_t)(R - 1) * H;
+  AddNormArgs an{1, H, w.r + last, w.delta2 + last, p.ns_down, (long long)R * H, m->g_final, m->h.eps, w.r2,
+                 nullptr, 0, 0};
+  MBT_CUDA(launch_add_rmsnorm(an, s));
+  const GemvLaunch g = gemv_plan(EPI_ARGMAX, m->wtype, 1, V, H, m->num_sms, 0, PRO_X, m->stream);
+  if (g.grid > w.g_lm_cap * w.cap) return MBT_ERR_UNSUPPORTED;
+  MBT_CUDA(gemv_rows(m, w, EPI_ARGMAX, nullptr, m->lm, m->s_lm, V, H, w.r2, 1, 1, g.grid, nullptr, 0, 0,
+                     nullptr, 0, logits, w.lm_part, 1, s));
+  MBT_CUDA(launch_argmax_reduce(1, w.lm_part, 1, g.grid, next_ids, m->err, s));
+  return MBT_OK;
+}
+
 // Layers, final norm and LM head at batch 16..128 on the tensor cores: each
 // projection reads BF16 high/low activation rows written by its producer
 // (residual add + RMSNorm, attention, the gate/up GEMM's SwiGLU epilogue).
-int run_layers_tc(mbt_model* m, mbt_kv* kv, const Plan& p, const int* pos, const int* bt, int bt_stride,
-                  const int* sl, int* next_ids, float* logits, cudaStream_t s) {
-  const Workspace& w = m->ws;
+int run_layers_tc(mbt_model* m, const Workspace& w, mbt_kv* kv, const Plan& p, const int* pos, const int* bt, int bt_stride,
+                  const int* sl, int* next_ids, float* logits, cudaStream_t s, bool prefill) {
   const int R = p.R, Rp = p.rp;
   const int H = (int)m->h.hidden, d = (int)m->h.head_dim;
   const int nq = (int)m->h.n_q_heads, nkv = (int)m->h.n_kv_heads;
@@ -328,6 +405,10 @@ int run_layers_tc(mbt_model* m, mbt_kv* kv, const Plan& p, const int* pos, const
     at.bps = p.attn_bps; at.nsplit = p.attn_nsplit;
     at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = nullptr; at.tickets = w.tickets; at.err = m->err;
     at.out_hl = w.o_hl; at.rp_hl = Rp; at.hl_f16 = f16;
+    if (prefill) {
+      MBT_CUDA(prefill_rope_kv(m, w, kv, l, R, p.ns_qkv, pos, bt, bt_stride, s));
+      at.qkv = nullptr; at.q = w.q; at.no_pdl = 1;
+    }
     MBT_CUDA(launch_attention(at, s));
     MBT_CUDA(partial(wm[1], xq, L.s_o, H, Q, w.delta, p.ns_o));
     MBT_CUDA(norm(w.delta, p.ns_o, L.g_ffn));
@@ -337,6 +418,7 @@ int run_layers_tc(mbt_model* m, mbt_kv* kv, const Plan& p, const int* pos, const
     MBT_CUDA(gemm(EPI_SWIGLU, &wm[2], &xh, g, 1));
     MBT_CUDA(partial(wm[3], xf, L.s_down, H, F, w.delta2, p.ns_down));
   }
+  if (prefill) return next_ids ? lm_head_last_row(m, w, p, next_ids, logits, s) : MBT_OK;
   MBT_CUDA(norm(w.delta2, p.ns_down, m->g_final));
   TcArgs a = {};
   a.N = V; a.K = H; a.R = R; a.Rp = Rp; a.scale = m->s_lm; a.logits = logits; a.ldl = V;
@@ -352,10 +434,12 @@ int run_layers_tc(mbt_model* m, mbt_kv* kv, const Plan& p, const int* pos, const
 // prologue and SwiGLU epilogue, down projection. The residual lives in two
 // fp32 buffers (read one, write the other); projections with residual
 // outputs leave split-K partials that the next norm prologue adds.
-int run_step(mbt_model* m, mbt_kv* kv, const Plan& p, const int* tok, const int* pos,
+// With `prefill` the rows are consecutive prompt tokens of one sequence: the
+// KV write is its own kernel before attention, and only the last row goes
+// through the final norm and the LM head (none when next_ids is null).
+int run_step(mbt_model* m, const Workspace& w, mbt_kv* kv, const Plan& p, const int* tok, const int* pos,
              const int* bt, int bt_stride, const int* sl, int* next_ids, float* logits,
-             cudaStream_t s) {
-  const Workspace& w = m->ws;
+             cudaStream_t s, bool prefill = false) {
   const int R = p.R;
   const int H = (int)m->h.hidden, d = (int)m->h.head_dim;
   const int nq = (int)m->h.n_q_heads, nkv = (int)m->h.n_kv_heads;
@@ -367,14 +451,14 @@ int run_step(mbt_model* m, mbt_kv* kv, const Plan& p, const int* tok, const int*
   EmbedNormArgs en{R, H, V, tok, m->embed, w.r, m->layers[0].g_attn, m->h.eps, nullptr, m->err,
                    w.sched, kSchedCap, p.use_tc ? 0 : m->stream.carveout};
   MBT_CUDA(launch_embed_rmsnorm(en, s));
-  if (p.use_tc) return run_layers_tc(m, kv, p, pos, bt, bt_stride, sl, next_ids, logits, s);
+  if (p.use_tc) return run_layers_tc(m, w, kv, p, pos, bt, bt_stride, sl, next_ids, logits, s, prefill);
   int sq = 0;                                        // work-queue counters taken so far
   for (int l = 0; l < (int)m->h.n_layers; ++l) {
     const Layer& L = m->layers[l];
     char* kbase = (char*)kv->pool + 2 * half * (size_t)l;
     // RMSNorm prologue + fused QKV projection
     NormIn n1{w.r, l ? w.delta2 : nullptr, l ? p.ns_down : 0, L.g_attn, w.r2};
-    MBT_CUDA(gemv_rows(m, EPI_PARTIAL, &n1, L.w_qkv, L.s_qkv, QKV, H, nullptr, R, 1, 0, w.qkv,
+    MBT_CUDA(gemv_rows(m, w, EPI_PARTIAL, &n1, L.w_qkv, L.s_qkv, QKV, H, nullptr, R, 1, 0, w.qkv,
                        (long long)R * QKV, QKV, nullptr, 0, nullptr, nullptr, 0, s, 0, &sq));
     // RoPE + paged KV write + split-K attention + merge
     AttnArgs at = {};
@@ -387,23 +471,28 @@ int run_step(mbt_model* m, mbt_kv* kv, const Plan& p, const int* tok, const int*
     at.bps = p.attn_bps; at.nsplit = p.attn_nsplit;
     at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = w.o; at.tickets = w.tickets; at.err = m->err;
     at.carveout = m->stream.carveout;
+    if (prefill) {
+      MBT_CUDA(prefill_rope_kv(m, w, kv, l, R, 1, pos, bt, bt_stride, s));
+      at.qkv = nullptr; at.q = w.q; at.no_pdl = 1;
+    }
     MBT_CUDA(launch_attention(at, s));
     // O projection (residual partials); it starts during attention, whose
     // batch-1 form leaves HBM idle, so it prefetches all of its weights and
-    MBT_CUDA(gemv_rows(m, EPI_PARTIAL, nullptr, L.w_o, L.s_o, H, Q, w.o, R, p.ns_o, 0, w.delta,
+    MBT_CUDA(gemv_rows(m, w, EPI_PARTIAL, nullptr, L.w_o, L.s_o, H, Q, w.o, R, p.ns_o, 0, w.delta,
                        rh, H, nullptr, 0, nullptr, nullptr, 0, s, 0xffffffffu));
     // RMSNorm prologue + gate/up projection + SwiGLU epilogue
     NormIn n2{w.r2, w.delta, p.ns_o, L.g_ffn, w.r};
-    MBT_CUDA(gemv_rows(m, EPI_SWIGLU, &n2, L.w_gu, L.s_gu, F, H, nullptr, R, 1, 0, nullptr, 0, 0,
+    MBT_CUDA(gemv_rows(m, w, EPI_SWIGLU, &n2, L.w_gu, L.s_gu, F, H, nullptr, R, 1, 0, nullptr, 0, 0,
                        w.act, F, nullptr, nullptr, 0, s, 0, &sq));
     // down projection (residual partials)
-    MBT_CUDA(gemv_rows(m, EPI_PARTIAL, nullptr, L.w_down, L.s_down, H, F, w.act, R, p.ns_down, 0,
+    MBT_CUDA(gemv_rows(m, w, EPI_PARTIAL, nullptr, L.w_down, L.s_down, H, F, w.act, R, p.ns_down, 0,
                        w.delta2, rh, H, nullptr, 0, nullptr, nullptr, 0, s, 0, &sq));
   }
+  if (prefill) return next_ids ? lm_head_last_row(m, w, p, next_ids, logits, s) : MBT_OK;
   // final RMSNorm prologue + LM head with the arg-max epilogue, then the
   // cross-CTA reduction
   NormIn nf{w.r, w.delta2, p.ns_down, m->g_final, w.r2};
-  MBT_CUDA(gemv_rows(m, EPI_ARGMAX, &nf, m->lm, m->s_lm, V, H, nullptr, R, 1, p.g_lm, nullptr, 0, 0,
+  MBT_CUDA(gemv_rows(m, w, EPI_ARGMAX, &nf, m->lm, m->s_lm, V, H, nullptr, R, 1, p.g_lm, nullptr, 0, 0,
                      nullptr, 0, logits, w.lm_part, R, s, 0, &sq));
   MBT_CUDA(launch_argmax_reduce(R, w.lm_part, R, p.g_lm, next_ids, m->err, s, m->stream.carveout));
   return MBT_OK;
@@ -618,6 +707,7 @@ int model_destroy(mbt_model* m) {
   cudaDeviceSynchronize();
   destroy_graphs(m);
   free_ws(m->ws);
+  free_ws(m->ws_eager);
   if (m->wmem) cudaFree(m->wmem);
   if (m->err) cudaFree(m->err);
   if (m->rope) cudaFree(m->rope);
@@ -705,7 +795,7 @@ int model_capture(mbt_model* m, mbt_kv* kv, const int* ladder, int n, int mbs, v
   cudaStream_t s = (cudaStream_t)stream;
   destroy_graphs(m);
   const int Rmax = rungs.back();
-  int rc = ensure_ws(m, Rmax, mbs);
+  int rc = ensure_ws(m, m->ws, Rmax, mbs);
   if (rc != MBT_OK) return rc;
   // static input buffers
   size_t off = 0;
@@ -724,11 +814,11 @@ int model_capture(mbt_model* m, mbt_kv* kv, const int* ladder, int n, int mbs, v
   for (int R : rungs) {
     // all rows padding: token 0, position 0, the null block
     StageArgs st{0, R, nullptr, nullptr, nullptr, 1, nullptr, m->s_tok, m->s_pos, m->s_bt, mbs,
-                 m->s_sl, kv->num_blocks};
+                 m->s_sl, kv->num_blocks, nullptr};
     if (launch_stage_inputs(st, s) != cudaSuccess) { rc = MBT_ERR_CUDA; break; }
     Plan p = make_plan(m, R, mbs);
     // warm-up run outside capture
-    rc = run_step(m, kv, p, m->s_tok, m->s_pos, m->s_bt, mbs, m->s_sl, m->s_next, m->s_logits, s);
+    rc = run_step(m, m->ws, kv, p, m->s_tok, m->s_pos, m->s_bt, mbs, m->s_sl, m->s_next, m->s_logits, s);
     if (rc != MBT_OK) break;
     if (cudaStreamSynchronize(s) != cudaSuccess) { rc = MBT_ERR_CUDA; break; }
     Graph g;
@@ -736,7 +826,7 @@ int model_capture(mbt_model* m, mbt_kv* kv, const int* ladder, int n, int mbs, v
     for (int v = 0; v < 2 && rc == MBT_OK; ++v) {
       cudaGraph_t graph;
       if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) { rc = MBT_ERR_CUDA; break; }
-      int rr = run_step(m, kv, p, m->s_tok, m->s_pos, m->s_bt, mbs, m->s_sl, m->s_next,
+      int rr = run_step(m, m->ws, kv, p, m->s_tok, m->s_pos, m->s_bt, mbs, m->s_sl, m->s_next,
                         v ? m->s_logits : nullptr, cs);
       cudaError_t ce = cudaStreamEndCapture(cs, &graph);
       if (rr != MBT_OK || ce != cudaSuccess) { rc = MBT_ERR_CUDA; if (ce == cudaSuccess) cudaGraphDestroy(graph); break; }
@@ -760,9 +850,11 @@ int model_capture(mbt_model* m, mbt_kv* kv, const int* ladder, int n, int mbs, v
   return MBT_OK;
 }
 
+// The graph that serves B rows with block tables of bt_stride entries: the
+// smallest captured rung >= B, provided the graphs are bound to this cache and
+// their static table (graph_mbs entries per row) can hold the caller's table.
 static const Graph* pick_graph(const mbt_model* m, const mbt_kv* kv, int B, int bt_stride) {
-  (void)bt_stride;
-  if (m->eager || m->graph_kv != kv) return nullptr;
+  if (m->eager || m->graph_kv != kv || bt_stride > m->graph_mbs) return nullptr;
   for (const Graph& g : m->graphs)
     if (g.R >= B) return &g;
   return nullptr;
@@ -777,8 +869,11 @@ int decode_step(mbt_model* m, mbt_kv* kv, int B, const int32_t* tok, const int32
   cudaStream_t s = (cudaStream_t)stream;
   const Graph* g = pick_graph(m, kv, B, bt_stride);
   if (g) {
+    // the staging kernel keeps the caller's table width: entries past
+    // bt_stride are invalid ids, and a row whose seq_len needs more than
+    // bt_stride blocks is flagged and attends over nothing, as it does eagerly
     StageArgs st{B, g->R, tok, pos, bt, bt_stride, sl, m->s_tok, m->s_pos, m->s_bt, m->graph_mbs,
-                 m->s_sl, kv->num_blocks};
+                 m->s_sl, kv->num_blocks, m->err};
     MBT_CUDA(launch_stage_inputs(st, s));
     MBT_CUDA(cudaGraphLaunch(g->exec[logits ? 1 : 0], s));
     MBT_CUDA(cudaMemcpyAsync(next_ids, m->s_next, (size_t)B * 4, cudaMemcpyDeviceToDevice, s));
@@ -786,10 +881,40 @@ int decode_step(mbt_model* m, mbt_kv* kv, int B, const int32_t* tok, const int32
       MBT_CUDA(cudaMemcpyAsync(logits, m->s_logits, (size_t)B * m->h.vocab * 4, cudaMemcpyDeviceToDevice, s));
     return MBT_OK;
   }
-  int rc = ensure_ws(m, B, bt_stride);
+  // eager: the graph-bound workspace when it is large enough or no graph is
+  // bound to it; otherwise a separate one, so that the graphs stay valid
+  Workspace* w = &m->ws;
+  if (!m->graphs.empty() && !ws_covers(m->ws, ws_need(m, m->ws, B, bt_stride))) w = &m->ws_eager;
+  int rc = ensure_ws(m, *w, B, bt_stride);
   if (rc != MBT_OK) return rc;
   Plan p = make_plan(m, B, bt_stride);
-  return run_step(m, kv, p, tok, pos, bt, bt_stride, sl, next_ids, logits, s);
+  return run_step(m, *w, kv, p, tok, pos, bt, bt_stride, sl, next_ids, logits, s);
+}
+
+int prefill(mbt_model* m, mbt_kv* kv, int n, const int32_t* tokens, int start_pos, const int32_t* block_table,
+            int bt_len, int32_t* next_id, float* logits, void* stream) {
+  if (!m || !kv) return MBT_ERR_BAD_ARG;
+  if (n < 1) return MBT_ERR_BATCH;
+  if (kv->m != m || !tokens || !block_table || !next_id || bt_len < 1 || start_pos < 0) return MBT_ERR_BAD_ARG;
+  const long long end = (long long)start_pos + n;
+  if (end > (long long)m->h.max_pos || end > (long long)bt_len * kBlockTokens) return MBT_ERR_BAD_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int C = std::min(n, kPrefillChunk);
+  Workspace* w = &m->ws;
+  if (!m->graphs.empty() && !ws_covers(m->ws, ws_need(m, m->ws, C, bt_len))) w = &m->ws_eager;
+  int rc = ensure_ws(m, *w, C, bt_len);
+  if (rc != MBT_OK) return rc;
+  for (int c0 = 0; c0 < n; c0 += C) {
+    const int R = std::min(C, n - c0);
+    const bool last = c0 + R == n;
+    PrefillStageArgs st{R, tokens + c0, start_pos + c0, block_table, bt_len, w->pf_tok, w->pf_pos, w->pf_sl, w->pf_bt};
+    MBT_CUDA(launch_stage_prefill(st, s));
+    const Plan p = make_plan(m, R, bt_len);
+    rc = run_step(m, *w, kv, p, w->pf_tok, w->pf_pos, w->pf_bt, bt_len, w->pf_sl, last ? next_id : nullptr,
+                  last ? logits : nullptr, s, true);
+    if (rc != MBT_OK) return rc;
+  }
+  return MBT_OK;
 }
 
 int model_poll_errors(mbt_model* m, void* stream, uint32_t* bits) {

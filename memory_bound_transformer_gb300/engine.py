@@ -46,6 +46,9 @@ class Engine:
         capi.decode_step(self.model, self.kv, tokens, positions, block_tables, seq_lens, next_ids,
                          logits, self.stream)
 
+    def prefill(self, tokens, start_pos, block_table, next_id, logits=None):
+        capi.prefill(self.model, self.kv, tokens, start_pos, block_table, next_id, logits, self.stream)
+
     def errors(self) -> int:
         return capi.model_poll_errors(self.model, self.stream)
 
