@@ -2,13 +2,14 @@
 
 A step is one decode step (the whole per-layer kernel sequence, final norm, LM
 head and greedy arg-max) for one batch of sequences, replayed from the captured
-CUDA graph. Default workload: the 8B-class BF16 decoder at batch 1 with a
+CUDA graph. The headline is the 8B-class BF16 decoder at batch 1 with a
 per-sequence context drawn uniformly from [256, 2048] (random-init weights and
 random cache contents), each step feeding back the previous step's token ids and
-advancing every position by one.
+advancing every position by one; the same line carries batch 64 of that model
+and the 70B-class FP8 decoder at batch 1 and 64 (context 2048).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 8b] [--batch 1]
-                  [--impl reference]
+                  [--also 70b_fp8,32b_fp8] [--impl reference]
 
 Under torchrun every rank runs its own replica on its own GPU (the decode step
 has no cross-sequence exchange, so there is no collective on the data path);
@@ -35,12 +36,14 @@ from memory_bound_transformer_gb300 import capi, ledger  # noqa: E402
 from memory_bound_transformer_gb300.engine import Engine  # noqa: E402
 from synth import WORKLOADS, SynthModel, random_contexts, random_kv_pool, seeded_block_tables  # noqa: E402
 
+METRIC = "decode tokens/s at batch 1 and 64; achieved HBM GB/s as % of GB300 peak"
 L2_BYTES = 126 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the gate/up GEMV
-# (8B shape, batch 1) from the ncu capture summarised in
-# profiles/gemv_swiglu_8b_b1.md; None until that capture matches this kernel.
-GEMV_TRAFFIC_BYTES = 238168320      # 234.93 MB read + 3.24 MB written (first captured launch)
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of each workload's
+# dominant batch-1 kernel (the gate/up projection with the norm prologue and
+# SwiGLU epilogue) from one ncu capture of the current kernel; a workload
+# without a capture of the current kernel reports null.
+DRAM_TRAFFIC = {}
 
 
 def parse():
@@ -50,18 +53,24 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="8b", choices=sorted(WORKLOADS))
     ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--also", default="70b_fp8",
+                    help="comma-separated workloads measured after the headline one at batch 1 and their "
+                         "largest batch ('' for none)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kernel-timing", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--ladder", default=None, help="comma-separated graph ladder (default: the workload's)")
     ap.add_argument("--context", default=None,
                     help="LO,HI: per-sequence context range instead of the workload's (context sweeps)")
     ap.add_argument("--sweep", action="store_true",
                     help="batch sweep over the graph ladder: one JSON line per batch (tok/s, step p50/p99, GB/s)")
-    ap.add_argument("--kernel-only", nargs="?", const="gemv", default=None, choices=["gemv", "attention", "tc"],
-                    help="time one kernel alone for profiling: the gate/up GEMV over 4 layers' matrices, "
-                         "or one layer's paged attention at the workload's contexts")
+    ap.add_argument("--kernel-only", nargs="?", const="gemv_norm", default=None,
+                    choices=["gemv", "gemv_norm", "attention", "tc"],
+                    help="time one kernel alone for profiling: the gate/up GEMV over 4 layers' matrices (x "
+                         "given, or with the step's norm prologue), the tensor-core gate/up, or one layer's "
+                         "paged attention at the workload's contexts")
     return ap.parse_args()
 
 
@@ -71,6 +80,14 @@ def peaks():
         d = json.load(open(p))
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense BF16 tensor peak (TFLOP/s): measured burst, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
 
 
 class Clocks:
@@ -192,36 +209,51 @@ def timed_steps(eng, cfg, ctx, tables, B, K, W, dev, world, clocks_on):
                 clocks=ck, kernels_per_step=kps, uses_graph=graph)
 
 
-def time_native(args, rank, world):
-    wl = WORKLOADS[args.workload]
-    batches = [args.batch] if args.batch else [b for b in wl.batches if b in (1, 64)] or [wl.batches[0]]
+def measure_workload(wl, batches, args, world, head):
+    """Build one workload (weights, random cache, graph ladder) and time its
+    decode step at each batch; the headline workload also times the eager
+    launch-tax ablation and the end-to-end path. Every workload times its
+    dominant batch-1 kernel (gate/up with the norm prologue) and, when a batch
+    runs on the tensor cores, the tensor-core gate/up at its largest batch."""
     Bmax = max(batches)
     K, W = args.steps, args.warmup
     dev = torch.device("cuda", torch.cuda.current_device())
-    context = tuple(int(v) for v in args.context.split(",")) if args.context else None
-    cfg, ctx, tables, nb, eng = build_case(wl, Bmax, K + W + (0 if args.no_e2e else K + 2), context=context)
+    context = tuple(int(v) for v in args.context.split(",")) if (args.context and head) else None
+    e2e_on = head and not args.no_e2e
+    cfg, ctx, tables, nb, eng = build_case(wl, Bmax, K + W + (K + 2 if e2e_on else 0), context=context)
     mbs = tables.shape[1]
-    ladder = [int(x) for x in args.ladder.split(",")] if args.ladder else list(wl.ladder)
+    ladder = [int(x) for x in args.ladder.split(",")] if (args.ladder and head) else list(wl.ladder)
     if Bmax > max(ladder):
         ladder = sorted(set(ladder) | {Bmax})
     eng.capture(ladder=ladder, max_blocks_per_seq=mbs)
-    runs = [timed_steps(eng, cfg, ctx, tables, B, K, W, dev, world, clocks_on=(i == 0))
+    runs = [timed_steps(eng, cfg, ctx, tables, B, K, W, dev, world, clocks_on=(head and i == 0))
             for i, B in enumerate(batches)]
-    # launch-tax ablation ("CUDA graphs & kernel fusion", "Direct answer":
-    # T_eager ~ T_compute + N tau, T_graph ~ T_compute + tau): the same step,
-    # same kernels, launched one by one from the host
-    eng.set_eager(True)
-    eager = timed_steps(eng, cfg, ctx, tables, batches[0], K, W, dev, world, clocks_on=False)
-    eng.set_eager(False)
-    # dominant kernel of the batch-1 step: the fused gate/up + SwiGLU GEMV
-    # (largest matrix of the layer), timed on its own stream over all layers'
-    # matrices (each larger than L2)
-    kern = None if args.no_kernel_timing else time_gemv_swiglu(cfg, wl, batches[0], dev)
+    eager = None
+    if head:
+        # launch-tax ablation ("CUDA graphs & kernel fusion", "Direct answer":
+        # T_eager ~ T_compute + N tau, T_graph ~ T_compute + tau): the same
+        # step, same kernels, launched one by one from the host
+        eng.set_eager(True)
+        eager = timed_steps(eng, cfg, ctx, tables, batches[0], K, W, dev, world, clocks_on=False)
+        eng.set_eager(False)
     B0 = batches[0]
-    bt0 = torch.tensor(tables[:B0], device=dev)
-    e2e = None if args.no_e2e else time_e2e(eng, cfg, ctx[:B0] + W + K, bt0, B0, K, dev, tables[:B0])
+    e2e = None
+    if e2e_on:
+        bt0 = torch.tensor(tables[:B0], device=dev)
+        e2e = time_e2e(eng, cfg, ctx[:B0] + W + K, bt0, B0, K, dev, tables[:B0])
+    pf = None
+    if head and not args.no_prefill:
+        pf = [time_prefill(eng, cfg, n, nb, dev) for n in (512, 2048) if -(-n // 16) <= nb]
     eng.close()
-    return dict(cfg=cfg, K=K, W=W, runs=runs, kern=kern, e2e=e2e, ctx=ctx, wl=wl, eager=eager)
+    del eng
+    torch.cuda.empty_cache()
+    kern = kern_tc = None
+    if not args.no_kernel_timing:
+        kern = time_gemv_norm_swiglu(cfg, wl, B0, dev)
+        if Bmax >= 16:
+            kern_tc = time_tc_swiglu(cfg, wl, Bmax, dev)
+    return dict(cfg=cfg, K=K, W=W, runs=runs, kern=kern, kern_tc=kern_tc, e2e=e2e, ctx=ctx, wl=wl, eager=eager,
+                prefill=pf)
 
 
 def batch_sweep(args):
@@ -248,14 +280,21 @@ def batch_sweep(args):
     eng.close()
 
 
-def time_gemv_swiglu(cfg, wl, B, dev, reps=3, layers=None):
-    """Average duration of the gate/up GEMV (SwiGLU epilogue) on its own stream
-    with CUDA events, cycling through every layer's matrix."""
+def _gate_up_mats(cfg, wl, dev, layers):
+    """Gate/up matrices of a few layers (each larger than L2), enough distinct
+    bytes that back-to-back launches read from HBM."""
     model = SynthModel(cfg, wl.seed + 17, device=dev, cache=False)
-    nl = min(cfg.n_layers, max(2, int(24e9 // (2 * cfg.ffn * cfg.hidden * (1 if cfg.weight_dtype == "fp8" else 2)))))
+    w = 1 if cfg.weight_dtype == "fp8" else 2
+    nl = min(cfg.n_layers, max(2, int(24e9 // (2 * cfg.ffn * cfg.hidden * w))))
     if layers:
         nl = min(nl, layers)
-    mats = [model.get("w_gu", l) for l in range(nl)]
+    return [model.get("w_gu", l) for l in range(nl)]
+
+
+def time_gemv_swiglu(cfg, wl, B, dev, reps=3, layers=None):
+    """Average duration of the gate/up GEMV (SwiGLU epilogue, x given) on its
+    own stream with CUDA events, cycling through several layers' matrices."""
+    mats = _gate_up_mats(cfg, wl, dev, layers)
     x = torch.randn((B, cfg.hidden), device=dev)
     act = torch.empty((B, cfg.ffn), device=dev)
     wdt = capi.DTYPE_E4M3 if cfg.weight_dtype == "fp8" else capi.DTYPE_BF16
@@ -287,11 +326,58 @@ def time_gemv_swiglu(cfg, wl, B, dev, reps=3, layers=None):
     return {"ms": ms, "bytes": nbytes, "launches": n}
 
 
+def time_gemv_norm_swiglu(cfg, wl, B, dev, reps=3, layers=None):
+    """The step's dominant batch-1 kernel as the step launches it: the gate/up
+    projection with the residual add + RMSNorm prologue (residual and two split
+    partials in, new residual out) and the SwiGLU epilogue, CUDA events on its
+    own stream over several layers' matrices. Algorithmic bytes per launch:
+    weights (+ FP8 scales) + gain + residual and partials read + residual
+    written + activation written."""
+    mats = _gate_up_mats(cfg, wl, dev, layers)
+    H, F = cfg.hidden, cfg.ffn
+    r = torch.randn((B, H), device=dev)
+    delta = torch.randn((2, B, H), device=dev) * 0.1
+    r_out = torch.empty_like(r)
+    gamma = (1.0 + 0.1 * torch.randn(H, device=dev)).to(torch.bfloat16)
+    act = torch.empty((B, F), device=dev)
+    wdt = capi.DTYPE_E4M3 if cfg.weight_dtype == "fp8" else capi.DTYPE_BF16
+    sched = torch.zeros(max(1, capi.op_gemv_norm_sched_ints(capi.EPI_SWIGLU, wdt, B, F, H)),
+                        dtype=torch.int32, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def launch(m):
+        capi.op_gemv_norm(capi.EPI_SWIGLU, wdt, m["w"], m.get("s"), F, H, r, delta, gamma, cfg.eps, r_out,
+                          sched=sched, act=act, stream=s)
+
+    with torch.cuda.stream(s):
+        for m in mats[:2]:
+            launch(m)
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        n = 0
+        for _ in range(reps):
+            for m in mats:
+                launch(m)
+                n += 1
+        e1.record(s)
+        s.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    w = 1 if cfg.weight_dtype == "fp8" else 2
+    nbytes = 2 * F * H * w + (2 * F * 4 if cfg.weight_dtype == "fp8" else 0) + H * 2 \
+        + 3 * B * H * 4 + B * H * 4 + B * F * 4
+    del mats
+    torch.cuda.empty_cache()
+    return {"ms": ms, "bytes": nbytes, "launches": n}
+
+
 def time_tc_swiglu(cfg, wl, B, dev, reps=3, layers=4):
     """Average duration of the tensor-core gate/up projection with the SwiGLU
-    epilogue (the e4m3 widening kernel for FP8 weights) at batch B over a few
-    layers' matrices, CUDA events on its stream. Includes the entry point's
-    fp32 -> high/low row split and act readback kernels (small next to it)."""
+    epilogue (the e4m3 kernel for FP8 weights) at batch B over a few layers'
+    matrices. The entry-point calls are captured once in a CUDA graph and the
+    graph is replayed between CUDA events, so host-side work per call (tensor
+    map encoding, argument marshalling) is not in the time; the entry point's
+    fp32 -> high/low row split and act read-back kernels are (a few us)."""
     model = SynthModel(cfg, wl.seed + 17, device=dev, cache=False)
     mats = [model.get("w_gu", l) for l in range(min(cfg.n_layers, layers))]
     x = torch.randn((B, cfg.hidden), device=dev)
@@ -303,22 +389,26 @@ def time_tc_swiglu(cfg, wl, B, dev, reps=3, layers=4):
         for m in mats[:2]:
             fn(capi.EPI_SWIGLU, m["w"], m.get("s"), cfg.ffn, cfg.hidden, x, B, act=act, stream=s)
         s.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        n = 0
-        for _ in range(reps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
             for m in mats:
                 fn(capi.EPI_SWIGLU, m["w"], m.get("s"), cfg.ffn, cfg.hidden, x, B, act=act, stream=s)
-                n += 1
+        g.replay()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(reps):
+            g.replay()
         e1.record(s)
         s.synchronize()
+    n = reps * len(mats)
     ms = e0.elapsed_time(e1) / n
     w = 1 if fp8 else 2
     nbytes = 2 * cfg.ffn * cfg.hidden * w + (2 * cfg.ffn * 4 if fp8 else 0) + B * cfg.hidden * 4 + B * cfg.ffn * 4
     flops = 2 * B * 2 * cfg.ffn * cfg.hidden
-    del mats
+    del g, mats
     torch.cuda.empty_cache()
-    return {"ms": ms, "bytes": nbytes, "flops": flops, "launches": n}
+    return {"ms": ms, "bytes": nbytes, "flops": flops, "launches": n, "B": B}
 
 
 def time_attention(wl, B, dev, reps=10):
@@ -351,6 +441,34 @@ def time_attention(wl, B, dev, reps=10):
     k = 1 if cfg.kv_dtype == "fp8" else 2
     nbytes = int(sum(int(c) for c in ctx)) * 2 * cfg.n_kv_heads * cfg.head_dim * k
     return {"ms": e0.elapsed_time(e1) / reps, "bytes": nbytes, "launches": reps}
+
+
+def time_prefill(eng, cfg, n, nb, dev, reps=3):
+    """Time to first token for an n-token prompt ("Kernel Fusion for
+    Large-Scale LLM Inference", section 12: TTFT): one prefill call from
+    position 0 over the first ceil(n / 16) blocks of the pool (their random
+    contents are overwritten), CUDA events on the current stream, the best of
+    `reps` after one warm-up. FLOPs: 2 x matmul params x n (the LM head once)
+    + the causal attention products."""
+    S = torch.cuda.current_stream()
+    toks = torch.randint(0, cfg.vocab, (n,), dtype=torch.int32, device=dev)
+    table = torch.arange(-(-n // 16), dtype=torch.int32, device=dev)
+    nid = torch.zeros(1, dtype=torch.int32, device=dev)
+    eng.prefill(toks, 0, table, nid)
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(S)
+        eng.prefill(toks, 0, table, nid)
+        e1.record(S)
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    per_tok = ledger.matmul_params(cfg) - cfg.vocab * cfg.hidden
+    flops = 2 * per_tok * n + 2 * cfg.vocab * cfg.hidden + \
+        2 * 2 * cfg.n_layers * cfg.n_q_heads * cfg.head_dim * (n * (n + 1) // 2)
+    return {"tokens": n, "ttft_ms": round(best, 3), "tokens_per_s": round(n / (best / 1e3), 1),
+            "flops": int(flops), "achieved_tflops": round(flops / (best / 1e3) / 1e12, 1)}
 
 
 def time_e2e(eng, cfg, ctx0, bt, B, K, dev, tables):
@@ -474,9 +592,12 @@ def main():
             k = time_tc_swiglu(wl.model, wl, args.batch or 64, dev)
             B = args.batch or 64
             name = "tensor-core gate/up with SwiGLU epilogue (" + wl.model.weight_dtype + " weights)"
-        else:
+        elif args.kernel_only == "gemv":
             k = time_gemv_swiglu(wl.model, wl, B, dev, reps=1, layers=4)
             name = "gate/up GEMV with SwiGLU epilogue"
+        else:
+            k = time_gemv_norm_swiglu(wl.model, wl, B, dev, reps=1, layers=4)
+            name = "gate/up GEMV with the norm prologue and SwiGLU epilogue"
         gbs = k["bytes"] / (k["ms"] / 1e3) / 1e9
         line = {"kernel": name, "workload": wl.key, "batch": B, "launches": k["launches"],
                 "avg_ms": round(k["ms"], 5), "bytes": k["bytes"], "achieved_gbs": round(gbs, 1),
@@ -488,11 +609,17 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     capi.load()
-    r = time_native(args, rank, world)
-    cfg, K = r["cfg"], r["K"]
     peak, src = peaks()
-    kern = r["kern"] or {"bytes": 0, "ms": float("nan"), "launches": 0}
-    k_gbs = kern["bytes"] / (kern["ms"] / 1e3) / 1e9
+    wl = WORKLOADS[args.workload]
+    batches = [args.batch] if args.batch else [b for b in wl.batches if b in (1, 64)] or [wl.batches[0]]
+    r = measure_workload(wl, batches, args, world, head=True)
+    extra = []
+    if not args.batch and args.also:
+        for key in [k for k in args.also.split(",") if k and k != wl.key]:
+            wx = WORKLOADS[key]
+            bx = sorted({wx.batches[0], max(wx.batches)})
+            extra.append(measure_workload(wx, bx, args, world, head=False))
+    cfg, K = r["cfg"], r["K"]
 
     def summary(run):
         step_ms = run["total_ms"] / K
@@ -506,10 +633,36 @@ def main():
                                   "frac_of_peak": round(gbs / peak, 4), "frac_of_8tbs": round(gbs / 8000, 4)},
                 "kernels_per_step": run["kernels_per_step"], "graph": run["uses_graph"]}
 
+    def roofline(res, B):
+        k = res["kern"]
+        if not k:
+            return None
+        gbs = k["bytes"] / (k["ms"] / 1e3) / 1e9
+        wt = res["cfg"].weight_dtype
+        return {"kernel": "gemv_kernel<NB=1,%s,EPI_SWIGLU,PRO_NORM> (residual add + RMSNorm prologue, fused "
+                          "gate/up, SiLU x mul epilogue; as the step launches it)" % ("W_E4M3" if wt == "fp8" else "W_BF16"),
+                "workload": res["wl"].key, "batch": B,
+                "bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "peak_source": src,
+                "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": DRAM_TRAFFIC.get((res["wl"].key, B)),
+                "algorithmic_bytes_per_launch": k["bytes"], "avg_launch_ms": round(k["ms"], 5),
+                "launches_timed": k["launches"]}
+
+    def roofline_tc(res):
+        k = res["kern_tc"]
+        if not k:
+            return None
+        gbs = k["bytes"] / (k["ms"] / 1e3) / 1e9
+        f8 = res["cfg"].weight_dtype == "fp8"
+        return {"kernel": ("tc_gemm_f8_kernel" if f8 else "tc_gemm_kernel") + "<EPI_SWIGLU> (tcgen05 gate/up at "
+                          "batch %d)" % k["B"], "bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(gbs / peak, 4),
+                "achieved_tflops": round(k["flops"] / (k["ms"] / 1e3) / 1e12, 1),
+                "algorithmic_bytes_per_launch": k["bytes"], "avg_launch_ms": round(k["ms"], 5)}
+
     head = summary(r["runs"][0])
     B = head["batch"]
     line = {
-        "metric": "decode tokens/s (batch %d; batch 64 in 'batch64'); achieved HBM GB/s as %% of GB300 peak" % B,
+        "metric": METRIC,
         "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": r["W"],
         "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if cfg.weight_dtype == "bf16" else "fp8-e4m3 weights, fp32 math",
@@ -521,20 +674,35 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "latency_ms": head["latency_ms"],
         "step_roofline": head["step_roofline"],
-        "roofline": {"kernel": "gemv_kernel<NB,WT,EPI_SWIGLU,PRO_X> (fused gate/up + SiLU x mul; the step runs the same loop with the norm prologue)",
-                     "bound": "hbm", "achieved": round(k_gbs, 1), "peak": peak, "peak_source": src,
-                     "unit": "GB/s", "frac": round(k_gbs / peak, 4), "traffic": GEMV_TRAFFIC_BYTES,
-                     "algorithmic_bytes_per_launch": kern["bytes"], "avg_launch_ms": round(kern["ms"], 5)},
-        "gpu_launches": int(sum(run["kernels_per_step"] * K for run in r["runs"])),
+        "roofline": roofline(r, B),
         "kernels_per_step": head["kernels_per_step"],
     }
     for run in r["runs"][1:]:
         line["batch%d" % run["B"]] = summary(run)
+        if run["B"] == max(batches) and roofline_tc(r):
+            line["batch%d" % run["B"]]["roofline_tc"] = roofline_tc(r)
+    for x in extra:
+        obj = {"workload": f"{x['wl'].key}: {x['wl'].description}", "model": x["cfg"].name}
+        for run in x["runs"]:
+            obj["batch%d" % run["B"]] = summary(run)
+        obj["roofline"] = roofline(x, x["runs"][0]["B"])
+        if roofline_tc(x):
+            obj["roofline_tc"] = roofline_tc(x)
+        line[x["wl"].key] = obj
     ge, ee = r["runs"][0]["total_ms"] / K, r["eager"]["total_ms"] / K
     n_k = r["eager"]["kernels_per_step"]
     line["launch_tax"] = {"batch": head["batch"], "graph_ms": round(ge, 4), "eager_ms": round(ee, 4),
                           "eager_kernels_per_step": n_k, "tau_us": round((ee - ge) / max(n_k - 1, 1) * 1e3, 3),
                           "speedup": round(ee / ge, 4)}
+    # kernels of this library launched inside the timed regions (graph replays:
+    # the graph's kernel nodes plus the staging kernel per step)
+    line["gpu_launches"] = int(sum(run["kernels_per_step"] * K for x in [r] + extra for run in x["runs"]))
+    if r["prefill"]:
+        tfl, tsrc = tensor_peak()
+        line["prefill"] = {"what": "time to first token: one prompt through prefill() (tensor-core passes of "
+                                   "128 tokens, BF16 high/low activations), best of 3",
+                           "runs": r["prefill"], "peak_tflops": tfl, "peak_source": tsrc,
+                           "frac_of_peak": [round(x["achieved_tflops"] / tfl, 4) for x in r["prefill"]]}
     if r["runs"][0]["clocks"]:
         line["clocks"] = r["runs"][0]["clocks"]
     if r["e2e"]:
@@ -593,7 +761,7 @@ def main_reference(args):
     v = float(np.mean(vals))
     threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
     cores = int(threads) if threads else (os.cpu_count() or 1)
-    line = {"impl": "reference", "metric": "decode tokens/s (batch %d); achieved HBM GB/s as %% of GB300 peak" % B,
+    line = {"impl": "reference", "metric": METRIC,
             "value": round(v, 6), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(wall / max(args.steps, 1) * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",

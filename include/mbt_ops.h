@@ -76,6 +76,25 @@ int op_gemv_ex(int epi, int w_dtype, const void* W, const float* scales, int N, 
                float* logits, int32_t* next_ids, int* nsplit_used, int* sched_ints, uint32_t* err,
                void* stream);
 
+/* op_gemv_norm_sched_ints: ints of work-queue counters op_gemv_norm may use. */
+int op_gemv_norm_sched_ints(int epi, int w_dtype, int B, int N, int K);
+
+/* op_gemv_norm: the projection as the decode step launches it at batch 1..15,
+ * with the residual add + RMSNorm as its prologue ("Kernels, Fusion & CUDA
+ * Graphs", "Fix 1: kernel fusion": residual add + RMSNorm in one pass, fused
+ * here into the projection that consumes it): every CTA forms
+ * x[b] = rmsnorm(r_in[b] + sum_s delta[s][b]) * gamma into its own tile and
+ * the call stores the new residual r_in[b] + sum_s delta[s][b] to r_out[b].
+ * r_in, r_out [B][K] fp32 (distinct buffers); delta [n_delta][B][K] fp32 or
+ * NULL with n_delta = 0; gamma [K] BF16; eps inside the square root. No K
+ * split: PARTIAL writes out [1][B][N]. Other arguments as op_gemv_ex
+ * (sched_ints from op_gemv_norm_sched_ints, or NULL). Launch geometry and
+ * shared-memory carveout are those of an 8B-class model's step. */
+int op_gemv_norm(int epi, int w_dtype, const void* W, const float* scales, int N, int K,
+                 const float* r_in, const float* delta, int n_delta, const uint16_t* gamma, float eps,
+                 float* r_out, int B, float* out, float* act, float* logits, int32_t* next_ids,
+                 int* sched_ints, uint32_t* err, void* stream);
+
 /* op_gemm_tc: the tensor-core (tcgen05) projection the decode step uses at
  * batch 16..128 with BF16 weights: W [rows][K] BF16 (K a multiple of 16,
  * >= 64), x [B][K] fp32 with 1 <= B <= 128, split internally into BF16

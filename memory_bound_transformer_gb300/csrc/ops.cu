@@ -64,12 +64,19 @@ int op_gemv_sched_ints(int epi, int w_dtype, int B, int N, int K) {
   return ((B + step - 1) / step) * g.nsplit;
 }
 
-int op_gemv_ex(int epi, int w_dtype, const void* W, const float* scales, int N, int K,
-               const float* x, int B, int force_nsplit, float* out, float* act,
-               float* logits, int32_t* next_ids, int* nsplit_used, int* sched_ints, uint32_t* err,
-               void* stream) {
+}  // extern "C"
+
+namespace {
+// The step's residual-add + RMSNorm prologue inputs (null: x is given).
+struct NormOp { const float* r_in; const float* delta; int n_delta; const uint16_t* gamma; float eps; float* r_out; };
+
+int gemv_impl(int epi, int w_dtype, const void* W, const float* scales, int N, int K, const float* x,
+              const NormOp* nin, int B, int force_nsplit, float* out, float* act, float* logits,
+              int32_t* next_ids, int* nsplit_used, int* sched_ints, uint32_t* err, void* stream) {
   if (epi < 0 || epi > 2 || (w_dtype != MBT_DTYPE_BF16 && w_dtype != MBT_DTYPE_E4M3)) return MBT_ERR_BAD_ARG;
-  if (!W || !x || B < 1 || N < 1 || K < 16 || K % 16) return MBT_ERR_BAD_ARG;
+  if (!W || (!x && !nin) || B < 1 || N < 1 || K < 16 || K % 16) return MBT_ERR_BAD_ARG;
+  if (nin && (!nin->r_in || !nin->gamma || !nin->r_out || nin->n_delta < 0 || (nin->n_delta && !nin->delta)))
+    return MBT_ERR_BAD_ARG;
   if (w_dtype == MBT_DTYPE_E4M3 && !scales) return MBT_ERR_BAD_ARG;
   if ((epi == EPI_PARTIAL && !out) || (epi == EPI_SWIGLU && !act) || (epi == EPI_ARGMAX && !next_ids))
     return MBT_ERR_BAD_ARG;
@@ -77,15 +84,16 @@ int op_gemv_ex(int epi, int w_dtype, const void* W, const float* scales, int N, 
   if (rc != MBT_OK) return rc;
   const int nsm = sm_count();
   const int wt = w_dtype == MBT_DTYPE_E4M3 ? W_E4M3 : W_BF16;
+  const int pro = nin ? PRO_NORM : PRO_X;
   cudaStream_t s = (cudaStream_t)stream;
-  const GemvLaunch g0 = gemv_plan(epi, wt, std::min(B, gemv_max_rows(epi, K)), N, K, nsm,
-                                  epi == EPI_PARTIAL ? force_nsplit : 0);
+  const int step = gemv_max_rows(epi, K, pro);
+  const GemvLaunch g0 = gemv_plan(epi, wt, std::min(B, step), N, K, nsm,
+                                  epi == EPI_PARTIAL ? force_nsplit : 0, pro);
   if (nsplit_used) *nsplit_used = g0.nsplit;
   ArgmaxPart* part = nullptr;
   if (epi == EPI_ARGMAX &&
       cudaMallocAsync((void**)&part, (size_t)g0.grid * B * sizeof(ArgmaxPart), s) != cudaSuccess)
     return MBT_ERR_OOM;
-  const int step = gemv_max_rows(epi, K);
   // work-queue counters, one per launch and K split, zero at launch (the
   // kernel leaves them at zero): the caller's, or allocated and zeroed here
   const int nlaunch = (B + step - 1) / step;
@@ -102,11 +110,18 @@ int op_gemv_ex(int epi, int w_dtype, const void* W, const float* scales, int N, 
   }
   for (int b0 = 0; b0 < B && rc == MBT_OK; b0 += step) {
     const int nb = std::min(step, B - b0);
-    GemvLaunch g = gemv_plan(epi, wt, nb, N, K, nsm, epi == EPI_PARTIAL ? g0.nsplit : 0);
+    GemvLaunch g = gemv_plan(epi, wt, nb, N, K, nsm, epi == EPI_PARTIAL ? g0.nsplit : 0, pro);
     if (epi == EPI_ARGMAX) g.grid = g0.grid;
     GemvArgs a = {};
     a.W = W; a.scale = scales; a.wtype = wt; a.N = N; a.K = K;
-    a.x = x + (size_t)b0 * K; a.ldx = K; a.nb = nb;
+    a.x = x ? x + (size_t)b0 * K : nullptr; a.ldx = K; a.nb = nb;
+    if (nin) {
+      a.r_in = nin->r_in + (size_t)b0 * K;
+      a.delta = nin->delta ? nin->delta + (size_t)b0 * K : nullptr;
+      a.n_delta = nin->n_delta; a.delta_stride = (long long)B * K;
+      a.gamma = (const bf16*)nin->gamma; a.eps = nin->eps;
+      a.r_out = nin->r_out + (size_t)b0 * K;
+    }
     a.out = out ? out + (size_t)b0 * N : nullptr; a.split_stride = (long long)B * N; a.ldo = N;
     a.act = act ? act + (size_t)b0 * N : nullptr; a.lda = N;
     a.logits = logits ? logits + (size_t)b0 * N : nullptr; a.ldl = N;
@@ -117,7 +132,7 @@ int op_gemv_ex(int epi, int w_dtype, const void* W, const float* scales, int N, 
       a.sched = sched + (size_t)(b0 / step) * g0.nsplit;
       a.static_groups = sg;
     }
-    if (gemv_launch(epi, PRO_X, a, g, s) != cudaSuccess) rc = MBT_ERR_CUDA;
+    if (gemv_launch(epi, pro, a, g, s) != cudaSuccess) rc = MBT_ERR_CUDA;
   }
   if (rc == MBT_OK && epi == EPI_ARGMAX &&
       launch_argmax_reduce(B, part, B, g0.grid, next_ids, err, s) != cudaSuccess)
@@ -125,6 +140,35 @@ int op_gemv_ex(int epi, int w_dtype, const void* W, const float* scales, int N, 
   if (part) cudaFreeAsync(part, s);
   if (own) cudaFreeAsync(sched, s);
   return rc;
+}
+}  // namespace
+
+extern "C" {
+
+int op_gemv_ex(int epi, int w_dtype, const void* W, const float* scales, int N, int K,
+               const float* x, int B, int force_nsplit, float* out, float* act,
+               float* logits, int32_t* next_ids, int* nsplit_used, int* sched_ints, uint32_t* err,
+               void* stream) {
+  return gemv_impl(epi, w_dtype, W, scales, N, K, x, nullptr, B, force_nsplit, out, act, logits, next_ids,
+                   nsplit_used, sched_ints, err, stream);
+}
+
+int op_gemv_norm_sched_ints(int epi, int w_dtype, int B, int N, int K) {
+  const int n = sm_count();
+  if (n <= 0 || B < 1 || N < 1 || K < 16) return 0;
+  const int step = gemv_max_rows(epi, K, PRO_NORM);
+  const GemvLaunch g = gemv_plan(epi, w_dtype == MBT_DTYPE_E4M3 ? W_E4M3 : W_BF16, std::min(B, step), N, K, n, 0,
+                                 PRO_NORM);
+  return ((B + step - 1) / step) * g.nsplit;
+}
+
+int op_gemv_norm(int epi, int w_dtype, const void* W, const float* scales, int N, int K,
+                 const float* r_in, const float* delta, int n_delta, const uint16_t* gamma, float eps,
+                 float* r_out, int B, float* out, float* act, float* logits, int32_t* next_ids,
+                 int* sched_ints, uint32_t* err, void* stream) {
+  const NormOp nin{r_in, delta, n_delta, gamma, eps, r_out};
+  return gemv_impl(epi, w_dtype, W, scales, N, K, nullptr, &nin, B, 0, out, act, logits, next_ids, nullptr,
+                   sched_ints, err, stream);
 }
 
 namespace {

@@ -101,6 +101,46 @@ def test_gemv_swiglu(cuda_lib, wt, B):
 
 
 @pytest.mark.parametrize("wt", ["bf16", "fp8"])
+@pytest.mark.parametrize("B", [1, 3, 4, 9])
+@pytest.mark.parametrize("epi", ["partial", "swiglu"])
+def test_gemv_norm_prologue(cuda_lib, wt, B, epi):
+    """The projection with the step's residual add + RMSNorm prologue: x =
+    rmsnorm(r + d0 + d1) * gamma formed per CTA, the new residual stored."""
+    K = 1040
+    N = 1000 if epi == "partial" else 344
+    rows = N if epi == "partial" else 2 * N
+    t, raw = _weights(wt, rows, K, seed=5 + B)
+    r = _f32_rand((B, K), seed=40 + B, scale=2.0).to(DEV)
+    delta = _f32_rand((2, B, K), seed=50 + B, scale=0.5).to(DEV)
+    gamma = (1.0 + 0.1 * _f32_rand((K,), seed=60)).to(torch.bfloat16).to(DEV)
+    r_out = torch.full((B, K), float("nan"), device=DEV)
+    out = torch.full((1, B, N), float("nan"), device=DEV)
+    act = torch.full((B, N), float("nan"), device=DEV)
+    e = capi.EPI_PARTIAL if epi == "partial" else capi.EPI_SWIGLU
+    capi.op_gemv_norm(e, _dtype(wt), t["w"], t.get("s"), N, K, r, delta, gamma, 1e-6, r_out,
+                      out=out if epi == "partial" else None, act=act if epi == "swiglu" else None)
+    torch.cuda.synchronize()
+    rsum = r.double() + delta.double()[0] + delta.double()[1]
+    # the residual: fp32 sums in the fixed order (r + d0) + d1, bit for bit
+    r32, d32 = r.cpu().numpy(), delta.cpu().numpy()
+    assert np.array_equal(r_out.cpu().numpy(), (r32 + d32[0]) + d32[1])
+    xv = rmsnorm(rsum.cpu().numpy(), bf16_decode(_np_bits(gamma)), 1e-6)
+    W = decode_weight(raw)
+    ref = xv @ W.T
+    # norm in fp32 (relative 1e-5 of each x element) then the fp32 dot product
+    bound = (TOL_REL + 1e-5) * (np.abs(xv) @ np.abs(W).T) + TOL_ABS
+    if epi == "partial":
+        got = out[0].double().cpu().numpy()
+        assert np.all(np.abs(got - ref) <= bound)
+    else:
+        g, u = ref[:, :N], ref[:, N:]
+        want = silu(g) * u
+        got = act.double().cpu().numpy()
+        tol = 1e-6 * np.abs(want) + 1.1 * np.abs(u) * bound[:, :N] + np.abs(silu(g)) * bound[:, N:] + 1e-30
+        assert np.all(np.abs(got - want) <= tol)
+
+
+@pytest.mark.parametrize("wt", ["bf16", "fp8"])
 @pytest.mark.parametrize("B", [1, 5, 8, 9])
 def test_gemv_argmax(cuda_lib, wt, B):
     V, K = 3001, 512
@@ -320,7 +360,7 @@ def test_rope_kv_write_range_errors(cuda_lib):
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 @pytest.mark.parametrize("nq,nkv,d", [(4, 4, 64), (4, 2, 64), (32, 8, 128), (10, 2, 64), (64, 8, 128),
-                                      (16, 1, 128)])
+                                      (16, 1, 128), (40, 8, 128)])
 @pytest.mark.parametrize("lens", [[1], [15, 16, 17], [128, 1, 33, 64, 65], [1000], [2049, 7]])
 def test_paged_attention(cuda_lib, kv, nq, nkv, d, lens):
     B = len(lens)

@@ -10,6 +10,8 @@ that nothing left in the shared array from one call leaks into the next.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it also passes alone in a fresh process."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -61,6 +63,57 @@ def test_noalloc_matches_allocating_entry_point(cuda_lib):
         # (2e-5 of max |V|; |V| < 5 for these N(0,1) caches times 1.25)
         assert torch.isfinite(got).all()
         assert torch.max(torch.abs(got - ref)).item() <= 2e-5 * 5.0 * 1.25
+
+
+class _DefaultPool:
+    """The device's default stream-ordered memory pool, read through the CUDA
+    runtime the library itself links (cudaMallocAsync draws from it)."""
+    USED_CURRENT, USED_HIGH = 7, 8          # cudaMemPoolAttrUsedMemCurrent / UsedMemHigh
+
+    def __init__(self):
+        self.rt = ctypes.CDLL("libcudart.so.13")
+        self.pool = ctypes.c_void_p()
+        assert self.rt.cudaDeviceGetDefaultMemPool(ctypes.byref(self.pool), torch.cuda.current_device()) == 0
+
+    def get(self, attr):
+        v = ctypes.c_uint64()
+        assert self.rt.cudaMemPoolGetAttribute(self.pool, attr, ctypes.byref(v)) == 0
+        return v.value
+
+    def reset_high(self):
+        zero = ctypes.c_uint64(0)                   # resets the high-water mark to the current use
+        assert self.rt.cudaMemPoolSetAttribute(self.pool, self.USED_HIGH, ctypes.byref(zero)) == 0
+
+
+def _raw_call(fn, c, out, err):
+    return fn(c["q"], c["nkv"], c["k"], c["v"], c["dt"], 0.75, 1.25, c["bt"], c["sl"], c["nb"], out, err)
+
+
+def test_noalloc_allocates_nothing(cuda_lib):
+    """After a first (set-up) call, a call reserves no device memory: the
+    default pool's high-water mark and the device's free memory are unchanged
+    across it. The allocating entry point, measured the same way, does move
+    the high-water mark (so the probe sees stream-ordered allocations)."""
+    c = _case(64, 8, 128, "bf16", [2049, 65, 300], seed=5)
+    out = torch.zeros((3, 64 * 128), device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    assert _raw_call(capi.op_paged_attention_noalloc, c, out, err) == 0     # set-up and module load
+    torch.cuda.synchronize()
+    pool = _DefaultPool()
+    for _ in range(2):
+        free0 = torch.cuda.mem_get_info()[0]
+        pool.reset_high()
+        used0 = pool.get(pool.USED_CURRENT)
+        assert _raw_call(capi.op_paged_attention_noalloc, c, out, err) == 0
+        torch.cuda.synchronize()
+        assert pool.get(pool.USED_HIGH) == used0
+        assert torch.cuda.mem_get_info()[0] == free0
+    assert err.item() == 0
+    pool.reset_high()
+    used0 = pool.get(pool.USED_CURRENT)
+    _raw_call(capi.op_paged_attention, c, out, err)
+    torch.cuda.synchronize()
+    assert pool.get(pool.USED_HIGH) > used0
 
 
 def test_noalloc_rejects_oversized_requests(cuda_lib):
