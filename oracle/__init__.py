@@ -32,7 +32,7 @@ pins live in tests/test_oracle_*.py):
 
 * sampling.philox4x32_10: the generator's published known-answer vectors
   (tests/golden/philox4x32_10_kat.json); sampling.uniforms: values strictly
-  inside (0, 1) on the 2^-24 grid, moments and a chi-square test of
+  inside (0, 1) on the 2^-23 grid, moments and a chi-square test of
   uniformity; sampling.sample: Gumbel-max frequencies against softmax
   probabilities (chi-square), arg-max at top_k = 1, at a vanishing temperature
   and at a tiny top_p, draws inside the top-k set; sampling.keep_set: the

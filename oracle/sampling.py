@@ -22,9 +22,10 @@ the readings taken here (each listed in the design notes):
   exp(z_j), so no normaliser and no sort are needed);
 * u_i comes from the counter-based generator Philox4x32-10 (Salmon, Moraes,
   Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011) with
-  key (seed mod 2^32, seed div 2^32) and counter (token id, row, step, 0):
-  the first output word x gives u = (floor(x / 256) + 1/2) / 2^24, a value
-  that float32 and float64 both hold exactly.
+  key (seed mod 2^32, seed div 2^32) and counter (token id, row, step mod
+  2^32, step div 2^32): the first output word x gives
+  u = (floor(x / 512) + 1/2) / 2^23, a value with 24 significant bits that
+  float32 and float64 both hold exactly.
 """
 from __future__ import annotations
 
@@ -62,9 +63,10 @@ def uniforms(seed: int, row: int, step: int, ids) -> np.ndarray:
     """u for the given token ids of one (row, step): float64 values in (0, 1)."""
     ids = np.asarray(ids, dtype=np.uint64)
     zero = np.zeros_like(ids)
-    x0, _, _, _ = philox4x32_10((ids, zero + np.uint64(row), zero + np.uint64(step), zero),
+    x0, _, _, _ = philox4x32_10((ids, zero + np.uint64(row), zero + np.uint64(step & _MASK),
+                                 zero + np.uint64((step >> 32) & _MASK)),
                                 (zero + np.uint64(seed & _MASK), zero + np.uint64((seed >> 32) & _MASK)))
-    return ((x0 >> np.uint64(8)).astype(np.float64) + 0.5) / 2.0 ** 24
+    return ((x0 >> np.uint64(9)).astype(np.float64) + 0.5) / 2.0 ** 23
 
 
 def gumbel(u: np.ndarray) -> np.ndarray:
