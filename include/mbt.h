@@ -200,6 +200,38 @@ int decode_step(mbt_model* m, mbt_kv* kv, int B, const int32_t* token_ids,
                 const int32_t* seq_lens, int32_t* next_ids, float* logits_or_null,
                 void* stream);
 
+/* Sampling parameters of decode_step_sample (host struct). */
+#define MBT_TOPK_MAX 1024
+typedef struct mbt_sampling {
+  float    temperature;     /* > 0: the logits are divided by it              */
+  int32_t  top_k;           /* 0 = no top-k cut, else 1..MBT_TOPK_MAX         */
+  float    top_p;           /* (0, 1]; 1 = no top-p cut                       */
+  uint32_t reserved;        /* 0                                              */
+  uint64_t seed;            /* generator key                                  */
+  uint64_t step;            /* generator counter word: a new value per step    */
+} mbt_sampling;             /* 32 bytes */
+
+/* decode_step_sample: decode_step with the next token drawn instead of taken
+ * by arg-max ("Kernels, Fusion & CUDA Graphs", "Fix 1: kernel fusion", the
+ * "Sampling" row: softmax, top-k / top-p, sample). Per row b: z = logits / T;
+ * the top_k largest z (a tie at the boundary keeps the lower id); softmax
+ * over them; the shortest prefix in order of decreasing probability whose
+ * probabilities reach top_p; then the Gumbel-max draw over that prefix: the
+ * token with the largest z + g, g = -log(-log(u)), u from Philox4x32-10 with
+ * key (seed mod 2^32, seed div 2^32) and counter (token id, b, step mod 2^32,
+ * step div 2^32), u = (floor(x / 512) + 1/2) / 2^23 of its first word x.
+ * With top_k = 0 and top_p = 1 the draw runs inside the LM head's epilogue
+ * and the logits never leave the chip; otherwise the LM head writes the
+ * logits once (B x vocab fp32) and a per-row kernel selects, normalises and
+ * draws. top_p < 1 with top_k = 0 applies top-p to the MBT_TOPK_MAX largest
+ * logits. Always runs eagerly (graphs, if any, stay valid). Arguments and
+ * errors as decode_step; MBT_ERR_BAD_ARG also for params out of range.
+ * logits_or_null receives the raw (unscaled) logits. */
+int decode_step_sample(mbt_model* m, mbt_kv* kv, int B, const int32_t* token_ids,
+                       const int32_t* positions, const int32_t* block_tables, int bt_stride,
+                       const int32_t* seq_lens, const mbt_sampling* params, int32_t* next_ids,
+                       float* logits_or_null, void* stream);
+
 /* prefill: ingest the prompt tokens[0..n) of one sequence, at positions
  * start_pos .. start_pos + n - 1, in passes of up to 128 tokens through the
  * whole layer stack ("GPU Inference Internals", "Roofline: Why Decode Is

@@ -95,23 +95,25 @@ int op_gemv_norm(int epi, int w_dtype, const void* W, const float* scales, int N
                  float* r_out, int B, float* out, float* act, float* logits, int32_t* next_ids,
                  int* sched_ints, uint32_t* err, void* stream);
 
-/* op_gemm_tc: the tensor-core (tcgen05) projection the decode step uses at
- * batch 16..128 with BF16 weights: W [rows][K] BF16 (K a multiple of 16,
- * >= 64), x [B][K] fp32 with 1 <= B <= 128, split internally into BF16
- * high/low rows so that the product keeps near-fp32 accuracy. Epilogues as
- * op_gemv: PARTIAL out [ksplit][B][N] (ksplit K-splits), SWIGLU act [B][N]
- * fp32 (W has 2N rows), ARGMAX next_ids [B] (+ logits [B][N] if non-NULL).
- * Returns MBT_ERR_UNSUPPORTED where the tensor-map encoder is unavailable.
- * ("GPU Inference Internals", "Roofline: Why Decode Is Memory-Bound": at batch
- * B the weight-only intensity is 2B / b_w FLOP per byte.) */
+/* op_gemm_tc: the tensor-core (tcgen05) projection the decode step uses from
+ * 2 rows on with BF16 weights: W [rows][K] BF16 (K a multiple of 16, >= 64),
+ * x [B][K] fp32 with 1 <= B <= 128, split internally into BF16 high/low rows
+ * so that the product keeps near-fp32 accuracy; launches of at most 64 rows,
+ * each CTA taking an equal share of the (tile, K) work and the fp32 sums kept
+ * in registers. Epilogues as op_gemv: PARTIAL out [B][N] (complete sums:
+ * `ksplit` is accepted and ignored), SWIGLU act [B][N] fp32 (W has 2N rows),
+ * ARGMAX next_ids [B] (+ logits [B][N] if non-NULL). Returns
+ * MBT_ERR_UNSUPPORTED where the tensor-map encoder is unavailable. ("GPU
+ * Inference Internals", "Roofline: Why Decode Is Memory-Bound": at batch B the
+ * weight-only intensity is 2B / b_w FLOP per byte.) */
 int op_gemm_tc(int epi, const void* W, const float* scales, int N, int K, const float* x, int B,
                int ksplit, float* out, float* act, float* logits, int32_t* next_ids, uint32_t* err,
                void* stream);
 
 /* op_gemm_tc_e4m3: as op_gemm_tc for e4m3 weights W [rows][K] (codes) with
- * fp32 per-row scales (required): the codes are widened to FP16 in shared
- * memory, x is split into FP16 high/low rows, the scale is applied in the
- * epilogue ("Kernel Fusion for Large-Scale LLM Inference", section 11, FP8
+ * fp32 per-row scales (required): the codes are widened to FP16 on the way to
+ * the tensor core, x is split into FP16 high/low rows, the scale is applied in
+ * the epilogue ("Kernel Fusion for Large-Scale LLM Inference", section 11, FP8
  * weights and "Epilogue and dequant fusion"). K a multiple of 16, >= 64;
  * 1 <= B <= 128. */
 int op_gemm_tc_e4m3(int epi, const void* W, const float* scales, int N, int K, const float* x, int B,

@@ -12,7 +12,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmbt.so")
-SOURCES = ["gemv.cu", "misc.cu", "attention.cu", "tc_gemm.cu", "tc_gemm_f8.cu", "runtime.cu", "ops.cu", "ops_noalloc.cu"]
+SOURCES = ["gemv.cu", "misc.cu", "attention.cu", "tc_gemm.cu", "tc_stream.cu", "sampling.cu", "runtime.cu", "ops.cu",
+           "ops_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -40,6 +40,7 @@ SIGNATURES = {
     "model_set_eager": (_I, [_P, _I]),
     "decode_step": (_I, [_P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P]),
     "prefill": (_I, [_P, _P, _I, _P, _I, _P, _I, _P, _P, _P]),
+    "decode_step_sample": (_I, [_P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
     "model_poll_errors": (_I, [_P, _P, ctypes.POINTER(_U)]),
     "model_stats": (_I, [_P, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "status_string": (ctypes.c_char_p, [_I]),
@@ -187,6 +188,35 @@ def decode_step_raw(model: int, kv: int, B: int, tok, pos, bt, bt_stride: int, s
     """Pointer-level call; returns the status code instead of raising."""
     return load().decode_step(model, kv, B, _ptr(tok), _ptr(pos), _ptr(bt), bt_stride, _ptr(sl),
                               _ptr(next_ids), _ptr(logits), _stream(stream))
+
+
+class Sampling(ctypes.Structure):
+    """mbt_sampling (include/mbt.h)."""
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float),
+                ("reserved", ctypes.c_uint32), ("seed", ctypes.c_uint64), ("step", ctypes.c_uint64)]
+
+
+TOPK_MAX = 1024
+
+
+def decode_step_sample(model: int, kv: int, token_ids, positions, block_tables, seq_lens, next_ids,
+                       temperature: float, top_k: int, top_p: float, seed: int, step: int,
+                       logits=None, stream=None) -> None:
+    """decode_step with the next token drawn (temperature, top-k, top-p, seeded)."""
+    _require_cuda(token_ids, positions, block_tables, seq_lens, next_ids, logits)
+    B = token_ids.shape[0]
+    sp = Sampling(float(temperature), int(top_k), float(top_p), 0, int(seed), int(step))
+    _check("decode_step_sample", load().decode_step_sample(
+        model, kv, B, _ptr(token_ids), _ptr(positions), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+        ctypes.byref(sp), _ptr(next_ids), _ptr(logits), _stream(stream)))
+
+
+def decode_step_sample_raw(model: int, kv: int, B: int, tok, pos, bt, bt_stride: int, sl, params, next_ids,
+                           logits=None, stream=None) -> int:
+    """Pointer-level call; returns the status code instead of raising."""
+    return load().decode_step_sample(model, kv, B, _ptr(tok), _ptr(pos), _ptr(bt), bt_stride, _ptr(sl),
+                                     ctypes.byref(params) if params is not None else None, _ptr(next_ids),
+                                     _ptr(logits), _stream(stream))
 
 
 def prefill(model: int, kv: int, tokens: torch.Tensor, start_pos: int, block_table: torch.Tensor,

@@ -23,6 +23,7 @@
 //     LM-head rows so that logits need not reach HBM (same table, "Sampling").
 #include "common.cuh"
 #include "internal.h"
+#include "sampling.cuh"
 
 namespace mbt {
 
@@ -381,7 +382,8 @@ gemv_kernel(const GemvArgs a) {
         for (int i = 0; i < RG; ++i) {
           const int ch = r0 + i;
           if (ch < re) {
-            const float t = fin[i * NB + tid];
+            float t = fin[i * NB + tid];
+            if (a.gum.on && t == t) t = gumbel_score(t, ch, tid, a.gum);
             if (t > best_v) { best_v = t; best_i = ch; }          // rows ascend: first max kept
             else if (!(t == t)) set_err(a.err, MBT_DEV_NONFINITE);
           }

@@ -26,6 +26,14 @@ inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem
 
 struct ArgmaxPart { float v; int i; };
 
+// Sampling draw fused into an arg-max epilogue: when `on`, the arg-max is taken
+// over logit * inv_t + Gumbel(token, row0 + row, step; seed) instead of the
+// logit (sampling.cuh); logits written out stay the raw ones.
+struct GumbelArgs {
+  int on; float inv_t; int row0;
+  uint32_t seed_lo, seed_hi, step_lo, step_hi;
+};
+
 // y = W x for up to 8 batch rows (weight-streaming GEMV, CUDA cores).
 // Shared-memory share of the unified L1 (percent) for every kernel of the
 // CUDA-core (batch 1..15) step. Two things pull on it: the weight stream
@@ -87,6 +95,7 @@ struct GemvArgs {
   // one at a time, from the counter sched[split] (zero at launch; the CTA
   // that makes the last claim sets it back to zero).
   int* sched; int static_groups;
+  GumbelArgs gum;           // EPI_ARGMAX: draw instead of arg-max when gum.on
 };
 
 struct GemvLaunch { int nb_tmpl; int nsplit; int grid; size_t smem; int group_rows; int carveout; };
@@ -112,29 +121,32 @@ cudaError_t gemv_init();   // raise dynamic shared-memory limits (once per proce
 // 128-byte blobs.
 struct TmaMap { alignas(64) unsigned char bytes[128]; };
 struct TcArgs {
-  int N, K, R, Rp;            // output channels (SWIGLU: ffn), K, live rows, padded rows (multiple of 8)
+  int N, K, R, Rp;            // output channels (SWIGLU: ffn), K, live rows of this launch, their padded count
+  int row0, rp_all;           // first row of this launch; padded rows of the whole high/low buffer
+  float* ts_scratch; int* ts_tickets; int tickets_cap;   // stream-K partial sums and per-tile tickets (zero)
   const float* scale;         // per-row weight scale or null
   float* out; long long split_stride; int ldo;       // EPI_PARTIAL: out[split][b][n]
   bf16* act_hl; int ld_act;                            // EPI_SWIGLU: [2 * Rp][ld_act] hi/lo rows
   int hl_f16;                                          // act_hl rows as FP16 (e4m3 weights), else BF16
   float* logits; int ldl; ArgmaxPart* part; int part_ld;   // EPI_ARGMAX
   uint32_t* err;
+  GumbelArgs gum;                                      // EPI_ARGMAX: draw instead of arg-max when gum.on
 };
 cudaError_t tc_init();
 cudaError_t tc_make_map(void* map, const void* base, int rows, int K, int box_rows);
-cudaError_t tc_launch(int epi, const void* mapW, const void* mapX, const TcArgs& a, int ksplit, cudaStream_t s);
-// e4m3 weights: [rows][K] codes, 64-code x 64-row boxes with 64-byte swizzle;
-// the activations as FP16 high/low rows (map from tc_make_map)
+// Stream-K tensor-core GEMM (tc_stream.cu): one CTA per SM, at most 64 rows
+// (a.R <= a.Rp <= 64, a.Rp a multiple of 16) per launch; x as 16-bit high rows [rp_all][K] followed by
+// low rows, read from row a.row0 with boxes of a.Rp rows. Outputs are complete
+// sums (no K split): PARTIAL out[(row0 + b) * ldo + n].
+cudaError_t ts_init();
+cudaError_t ts_launch(int wt, int epi, const void* mapW, const void* mapX, const TcArgs& a, int num_sms,
+                      cudaStream_t s);
+int ts_tiles(int epi, int N);
+size_t ts_scratch_floats(int num_sms);
+constexpr int kTsMaxRows = 64;
+// e4m3 weights: [rows][K] codes, 128-code x 64-row boxes with 128-byte
+// swizzle; the activations as FP16 high/low rows (map from tc_make_map)
 cudaError_t tc_make_map_u8(void* map, const void* base, int rows, int K);
-cudaError_t tc8_init();
-cudaError_t tc8_launch(int epi, const void* mapW, const void* mapX, const TcArgs& a, int ksplit, cudaStream_t s);
-size_t tc8_smem(int Rp);
-int tc_tiles(int epi, int N);
-#ifndef MBT_TC_TP
-#define MBT_TC_TP 1
-#endif
-constexpr int kTcTP = MBT_TC_TP;        // BF16 GEMM: weight tiles per CTA sharing each activation tile
-size_t tc_smem(int Rp);
 cudaError_t tc_to_hl(const float* x, int B, int Rp, int K, bf16* hl, cudaStream_t s, int f16 = 0);
 cudaError_t tc_from_hl(const bf16* hl, int B, int Rp, int N, float* out, cudaStream_t s, int f16 = 0);
 
@@ -196,6 +208,17 @@ size_t attn_smem_bytes(int d, int kv8, int G);   // static + dynamic shared memo
 // next_ids[b] = index of the best of part[0..G)[b]
 cudaError_t launch_argmax_reduce(int B, const ArgmaxPart* part, int part_ld, int G,
                                  int* next_ids, uint32_t* err, cudaStream_t s, int carveout = -1);
+
+// Top-k / top-p draw per row from logits in memory (rows of ldl floats): the
+// k largest logit * inv_t (ties: lower id), softmax over them, the shortest
+// most-probable prefix reaching top_p, and the Gumbel-max draw over it.
+// k in 1..kTopKMax.
+constexpr int kTopKMax = 1024;
+struct TopKArgs {
+  int B, V, ldl; const float* logits; float inv_t; int k; float top_p;
+  GumbelArgs gum; int* next_ids; uint32_t* err;
+};
+cudaError_t launch_sample_topk(const TopKArgs& a, cudaStream_t s);
 
 // Copy B caller rows into the graph's static buffers and fill pad rows [B, R).
 // Live rows keep the caller's table width: entries from bt_stride on are

@@ -52,8 +52,16 @@ struct Plan {
   int ns_qkv = 1, ns_o = 1, ns_down = 1;   // split-K counts of the residual-feeding projections
   int g_lm = 1;                            // LM-head CTAs (arg-max partials per row)
   bool use_tc = false;                     // tensor-core GEMMs (batch 16..128, BF16 weights)
-  int rp = 0;                              // rows padded to a multiple of 8 (tensor-core path)
+  int rp = 0;                              // rows padded to a multiple of 16 (tensor-core path)
   int kernels = 0;
+};
+
+// Sampling in place of the greedy arg-max (null: arg-max). mode 1: the draw
+// is fused into the LM head's arg-max epilogue (temperature only, the logits
+// stay on chip); mode 2: the LM head writes the logits to `z` (rows of vocab
+// floats) and the top-k / top-p kernel draws from them.
+struct SampleCfg {
+  int mode; GumbelArgs gum; int k; float top_p; float* z;
 };
 
 // Device workspace for up to `cap` rows.
@@ -67,8 +75,10 @@ struct Workspace {
   float* part_o = nullptr; float2* part_ml = nullptr; float* o = nullptr;
   float* delta = nullptr; float* delta2 = nullptr;   // O and down partials [splits][cap][H]
   float* act = nullptr; ArgmaxPart* lm_part = nullptr;
-  int* tickets = nullptr;
+  int* attn_tickets = nullptr;
   int* sched = nullptr;                              // GEMV work-queue counters, zeroed each step
+  int* tickets = nullptr; int tickets_cap = 0;       // tensor-core GEMM per-tile tickets (right after sched)
+  float* ts_scratch = nullptr;                       // tensor-core GEMM partial sums
   int rp_cap = 0;                                    // tensor-core path: BF16 high/low rows
   bf16* x_hl = nullptr; bf16* o_hl = nullptr; bf16* act_hl = nullptr;
   float* q = nullptr;                                // prefill: rotated queries [cap][nq * d]
@@ -108,6 +118,7 @@ struct mbt_model {
   void* statics = nullptr;
   int* s_tok = nullptr; int* s_pos = nullptr; int* s_sl = nullptr; int* s_bt = nullptr;
   int* s_next = nullptr; float* s_logits = nullptr;
+  float* samp_z = nullptr; int samp_rows = 0;   // logits of a top-k / top-p step
 };
 
 struct mbt_kv {
@@ -134,15 +145,6 @@ size_t kv_layer_half_bytes(const mbt_model* m, int num_blocks) {
   return (size_t)(num_blocks + 1) * m->h.n_kv_heads * kBlockTokens * m->h.head_dim * esz;
 }
 
-int tc_ksplit(const mbt_model* m, int epi, int N, int K) {
-  const int tiles = m->wtype == W_E4M3 ? tc_tiles(epi, N) : (tc_tiles(epi, N) + kTcTP - 1) / kTcTP;
-  // two CTAs per SM (BF16, one tile each), one (e4m3: its deeper copy ring fills the SM)
-  int ks = (m->wtype == W_E4M3 || kTcTP > 1 ? 1 : 2) * m->num_sms / tiles;
-  const int chunks = (K + 63) / 64;
-  if (ks > chunks / 4) ks = chunks / 4;        // at least 4 stages of K per split
-  return ks < 1 ? 1 : ks;
-}
-
 Plan make_plan(const mbt_model* m, int R, int mbs) {
   Plan p;
   p.R = R;
@@ -150,16 +152,16 @@ Plan make_plan(const mbt_model* m, int R, int mbs) {
   attn_plan(R, (int)m->h.n_kv_heads, mbs, m->num_sms, &p.attn_bps, &p.attn_nsplit);
   const int nb0 = std::min(R, 8);
   const int H = (int)m->h.hidden, Q = (int)(m->h.n_q_heads * m->h.head_dim), F = (int)m->h.ffn;
-  const int QKV = (int)((m->h.n_q_heads + 2 * m->h.n_kv_heads) * m->h.head_dim);
   const int L = (int)m->h.n_layers;
-  p.use_tc = m->tc_ok && R >= kTcMinRows && R <= 128;
+  p.use_tc = m->tc_ok && R >= kTcMinRows;
   if (p.use_tc) {
-    p.rp = (R + 7) / 8 * 8;
-    p.ns_qkv = tc_ksplit(m, EPI_PARTIAL, QKV, H);
-    p.ns_o = tc_ksplit(m, EPI_PARTIAL, H, Q);
-    p.ns_down = tc_ksplit(m, EPI_PARTIAL, H, F);
-    p.g_lm = tc_tiles(EPI_ARGMAX, (int)m->h.vocab);
-    p.kernels = 1 + 7 * L + 3;
+    // the stream-K GEMM leaves complete sums (no K-split partials) and runs
+    // in launches of at most 64 rows
+    p.rp = (R + 15) / 16 * 16;
+    p.ns_qkv = p.ns_o = p.ns_down = 1;
+    p.g_lm = ts_tiles(EPI_ARGMAX, (int)m->h.vocab);
+    const int chunks = (R + kTsMaxRows - 1) / kTsMaxRows;
+    p.kernels = 1 + (3 + 4 * chunks) * L + 2 + chunks;
     return p;
   }
   p.ns_qkv = 1;                                          // norm prologue: whole rows per CTA
@@ -239,8 +241,12 @@ int ensure_ws(mbt_model* m, Workspace& w, int R, int mbs) {
   const size_t o_a = take((size_t)cap * F * 4);
   const size_t o_lp = take((size_t)g_lm * cap * sizeof(ArgmaxPart));
   const size_t o_tk = take((size_t)cap * m->h.n_kv_heads * 4);
-  const size_t o_sc = take((size_t)kSchedCap * 4);
-  const int rp_cap = (cap + 7) / 8 * 8;
+  const int QKVn = (int)QKV, Hn = (int)H, Fn = (int)F, Vn = (int)m->h.vocab;
+  const int tcap = std::max({ts_tiles(EPI_PARTIAL, QKVn), ts_tiles(EPI_PARTIAL, Hn), ts_tiles(EPI_SWIGLU, Fn),
+                             ts_tiles(EPI_ARGMAX, Vn)});
+  const size_t o_sc = take((size_t)(kSchedCap + tcap) * 4);
+  const size_t o_ts = take(ts_scratch_floats(m->num_sms) * 4);
+  const int rp_cap = (cap + 15) / 16 * 16;
   const size_t b_xhl = (size_t)2 * rp_cap * H * 2, b_ohl = (size_t)2 * rp_cap * Q * 2;
   const size_t b_ahl = (size_t)2 * rp_cap * F * 2;
   const size_t o_xhl = take(b_xhl), o_ohl = take(b_ohl), o_ahl = take(b_ahl);
@@ -257,8 +263,10 @@ int ensure_ws(mbt_model* m, Workspace& w, int R, int mbs) {
   w.o = (float*)(base + o_o); w.delta = (float*)(base + o_d); w.delta2 = (float*)(base + o_d2);
   w.act = (float*)(base + o_a);
   w.lm_part = (ArgmaxPart*)(base + o_lp);
-  w.tickets = (int*)(base + o_tk);
+  w.attn_tickets = (int*)(base + o_tk);
   w.sched = (int*)(base + o_sc);
+  w.tickets = w.sched + kSchedCap; w.tickets_cap = tcap;
+  w.ts_scratch = (float*)(base + o_ts);
   w.rp_cap = rp_cap;
   w.x_hl = (bf16*)(base + o_xhl); w.o_hl = (bf16*)(base + o_ohl); w.act_hl = (bf16*)(base + o_ahl);
   w.q = (float*)(base + o_q);
@@ -282,7 +290,7 @@ cudaError_t gemv_rows(const mbt_model* m, const Workspace& ws, int epi, const No
                       int N, int K, const float* x, int R, int nsplit, int grid_fixed, float* out,
                       long long split_stride, int ldo, float* act, int lda, float* logits,
                       ArgmaxPart* part, int part_ld, cudaStream_t s, uint32_t prefetch = 0,
-                      int* sched_used = nullptr) {
+                      int* sched_used = nullptr, const GumbelArgs* gum = nullptr) {
   const int pro = nin ? PRO_NORM : PRO_X;
   const int step = gemv_max_rows(epi, K, pro);
   for (int b0 = 0; b0 < R; b0 += step) {
@@ -306,6 +314,7 @@ cudaError_t gemv_rows(const mbt_model* m, const Workspace& ws, int epi, const No
     a.part = part ? part + b0 : nullptr; a.part_ld = part_ld;
     a.err = m->err;
     a.prefetch_bytes = prefetch;
+    if (gum) { a.gum = *gum; a.gum.row0 = b0; }
     // work-queue tail: a fixed share of each CTA's rows, the rest claimed one
     // group at a time (kernels that prefetch their whole slice keep it fixed)
     const int sg = gemv_queue_static_groups(g, N);
@@ -341,6 +350,14 @@ cudaError_t prefill_rope_kv(const mbt_model* m, const Workspace& w, const mbt_kv
   return launch_rope_kv_write(rk, s);
 }
 
+// After an LM head that wrote the logits to smp->z: the top-k / top-p draw.
+cudaError_t sample_from_logits(const mbt_model* m, const SampleCfg* smp, int R, int* next_ids, cudaStream_t s) {
+  TopKArgs t = {};
+  t.B = R; t.V = (int)m->h.vocab; t.ldl = (int)m->h.vocab; t.logits = smp->z; t.inv_t = smp->gum.inv_t;
+  t.k = smp->k; t.top_p = smp->top_p; t.gum = smp->gum; t.next_ids = next_ids; t.err = m->err;
+  return launch_sample_topk(t, s);
+}
+
 // Prefill tail: final norm and LM head for the chunk's last row only (the
 // sequence's next token); the residual of that row plus the down projection's
 // pending partials, normalised into w.r2, then the arg-max GEMV.
@@ -362,7 +379,8 @@ int lm_head_last_row(mbt_model* m, const Workspace& w, const Plan& p, int* next_
 // projection reads BF16 high/low activation rows written by its producer
 // (residual add + RMSNorm, attention, the gate/up GEMM's SwiGLU epilogue).
 int run_layers_tc(mbt_model* m, const Workspace& w, mbt_kv* kv, const Plan& p, const int* pos, const int* bt, int bt_stride,
-                  const int* sl, int* next_ids, float* logits, cudaStream_t s, bool prefill) {
+                  const int* sl, int* next_ids, float* logits, cudaStream_t s, bool prefill,
+                  const SampleCfg* smp) {
   const int R = p.R, Rp = p.rp;
   const int H = (int)m->h.hidden, d = (int)m->h.head_dim;
   const int nq = (int)m->h.n_q_heads, nkv = (int)m->h.n_kv_heads;
@@ -370,31 +388,40 @@ int run_layers_tc(mbt_model* m, const Workspace& w, mbt_kv* kv, const Plan& p, c
   const int QKV = (nq + 2 * nkv) * d;
   const size_t half = kv_layer_half_bytes(m, kv->num_blocks);
   const long long rh = (long long)R * H;
-  TmaMap xh, xq, xf;
-  MBT_CUDA(tc_make_map(&xh, w.x_hl, 2 * Rp, H, 2 * Rp));
-  MBT_CUDA(tc_make_map(&xq, w.o_hl, 2 * Rp, Q, 2 * Rp));
-  MBT_CUDA(tc_make_map(&xf, w.act_hl, 2 * Rp, F, 2 * Rp));
-  // e4m3 weights: FP16 activations and the widening kernel; BF16 otherwise
+  // e4m3 weights: FP16 activation rows; BF16 otherwise
   const int f16 = m->wtype == W_E4M3;
-  auto gemm = [&](int epi, const void* wm, const void* xm, const TcArgs& a, int ks) {
-    return f16 ? tc8_launch(epi, wm, xm, a, ks, s) : tc_launch(epi, wm, xm, a, ks, s);
+  // one projection over the R rows, in launches of at most 64 rows that read
+  // the high/low buffer from their first row on
+  auto gemm = [&](int epi, const TmaMap& wm, const bf16* xbuf, int K, const TcArgs& base) -> cudaError_t {
+    for (int r0 = 0; r0 < R; r0 += kTsMaxRows) {
+      const int rl = std::min(kTsMaxRows, R - r0), rc = (rl + 15) / 16 * 16;
+      TmaMap xm;
+      cudaError_t e = tc_make_map(&xm, xbuf, 2 * Rp, K, rc);
+      if (e != cudaSuccess) return e;
+      TcArgs a = base;
+      a.R = rl; a.Rp = rc; a.row0 = r0; a.rp_all = Rp;
+      a.ts_scratch = w.ts_scratch; a.ts_tickets = w.tickets; a.tickets_cap = w.tickets_cap;
+      e = ts_launch(m->wtype, epi, &wm, &xm, a, m->num_sms, s);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
   };
   auto norm = [&](const float* delta, int n_delta, const bf16* gamma) {
     AddNormArgs an{R, H, w.r, delta, n_delta, rh, gamma, m->h.eps, nullptr, w.x_hl, Rp, f16};
     return launch_add_rmsnorm(an, s);
   };
-  auto partial = [&](const TmaMap& wm, const TmaMap& xm, const float* sc, int N, int K, float* out, int ks) {
+  auto partial = [&](const TmaMap& wm, const bf16* xbuf, const float* sc, int N, int K, float* out) {
     TcArgs a = {};
-    a.N = N; a.K = K; a.R = R; a.Rp = Rp; a.scale = sc;
+    a.N = N; a.K = K; a.scale = sc;
     a.out = out; a.split_stride = (long long)R * N; a.ldo = N; a.err = m->err;
-    return gemm(EPI_PARTIAL, &wm, &xm, a, ks);
+    return gemm(EPI_PARTIAL, wm, xbuf, K, a);
   };
   for (int l = 0; l < (int)m->h.n_layers; ++l) {
     const Layer& L = m->layers[l];
     const TmaMap* wm = &m->wmaps[(size_t)l * 4];
     char* kbase = (char*)kv->pool + 2 * half * (size_t)l;
     MBT_CUDA(norm(l ? w.delta2 : nullptr, l ? p.ns_down : 0, L.g_attn));
-    MBT_CUDA(partial(wm[0], xh, L.s_qkv, QKV, H, w.qkv, p.ns_qkv));
+    MBT_CUDA(partial(wm[0], w.x_hl, L.s_qkv, QKV, H, w.qkv));
     AttnArgs at = {};
     at.B = R; at.nq = nq; at.nkv = nkv; at.d = d;
     at.qkv = w.qkv; at.qkv_nsplit = p.ns_qkv; at.qkv_split_stride = (long long)R * QKV; at.ld_qkv = QKV;
@@ -403,27 +430,34 @@ int run_layers_tc(mbt_model* m, const Workspace& w, mbt_kv* kv, const Plan& p, c
     at.k_scale = kv->k_scale[l]; at.v_scale = kv->v_scale[l];
     at.bt = bt; at.bt_stride = bt_stride; at.seq_lens = sl; at.num_blocks = kv->num_blocks;
     at.bps = p.attn_bps; at.nsplit = p.attn_nsplit;
-    at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = nullptr; at.tickets = w.tickets; at.err = m->err;
+    at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = nullptr; at.tickets = w.attn_tickets; at.err = m->err;
     at.out_hl = w.o_hl; at.rp_hl = Rp; at.hl_f16 = f16;
     if (prefill) {
       MBT_CUDA(prefill_rope_kv(m, w, kv, l, R, p.ns_qkv, pos, bt, bt_stride, s));
       at.qkv = nullptr; at.q = w.q; at.no_pdl = 1;
     }
     MBT_CUDA(launch_attention(at, s));
-    MBT_CUDA(partial(wm[1], xq, L.s_o, H, Q, w.delta, p.ns_o));
+    MBT_CUDA(partial(wm[1], w.o_hl, L.s_o, H, Q, w.delta));
     MBT_CUDA(norm(w.delta, p.ns_o, L.g_ffn));
     TcArgs g = {};
-    g.N = F; g.K = H; g.R = R; g.Rp = Rp; g.scale = L.s_gu; g.act_hl = w.act_hl; g.ld_act = F; g.err = m->err;
+    g.N = F; g.K = H; g.scale = L.s_gu; g.act_hl = w.act_hl; g.ld_act = F; g.err = m->err;
     g.hl_f16 = f16;
-    MBT_CUDA(gemm(EPI_SWIGLU, &wm[2], &xh, g, 1));
-    MBT_CUDA(partial(wm[3], xf, L.s_down, H, F, w.delta2, p.ns_down));
+    MBT_CUDA(gemm(EPI_SWIGLU, wm[2], w.x_hl, H, g));
+    MBT_CUDA(partial(wm[3], w.act_hl, L.s_down, H, F, w.delta2));
   }
   if (prefill) return next_ids ? lm_head_last_row(m, w, p, next_ids, logits, s) : MBT_OK;
   MBT_CUDA(norm(w.delta2, p.ns_down, m->g_final));
   TcArgs a = {};
-  a.N = V; a.K = H; a.R = R; a.Rp = Rp; a.scale = m->s_lm; a.logits = logits; a.ldl = V;
+  a.N = V; a.K = H; a.scale = m->s_lm; a.logits = logits; a.ldl = V;
   a.part = w.lm_part; a.part_ld = R; a.err = m->err;
-  MBT_CUDA(gemm(EPI_ARGMAX, &m->wmaps[(size_t)m->h.n_layers * 4], &xh, a, 1));
+  if (smp && smp->mode == 1) a.gum = smp->gum;
+  if (smp && smp->mode == 2) a.logits = smp->z;
+  MBT_CUDA(gemm(EPI_ARGMAX, m->wmaps[(size_t)m->h.n_layers * 4], w.x_hl, H, a));
+  if (smp && smp->mode == 2) {
+    MBT_CUDA(sample_from_logits(m, smp, R, next_ids, s));
+    if (logits) MBT_CUDA(cudaMemcpyAsync(logits, smp->z, (size_t)R * V * 4, cudaMemcpyDeviceToDevice, s));
+    return MBT_OK;
+  }
   MBT_CUDA(launch_argmax_reduce(R, w.lm_part, R, p.g_lm, next_ids, m->err, s));
   return MBT_OK;
 }
@@ -439,7 +473,7 @@ int run_layers_tc(mbt_model* m, const Workspace& w, mbt_kv* kv, const Plan& p, c
 // through the final norm and the LM head (none when next_ids is null).
 int run_step(mbt_model* m, const Workspace& w, mbt_kv* kv, const Plan& p, const int* tok, const int* pos,
              const int* bt, int bt_stride, const int* sl, int* next_ids, float* logits,
-             cudaStream_t s, bool prefill = false) {
+             cudaStream_t s, bool prefill = false, const SampleCfg* smp = nullptr) {
   const int R = p.R;
   const int H = (int)m->h.hidden, d = (int)m->h.head_dim;
   const int nq = (int)m->h.n_q_heads, nkv = (int)m->h.n_kv_heads;
@@ -449,9 +483,9 @@ int run_step(mbt_model* m, const Workspace& w, mbt_kv* kv, const Plan& p, const 
   const long long rh = (long long)R * H;
 
   EmbedNormArgs en{R, H, V, tok, m->embed, w.r, m->layers[0].g_attn, m->h.eps, nullptr, m->err,
-                   w.sched, kSchedCap, p.use_tc ? 0 : m->stream.carveout};
+                   w.sched, kSchedCap + w.tickets_cap, p.use_tc ? 0 : m->stream.carveout};
   MBT_CUDA(launch_embed_rmsnorm(en, s));
-  if (p.use_tc) return run_layers_tc(m, w, kv, p, pos, bt, bt_stride, sl, next_ids, logits, s, prefill);
+  if (p.use_tc) return run_layers_tc(m, w, kv, p, pos, bt, bt_stride, sl, next_ids, logits, s, prefill, smp);
   int sq = 0;                                        // work-queue counters taken so far
   for (int l = 0; l < (int)m->h.n_layers; ++l) {
     const Layer& L = m->layers[l];
@@ -469,7 +503,7 @@ int run_step(mbt_model* m, const Workspace& w, mbt_kv* kv, const Plan& p, const 
     at.k_scale = kv->k_scale[l]; at.v_scale = kv->v_scale[l];
     at.bt = bt; at.bt_stride = bt_stride; at.seq_lens = sl; at.num_blocks = kv->num_blocks;
     at.bps = p.attn_bps; at.nsplit = p.attn_nsplit;
-    at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = w.o; at.tickets = w.tickets; at.err = m->err;
+    at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = w.o; at.tickets = w.attn_tickets; at.err = m->err;
     at.carveout = m->stream.carveout;
     if (prefill) {
       MBT_CUDA(prefill_rope_kv(m, w, kv, l, R, 1, pos, bt, bt_stride, s));
@@ -492,8 +526,14 @@ int run_step(mbt_model* m, const Workspace& w, mbt_kv* kv, const Plan& p, const 
   // final RMSNorm prologue + LM head with the arg-max epilogue, then the
   // cross-CTA reduction
   NormIn nf{w.r, w.delta2, p.ns_down, m->g_final, w.r2};
+  float* lg = smp && smp->mode == 2 ? smp->z : logits;
   MBT_CUDA(gemv_rows(m, w, EPI_ARGMAX, &nf, m->lm, m->s_lm, V, H, nullptr, R, 1, p.g_lm, nullptr, 0, 0,
-                     nullptr, 0, logits, w.lm_part, R, s, 0, &sq));
+                     nullptr, 0, lg, w.lm_part, R, s, 0, &sq, smp && smp->mode == 1 ? &smp->gum : nullptr));
+  if (smp && smp->mode == 2) {
+    MBT_CUDA(sample_from_logits(m, smp, R, next_ids, s));
+    if (logits) MBT_CUDA(cudaMemcpyAsync(logits, smp->z, (size_t)R * V * 4, cudaMemcpyDeviceToDevice, s));
+    return MBT_OK;
+  }
   MBT_CUDA(launch_argmax_reduce(R, w.lm_part, R, p.g_lm, next_ids, m->err, s, m->stream.carveout));
   return MBT_OK;
 }
@@ -680,7 +720,7 @@ int model_create(const void* blob, size_t bytes, int blob_is_device, void* strea
   }
   // tensor maps for the tensor-core path (64-row boxes: BF16 tiles swizzled
   // for the MMA, e4m3 tiles plain for the widening warps)
-  if (tc_init() == cudaSuccess && (m->wtype == W_BF16 || tc8_init() == cudaSuccess)) {
+  if (tc_init() == cudaSuccess) {
     const int Hh = (int)h.hidden, Qd = (int)(h.n_q_heads * h.head_dim), Ff = (int)h.ffn;
     const int QKVr = (int)((h.n_q_heads + 2 * h.n_kv_heads) * h.head_dim);
     auto mk = [&](TmaMap* map, const void* base, int rows, int K) {
@@ -708,6 +748,7 @@ int model_destroy(mbt_model* m) {
   destroy_graphs(m);
   free_ws(m->ws);
   free_ws(m->ws_eager);
+  if (m->samp_z) cudaFree(m->samp_z);
   if (m->wmem) cudaFree(m->wmem);
   if (m->err) cudaFree(m->err);
   if (m->rope) cudaFree(m->rope);
@@ -889,6 +930,44 @@ int decode_step(mbt_model* m, mbt_kv* kv, int B, const int32_t* tok, const int32
   if (rc != MBT_OK) return rc;
   Plan p = make_plan(m, B, bt_stride);
   return run_step(m, *w, kv, p, tok, pos, bt, bt_stride, sl, next_ids, logits, s);
+}
+
+int decode_step_sample(mbt_model* m, mbt_kv* kv, int B, const int32_t* tok, const int32_t* pos,
+                       const int32_t* bt, int bt_stride, const int32_t* sl, const mbt_sampling* sp,
+                       int32_t* next_ids, float* logits, void* stream) {
+  if (!m || !kv || !sp) return MBT_ERR_BAD_ARG;
+  if (B <= 0) return MBT_ERR_BATCH;
+  if (kv->m != m || !tok || !pos || !bt || !sl || !next_ids || bt_stride < 1) return MBT_ERR_BAD_ARG;
+  if (!(sp->temperature > 0.f) || !std::isfinite(sp->temperature) || sp->top_k < 0 || sp->top_k > MBT_TOPK_MAX ||
+      !(sp->top_p > 0.f) || !(sp->top_p <= 1.f))
+    return MBT_ERR_BAD_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  SampleCfg smp = {};
+  smp.gum.on = 1;
+  smp.gum.inv_t = 1.0f / sp->temperature;
+  smp.gum.seed_lo = (uint32_t)(sp->seed & 0xffffffffu); smp.gum.seed_hi = (uint32_t)(sp->seed >> 32);
+  smp.gum.step_lo = (uint32_t)(sp->step & 0xffffffffu); smp.gum.step_hi = (uint32_t)(sp->step >> 32);
+  const bool cut = sp->top_k > 0 || sp->top_p < 1.f;
+  smp.mode = cut ? 2 : 1;
+  smp.k = sp->top_k > 0 ? sp->top_k : kTopKMax;
+  smp.top_p = sp->top_p;
+  if (cut) {
+    if (m->samp_rows < B) {
+      if (cudaStreamSynchronize(s) != cudaSuccess) return MBT_ERR_CUDA;
+      if (m->samp_z) cudaFree(m->samp_z);
+      m->samp_z = nullptr;
+      m->samp_rows = 0;
+      if (cudaMalloc(&m->samp_z, (size_t)B * m->h.vocab * 4) != cudaSuccess) { cudaGetLastError(); return MBT_ERR_OOM; }
+      m->samp_rows = B;
+    }
+    smp.z = m->samp_z;
+  }
+  Workspace* w = &m->ws;
+  if (!m->graphs.empty() && !ws_covers(m->ws, ws_need(m, m->ws, B, bt_stride))) w = &m->ws_eager;
+  int rc = ensure_ws(m, *w, B, bt_stride);
+  if (rc != MBT_OK) return rc;
+  Plan p = make_plan(m, B, bt_stride);
+  return run_step(m, *w, kv, p, tok, pos, bt, bt_stride, sl, next_ids, logits, s, false, &smp);
 }
 
 int prefill(mbt_model* m, mbt_kv* kv, int n, const int32_t* tokens, int start_pos, const int32_t* block_table,

@@ -1,0 +1,497 @@
+// Skinny GEMM on the tcgen05 tensor cores for decode at batch 2..64 rows per
+// launch, BF16 or e4m3 weights: y = W x with W [rows][K] the M operand
+// (swap-AB: 128 weight rows per tile) and the fp32 activation rows, split into
+// 16-bit high and low parts, the N operand. At these batches the weight-only
+// arithmetic intensity 2B / b_w ("GPU Inference Internals", "Roofline: Why
+// Decode Is Memory-Bound") is far below the ridge: the kernel must move the
+// weights at the HBM rate. Three measurements on the GB300 shape it:
+//
+// * DRAM efficiency depends on how many contiguous bytes of a weight row one
+//   copy fetches: streaming 128-row tiles with TMA boxes of 64 / 128 / 256
+//   bytes per row reached 3.9-5.2 / 6.2-6.5 / 6.7 TB/s. Every weight stage
+//   here covers 256 bytes of each of its 128 rows (128 BF16 values or 256 e4m3
+//   codes), 32 KB per stage.
+// * The tensor core's fp32 accumulation drifts toward zero over long chains
+//   (a bias proportional to K: 2.3e-5 of the output rms at K = 28672, halving
+//   with each halving of the chain). The accumulator therefore lives in TMEM
+//   for at most 512 K values: three TMEM accumulators rotate, and the drain
+//   warps add the finished one into fp32 registers (IEEE adds) while the MMAs
+//   fill the others.
+// * Whole tiles per CTA quantise badly (224 tiles on 152 SMs run as two
+//   waves). One CTA per SM takes an equal contiguous share of the flattened
+//   (tile, K stage) work ("stream-K"). A tile whose K range spans several
+//   CTAs belongs to the CTA holding its head (K stage 0): the others did
+//   their parts at the start of their shares and published them (coalesced
+//   fp32 rows, then a counter), and the owner adds them after its own sums
+//   in CTA order, so results do not depend on timing and graph replays match
+//   eager runs bit for bit. Under full HBM load one dependent round trip to
+//   L2 costs microseconds, so the owner's tail is one acquire and one batch
+//   of loads.
+//
+// Warp roles: warp 0 (one thread) copies weight stages with TMA (it never
+// waits on the previous kernel: the weights do not depend on it); warp 1 (one
+// thread) copies activation sub-stages (64 K values, high and low rows);
+// warp 2 (one thread) issues the MMAs (M = 128, N = 2 x rows, K = 16) and
+// their commits; warp 3 owns the TMEM allocation. For e4m3 weights warps 4-7
+// widen each thread's weight row into FP16 in TMEM (the MMA reads A from
+// there; kind::f16 needs two 16-bit operands of one type; the bit pattern
+// s.0eeee.mmm0000000 is exactly the e4m3 value / 256, the 256 joining the
+// per-row scale). The last four warps drain the accumulators, finish tiles
+// and run the epilogues: split outputs, SwiGLU over 64 gate + 64 up rows
+// (written as 16-bit high/low rows for the down projection), the tile's arg-max
+// per row (or the sampling draw). Every wait is bounded (about 2 s): on a
+// timeout the kernel flags MBT_DEV_WAIT_LIMIT, lets its MMAs and copies finish
+// (bounded), frees TMEM and returns.
+#include <algorithm>
+
+#include "tcgen05.cuh"
+
+namespace mbt {
+
+constexpr int kTsRows = 64;                        // batch rows per launch (hi + lo = 128 MMA columns)
+constexpr int kTsSub = 64;                         // K values per MMA sub-stage (one 128-byte row of 16-bit values)
+constexpr int kTsFlushK = 512;                     // K values accumulated in TMEM before the fp32 drain
+constexpr uint32_t kTsAStage = 128 * 256;          // weight stage: 128 rows x 256 bytes
+constexpr uint32_t kTsBStage = 2 * kTsRows * 128;  // activation sub-stage: 2 x 64 rows x 64 K x 2 bytes
+constexpr uint32_t kTsScratch = 32 * 128 * 4 + 4 * kTsRows * 8;  // epilogue staging (32 batch rows) + arg-max partials
+constexpr uint32_t kTsAcc = 64;                    // TMEM columns per accumulator (one per batch row)
+constexpr int kTsNAcc = 3;                         // accumulators in rotation
+constexpr uint32_t kTsTmemCols = 512;
+
+template <int WT> struct TsCfg;
+template <> struct TsCfg<W_BF16> {
+  static constexpr int SA = 4, SB = 4, SUBS = 2, WARPS = 8, DRAIN = 4, ST = 0;
+};
+template <> struct TsCfg<W_E4M3> {
+  static constexpr int SA = 3, SB = 6, SUBS = 4, WARPS = 12, DRAIN = 8, ST = 8;
+};
+
+template <int WT>
+constexpr size_t ts_smem() {
+  return 1024 + (size_t)TsCfg<WT>::SA * kTsAStage + (size_t)TsCfg<WT>::SB * kTsBStage + kTsScratch;
+}
+
+// First unit (weight stage) of CTA c's share of W units over G CTAs.
+__device__ __forceinline__ long long ts_u0(long long W, int G, int c) { return W * c / G; }
+// The CTA whose share holds unit u.
+__device__ __forceinline__ int ts_owner(long long W, int G, long long u) {
+  int c = (int)((u * G) / W);
+  while (c + 1 < G && ts_u0(W, G, c + 1) <= u) ++c;
+  while (c > 0 && ts_u0(W, G, c) > u) --c;
+  return c;
+}
+
+// Four e4m3 codes (lowest byte first) -> two FP16x2 words of value / 256.
+__device__ __forceinline__ void ts_widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t t0 = __byte_perm(w, 0u, 0x1404), t1 = __byte_perm(w, 0u, 0x3424);
+  lo = ((t0 >> 1) & 0x3F803F80u) | (t0 & 0x80008000u);
+  hi = ((t1 >> 1) & 0x3F803F80u) | (t1 & 0x80008000u);
+}
+
+template <int WT, int EPI>
+__global__ void __launch_bounds__(TsCfg<WT>::WARPS * 32, 1)
+tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const TcArgs a) {
+  using C = TsCfg<WT>;
+  constexpr int SA = C::SA, SB = C::SB, SUBS = C::SUBS, ST = C::ST > 0 ? C::ST : 1;
+  constexpr int FG = kTsFlushK / (kTsSub * SUBS);    // weight stages per accumulation group
+  constexpr int DW = C::DRAIN;                       // first drain warp
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ __align__(8) uint64_t a_full[SA], a_empty[SA], b_full[SB], b_empty[SB];
+  __shared__ __align__(8) uint64_t t_full[ST], t_empty[ST], acc_full[kTsNAcc], acc_empty[kTsNAcc], done;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  __shared__ int a_issued_s, a_used_s, b_issued_s, b_used_s, last_s;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int Rc = a.Rp;                                // padded rows of this launch (multiple of 16, <= 64)
+  const uint32_t b_bytes = (uint32_t)(2 * Rc) * 128;
+  unsigned char* sA = smem;                                   // [SA][K block][128 rows][128 B], 128-B swizzle
+  unsigned char* sB = sA + SA * kTsAStage;                    // [SB][2 Rc rows][128 B], 128-B swizzle
+  float* scr = reinterpret_cast<float*>(sB + SB * kTsBStage);  // epilogue exchange
+  const int tiles = EPI == EPI_SWIGLU ? (a.N + 63) / 64 : (a.N + 127) / 128;
+  const int nA = (a.K + kTsSub * SUBS - 1) / (kTsSub * SUBS);
+  const long long W = (long long)tiles * nA;
+  const long long u0 = ts_u0(W, G, cta), u1 = ts_u0(W, G, cta + 1);
+  auto rowA0 = [&](int t) { return EPI == EPI_SWIGLU ? t * 64 : t * 128; };
+  auto rowA1 = [&](int t) { return EPI == EPI_SWIGLU ? a.N + t * 64 : t * 128 + 64; };
+
+  pdl_launch_dependents();
+  if (tid == 0) {
+    for (int s = 0; s < SA; ++s) { mbar_init(&a_full[s], 1); mbar_init(&a_empty[s], WT == W_E4M3 ? 4 : 1); }
+    for (int s = 0; s < SB; ++s) { mbar_init(&b_full[s], 1); mbar_init(&b_empty[s], 1); }
+    for (int s = 0; s < ST; ++s) { mbar_init(&t_full[s], 4); mbar_init(&t_empty[s], 1); }
+    for (int s = 0; s < kTsNAcc; ++s) { mbar_init(&acc_full[s], 1); mbar_init(&acc_empty[s], 4); }
+    mbar_init(&done, 1);
+    abort_flag = 0;
+    a_issued_s = a_used_s = b_issued_s = b_used_s = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
+  }
+  if (warp == 3) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(&tmem_slot)), "r"(kTsTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;                  // accumulators at columns 0, 64, 128
+  const uint32_t tmem_a = tmem + kTsNAcc * kTsAcc;  // e4m3: widened A sub-stages, 32 columns each
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // weight stages of this CTA's units, in order
+      long long i = 0;
+      for (long long u = u0; u < u1; ++u, ++i) {
+        const int s = (int)(i % SA);
+        if (i >= SA && (abort_flag || !mbar_wait(&a_empty[s], (uint32_t)(((i / SA) - 1) & 1)))) { abort_flag = 1; break; }
+        const int t = (int)(u / nA), k = (int)(u % nA);
+        mbar_arrive_tx(&a_full[s], kTsAStage);
+        unsigned char* dst = sA + (size_t)s * kTsAStage;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {                 // two 128-byte K blocks of each row
+          const int kx = WT == W_E4M3 ? k * 256 + h * 128 : (k * 2 + h) * 64;
+          tma_load_2d(dst + h * 16384, &tmW, kx, rowA0(t), &a_full[s]);
+          tma_load_2d(dst + h * 16384 + 8192, &tmW, kx, rowA1(t), &a_full[s]);
+        }
+        a_issued_s = (int)(i + 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      pdl_wait();
+      long long i = 0;
+      for (long long u = u0; u < u1 && !abort_flag; ++u) {
+        const int k = (int)(u % nA);
+        for (int j = 0; j < SUBS; ++j, ++i) {
+          const int s = (int)(i % SB);
+          if (i >= SB && (abort_flag || !mbar_wait(&b_empty[s], (uint32_t)(((i / SB) - 1) & 1)))) { abort_flag = 1; break; }
+          const int kx = (k * SUBS + j) * kTsSub;
+          mbar_arrive_tx(&b_full[s], b_bytes);
+          unsigned char* dst = sB + (size_t)s * kTsBStage;
+          tma_load_2d(dst, &tmX, kx, a.row0, &b_full[s]);                        // high rows
+          tma_load_2d(dst + (size_t)Rc * 128, &tmX, kx, a.rp_all + a.row0, &b_full[s]);   // low rows
+          b_issued_s = (int)(i + 1);
+        }
+      }
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {
+      pdl_wait();
+      // N = Rc: the high rows and the low rows are two MMAs into one accumulator
+      const uint32_t idesc = idesc_16(128, Rc, WT == W_E4M3 ? 1 : 0);
+      long long ia = 0, ib = 0, it = 0, gi = 0;
+      bool ok = true;
+      for (long long u = u0; u < u1 && ok;) {
+        const int k0 = (int)(u % nA);
+        const int seg = (int)min((long long)(nA - k0), u1 - u);
+        for (int g0 = 0; g0 < seg && ok; g0 += FG, ++gi) {
+          const int gn = min(FG, seg - g0);
+          const int buf = (int)(gi % kTsNAcc);
+          if (gi >= kTsNAcc && !mbar_wait(&acc_empty[buf], (uint32_t)(((gi / kTsNAcc) - 1) & 1))) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t acc = tmem + (uint32_t)buf * kTsAcc;
+          for (int x = 0; x < gn && ok; ++x, ++ia) {
+            const int sa = (int)(ia % SA);
+            if (WT == W_BF16 && (abort_flag || !mbar_wait(&a_full[sa], (uint32_t)((ia / SA) & 1)))) { ok = false; break; }
+            for (int j = 0; j < SUBS; ++j, ++ib) {
+              const int sb = (int)(ib % SB);
+              if (abort_flag || !mbar_wait(&b_full[sb], (uint32_t)((ib / SB) & 1))) { ok = false; break; }
+              const int stt = (int)(it % ST);
+              if (WT == W_E4M3 && !mbar_wait(&t_full[stt], (uint32_t)((it / ST) & 1))) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t bh = sw128_desc(smem_u32(sB + (size_t)sb * kTsBStage));
+              const uint64_t bl = sw128_desc(smem_u32(sB + (size_t)sb * kTsBStage + (size_t)Rc * 128));
+#pragma unroll
+              for (int kk = 0; kk < kTsSub / 16; ++kk) {
+                const uint32_t accum = (x > 0 || j > 0 || kk > 0) ? 1u : 0u;
+                if (WT == W_E4M3) {
+                  const uint32_t ta = tmem_a + (uint32_t)(stt * 32 + kk * 8);
+                  umma_kf16_tmem_a(acc, ta, bh + (uint64_t)(kk * 2), idesc, accum);
+                  umma_kf16_tmem_a(acc, ta, bl + (uint64_t)(kk * 2), idesc, 1u);
+                } else {
+                  const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)sa * kTsAStage + j * 16384)) + (uint64_t)(kk * 2);
+                  umma_kf16(acc, ad, bh + (uint64_t)(kk * 2), idesc, accum);
+                  umma_kf16(acc, ad, bl + (uint64_t)(kk * 2), idesc, 1u);
+                }
+              }
+              umma_commit(&b_empty[sb]);
+              if (WT == W_E4M3) { umma_commit(&t_empty[stt]); ++it; }
+              b_used_s = (int)(ib + 1);
+            }
+            if (WT == W_BF16 && ok) { umma_commit(&a_empty[sa]); a_used_s = (int)(ia + 1); }
+          }
+          if (ok) umma_commit(&acc_full[buf]);
+        }
+        u += seg;
+      }
+      if (!ok) abort_flag = 1;
+      umma_commit(&done);                              // fires once every MMA issued above has completed
+    }
+  } else if (WT == W_E4M3 && warp >= 4 && warp < 8) {
+    // widening: thread = weight row q * 32 + lane = TMEM lane
+    const int q = warp - 4, row = q * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    long long ia = 0, it = 0;
+    for (long long u = u0; u < u1; ++u, ++ia) {
+      const int sa = (int)(ia % SA);
+      if (abort_flag || !mbar_wait(&a_full[sa], (uint32_t)((ia / SA) & 1))) { abort_flag = 1; break; }
+      const unsigned char* src = sA + (size_t)sa * kTsAStage + row * 128;
+      uint4 w[16];                                     // the row's 256 codes: two 128-byte K blocks
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        w[c] = *reinterpret_cast<const uint4*>(src + (c >> 3) * 16384 + (((c & 7) ^ (row & 7)) * 16));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_empty[sa]);
+      if (q == 0 && lane == 0) a_used_s = (int)(ia + 1);
+      bool ok = true;
+#pragma unroll
+      for (int j = 0; j < 4; ++j, ++it) {              // four 64-code sub-stages
+        const int stt = (int)(it % ST);
+        if (it >= ST && (abort_flag || !mbar_wait(&t_empty[stt], (uint32_t)(((it / ST) - 1) & 1)))) { ok = false; break; }
+        uint32_t h[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = w[j * 4 + c];
+          ts_widen4(v.x, h[8 * c + 0], h[8 * c + 1]);
+          ts_widen4(v.y, h[8 * c + 2], h[8 * c + 3]);
+          ts_widen4(v.z, h[8 * c + 4], h[8 * c + 5]);
+          ts_widen4(v.w, h[8 * c + 6], h[8 * c + 7]);
+        }
+        tmem_st32(tmem_a + lane_off + (uint32_t)(stt * 32), h);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&t_full[stt]);
+      }
+      if (!ok) { abort_flag = 1; break; }
+    }
+  } else if (warp >= DW) {
+    // drain, finish and epilogue: thread = weight row q * 32 + lane of the tile
+    const int q = warp - DW, row = q * 32 + lane, et = tid - DW * 32;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const float mul = WT == W_E4M3 ? 256.f : 1.f;
+    float sum[kTsRows];
+    long long gi = 0;
+    bool ok = true;
+    for (long long u = u0; u < u1 && ok;) {
+      const int t = (int)(u / nA), k0 = (int)(u % nA);
+      const int seg = (int)min((long long)(nA - k0), u1 - u);
+#pragma unroll
+      for (int b = 0; b < kTsRows; ++b) sum[b] = 0.f;
+      for (int g0 = 0; g0 < seg; g0 += FG, ++gi) {
+        const int buf = (int)(gi % kTsNAcc);
+        if (abort_flag || !mbar_wait(&acc_full[buf], (uint32_t)((gi / kTsNAcc) & 1))) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t acc = tmem + (uint32_t)buf * kTsAcc + lane_base;
+        // all of the row's columns in flight at once, one wait
+        uint32_t v0[16], v1[16], v2[16], v3[16];
+        tmem_ld16_async(acc, v0);
+        if (Rc > 16) tmem_ld16_async(acc + 16, v1);
+        if (Rc > 32) tmem_ld16_async(acc + 32, v2);
+        if (Rc > 48) tmem_ld16_async(acc + 48, v3);
+        tmem_ld_wait16(v0);
+        tmem_ld_wait16(v1);
+        tmem_ld_wait16(v2);
+        tmem_ld_wait16(v3);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          sum[j] += __uint_as_float(v0[j]);
+          if (Rc > 16) sum[16 + j] += __uint_as_float(v1[j]);
+          if (Rc > 32) sum[32 + j] += __uint_as_float(v2[j]);
+          if (Rc > 48) sum[48 + j] += __uint_as_float(v3[j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      }
+      if (!ok) break;
+      const bool whole = k0 == 0 && seg == nA;
+      if (!whole) {
+        // A tile cut by a share boundary. A share can only begin inside a
+        // tile, so the part of a tile that is not its head is always the
+        // first segment of its CTA, done early: those CTAs publish their sums
+        // and move on. The CTA holding the head of the tile (its last segment,
+        // or a head that ends its share) owns the tile: it waits for the
+        // others (bounded), adds their sums after its own in CTA order (the
+        // same order on every run) and runs the epilogue.
+        const int c_first = ts_owner(W, G, (long long)t * nA);
+        const int c_last = ts_owner(W, G, (long long)t * nA + nA - 1);
+        if (k0 != 0) {
+          float* mine = a.ts_scratch + (size_t)cta * 128 * kTsRows + row;   // [row b][weight row]
+#pragma unroll
+          for (int b = 0; b < kTsRows; ++b) if (b < Rc) mine[(size_t)b * 128] = sum[b];
+          __threadfence();
+          named_bar(1, 128);
+          if (et == 0) atomicAdd(a.ts_tickets + t, 1);
+          u += seg;
+          continue;
+        }
+        if (et == 0) {
+          const int want = c_last - c_first;
+          int seen = ld_acquire_gpu(a.ts_tickets + t);
+          if (seen < want) {
+            const long long w0 = clock64();
+            while ((seen = ld_acquire_gpu(a.ts_tickets + t)) < want && clock64() - w0 < kTcWaitCycles) {}
+          }
+          last_s = seen == want;
+        }
+        named_bar(1, 128);
+        if (!last_s) { ok = false; break; }
+        for (int cc = c_first + 1; cc <= c_last; ++cc) {
+          const float* src = a.ts_scratch + (size_t)cc * 128 * kTsRows + row;
+          float p[kTsRows];
+#pragma unroll
+          for (int b = 0; b < kTsRows; ++b) p[b] = b < Rc ? __ldcg(src + (size_t)b * 128) : 0.f;
+#pragma unroll
+          for (int b = 0; b < kTsRows; ++b) sum[b] += p[b];
+        }
+        if (et == 0) a.ts_tickets[t] = 0;              // every contributor has arrived: ready for the next launch
+      }
+      // ---- epilogue of tile t. The scaled sums pass through shared memory
+      // ([batch row][weight row], conflict-free) in two halves of 32 batch
+      // rows and are consumed by rolled loops: epilogues unrolled over the 64
+      // rows were tens of KB of instructions, fetched cold once per tile, and
+      // under full HBM load that cost ~300 cycles per batch row at the tail.
+      float sc;
+      if (EPI == EPI_SWIGLU) {
+        const int j = t * 64 + (row & 63);              // rows 0..63: gate, 64..127: up of channel j
+        sc = (a.scale && j < a.N) ? a.scale[row < 64 ? j : a.N + j] : 1.f;
+      } else {
+        const int n = t * 128 + row;
+        sc = (a.scale && n < a.N) ? a.scale[n] : 1.f;
+      }
+      sc *= mul;
+      float* bv = scr + 32 * 128;                        // arg-max: [4 warps][kTsRows] best value, index
+      int* bi = reinterpret_cast<int*>(bv + 4 * kTsRows);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int b0 = h * 32;
+        if (b0 >= Rc) break;
+        named_bar(2, 128);                               // the staging buffer is free
+#pragma unroll
+        for (int i = 0; i < 32; ++i) if (b0 + i < Rc) scr[i * 128 + row] = sum[b0 + i] * sc;
+        named_bar(2, 128);
+        const int nb = min(32, Rc - b0);
+        if (EPI == EPI_PARTIAL) {
+          const int n = t * 128 + row;
+          if (n < a.N)
+            for (int i = 0; i < nb && b0 + i < a.R; ++i) a.out[(size_t)(a.row0 + b0 + i) * a.ldo + n] = scr[i * 128 + row];
+        } else if (EPI == EPI_SWIGLU) {
+          uint16_t* act = reinterpret_cast<uint16_t*>(a.act_hl);
+          for (int e = et; e < nb * 64; e += 128) {
+            const int i = e >> 6, c = e & 63, j = t * 64 + c, b = b0 + i;
+            if (j < a.N) {
+              const float g = scr[i * 128 + c], up = scr[i * 128 + 64 + c];
+              const float v = b < a.R ? g / (1.f + expf(-g)) * up : 0.f;   // padding rows stay finite
+              store_hl16(act + (size_t)(a.row0 + b) * a.ld_act + j,
+                         act + (size_t)(a.rp_all + a.row0 + b) * a.ld_act + j, v, a.hl_f16);
+            }
+          }
+        } else {  // EPI_ARGMAX: the tile's best (value, index) per batch row
+          const int n = t * 128 + row;
+          for (int i = 0; i < nb; ++i) {
+            const int b = b0 + i;
+            float v = n < a.N ? scr[i * 128 + row] : -INFINITY;
+            if (!(v == v)) { set_err(a.err, MBT_DEV_NONFINITE); v = -INFINITY; }
+            if (n < a.N && b < a.R && a.logits) a.logits[(size_t)(a.row0 + b) * a.ldl + n] = v;
+            if (a.gum.on && n < a.N) v = gumbel_score(v, n, b, a.gum);
+            int idx = n;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+              const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+              if (ov > v || (ov == v && oi < idx)) { v = ov; idx = oi; }
+            }
+            if (lane == 0) { bv[q * kTsRows + b] = v; bi[q * kTsRows + b] = idx; }
+          }
+        }
+      }
+      if (EPI == EPI_ARGMAX) {
+        named_bar(2, 128);
+        for (int b = et; b < a.R; b += 128) {
+          float v = bv[b];
+          int idx = bi[b];
+          for (int w2 = 1; w2 < 4; ++w2) {
+            const float ov = bv[w2 * kTsRows + b];
+            const int oi = bi[w2 * kTsRows + b];
+            if (ov > v || (ov == v && oi < idx)) { v = ov; idx = oi; }
+          }
+          ArgmaxPart p;
+          p.v = v; p.i = idx;
+          a.part[(size_t)t * a.part_ld + a.row0 + b] = p;
+        }
+      }
+      u += seg;
+    }
+    if (!ok) abort_flag = 1;
+  }
+  __syncwarp();
+
+  // teardown: `done` covers every MMA; after a timeout, wait (bounded) for the
+  // copies that were issued and never consumed before shared memory goes
+  const bool done_ok = mbar_wait(&done, 0);
+  __syncthreads();
+  if (tid == 0 && (abort_flag || !done_ok)) {
+    set_err(a.err, MBT_DEV_WAIT_LIMIT);
+    for (int i = a_used_s; i < a_issued_s; ++i) mbar_wait(&a_full[i % SA], (uint32_t)((i / SA) & 1));
+    for (int i = b_used_s; i < b_issued_s; ++i) mbar_wait(&b_full[i % SB], (uint32_t)((i / SB) & 1));
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 3) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTsTmemCols) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+namespace {
+template <int WT, int EPI>
+void* ts_fn() { return (void*)tc_stream_kernel<WT, EPI>; }
+template <int WT>
+void* ts_pick_w(int epi) {
+  return epi == EPI_PARTIAL ? ts_fn<WT, EPI_PARTIAL>() : epi == EPI_SWIGLU ? ts_fn<WT, EPI_SWIGLU>()
+                                                                            : ts_fn<WT, EPI_ARGMAX>();
+}
+void* ts_pick(int wt, int epi) { return wt == W_E4M3 ? ts_pick_w<W_E4M3>(epi) : ts_pick_w<W_BF16>(epi); }
+}  // namespace
+
+cudaError_t ts_init() {
+  for (int wt = 0; wt < 2; ++wt)
+    for (int epi = 0; epi < 3; ++epi) {
+      const size_t sm = wt == W_E4M3 ? ts_smem<W_E4M3>() : ts_smem<W_BF16>();
+      cudaError_t e = cudaFuncSetAttribute(ts_pick(wt, epi), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      if (e != cudaSuccess) return e;
+    }
+  return cudaSuccess;
+}
+
+int ts_tiles(int epi, int N) { return epi == EPI_SWIGLU ? (N + 63) / 64 : (N + 127) / 128; }
+
+size_t ts_scratch_floats(int num_sms) { return (size_t)num_sms * 128 * kTsRows; }
+
+cudaError_t ts_launch(int wt, int epi, const void* mapW, const void* mapX, const TcArgs& a, int num_sms,
+                      cudaStream_t s) {
+  if (a.Rp < 16 || a.Rp > kTsRows || a.Rp % 16 || a.R < 1 || a.R > a.Rp || a.rp_all < a.row0 + a.Rp ||
+      !a.ts_scratch || !a.ts_tickets || a.tickets_cap < ts_tiles(epi, a.N))
+    return cudaErrorInvalidValue;
+  CUtensorMap w = *(const CUtensorMap*)mapW, x = *(const CUtensorMap*)mapX;
+  TcArgs args = a;
+  args.gum.row0 += a.row0;
+  void* params[] = {&w, &x, &args};
+  const int threads = (wt == W_E4M3 ? TsCfg<W_E4M3>::WARPS : TsCfg<W_BF16>::WARPS) * 32;
+  const size_t sm = wt == W_E4M3 ? ts_smem<W_E4M3>() : ts_smem<W_BF16>();
+  // one CTA per SM, but never more CTAs than weight stages: every CTA's share
+  // is then non-empty, so a tile's contributors are consecutive CTAs
+  const int subs = wt == W_E4M3 ? TsCfg<W_E4M3>::SUBS : TsCfg<W_BF16>::SUBS;
+  const long long units = (long long)ts_tiles(epi, a.N) * ((a.K + kTsSub * subs - 1) / (kTsSub * subs));
+  const int grid = (int)std::min<long long>(num_sms, units);
+  return launch_pdl(ts_pick(wt, epi), dim3(grid), dim3(threads), sm, s, params);
+}
+
+}  // namespace mbt

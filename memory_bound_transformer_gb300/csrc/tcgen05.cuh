@@ -1,12 +1,12 @@
-// tcgen05 building blocks shared by the BF16 and the e4m3 skinny GEMMs:
-// mbarriers (every wait bounded), TMA tile loads, shared-memory and
-// instruction descriptors, the MMA and commit, TMEM loads, and the epilogues
-// that read the fp32 accumulator out of TMEM.
+// tcgen05 building blocks of the skinny GEMM: mbarriers (every wait bounded),
+// TMA tile loads, shared-memory and instruction descriptors, the MMA (A from
+// shared memory or from TMEM) and its commit, TMEM loads and stores.
 #pragma once
 #include <cuda.h>
 
 #include "common.cuh"
 #include "internal.h"
+#include "sampling.cuh"
 
 namespace mbt {
 
@@ -95,6 +95,23 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive fp32 columns of this thread's TMEM lane, without waiting:
+// the values are valid after tmem_ld_wait16 on the same array.
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                 "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+               : "r"(taddr));
+}
+// Wait for this thread's outstanding TMEM loads; the array is threaded
+// through so that no use of it is scheduled before the wait.
+__device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :: "memory");
+}
+
 // 32 consecutive 32-bit columns of this thread's TMEM lane from registers
 // (the warp covers the 32 lanes of its quarter); then wait for the stores.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
@@ -111,110 +128,14 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 // Barrier among `n` threads (a multiple of 32) under id `id` (1..15).
-__device__ __forceinline__ void named_bar(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
-// Epilogue of one 128-row tile, run by four warps whose TMEM lane quarters are
-// q = 0..3 (lane `lane` of quarter q holds weight row q*32 + lane): split-K
-// partials, SwiGLU over 64 gate + 64 up rows (written as 16-bit high/low rows
-// for the down projection), or the tile's arg-max per batch row. `scratch`
-// (free shared memory, >= 64 * Rp * 4 bytes) and barrier `bar` of the 128
-// epilogue threads are the epilogue's own. `et` = the thread's index among them.
-template <int EPI>
-__device__ __forceinline__ void tc_epilogue(const TcArgs& a, uint32_t tmem, int q, int lane, int et, int tile,
-                                            int split, unsigned char* scratch, int bar, float mul = 1.f) {
-  const int Rp = a.Rp;
-  const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-  const int row = q * 32 + lane;
-  if (EPI == EPI_PARTIAL) {
-    const int n = tile * kTcBM + row;
-    const float sc = ((a.scale && n < a.N) ? a.scale[n] : 1.f) * mul;
-    for (int c0 = 0; c0 < Rp; c0 += 8) {
-      float hi[8], lo[8];
-      tmem_ld8(lane_base + c0, hi);
-      tmem_ld8(lane_base + Rp + c0, lo);
-      if (n < a.N) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (c0 + j < a.R)
-            a.out[(size_t)split * a.split_stride + (size_t)(c0 + j) * a.ldo + n] = (hi[j] + lo[j]) * sc;
-      }
-    }
-  } else if (EPI == EPI_SWIGLU) {
-    // lanes 0..63: gate rows, 64..127: up rows of channels tile*64 + (row % 64)
-    float* ex = reinterpret_cast<float*>(scratch);   // [64][Rp] up values
-    const int j = tile * 64 + (row & 63);
-    const bool ch_ok = j < a.N;
-    uint16_t* act = reinterpret_cast<uint16_t*>(a.act_hl);
-    if (q >= 2) {
-      const float su = ((a.scale && ch_ok) ? a.scale[a.N + j] : 1.f) * mul;
-      for (int c0 = 0; c0 < Rp; c0 += 8) {
-        float hi[8], lo[8];
-        tmem_ld8(lane_base + c0, hi);
-        tmem_ld8(lane_base + Rp + c0, lo);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) ex[(row - 64) * Rp + c0 + k] = (hi[k] + lo[k]) * su;
-      }
-    }
-    named_bar(bar, 128);
-    if (q < 2) {
-      const float sg = ((a.scale && ch_ok) ? a.scale[j] : 1.f) * mul;
-      for (int c0 = 0; c0 < Rp; c0 += 8) {
-        float hi[8], lo[8];
-        tmem_ld8(lane_base + c0, hi);
-        tmem_ld8(lane_base + Rp + c0, lo);
-        if (ch_ok) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int b = c0 + k;
-            const float g = (hi[k] + lo[k]) * sg;
-            const float u = ex[row * Rp + b];
-            const float v = b < a.R ? g / (1.f + expf(-g)) * u : 0.f;
-            store_hl16(act + (size_t)b * a.ld_act + j, act + (size_t)(Rp + b) * a.ld_act + j, v, a.hl_f16);
-          }
-        }
-      }
-    }
-  } else {  // EPI_ARGMAX
-    float* bv = reinterpret_cast<float*>(scratch);   // [4 quarters][Rp]
-    int* bi = reinterpret_cast<int*>(scratch + 4 * Rp * 4);
-    const int n = tile * kTcBM + row;
-    const float sc = ((a.scale && n < a.N) ? a.scale[n] : 1.f) * mul;
-    for (int c0 = 0; c0 < Rp; c0 += 8) {
-      float hi[8], lo[8];
-      tmem_ld8(lane_base + c0, hi);
-      tmem_ld8(lane_base + Rp + c0, lo);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int b = c0 + k;
-        float v = n < a.N ? (hi[k] + lo[k]) * sc : -INFINITY;
-        if (!(v == v)) { set_err(a.err, MBT_DEV_NONFINITE); v = -INFINITY; }
-        if (n < a.N && b < a.R && a.logits) a.logits[(size_t)b * a.ldl + n] = v;
-        int idx = n;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-          if (ov > v || (ov == v && oi < idx)) { v = ov; idx = oi; }
-        }
-        if (lane == 0) { bv[q * Rp + b] = v; bi[q * Rp + b] = idx; }
-      }
-    }
-    named_bar(bar, 128);
-    for (int b = et; b < a.R; b += 128) {
-      float v = bv[b];
-      int idx = bi[b];
-      for (int w2 = 1; w2 < 4; ++w2) {
-        const float ov = bv[w2 * Rp + b];
-        const int oi = bi[w2 * Rp + b];
-        if (ov > v || (ov == v && oi < idx)) { v = ov; idx = oi; }
-      }
-      ArgmaxPart p;
-      p.v = v; p.i = idx;
-      a.part[(size_t)tile * a.part_ld + b] = p;
-    }
-  }
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 }  // namespace mbt

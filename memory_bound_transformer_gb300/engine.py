@@ -46,6 +46,11 @@ class Engine:
         capi.decode_step(self.model, self.kv, tokens, positions, block_tables, seq_lens, next_ids,
                          logits, self.stream)
 
+    def step_sample(self, tokens, positions, block_tables, seq_lens, next_ids, temperature, top_k, top_p, seed,
+                    step, logits=None):
+        capi.decode_step_sample(self.model, self.kv, tokens, positions, block_tables, seq_lens, next_ids,
+                                temperature, top_k, top_p, seed, step, logits, self.stream)
+
     def prefill(self, tokens, start_pos, block_table, next_id, logits=None):
         capi.prefill(self.model, self.kv, tokens, start_pos, block_table, next_id, logits, self.stream)
 

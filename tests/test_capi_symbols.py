@@ -66,6 +66,13 @@ def test_blob_layout_matches_header():
     assert {(e[0], e[1]) for e in ents} >= {(0, -1), (12, -1), (2, 0), (7, 0)}
 
 
+def test_sampling_struct_matches_header():
+    text = open(os.path.join(INCLUDE, "mbt.h")).read()
+    assert "} mbt_sampling;             /* 32 bytes */" in text
+    assert ctypes.sizeof(capi.Sampling) == 32
+    assert "#define MBT_TOPK_MAX 1024" in text and capi.TOPK_MAX == 1024
+
+
 def test_argument_checks_before_any_device_call(lib):
     """Entry points reject malformed arguments with a status code before they
     touch the device (these run on a machine without a GPU)."""
@@ -86,3 +93,6 @@ def test_argument_checks_before_any_device_call(lib):
     assert l.model_create(None, 0, 0, None, None) == BAD
     assert l.kv_alloc(None, 4, None, None) == BAD
     assert l.model_capture(None, None, None, 0, 0, None) == BAD
+    # sampling and prefill without handles or parameters
+    assert l.decode_step_sample(None, None, 1, None, None, None, 1, None, None, None, None, None) == BAD
+    assert l.prefill(None, None, 4, None, 0, None, 1, None, None, None) == BAD
