@@ -52,23 +52,37 @@ constexpr int kTsRows = 64;                        // batch rows per launch (hi 
 constexpr int kTsSub = 64;                         // K values per MMA sub-stage (one 128-byte row of 16-bit values)
 constexpr int kTsFlushK = 512;                     // K values accumulated in TMEM before the fp32 drain
 constexpr uint32_t kTsAStage = 128 * 256;          // weight stage: 128 rows x 256 bytes
-constexpr uint32_t kTsBStage = 2 * kTsRows * 128;  // activation sub-stage: 2 x 64 rows x 64 K x 2 bytes
+constexpr uint32_t kTsRings = 192 * 1024;          // weight ring + activation ring
 constexpr uint32_t kTsScratch = 32 * 128 * 4 + 4 * kTsRows * 8;  // epilogue staging (32 batch rows) + arg-max partials
 constexpr uint32_t kTsAcc = 64;                    // TMEM columns per accumulator (one per batch row)
 constexpr int kTsNAcc = 3;                         // accumulators in rotation
 constexpr uint32_t kTsTmemCols = 512;
 
+// SUBS: activation sub-stages (64 K each) per weight stage; XR: activation
+// rows per batch row in a sub-stage (high and low parts); MAXA / MAXB: ring
+// depth limits (the depths themselves depend on the batch).
 template <int WT> struct TsCfg;
 template <> struct TsCfg<W_BF16> {
-  static constexpr int SA = 4, SB = 4, SUBS = 2, WARPS = 8, DRAIN = 4, ST = 0;
+  static constexpr int SUBS = 2, XR = 2, WARPS = 8, DRAIN = 4, ST = 0, MAXA = 5, MAXB = 8;
 };
 template <> struct TsCfg<W_E4M3> {
-  static constexpr int SA = 3, SB = 6, SUBS = 4, WARPS = 12, DRAIN = 8, ST = 8;
+  static constexpr int SUBS = 4, XR = 2, WARPS = 12, DRAIN = 8, ST = 8, MAXA = 4, MAXB = 16;
 };
 
+constexpr size_t ts_smem() { return 1024 + (size_t)kTsRings + kTsScratch; }
+
+// Ring depths for Rc padded batch rows. Under full HBM load an activation
+// copy from L2 takes as long as a weight copy from HBM (3,400-7,000 cycles
+// measured against 6,000), so both rings are sized against that latency: the
+// activation bytes per weight byte are XR * Rc * 2 / (128 * w), and the rings
+// split the 192 KB in roughly that proportion.
 template <int WT>
-constexpr size_t ts_smem() {
-  return 1024 + (size_t)TsCfg<WT>::SA * kTsAStage + (size_t)TsCfg<WT>::SB * kTsBStage + kTsScratch;
+__host__ __device__ __forceinline__ void ts_rings(int Rc, int& sa, int& sb) {
+  using C = TsCfg<WT>;
+  const int xs = C::XR * Rc * 128;
+  sa = WT == W_E4M3 ? (Rc <= 16 ? 4 : Rc <= 48 ? 3 : 2) : (Rc <= 16 ? 5 : 4);
+  sb = ((int)kTsRings - sa * (int)kTsAStage) / xs;
+  if (sb > C::MAXB) sb = C::MAXB;
 }
 
 // First unit (weight stage) of CTA c's share of W units over G CTAs.
@@ -92,12 +106,12 @@ template <int WT, int EPI>
 __global__ void __launch_bounds__(TsCfg<WT>::WARPS * 32, 1)
 tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const TcArgs a) {
   using C = TsCfg<WT>;
-  constexpr int SA = C::SA, SB = C::SB, SUBS = C::SUBS, ST = C::ST > 0 ? C::ST : 1;
+  constexpr int SUBS = C::SUBS, ST = C::ST > 0 ? C::ST : 1;
   constexpr int FG = kTsFlushK / (kTsSub * SUBS);    // weight stages per accumulation group
   constexpr int DW = C::DRAIN;                       // first drain warp
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t a_full[SA], a_empty[SA], b_full[SB], b_empty[SB];
+  __shared__ __align__(8) uint64_t a_full[C::MAXA], a_empty[C::MAXA], b_full[C::MAXB], b_empty[C::MAXB];
   __shared__ __align__(8) uint64_t t_full[ST], t_empty[ST], acc_full[kTsNAcc], acc_empty[kTsNAcc], done;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
@@ -106,10 +120,12 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x;
   const int Rc = a.Rp;                                // padded rows of this launch (multiple of 16, <= 64)
-  const uint32_t b_bytes = (uint32_t)(2 * Rc) * 128;
+  int SA, SB;
+  ts_rings<WT>(Rc, SA, SB);
+  const uint32_t b_bytes = (uint32_t)(C::XR * Rc) * 128;    // one activation sub-stage
   unsigned char* sA = smem;                                   // [SA][K block][128 rows][128 B], 128-B swizzle
-  unsigned char* sB = sA + SA * kTsAStage;                    // [SB][2 Rc rows][128 B], 128-B swizzle
-  float* scr = reinterpret_cast<float*>(sB + SB * kTsBStage);  // epilogue exchange
+  unsigned char* sB = sA + SA * kTsAStage;                    // [SB][XR * Rc rows][128 B], 128-B swizzle
+  float* scr = reinterpret_cast<float*>(smem + kTsRings);     // epilogue staging
   const int tiles = EPI == EPI_SWIGLU ? (a.N + 63) / 64 : (a.N + 127) / 128;
   const int nA = (a.K + kTsSub * SUBS - 1) / (kTsSub * SUBS);
   const long long W = (long long)tiles * nA;
@@ -144,10 +160,9 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   if (warp == 0) {
     if (lane == 0) {
       // weight stages of this CTA's units, in order
-      long long i = 0;
-      for (long long u = u0; u < u1; ++u, ++i) {
-        const int s = (int)(i % SA);
-        if (i >= SA && (abort_flag || !mbar_wait(&a_empty[s], (uint32_t)(((i / SA) - 1) & 1)))) { abort_flag = 1; break; }
+      int i = 0, s = 0, r = 0;                         // copy count, its slot and round
+      for (long long u = u0; u < u1; ++u, ++i, s = s + 1 == SA ? 0 : s + 1, r += s == 0) {
+        if (r > 0 && (abort_flag || !mbar_wait(&a_empty[s], (uint32_t)((r - 1) & 1)))) { abort_flag = 1; break; }
         const int t = (int)(u / nA), k = (int)(u % nA);
         mbar_arrive_tx(&a_full[s], kTsAStage);
         unsigned char* dst = sA + (size_t)s * kTsAStage;
@@ -157,24 +172,23 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
           tma_load_2d(dst + h * 16384, &tmW, kx, rowA0(t), &a_full[s]);
           tma_load_2d(dst + h * 16384 + 8192, &tmW, kx, rowA1(t), &a_full[s]);
         }
-        a_issued_s = (int)(i + 1);
+        a_issued_s = i + 1;
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       pdl_wait();
-      long long i = 0;
+      int i = 0, s = 0, r = 0;
       for (long long u = u0; u < u1 && !abort_flag; ++u) {
         const int k = (int)(u % nA);
-        for (int j = 0; j < SUBS; ++j, ++i) {
-          const int s = (int)(i % SB);
-          if (i >= SB && (abort_flag || !mbar_wait(&b_empty[s], (uint32_t)(((i / SB) - 1) & 1)))) { abort_flag = 1; break; }
+        for (int j = 0; j < SUBS; ++j, ++i, s = s + 1 == SB ? 0 : s + 1, r += s == 0) {
+          if (r > 0 && (abort_flag || !mbar_wait(&b_empty[s], (uint32_t)((r - 1) & 1)))) { abort_flag = 1; break; }
           const int kx = (k * SUBS + j) * kTsSub;
           mbar_arrive_tx(&b_full[s], b_bytes);
-          unsigned char* dst = sB + (size_t)s * kTsBStage;
+          unsigned char* dst = sB + (size_t)s * b_bytes;
           tma_load_2d(dst, &tmX, kx, a.row0, &b_full[s]);                        // high rows
           tma_load_2d(dst + (size_t)Rc * 128, &tmX, kx, a.rp_all + a.row0, &b_full[s]);   // low rows
-          b_issued_s = (int)(i + 1);
+          b_issued_s = i + 1;
         }
       }
     }
@@ -183,7 +197,7 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
       pdl_wait();
       // N = Rc: the high rows and the low rows are two MMAs into one accumulator
       const uint32_t idesc = idesc_16(128, Rc, WT == W_E4M3 ? 1 : 0);
-      long long ia = 0, ib = 0, it = 0, gi = 0;
+      int ia = 0, sa = 0, ra = 0, ib = 0, sb = 0, rb = 0, it = 0, gi = 0;   // counts, slots, rounds
       bool ok = true;
       for (long long u = u0; u < u1 && ok;) {
         const int k0 = (int)(u % nA);
@@ -194,17 +208,15 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
           if (gi >= kTsNAcc && !mbar_wait(&acc_empty[buf], (uint32_t)(((gi / kTsNAcc) - 1) & 1))) { ok = false; break; }
           tc_fence_after();
           const uint32_t acc = tmem + (uint32_t)buf * kTsAcc;
-          for (int x = 0; x < gn && ok; ++x, ++ia) {
-            const int sa = (int)(ia % SA);
-            if (WT == W_BF16 && (abort_flag || !mbar_wait(&a_full[sa], (uint32_t)((ia / SA) & 1)))) { ok = false; break; }
-            for (int j = 0; j < SUBS; ++j, ++ib) {
-              const int sb = (int)(ib % SB);
-              if (abort_flag || !mbar_wait(&b_full[sb], (uint32_t)((ib / SB) & 1))) { ok = false; break; }
-              const int stt = (int)(it % ST);
+          for (int x = 0; x < gn && ok; ++x, ++ia, sa = sa + 1 == SA ? 0 : sa + 1, ra += sa == 0) {
+            if (WT == W_BF16 && (abort_flag || !mbar_wait(&a_full[sa], (uint32_t)(ra & 1)))) { ok = false; break; }
+            for (int j = 0; j < SUBS; ++j, ++ib, sb = sb + 1 == SB ? 0 : sb + 1, rb += sb == 0) {
+              if (abort_flag || !mbar_wait(&b_full[sb], (uint32_t)(rb & 1))) { ok = false; break; }
+              const int stt = it % ST;
               if (WT == W_E4M3 && !mbar_wait(&t_full[stt], (uint32_t)((it / ST) & 1))) { ok = false; break; }
               tc_fence_after();
-              const uint64_t bh = sw128_desc(smem_u32(sB + (size_t)sb * kTsBStage));
-              const uint64_t bl = sw128_desc(smem_u32(sB + (size_t)sb * kTsBStage + (size_t)Rc * 128));
+              const uint64_t bh = sw128_desc(smem_u32(sB + (size_t)sb * b_bytes));
+              const uint64_t bl = sw128_desc(smem_u32(sB + (size_t)sb * b_bytes + (size_t)Rc * 128));
 #pragma unroll
               for (int kk = 0; kk < kTsSub / 16; ++kk) {
                 const uint32_t accum = (x > 0 || j > 0 || kk > 0) ? 1u : 0u;
@@ -220,9 +232,9 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
               }
               umma_commit(&b_empty[sb]);
               if (WT == W_E4M3) { umma_commit(&t_empty[stt]); ++it; }
-              b_used_s = (int)(ib + 1);
+              b_used_s = ib + 1;
             }
-            if (WT == W_BF16 && ok) { umma_commit(&a_empty[sa]); a_used_s = (int)(ia + 1); }
+            if (WT == W_BF16 && ok) { umma_commit(&a_empty[sa]); a_used_s = ia + 1; }
           }
           if (ok) umma_commit(&acc_full[buf]);
         }
@@ -235,10 +247,9 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     // widening: thread = weight row q * 32 + lane = TMEM lane
     const int q = warp - 4, row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    long long ia = 0, it = 0;
-    for (long long u = u0; u < u1; ++u, ++ia) {
-      const int sa = (int)(ia % SA);
-      if (abort_flag || !mbar_wait(&a_full[sa], (uint32_t)((ia / SA) & 1))) { abort_flag = 1; break; }
+    int ia = 0, sa = 0, ra = 0, it = 0;
+    for (long long u = u0; u < u1; ++u, ++ia, sa = sa + 1 == SA ? 0 : sa + 1, ra += sa == 0) {
+      if (abort_flag || !mbar_wait(&a_full[sa], (uint32_t)(ra & 1))) { abort_flag = 1; break; }
       const unsigned char* src = sA + (size_t)sa * kTsAStage + row * 128;
       uint4 w[16];                                     // the row's 256 codes: two 128-byte K blocks
 #pragma unroll
@@ -246,7 +257,7 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         w[c] = *reinterpret_cast<const uint4*>(src + (c >> 3) * 16384 + (((c & 7) ^ (row & 7)) * 16));
       __syncwarp();
       if (lane == 0) mbar_arrive(&a_empty[sa]);
-      if (q == 0 && lane == 0) a_used_s = (int)(ia + 1);
+      if (q == 0 && lane == 0) a_used_s = ia + 1;
       bool ok = true;
 #pragma unroll
       for (int j = 0; j < 4; ++j, ++it) {              // four 64-code sub-stages
@@ -275,7 +286,7 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const float mul = WT == W_E4M3 ? 256.f : 1.f;
     float sum[kTsRows];
-    long long gi = 0;
+    int gi = 0;
     bool ok = true;
     for (long long u = u0; u < u1 && ok;) {
       const int t = (int)(u / nA), k0 = (int)(u % nA);
@@ -464,7 +475,7 @@ void* ts_pick(int wt, int epi) { return wt == W_E4M3 ? ts_pick_w<W_E4M3>(epi) : 
 cudaError_t ts_init() {
   for (int wt = 0; wt < 2; ++wt)
     for (int epi = 0; epi < 3; ++epi) {
-      const size_t sm = wt == W_E4M3 ? ts_smem<W_E4M3>() : ts_smem<W_BF16>();
+      const size_t sm = ts_smem();
       cudaError_t e = cudaFuncSetAttribute(ts_pick(wt, epi), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
       if (e != cudaSuccess) return e;
     }
@@ -485,7 +496,7 @@ cudaError_t ts_launch(int wt, int epi, const void* mapW, const void* mapX, const
   args.gum.row0 += a.row0;
   void* params[] = {&w, &x, &args};
   const int threads = (wt == W_E4M3 ? TsCfg<W_E4M3>::WARPS : TsCfg<W_BF16>::WARPS) * 32;
-  const size_t sm = wt == W_E4M3 ? ts_smem<W_E4M3>() : ts_smem<W_BF16>();
+  const size_t sm = ts_smem();
   // one CTA per SM, but never more CTAs than weight stages: every CTA's share
   // is then non-empty, so a tile's contributors are consecutive CTAs
   const int subs = wt == W_E4M3 ? TsCfg<W_E4M3>::SUBS : TsCfg<W_BF16>::SUBS;
