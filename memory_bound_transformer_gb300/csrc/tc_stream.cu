@@ -101,6 +101,23 @@ __device__ __forceinline__ int ts_owner(long long W, int G, long long u) {
   return c;
 }
 
+// silu(x) = x / (1 + e^-x) with the hardware exponential and divide
+// (a few ulp; exact limits: 0 for x -> -inf, x for x -> +inf).
+__device__ __forceinline__ float ts_silu(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+
+// x = hi + lo as 16-bit bit patterns (FP16 or BF16), the same rounding as store_hl16.
+__device__ __forceinline__ void split_hl16(float x, int f16, uint32_t& hi, uint32_t& lo) {
+  if (f16) {
+    const __half h = __float2half_rn(x);
+    hi = __half_as_ushort(h);
+    lo = __half_as_ushort(__float2half_rn(x - __half2float(h)));
+  } else {
+    const bf16 h = __float2bfloat16_rn(x);
+    hi = __bfloat16_as_ushort(h);
+    lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+  }
+}
+
 // Four e4m3 codes (lowest byte first) -> two FP16x2 words of value / 256.
 __device__ __forceinline__ void ts_widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t t0 = __byte_perm(w, 0u, 0x1404), t1 = __byte_perm(w, 0u, 0x3424);
@@ -284,7 +301,10 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
       if (!ok) { abort_flag = 1; break; }
     }
   } else if (warp >= DW) {
-    // drain, finish and epilogue: thread = weight row q * 32 + lane of the tile
+    // drain, finish and epilogue: thread = weight row q * 32 + lane of the tile.
+    // The tile counters and partial sums are shared with the previous launch
+    // on the stream: nothing here touches them before that launch is done.
+    pdl_wait();
     const int q = warp - DW, row = q * 32 + lane, et = tid - DW * 32;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const float mul = WT == W_E4M3 ? 256.f : 1.f;
@@ -296,8 +316,13 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
       const int seg = (int)min((long long)(nA - k0), u1 - u);
 #pragma unroll
       for (int b = 0; b < kTsRows; ++b) sum[b] = 0.f;
+      // the head of a cut tile: read the tile's counter while the last MMAs
+      // still run (the other contributors published long ago, as a rule)
+      const bool owned = k0 == 0 && seg < nA;
+      int early = -1;
       for (int g0 = 0; g0 < seg; g0 += FG, ++gi) {
         const int buf = gi % C::NACC;
+        if (owned && et == 0 && g0 + FG >= seg) early = ld_acquire_gpu(a.ts_tickets + t);
         if (abort_flag || !mbar_wait(&acc_full[buf], (uint32_t)((gi / C::NACC) & 1))) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
@@ -349,7 +374,7 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         }
         if (et == 0) {
           const int want = c_last - c_first;
-          int seen = ld_acquire_gpu(a.ts_tickets + t);
+          int seen = early >= want ? early : ld_acquire_gpu(a.ts_tickets + t);
           if (seen < want) {
             const long long w0 = clock64();
             while ((seen = ld_acquire_gpu(a.ts_tickets + t)) < want && clock64() - w0 < kTcWaitCycles) {}
@@ -394,18 +419,45 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         named_bar(2, 128);
         const int nb = min(32, Rc - b0);
         if (EPI == EPI_PARTIAL) {
-          const int n = t * 128 + row;
-          if (n < a.N)
-            for (int i = 0; i < nb && b0 + i < a.R; ++i) a.out[(size_t)(a.row0 + b0 + i) * a.ldo + n] = scr[i * 128 + row];
+          // four consecutive outputs of one batch row per thread and pass
+          const bool vec = ((a.ldo & 3) == 0) && (((uintptr_t)a.out & 15) == 0);
+          for (int e = et; e < nb * 32; e += 128) {
+            const int i = e >> 5, n4 = (e & 31) * 4, b = b0 + i, n = t * 128 + n4;
+            if (b >= a.R || n >= a.N) continue;
+            const float4 v = *reinterpret_cast<const float4*>(scr + i * 128 + n4);
+            float* o = a.out + (size_t)(a.row0 + b) * a.ldo + n;
+            if (vec && n + 3 < a.N) {
+              *reinterpret_cast<float4*>(o) = v;
+            } else {
+              o[0] = v.x;
+              if (n + 1 < a.N) o[1] = v.y;
+              if (n + 2 < a.N) o[2] = v.z;
+              if (n + 3 < a.N) o[3] = v.w;
+            }
+          }
         } else if (EPI == EPI_SWIGLU) {
+          // four consecutive channels of one batch row per thread and pass,
+          // written as 8-byte high and low words
           uint16_t* act = reinterpret_cast<uint16_t*>(a.act_hl);
-          for (int e = et; e < nb * 64; e += 128) {
-            const int i = e >> 6, c = e & 63, j = t * 64 + c, b = b0 + i;
-            if (j < a.N) {
-              const float g = scr[i * 128 + c], up = scr[i * 128 + 64 + c];
-              const float v = b < a.R ? g / (1.f + expf(-g)) * up : 0.f;   // padding rows stay finite
-              store_hl16(act + (size_t)(a.row0 + b) * a.ld_act + j,
-                         act + (size_t)(a.rp_all + a.row0 + b) * a.ld_act + j, v, a.hl_f16);
+          const bool vec = (a.ld_act & 3) == 0;
+          for (int e = et; e < nb * 16; e += 128) {
+            const int i = e >> 4, c4 = (e & 15) * 4, j = t * 64 + c4, b = b0 + i;
+            if (j >= a.N) continue;
+            const float4 g = *reinterpret_cast<const float4*>(scr + i * 128 + c4);
+            const float4 u = *reinterpret_cast<const float4*>(scr + i * 128 + 64 + c4);
+            const bool live = b < a.R;                    // padding rows stay finite (zero)
+            const float v[4] = {live ? ts_silu(g.x) * u.x : 0.f, live ? ts_silu(g.y) * u.y : 0.f,
+                                live ? ts_silu(g.z) * u.z : 0.f, live ? ts_silu(g.w) * u.w : 0.f};
+            uint16_t* hi = act + (size_t)(a.row0 + b) * a.ld_act + j;
+            uint16_t* lo = act + (size_t)(a.rp_all + a.row0 + b) * a.ld_act + j;
+            if (vec && j + 3 < a.N) {
+              uint32_t h[4], l[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) split_hl16(v[q], a.hl_f16, h[q], l[q]);
+              *reinterpret_cast<uint2*>(hi) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+              *reinterpret_cast<uint2*>(lo) = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+            } else {
+              for (int q = 0; q < 4 && j + q < a.N; ++q) store_hl16(hi + q, lo + q, v[q], a.hl_f16);
             }
           }
         } else {  // EPI_ARGMAX: the tile's best (value, index) per batch row
