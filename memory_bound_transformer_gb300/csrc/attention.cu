@@ -51,10 +51,14 @@ struct AttnShape {
   static constexpr size_t Q_BYTES = (size_t)16 * D * 4;
   static constexpr size_t T_BYTES = (size_t)kAttnTile * BROWB;
   static constexpr size_t R_BYTES = (size_t)kAttnTile * ROWB;
-  // BF16 caches: K and V tiles double-buffered in place. e4m3 caches: the raw
-  // tiles are double-buffered and widened into one FP16 K and V tile.
-  static constexpr int NBUF = KV8 ? 1 : 2;
-  static constexpr size_t SMEM = Q_BYTES + 2 * NBUF * T_BYTES + (KV8 ? 4 * R_BYTES : 0);
+  // BF16 caches: K and V tiles double-buffered in place. e4m3 caches: three
+  // stages of raw (K, V) tiles in flight (half the bytes of a BF16 tile, so
+  // more of them to keep as many bytes moving); K is widened into MMA
+  // fragments straight from its raw tile, V into one FP16 tile.
+  static constexpr int NBUF = KV8 ? 0 : 2;
+  static constexpr int NRAW = KV8 ? 3 : 0;
+  static constexpr int NPRO = KV8 ? NRAW : 2;          // tiles requested before the PDL wait
+  static constexpr size_t SMEM = Q_BYTES + (KV8 ? T_BYTES : 2 * NBUF * T_BYTES) + (size_t)NRAW * 2 * R_BYTES;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -170,9 +174,9 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
                                        int pos, int wblk) {
   using S = AttnShape<D, KV8>;
   float* qs = reinterpret_cast<float*>(smem);                        // [16][D], rows >= G are zero
-  unsigned char* kbf = smem + S::Q_BYTES;                             // [NBUF][tile][BROWB] BF16, swizzled
-  unsigned char* vbf = kbf + S::NBUF * S::T_BYTES;
-  unsigned char* raw = vbf + S::NBUF * S::T_BYTES;                    // e4m3 caches: [2][K|V][tile][ROWB]
+  unsigned char* kbf = smem + S::Q_BYTES;                             // BF16: [NBUF][tile][BROWB], swizzled
+  unsigned char* vbf = KV8 ? kbf : kbf + S::NBUF * S::T_BYTES;        // BF16: V tiles; e4m3: the FP16 V tile
+  unsigned char* raw = vbf + (KV8 ? S::T_BYTES : S::NBUF * S::T_BYTES);   // e4m3: [NRAW][K|V][tile][ROWB]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t4 = lane & 3;
 
@@ -205,18 +209,21 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
       const int tok = tok0 + row;
       const int blk = sblk[tok / kBlockTokens - blk0];
       const size_t off = (((size_t)blk * a.nkv + h) * kBlockTokens + (tok % kBlockTokens)) * S::ROWB + ch * 16;
-      const int sch = KV8 ? ch : (ch ^ (row & 7));                   // BF16 tiles are swizzled in place
-      cp_async16(kd + row * S::ROWB + sch * 16, kpool + off);
-      cp_async16(vd + row * S::ROWB + sch * 16, vpool + off);
+      // BF16 tiles are swizzled in place; the raw e4m3 K tile too (its
+      // fragments are read straight from it), the raw V tile is not
+      const int ksch = KV8 ? (ch ^ (row & (S::NCH - 1))) : (ch ^ (row & 7));
+      const int vsch = KV8 ? ch : (ch ^ (row & 7));
+      cp_async16(kd + row * S::ROWB + ksch * 16, kpool + off);
+      cp_async16(vd + row * S::ROWB + vsch * 16, vpool + off);
     }
     cp_async_commit();
   };
 
   __syncthreads();                                                    // block ids complete
-  for (int t = 0; t < 2 && t < ntiles; ++t) load_tile(t, t);
+  for (int t = 0; t < S::NPRO && t < ntiles; ++t) load_tile(t, t);
   // the next two tiles towards L2
-  if (ntiles > 2) {
-    const int j = 2 * kAttnTile / kBlockTokens + (tid >> 1);
+  if (ntiles > S::NPRO) {
+    const int j = S::NPRO * kAttnTile / kBlockTokens + (tid >> 1);
     if ((tid >> 1) < 2 * kAttnTile / kBlockTokens && j < blk1 - blk0) {
       const size_t off = ((size_t)sblk[j] * a.nkv + h) * kBlockTokens * S::ROWB;
       prefetch_l2((const unsigned char*)((tid & 1) ? a.vpool : a.kpool) + off, kBlockTokens * S::ROWB);
@@ -227,18 +234,18 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
 
   if (writer) {
     // the new token's K (rotated) and V go into the cache, and into the tile
-    // already requested when it is one of the first two
+    // already requested when it is one of those requested before the wait
     uint32_t kc = 0, vc = 0;
     write_new_kv<D, KV8>(a, b, h, pos, wblk, kc, vc);
-    if (tnew == 0 || tnew == 1) {
+    if (tnew >= 0 && tnew < S::NPRO) {
       cp_async_wait<0>();
       __syncthreads();                                                // the tile's copies have landed
       const int r = pos - (tok_begin + tnew * kAttnTile);
       if (tid < D) {
         if (KV8) {
-          unsigned char* rk = raw + (size_t)tnew * 2 * S::R_BYTES + (size_t)r * S::ROWB + tid;
-          rk[0] = (unsigned char)kc;
-          rk[S::R_BYTES] = (unsigned char)vc;
+          unsigned char* rk = raw + (size_t)tnew * 2 * S::R_BYTES + (size_t)r * S::ROWB;
+          rk[(((tid >> 4) ^ (r & (S::NCH - 1))) << 4) + (tid & 15)] = (unsigned char)kc;
+          rk[S::R_BYTES + tid] = (unsigned char)vc;
         } else {
           const size_t off = (size_t)tnew * S::T_BYTES + (size_t)r * S::BROWB +
                              (size_t)(((tid >> 3) ^ (r & 7)) * 16 + (tid & 7) * 2);
@@ -319,33 +326,43 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
     for (int i = 0; i < S::MT; ++i) o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
   }
 
+  constexpr int NR = S::NRAW > 0 ? S::NRAW : 1;
   for (int t = 0; t < ntiles; ++t) {
-    const int buf = t & 1;
-    // tiles 0 and 1 were requested up front; from tile 1 on, the tile after
-    // next goes into the buffer the previous tile has left
-    if (t >= 1 && t + 1 < ntiles) { load_tile(t + 1, buf ^ 1); cp_async_wait<1>(); }
-    else cp_async_wait<0>();
+    const int buf = KV8 ? t % NR : (t & 1);
+    if (KV8) {
+      // tiles 0 .. NRAW-1 were requested up front; from tile 1 on, tile
+      // t + NRAW - 1 goes into the stage tile t - 1 has left
+      if (t >= 1 && t + NR - 1 < ntiles) load_tile(t + NR - 1, (t + NR - 1) % NR);
+      const int after = min(NR - 1, ntiles - 1 - t);                   // copy groups still allowed in flight
+      if (after >= 2) cp_async_wait<2>();
+      else if (after == 1) cp_async_wait<1>();
+      else cp_async_wait<0>();
+    } else {
+      // tiles 0 and 1 were requested up front; from tile 1 on, the tile after
+      // next goes into the buffer the previous tile has left
+      if (t >= 1 && t + 1 < ntiles) { load_tile(t + 1, buf ^ 1); cp_async_wait<1>(); }
+      else cp_async_wait<0>();
+    }
     __syncthreads();
     const int tok0 = tok_begin + t * kAttnTile;
     const int nvalid = min(kAttnTile, min(seq, tok_end_blk) - tok0);   // this split's tokens only
     unsigned char* kt = kbf + (size_t)(KV8 ? 0 : buf) * S::T_BYTES;
     unsigned char* vt = vbf + (size_t)(KV8 ? 0 : buf) * S::T_BYTES;
+    const unsigned char* rk = raw + (size_t)buf * 2 * S::R_BYTES;      // e4m3: this tile's raw K, then V
     if (KV8) {
-      // widen the e4m3 tile to FP16 (exact, one conversion per two codes),
+      // widen the e4m3 V tile to FP16 (exact, one conversion per two codes),
       // swizzled; rows past the context are zero
-      const unsigned char* rk = raw + (size_t)buf * 2 * S::R_BYTES;
-      for (int i = tid; i < 2 * kAttnTile * S::NCH; i += kAttnThreads) {
-        const int which = i / (kAttnTile * S::NCH), j = i - which * kAttnTile * S::NCH;
-        const int row = j / S::NCH, ch = j - row * S::NCH;
+      for (int i = tid; i < kAttnTile * S::NCH; i += kAttnThreads) {
+        const int row = i / S::NCH, ch = i - row * S::NCH;
         uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
         if (row < nvalid) {
-          const uint4 c = *reinterpret_cast<const uint4*>(rk + which * S::R_BYTES + row * S::ROWB + ch * 16);
+          const uint4 c = *reinterpret_cast<const uint4*>(rk + S::R_BYTES + row * S::ROWB + ch * 16);
           lo = make_uint4(e4m3x2_to_h2bits(c.x), e4m3x2_to_h2bits(c.x >> 16), e4m3x2_to_h2bits(c.y),
                           e4m3x2_to_h2bits(c.y >> 16));
           hi = make_uint4(e4m3x2_to_h2bits(c.z), e4m3x2_to_h2bits(c.z >> 16), e4m3x2_to_h2bits(c.w),
                           e4m3x2_to_h2bits(c.w >> 16));
         }
-        unsigned char* dst = (which ? vt : kt) + row * S::BROWB;
+        unsigned char* dst = vt + row * S::BROWB;
         *reinterpret_cast<uint4*>(dst + (((2 * ch) ^ (row & 7)) * 16)) = lo;
         *reinterpret_cast<uint4*>(dst + (((2 * ch + 1) ^ (row & 7)) * 16)) = hi;
       }
@@ -373,8 +390,22 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
 #pragma unroll
         for (int kk = 0; kk < S::KSTEPS; ++kk) {
           uint32_t kf[4];
-          const int ch = 2 * kk + (lm >> 1);
-          ldsm_x4(kbase + krow * S::BROWB + ((ch ^ (krow & 7)) * 16), kf);
+          if (KV8) {
+            // the A fragment (rows g, g + 8; columns 2 t4, 2 t4 + 8 of this
+            // 16-wide k step) widened from the raw, swizzled K tile
+            const int ra = n0 + g, rb = ra + 8, c0 = 16 * kk + 2 * t4;
+            auto code2 = [&](int r, int c) {
+              return (uint32_t)*reinterpret_cast<const uint16_t*>(
+                  rk + r * S::ROWB + ((((c >> 4) ^ (r & (S::NCH - 1)))) << 4) + (c & 15));
+            };
+            kf[0] = e4m3x2_to_h2bits(code2(ra, c0));
+            kf[1] = e4m3x2_to_h2bits(code2(rb, c0));
+            kf[2] = e4m3x2_to_h2bits(code2(ra, c0 + 8));
+            kf[3] = e4m3x2_to_h2bits(code2(rb, c0 + 8));
+          } else {
+            const int ch = 2 * kk + (lm >> 1);
+            ldsm_x4(kbase + krow * S::BROWB + ((ch ^ (krow & 7)) * 16), kf);
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             mma_t<KV8>(st[nt], kf, qh[nt][kk][0], qh[nt][kk][1]);
@@ -443,7 +474,7 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
   }
 
   // merge the four warps' (m, l, o) per head and write this split's partial
-  float* sm_m = reinterpret_cast<float*>(kbf);                        // [4][16]
+  float* sm_m = reinterpret_cast<float*>(smem + S::Q_BYTES);          // [4][16]
   float* sm_l = sm_m + 4 * 16;
   float* sm_o = sm_l + 4 * 16;                                        // [4][16][D]
 #pragma unroll
