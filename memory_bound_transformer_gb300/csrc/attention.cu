@@ -230,6 +230,22 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
     }
   }
 
+  // the query rotation's cos/sin at this row's position: a step input and a
+  // table, neither written by the previous kernel, so loaded before the wait
+  constexpr int QE = 16 * (D / 2) / kAttnThreads;                     // elements per thread at G <= 16
+  float2 tc[QE];
+  if (a.qkv) {
+    const int half = D / 2;
+    int qpos = a.positions[b];
+    if (qpos < 0 || qpos >= a.max_pos) qpos = 0;
+    const float2* cs = a.rope + (size_t)qpos * half;
+#pragma unroll
+    for (int j = 0; j < QE; ++j) {
+      const int e = tid + j * kAttnThreads;
+      tc[j] = e < G * half ? cs[e % half] : make_float2(0.f, 0.f);
+    }
+  }
+
   pdl_wait();
 
   if (writer) {
@@ -265,25 +281,19 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
     // RoPE (rotate-half: element i pairs with i + D/2) straight from the QKV
     // projection's partial sums
     const int half = D / 2;
-    int qpos = a.positions[b];
-    if (qpos < 0 || qpos >= a.max_pos) qpos = 0;
     const float* src = a.qkv + (size_t)b * a.ld_qkv + (size_t)h * G * D;
-    const float2* cs = a.rope + (size_t)qpos * half;
     // every load of the thread's elements first (one round trip), then the rotation
-    constexpr int QE = 16 * (D / 2) / kAttnThreads;               // elements per thread at G <= 16
     float x1[QE], x2[QE];
-    float2 tc[QE];
 #pragma unroll
     for (int j = 0; j < QE; ++j) {
       const int e = tid + j * kAttnThreads;
-      x1[j] = 0.f; x2[j] = 0.f; tc[j] = make_float2(0.f, 0.f);
+      x1[j] = 0.f; x2[j] = 0.f;
       if (e < G * half) {
         const int gg = e / half, i = e - gg * half;
         for (int s2 = 0; s2 < a.qkv_nsplit; ++s2) {
           x1[j] += src[(size_t)s2 * a.qkv_split_stride + gg * D + i];
           x2[j] += src[(size_t)s2 * a.qkv_split_stride + gg * D + i + half];
         }
-        tc[j] = cs[i];
       }
     }
 #pragma unroll
