@@ -30,6 +30,7 @@ namespace mbt {
 constexpr int kAttnThreads = 128;
 constexpr int kAttnTile = 64;      // tokens per shared-memory tile (4 blocks)
 constexpr int kMaxSplitBlocks = 512;   // KV blocks one split may cover (8192 tokens)
+constexpr int kAttnCluster = 8;        // most splits per (row, KV head): a portable cluster
 
 __device__ __forceinline__ void cp_async16(void* s, const void* g) {
   const unsigned sa = (unsigned)__cvta_generic_to_shared(s);
@@ -115,6 +116,28 @@ __device__ __forceinline__ void mma_t(float (&d)[4], const uint32_t (&a)[4], uin
 }
 
 
+// All threads of all CTAs of the cluster: writes to shared memory before it
+// are visible to every CTA of the cluster after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Loads from the shared memory of CTA `rank` of the cluster, at the address
+// that p has in this CTA.
+__device__ __forceinline__ float ld_dsmem_f32(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 ld_dsmem_f2(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(r) : "memory");
+  return v;
+}
+
 // Fused "RoPE + KV-cache write" ("Kernels, Fusion & CUDA Graphs", "Fix 1:
 // kernel fusion"): rotate the new token's key for KV head h and store it and its
 // value at block bt[p / 16], slot p % 16, rounded to the cache format. Thread
@@ -168,10 +191,10 @@ __device__ __forceinline__ void write_new_kv(const AttnArgs& a, int b, int h, in
 // before the wait on the QKV projection. The new token's row, which this CTA
 // writes after the wait, is patched into a tile already in shared memory
 // (tiles loaded later read it from the cache).
-template <int D, int KV8, int NT>
+template <int D, int KV8, int NT, int CL>
 __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, int b, int h, int sp,
                                        int G, size_t head0, int seq, int blk0, int blk1, bool writer,
-                                       int pos, int wblk) {
+                                       int pos, int wblk, float2* cl_ml) {
   using S = AttnShape<D, KV8>;
   float* qs = reinterpret_cast<float*>(smem);                        // [16][D], rows >= G are zero
   unsigned char* kbf = smem + S::Q_BYTES;                             // BF16: [NBUF][tile][BROWB], swizzled
@@ -518,8 +541,59 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
         acc += sm_o[(w * 16 + hr) * D + d] * sc;
       }
     }
-    a.part_o[((head0 + hr) * a.nsplit + sp) * D + d] = acc;
-    if (d == 0) a.part_ml[(head0 + hr) * a.nsplit + sp] = make_float2(L > 0.f ? M : -INFINITY, L);
+    if (CL) {
+      // the cluster's merging CTA reads it from this CTA's shared memory (the
+      // query tile, no longer needed)
+      qs[hr * D + d] = acc;
+      if (d == 0) cl_ml[hr] = make_float2(L > 0.f ? M : -INFINITY, L);
+    } else {
+      a.part_o[((head0 + hr) * a.nsplit + sp) * D + d] = acc;
+      if (d == 0) a.part_ml[(head0 + hr) * a.nsplit + sp] = make_float2(L > 0.f ? M : -INFINITY, L);
+    }
+  }
+}
+
+// Merge of the splits of one (row, KV head) inside a thread-block cluster:
+// every split left its (max, mass) pairs and unnormalised outputs in its own
+// shared memory; the cluster's first CTA reads them through distributed
+// shared memory, in split order, and writes the group's output.
+template <int D>
+__device__ __forceinline__ void merge_cluster(const AttnArgs& a, const float* qs, const float2* ml, int G,
+                                              size_t head0, int ns) {
+  for (int e = threadIdx.x; e < G * D; e += kAttnThreads) {
+    const int hr = e / D, d = e - hr * D;
+    // every split's (max, mass) and output first, all loads in flight at once
+    float2 v[kAttnCluster];
+    float ov[kAttnCluster];
+#pragma unroll
+    for (int sp = 0; sp < kAttnCluster; ++sp) {
+      v[sp] = sp < ns ? ld_dsmem_f2(ml + hr, (uint32_t)sp) : make_float2(-INFINITY, 0.f);
+      ov[sp] = sp < ns ? ld_dsmem_f32(qs + hr * D + d, (uint32_t)sp) : 0.f;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int sp = 0; sp < kAttnCluster; ++sp) if (v[sp].y > 0.f) M = fmaxf(M, v[sp].x);
+    float L = 0.f, acc = 0.f;
+#pragma unroll
+    for (int sp = 0; sp < kAttnCluster; ++sp) {
+      if (v[sp].y > 0.f) {
+        const float w = exp2f(v[sp].x - M);
+        L += w * v[sp].y;
+        acc += w * ov[sp];
+      }
+    }
+    const float o = L > 0.f ? acc * (a.v_scale / L) : 0.f;
+    const size_t oi = (head0 + hr) * D + d;
+    if (a.out) a.out[oi] = o;
+    if (a.out_hl) {                                // high/low 16-bit rows for the tensor-core GEMM
+      const size_t row = oi / ((size_t)a.nq * D), col = oi % ((size_t)a.nq * D);
+      uint16_t* hl = reinterpret_cast<uint16_t*>(a.out_hl);
+      const float hv = a.hl_f16 ? __half2float(__float2half_rn(o)) : __bfloat162float(__float2bfloat16_rn(o));
+      hl[row * a.nq * D + col] = a.hl_f16 ? __half_as_ushort(__float2half_rn(o))
+                                          : __bfloat16_as_ushort(__float2bfloat16_rn(o));
+      hl[(a.rp_hl + row) * a.nq * D + col] = a.hl_f16 ? __half_as_ushort(__float2half_rn(o - hv))
+                                                       : __bfloat16_as_ushort(__float2bfloat16_rn(o - hv));
+    }
   }
 }
 
@@ -612,7 +686,7 @@ __device__ __forceinline__ void merge_splits(const AttnArgs& a, unsigned char* s
 
 // One work item: split sp of the context of (row b, KV head h), and the merge
 // of that group's splits when this is the last of them to finish.
-template <int D, int KV8, int NT>
+template <int D, int KV8, int NT, int CL>
 __device__ __forceinline__ void attn_item(const AttnArgs& a, unsigned char* smem, int sp, int h, int b) {
   using S = AttnShape<D, KV8>;
   const int G = a.nq / a.nkv;
@@ -645,13 +719,28 @@ __device__ __forceinline__ void attn_item(const AttnArgs& a, unsigned char* smem
     }
   }
 
+  __shared__ float2 cl_ml[16];                                        // cluster merge: (max, mass) per head
   if (blk0 < nblk) {
-    attend<D, KV8, NT>(a, smem, b, h, sp, G, head0, seq, blk0, blk1, writer, pos, wblk);
+    attend<D, KV8, NT, CL>(a, smem, b, h, sp, G, head0, seq, blk0, blk1, writer, pos, wblk, cl_ml);
   } else {
     pdl_wait();
     uint32_t kc, vc;
     if (writer) write_new_kv<D, KV8>(a, b, h, pos, wblk, kc, vc);
-    if (tid < G) a.part_ml[(head0 + tid) * a.nsplit + sp] = make_float2(-INFINITY, 0.f);
+    if (CL) {
+      if (tid < G) cl_ml[tid] = make_float2(-INFINITY, 0.f);
+    } else {
+      if (tid < G) a.part_ml[(head0 + tid) * a.nsplit + sp] = make_float2(-INFINITY, 0.f);
+    }
+  }
+
+  if (CL) {
+    // the splits of this (row, KV head) are one cluster: merge through
+    // distributed shared memory, then keep every CTA resident until the
+    // merging CTA has read it
+    cluster_sync_all();
+    if (sp == 0) merge_cluster<D>(a, reinterpret_cast<const float*>(smem), cl_ml, G, head0, a.nsplit);
+    cluster_sync_all();
+    return;
   }
 
   // ticket: the last CTA of this (row, KV head) merges the splits
@@ -675,11 +764,11 @@ __device__ __forceinline__ void attn_item(const AttnArgs& a, unsigned char* smem
 // ones finish, which already balances splits of unequal length (a persistent
 // grid claiming items from an atomic counter was measured slower: 91 vs 74 us
 // per batch-64 8B-class layer).
-template <int D, int KV8, int NT>
+template <int D, int KV8, int NT, int CL>
 __global__ void __launch_bounds__(kAttnThreads, MBT_ATTN_MINB) attn_split_kernel(const AttnArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   pdl_launch_dependents();
-  attn_item<D, KV8, NT>(a, smem, blockIdx.x, blockIdx.y, blockIdx.z);
+  attn_item<D, KV8, NT, CL>(a, smem, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
 void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nsplit) {
@@ -695,6 +784,9 @@ void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nspli
   const int min_per = MBT_ATTN_MIN_TILES * kAttnTile / kBlockTokens;
   if (per < min_per) per = min_per;
   if (per > max_blocks) per = max_blocks;
+  // at most kAttnCluster splits, so that a (row, KV head) is one thread-block
+  // cluster and its splits merge through distributed shared memory
+  if (per < (max_blocks + kAttnCluster - 1) / kAttnCluster) per = (max_blocks + kAttnCluster - 1) / kAttnCluster;
   if (per > kMaxSplitBlocks) per = kMaxSplitBlocks;
   if (per < 1) per = 1;
   *bps = per;
@@ -702,49 +794,55 @@ void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nspli
 }
 
 namespace {
-template <int D, int KV8, int NT>
-void* attn_fn() { return (void*)attn_split_kernel<D, KV8, NT>; }
+template <int D, int KV8, int NT, int CL>
+void* attn_fn() { return (void*)attn_split_kernel<D, KV8, NT, CL>; }
+template <int D, int KV8, int CL>
+void* attn_fn_nt(int nt) { return nt == 2 ? attn_fn<D, KV8, 2, CL>() : attn_fn<D, KV8, 1, CL>(); }
 template <int D, int KV8>
-void* attn_fn_nt(int nt) { return nt == 2 ? attn_fn<D, KV8, 2>() : attn_fn<D, KV8, 1>(); }
-// query heads per KV head: up to 8 in one n-tile of the MMA, up to 16 in two
-void* attn_pick(int d, int kv8, int nt, size_t* smem) {
+void* attn_fn_cl(int nt, int cl) { return cl ? attn_fn_nt<D, KV8, 1>(nt) : attn_fn_nt<D, KV8, 0>(nt); }
+// query heads per KV head: up to 8 in one n-tile of the MMA, up to 16 in two;
+// cl: the splits of a (row, KV head) form one cluster
+void* attn_pick(int d, int kv8, int nt, int cl, size_t* smem) {
   if (d == 64) {
     *smem = kv8 ? AttnShape<64, 1>::SMEM : AttnShape<64, 0>::SMEM;
-    return kv8 ? attn_fn_nt<64, 1>(nt) : attn_fn_nt<64, 0>(nt);
+    return kv8 ? attn_fn_cl<64, 1>(nt, cl) : attn_fn_cl<64, 0>(nt, cl);
   }
   *smem = kv8 ? AttnShape<128, 1>::SMEM : AttnShape<128, 0>::SMEM;
-  return kv8 ? attn_fn_nt<128, 1>(nt) : attn_fn_nt<128, 0>(nt);
+  return kv8 ? attn_fn_cl<128, 1>(nt, cl) : attn_fn_cl<128, 0>(nt, cl);
 }
 }  // namespace
 
 cudaError_t attn_init() {
   for (int d : {64, 128})
     for (int kv8 = 0; kv8 < 2; ++kv8)
-      for (int nt = 1; nt <= 2; ++nt) {
-        size_t sm;
-        void* fn = attn_pick(d, kv8, nt, &sm);
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        if (e != cudaSuccess) return e;
-      }
+      for (int nt = 1; nt <= 2; ++nt)
+        for (int cl = 0; cl < 2; ++cl) {
+          size_t sm;
+          void* fn = attn_pick(d, kv8, nt, cl, &sm);
+          cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+          if (e != cudaSuccess) return e;
+        }
   return cudaSuccess;
 }
 
 size_t attn_smem_bytes(int d, int kv8, int G) {
   size_t sm;
-  attn_pick(d, kv8, G > 8 ? 2 : 1, &sm);
+  attn_pick(d, kv8, G > 8 ? 2 : 1, 0, &sm);
   return sm + sizeof(int) * kMaxSplitBlocks + 16;     // + the staged block ids and the ticket flag
 }
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
   size_t sm;
-  void* fn = attn_pick(a.d, a.kv_fp8, (a.nq / a.nkv) > 8 ? 2 : 1, &sm);
+  const int cl = a.nsplit >= 4 && a.nsplit <= kAttnCluster;
+  void* fn = attn_pick(a.d, a.kv_fp8, (a.nq / a.nkv) > 8 ? 2 : 1, cl, &sm);
   // the merge needs the group's weights and at least one split of partials in shared memory
   const int G = a.nq / a.nkv;
   const size_t w_bytes = (((size_t)G * a.nsplit * 8 + 15) & ~(size_t)15) + (((size_t)G * a.nsplit * 4 + 15) & ~(size_t)15);
   if (G * a.d > kMergeMaxE * kAttnThreads || w_bytes + (size_t)2 * G * a.d * 4 > sm) return cudaErrorInvalidValue;
   AttnArgs args = a;
   void* params[] = {&args};
-  return launch_ex(fn, dim3(a.nsplit, a.nkv, a.B), dim3(kAttnThreads), sm, s, params, !a.no_pdl, a.carveout > 0 ? a.carveout : -1);
+  return launch_ex(fn, dim3(a.nsplit, a.nkv, a.B), dim3(kAttnThreads), sm, s, params, !a.no_pdl,
+                   a.carveout > 0 ? a.carveout : -1, cl ? a.nsplit : 0);
 }
 
 }  // namespace mbt

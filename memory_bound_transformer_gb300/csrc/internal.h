@@ -17,8 +17,9 @@ enum Prologue { PRO_X = 0, PRO_NORM = 1 };
 // Launch with programmatic dependent launch allowed (pdl = true) or as an
 // ordinary stream-ordered launch; carveout >= 0 sets the shared-memory share
 // of the unified L1 (percent) for this launch.
+// cluster_x > 0: thread-block clusters of cluster_x CTAs along x
 cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args,
-                      bool pdl, int carveout);
+                      bool pdl, int carveout, int cluster_x = 0);
 inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args,
                               int carveout = -1) {
   return launch_ex(fn, grid, block, smem, s, args, true, carveout);
