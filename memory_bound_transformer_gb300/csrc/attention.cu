@@ -12,9 +12,12 @@
 // incrementally, no score matrix in HBM). One CTA per (split of the context,
 // KV head, row) so that a batch-1 step still spreads the KV stream over all SMs;
 // each CTA reads its KV blocks once for all query heads of the group, keeps a
-// running max and sum per head and writes an unnormalised partial. The last
-// CTA of a (row, KV head) to finish -- found with an atomic ticket, nothing
-// waits -- merges that group's splits.
+// running max and sum per head and writes an unnormalised partial. With four
+// to eight splits the splits of a (row, KV head) are one thread-block cluster
+// and the first of them merges the others' partials through distributed
+// shared memory after a cluster barrier; otherwise the last CTA of the group to
+// finish -- found with an atomic ticket, nothing waits -- merges them from
+// global memory.
 #include "common.cuh"
 #include "internal.h"
 
