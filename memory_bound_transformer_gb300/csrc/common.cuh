@@ -87,6 +87,43 @@ __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
   return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
 }
 
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  return __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3)));
+}
+
+// Activation rows for e4m3 x e4m3 tensor-core products: four e4m3 terms per
+// value, x = s * (c0 + c1 / 16 + c2 / 256 + c3 / 4096) + e, with s a power of
+// two per row such that max |x| / s < 448. Each step rounds the scaled residual
+// to e4m3 and carries the rest, times 16, to the next code; the residual is
+// exact in fp32 (a rounding to the nearest e4m3 value is within a factor
+// 1 +- 1/16 of the value, or on a grid no finer than the value's own), so
+// |e| <= |x| / 2^16 plus, for values far below the row's largest, s / 2^22.
+constexpr int kTerms = 4;
+
+// Scale of a row whose largest magnitude is m: s = 2^e with m / s in [224, 448);
+// 1 for an all-zero row; NaN when m is not finite (the products then carry it).
+__device__ __forceinline__ void term_scale(float m, float& s, float& inv) {
+  if (!(m <= 3.0e38f)) { s = inv = __int_as_float(0x7fc00000); return; }
+  if (m == 0.f) { s = inv = 1.f; return; }
+  int e;
+  frexpf(m * (1.f / 448.f), &e);
+  s = ldexpf(1.f, e);
+  inv = ldexpf(1.f, -e);
+}
+
+// The four codes of x (term j in byte j) given 1 / s.
+__device__ __forceinline__ uint32_t split_terms(float x, float inv_s) {
+  float r = x * inv_s;
+  uint32_t out = 0;
+#pragma unroll
+  for (int j = 0; j < kTerms; ++j) {
+    const uint32_t c = f32_to_e4m3(r);
+    out |= c << (8 * j);
+    r = (r - e4m3_to_f32(c)) * 16.f;
+  }
+  return out;
+}
+
 // ---------------------------------------------------------------------------
 // reductions
 
@@ -104,6 +141,17 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // Block-wide sum for blockDim.x a multiple of 32 (<= 1024). `scratch` holds
 // >= 32 floats. Every thread returns the total.
+__device__ __forceinline__ float block_max(float v, float* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  const int nw = blockDim.x >> 5;
+  float t = lane < nw ? scratch[lane] : 0.f;
+  return warp_max(t);
+}
+
 __device__ __forceinline__ float block_sum(float v, float* scratch) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   v = warp_sum(v);

@@ -115,11 +115,11 @@ int gemv_max_rows(int epi, int K, int pro = PRO_X);
 cudaError_t gemv_launch(int epi, int pro, const GemvArgs& a, const GemvLaunch& g, cudaStream_t s);
 cudaError_t gemv_init();   // raise dynamic shared-memory limits (once per process)
 
-// Tensor-core skinny GEMMs (batch 16..128): y = W x with x given as
-// [2 * Rp][K] 16-bit rows (rows 0..Rp-1 the high parts, Rp..2Rp-1 the low
-// parts of the fp32 activations; BF16 for BF16 weights, FP16 for e4m3 weights,
-// whose codes are widened to FP16 in shared memory). Tensor maps are opaque
-// 128-byte blobs.
+// Tensor-core skinny GEMMs (batch 2..128): y = W x. BF16 weights: x given as
+// [2 * Rp][K] BF16 rows (rows 0..Rp-1 the high parts, Rp..2Rp-1 the low parts
+// of the fp32 activations). e4m3 weights: x given as four e4m3 term rows
+// [4][Rp][K] and one power-of-two scale per row (split_terms), multiplied
+// e4m3 x e4m3. Tensor maps are opaque 128-byte blobs.
 struct TmaMap { alignas(64) unsigned char bytes[128]; };
 struct TcArgs {
   int N, K, R, Rp;            // output channels (SWIGLU: ffn), K, live rows of this launch, their padded count
@@ -132,12 +132,14 @@ struct TcArgs {
   float* logits; int ldl; ArgmaxPart* part; int part_ld;   // EPI_ARGMAX
   uint32_t* err;
   GumbelArgs gum;                                      // EPI_ARGMAX: draw instead of arg-max when gum.on
+  const float* x_scale;                                // e4m3 weights: the term rows' scales [rp_all]
 };
 cudaError_t tc_init();
 cudaError_t tc_make_map(void* map, const void* base, int rows, int K, int box_rows);
 // Stream-K tensor-core GEMM (tc_stream.cu): one CTA per SM, at most 64 rows
-// (a.R <= a.Rp <= 64, a.Rp a multiple of 16) per launch; x as 16-bit high rows [rp_all][K] followed by
-// low rows, read from row a.row0 with boxes of a.Rp rows. Outputs are complete
+// (a.R <= a.Rp <= 64, a.Rp a multiple of 16) per launch; x as XR row blocks of
+// [rp_all][K] (BF16 high then low rows; e4m3 terms 0..3, with a.x_scale), read
+// from row a.row0 of each block with boxes of a.Rp rows. Outputs are complete
 // sums (no K split): PARTIAL out[(row0 + b) * ldo + n].
 cudaError_t ts_init();
 cudaError_t ts_launch(int wt, int epi, const void* mapW, const void* mapX, const TcArgs& a, int num_sms,
@@ -145,9 +147,13 @@ cudaError_t ts_launch(int wt, int epi, const void* mapW, const void* mapX, const
 int ts_tiles(int epi, int N);
 size_t ts_scratch_floats(int num_sms);
 constexpr int kTsMaxRows = 64;
-// e4m3 weights: [rows][K] codes, 128-code x 64-row boxes with 128-byte
-// swizzle; the activations as FP16 high/low rows (map from tc_make_map)
-cudaError_t tc_make_map_u8(void* map, const void* base, int rows, int K);
+// e4m3 codes [rows][K] (weights, with 64-row boxes, or activation term rows,
+// with boxes of a launch's padded rows), 128-code boxes, 128-byte swizzle
+cudaError_t tc_make_map_u8(void* map, const void* base, int rows, int K, int box_rows);
+// fp32 rows x (or 16-bit high/low rows hl when x is null) -> term rows
+// t [4][Rp][K] and scales ts[Rp]; rows B..Rp-1 zero with scale 1
+cudaError_t tc_to_terms(const float* x, const bf16* hl, int f16, int B, int Rp, int K, uint8_t* t, float* ts,
+                        cudaStream_t s);
 cudaError_t tc_to_hl(const float* x, int B, int Rp, int K, bf16* hl, cudaStream_t s, int f16 = 0);
 cudaError_t tc_from_hl(const bf16* hl, int B, int Rp, int N, float* out, cudaStream_t s, int f16 = 0);
 
@@ -168,6 +174,9 @@ struct AddNormArgs {
   const bf16* gamma; float eps; float* y;
   bf16* y_hl; int rp;
   int hl_f16;               // y_hl rows as FP16 (for e4m3 weights) rather than BF16
+  // when set (and y_hl null): y as four e4m3 term rows [4][rp][H] with one
+  // power-of-two scale per row, y_s[rp] (rows B..rp-1: zero codes, scale 1)
+  uint8_t* y_t; float* y_s;
 };
 cudaError_t launch_add_rmsnorm(const AddNormArgs& a, cudaStream_t s);
 

@@ -124,11 +124,61 @@ __device__ __forceinline__ void norm_store_hl(const float4 (&v)[kNormMaxV], floa
   }
 }
 
+// y as four e4m3 term rows plus the row's power-of-two scale (for e4m3 x e4m3
+// tensor-core products): one pass for the largest |y|, one to split.
+__device__ __forceinline__ void norm_store_terms(const float4 (&v)[kNormMaxV], float ss, int H,
+                                                const bf16* __restrict__ gamma, float eps, uint8_t* t_row,
+                                                size_t t_stride, float* s_out, float* scratch) {
+  const float tot = block_sum(ss, scratch);
+  const float inv = 1.0f / sqrtf(tot / (float)H + eps);
+  const int nv = H / 4;
+  const uint2* g2 = reinterpret_cast<const uint2*>(gamma);
+  float o[kNormMaxV][4];
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < kNormMaxV; ++j) {
+    const int i = threadIdx.x + j * blockDim.x;
+    if (i < nv) {
+      const uint2 g = g2[i];
+      o[j][0] = v[j].x * inv * bf16_lo(g.x); o[j][1] = v[j].y * inv * bf16_hi(g.x);
+      o[j][2] = v[j].z * inv * bf16_lo(g.y); o[j][3] = v[j].w * inv * bf16_hi(g.y);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(o[j][e]));
+    }
+  }
+  m = block_max(m, scratch);
+  float sc, isc;
+  term_scale(m, sc, isc);
+  if (threadIdx.x == 0) *s_out = sc;
+#pragma unroll
+  for (int j = 0; j < kNormMaxV; ++j) {
+    const int i = threadIdx.x + j * blockDim.x;
+    if (i < nv) {
+      uint32_t c[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c[e] = split_terms(o[j][e], isc);
+#pragma unroll
+      for (int tj = 0; tj < kTerms; ++tj) {
+        const uint32_t w = ((c[0] >> (8 * tj)) & 255u) | (((c[1] >> (8 * tj)) & 255u) << 8) |
+                           (((c[2] >> (8 * tj)) & 255u) << 16) | (((c[3] >> (8 * tj)) & 255u) << 24);
+        reinterpret_cast<uint32_t*>(t_row + tj * t_stride)[i] = w;
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(1024) add_rmsnorm_kernel(const AddNormArgs a) {
   __shared__ float scratch[32];
   const int b = blockIdx.x;
   pdl_launch_dependents();
   pdl_wait();
+  if (b >= a.B && a.y_t) {                          // padding rows of the term output
+    for (int tj = 0; tj < kTerms; ++tj)
+      for (int i = threadIdx.x; i < a.H / 4; i += blockDim.x)
+        reinterpret_cast<uint32_t*>(a.y_t + ((size_t)tj * a.rp + b) * a.H)[i] = 0u;
+    if (threadIdx.x == 0) a.y_s[b] = 1.f;
+    return;
+  }
   if (b >= a.B) {                                   // padding rows of the high/low output
     const bf16 z = __float2bfloat16_rn(0.f);
     for (int i = threadIdx.x; i < a.H; i += blockDim.x) {
@@ -161,7 +211,9 @@ __global__ void __launch_bounds__(1024) add_rmsnorm_kernel(const AddNormArgs a) 
     const int i = threadIdx.x + j * blockDim.x;
     if (i < nv) r[i] = v[j];
   }
-  if (a.y_hl) {
+  if (a.y_t)
+    norm_store_terms(v, ss, a.H, a.gamma, a.eps, a.y_t + (size_t)b * a.H, (size_t)a.rp * a.H, a.y_s + b, scratch);
+  else if (a.y_hl) {
     uint16_t* hl = reinterpret_cast<uint16_t*>(a.y_hl);
     norm_store_hl(v, ss, a.H, a.gamma, a.eps, hl + (size_t)b * a.H, hl + (size_t)(a.rp + b) * a.H, scratch, a.hl_f16);
   }
@@ -195,7 +247,8 @@ cudaError_t launch_add_rmsnorm(const AddNormArgs& a, cudaStream_t s) {
   if (a.H % 4 || a.H > 4 * kNormMaxV * 1024) return cudaErrorInvalidValue;
   AddNormArgs args = a;
   void* p[] = {&args};
-  const int rows = a.y_hl ? a.rp : a.B;
+  if (a.y_t && (!a.y_s || a.y_hl)) return cudaErrorInvalidValue;
+  const int rows = (a.y_hl || a.y_t) ? a.rp : a.B;
   return launch_pdl((const void*)add_rmsnorm_kernel, dim3(rows), dim3(norm_threads(a.H)), 0, s, p);
 }
 

@@ -173,8 +173,9 @@ int op_gemv_norm(int epi, int w_dtype, const void* W, const float* scales, int N
 
 namespace {
 // Shared body of the BF16 (f8 = 0) and e4m3 (f8 = 1) tensor-core entry points:
-// x split into 16-bit high/low rows, the stream-K GEMM in launches of at most
-// 64 rows (the decode step's geometry), SwiGLU rows read back to fp32.
+// x split into BF16 high/low rows (BF16 weights) or e4m3 term rows and row
+// scales (e4m3 weights), the stream-K GEMM in launches of at most 64 rows (the
+// decode step's geometry), SwiGLU rows (16-bit high/low) read back to fp32.
 int gemm_tc_impl(int f8, int epi, const void* W, const float* scales, int N, int K, const float* x, int B,
                  int ksplit, float* out, float* act, float* logits, int32_t* next_ids, uint32_t* err,
                  void* stream) {
@@ -195,31 +196,36 @@ int gemm_tc_impl(int f8, int epi, const void* W, const float* scales, int N, int
   const int Rp = (B + 15) / 16 * 16;
   const int wrows = epi == EPI_SWIGLU ? 2 * N : N;
   const int tiles = ts_tiles(epi, N);
-  const size_t b_x = (size_t)2 * Rp * K * 2, b_a = epi == EPI_SWIGLU ? (size_t)2 * Rp * N * 2 : 0;
+  const size_t b_x = (size_t)2 * Rp * K * 2 + (size_t)Rp * 4, b_a = epi == EPI_SWIGLU ? (size_t)2 * Rp * N * 2 : 0;
   const size_t b_p = epi == EPI_ARGMAX ? (size_t)tiles * B * sizeof(ArgmaxPart) : 0;
   const size_t b_s = ts_scratch_floats(nsm) * 4, b_t = (size_t)tiles * 4;
   auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
   char* scratch = nullptr;
   if (cudaMallocAsync((void**)&scratch, al(b_x) + al(b_a) + al(b_p) + al(b_s) + al(b_t), s) != cudaSuccess)
     return MBT_ERR_OOM;
-  bf16* xhl = (bf16*)scratch;
+  bf16* xhl = (bf16*)scratch;                    // BF16 high/low rows, or e4m3 term rows (same bytes)
+  float* xsc = (float*)(scratch + (size_t)2 * Rp * K * 2);
   bf16* ahl = (bf16*)(scratch + al(b_x));
   ArgmaxPart* part = (ArgmaxPart*)((char*)ahl + al(b_a));
   float* tss = (float*)((char*)part + al(b_p));
   int* tickets = (int*)((char*)tss + al(b_s));
   TmaMap wm;
-  const cudaError_t me = f8 ? tc_make_map_u8(&wm, W, wrows, K) : tc_make_map(&wm, W, wrows, K, 64);
+  const cudaError_t me = f8 ? tc_make_map_u8(&wm, W, wrows, K, 64) : tc_make_map(&wm, W, wrows, K, 64);
   if (me != cudaSuccess) rc = MBT_ERR_BAD_ARG;
   if (rc == MBT_OK && cudaMemsetAsync(tickets, 0, b_t, s) != cudaSuccess) rc = MBT_ERR_CUDA;
-  if (rc == MBT_OK && tc_to_hl(x, B, Rp, K, xhl, s, f8) != cudaSuccess) rc = MBT_ERR_CUDA;
+  if (rc == MBT_OK) {
+    const cudaError_t e = f8 ? tc_to_terms(x, nullptr, 0, B, Rp, K, (uint8_t*)xhl, xsc, s) : tc_to_hl(x, B, Rp, K, xhl, s, 0);
+    if (e != cudaSuccess) rc = MBT_ERR_CUDA;
+  }
   for (int r0 = 0; r0 < B && rc == MBT_OK; r0 += kTsMaxRows) {
     const int rl = std::min(kTsMaxRows, B - r0), rcp = (rl + 15) / 16 * 16;
     TmaMap xm;
-    if (tc_make_map(&xm, xhl, 2 * Rp, K, rcp) != cudaSuccess) { rc = MBT_ERR_BAD_ARG; break; }
+    const cudaError_t xe = f8 ? tc_make_map_u8(&xm, xhl, kTerms * Rp, K, rcp) : tc_make_map(&xm, xhl, 2 * Rp, K, rcp);
+    if (xe != cudaSuccess) { rc = MBT_ERR_BAD_ARG; break; }
     TcArgs a = {};
     a.N = N; a.K = K; a.R = rl; a.Rp = rcp; a.row0 = r0; a.rp_all = Rp; a.scale = scales;
     a.out = out; a.split_stride = (long long)B * N; a.ldo = N;
-    a.act_hl = ahl; a.ld_act = N; a.hl_f16 = f8;
+    a.act_hl = ahl; a.ld_act = N; a.hl_f16 = f8; a.x_scale = f8 ? xsc : nullptr;
     a.logits = logits; a.ldl = N; a.part = part; a.part_ld = B; a.err = err;
     a.ts_scratch = tss; a.ts_tickets = tickets; a.tickets_cap = tiles;
     if (ts_launch(f8 ? W_E4M3 : W_BF16, epi, &wm, &xm, a, nsm, s) != cudaSuccess) rc = MBT_ERR_CUDA;

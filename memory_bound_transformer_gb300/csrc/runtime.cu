@@ -79,8 +79,12 @@ struct Workspace {
   int* sched = nullptr;                              // GEMV work-queue counters, zeroed each step
   int* tickets = nullptr; int tickets_cap = 0;       // tensor-core GEMM per-tile tickets (right after sched)
   float* ts_scratch = nullptr;                       // tensor-core GEMM partial sums
-  int rp_cap = 0;                                    // tensor-core path: BF16 high/low rows
+  int rp_cap = 0;                                    // tensor-core path: 16-bit high/low rows
   bf16* x_hl = nullptr; bf16* o_hl = nullptr; bf16* act_hl = nullptr;
+  // e4m3 weights: the projections' inputs as e4m3 term rows [4][rp_cap][K]
+  // (the norm output reuses x_hl's bytes) and their row scales
+  uint8_t* o_t = nullptr; uint8_t* act_t = nullptr;
+  float* x_s = nullptr; float* o_s = nullptr; float* act_s = nullptr;
   float* q = nullptr;                                // prefill: rotated queries [cap][nq * d]
   int* pf_tok = nullptr; int* pf_pos = nullptr; int* pf_sl = nullptr;   // prefill rows [cap]
   int* pf_bt = nullptr;                              // prefill block tables [cap][mbs_cap]
@@ -250,6 +254,9 @@ int ensure_ws(mbt_model* m, Workspace& w, int R, int mbs) {
   const size_t b_xhl = (size_t)2 * rp_cap * H * 2, b_ohl = (size_t)2 * rp_cap * Q * 2;
   const size_t b_ahl = (size_t)2 * rp_cap * F * 2;
   const size_t o_xhl = take(b_xhl), o_ohl = take(b_ohl), o_ahl = take(b_ahl);
+  const bool t8 = m->wtype == W_E4M3;
+  const size_t o_ot = take(t8 ? (size_t)kTerms * rp_cap * Q : 0), o_at = take(t8 ? (size_t)kTerms * rp_cap * F : 0);
+  const size_t o_xs = take(t8 ? (size_t)3 * rp_cap * 4 : 0);
   const size_t o_q = take((size_t)cap * Q * 4);
   const size_t o_pf = take((size_t)cap * 3 * 4), o_pfbt = take((size_t)cap * mbs_cap * 4);
   void* mem = nullptr;
@@ -269,6 +276,10 @@ int ensure_ws(mbt_model* m, Workspace& w, int R, int mbs) {
   w.ts_scratch = (float*)(base + o_ts);
   w.rp_cap = rp_cap;
   w.x_hl = (bf16*)(base + o_xhl); w.o_hl = (bf16*)(base + o_ohl); w.act_hl = (bf16*)(base + o_ahl);
+  if (t8) {
+    w.o_t = (uint8_t*)(base + o_ot); w.act_t = (uint8_t*)(base + o_at);
+    w.x_s = (float*)(base + o_xs); w.o_s = w.x_s + rp_cap; w.act_s = w.o_s + rp_cap;
+  }
   w.q = (float*)(base + o_q);
   w.pf_tok = (int*)(base + o_pf); w.pf_pos = w.pf_tok + cap; w.pf_sl = w.pf_pos + cap;
   w.pf_bt = (int*)(base + o_pfbt);
@@ -388,17 +399,22 @@ int run_layers_tc(mbt_model* m, const Workspace& w, mbt_kv* kv, const Plan& p, c
   const int QKV = (nq + 2 * nkv) * d;
   const size_t half = kv_layer_half_bytes(m, kv->num_blocks);
   const long long rh = (long long)R * H;
-  // e4m3 weights: FP16 activation rows; BF16 otherwise
+  // e4m3 weights: the projections read e4m3 term rows (the 16-bit rows that
+  // attention and the SwiGLU epilogue write are FP16 and are split into terms);
+  // BF16 weights: BF16 high/low rows
   const int f16 = m->wtype == W_E4M3;
+  uint8_t* x_t = reinterpret_cast<uint8_t*>(w.x_hl);
   // one projection over the R rows, in launches of at most 64 rows that read
-  // the high/low buffer from their first row on
-  auto gemm = [&](int epi, const TmaMap& wm, const bf16* xbuf, int K, const TcArgs& base) -> cudaError_t {
+  // the activation rows from their first row on
+  auto gemm = [&](int epi, const TmaMap& wm, const void* xbuf, const float* xs, int K,
+                  const TcArgs& base) -> cudaError_t {
     for (int r0 = 0; r0 < R; r0 += kTsMaxRows) {
       const int rl = std::min(kTsMaxRows, R - r0), rc = (rl + 15) / 16 * 16;
       TmaMap xm;
-      cudaError_t e = tc_make_map(&xm, xbuf, 2 * Rp, K, rc);
+      cudaError_t e = f16 ? tc_make_map_u8(&xm, xbuf, kTerms * Rp, K, rc) : tc_make_map(&xm, xbuf, 2 * Rp, K, rc);
       if (e != cudaSuccess) return e;
       TcArgs a = base;
+      a.x_scale = xs;
       a.R = rl; a.Rp = rc; a.row0 = r0; a.rp_all = Rp;
       a.ts_scratch = w.ts_scratch; a.ts_tickets = w.tickets; a.tickets_cap = w.tickets_cap;
       e = ts_launch(m->wtype, epi, &wm, &xm, a, m->num_sms, s);
@@ -407,21 +423,24 @@ int run_layers_tc(mbt_model* m, const Workspace& w, mbt_kv* kv, const Plan& p, c
     return cudaSuccess;
   };
   auto norm = [&](const float* delta, int n_delta, const bf16* gamma) {
-    AddNormArgs an{R, H, w.r, delta, n_delta, rh, gamma, m->h.eps, nullptr, w.x_hl, Rp, f16};
+    AddNormArgs an{R, H, w.r, delta, n_delta, rh, gamma, m->h.eps, nullptr, f16 ? nullptr : w.x_hl, Rp, 0};
+    if (f16) { an.y_t = x_t; an.y_s = w.x_s; }
     return launch_add_rmsnorm(an, s);
   };
-  auto partial = [&](const TmaMap& wm, const bf16* xbuf, const float* sc, int N, int K, float* out) {
+  auto partial = [&](const TmaMap& wm, const void* xbuf, const float* xs, const float* sc, int N, int K,
+                     float* out) {
     TcArgs a = {};
     a.N = N; a.K = K; a.scale = sc;
     a.out = out; a.split_stride = (long long)R * N; a.ldo = N; a.err = m->err;
-    return gemm(EPI_PARTIAL, wm, xbuf, K, a);
+    return gemm(EPI_PARTIAL, wm, xbuf, xs, K, a);
   };
+  const void* x_in = f16 ? (const void*)x_t : (const void*)w.x_hl;
   for (int l = 0; l < (int)m->h.n_layers; ++l) {
     const Layer& L = m->layers[l];
     const TmaMap* wm = &m->wmaps[(size_t)l * 4];
     char* kbase = (char*)kv->pool + 2 * half * (size_t)l;
     MBT_CUDA(norm(l ? w.delta2 : nullptr, l ? p.ns_down : 0, L.g_attn));
-    MBT_CUDA(partial(wm[0], w.x_hl, L.s_qkv, QKV, H, w.qkv));
+    MBT_CUDA(partial(wm[0], x_in, w.x_s, L.s_qkv, QKV, H, w.qkv));
     AttnArgs at = {};
     at.B = R; at.nq = nq; at.nkv = nkv; at.d = d;
     at.qkv = w.qkv; at.qkv_nsplit = p.ns_qkv; at.qkv_split_stride = (long long)R * QKV; at.ld_qkv = QKV;
@@ -437,13 +456,15 @@ int run_layers_tc(mbt_model* m, const Workspace& w, mbt_kv* kv, const Plan& p, c
       at.qkv = nullptr; at.q = w.q; at.no_pdl = 1;
     }
     MBT_CUDA(launch_attention(at, s));
-    MBT_CUDA(partial(wm[1], w.o_hl, L.s_o, H, Q, w.delta));
+    if (f16) MBT_CUDA(tc_to_terms(nullptr, w.o_hl, 1, R, Rp, Q, w.o_t, w.o_s, s));
+    MBT_CUDA(partial(wm[1], f16 ? (const void*)w.o_t : (const void*)w.o_hl, w.o_s, L.s_o, H, Q, w.delta));
     MBT_CUDA(norm(w.delta, p.ns_o, L.g_ffn));
     TcArgs g = {};
     g.N = F; g.K = H; g.scale = L.s_gu; g.act_hl = w.act_hl; g.ld_act = F; g.err = m->err;
     g.hl_f16 = f16;
-    MBT_CUDA(gemm(EPI_SWIGLU, wm[2], w.x_hl, H, g));
-    MBT_CUDA(partial(wm[3], w.act_hl, L.s_down, H, F, w.delta2));
+    MBT_CUDA(gemm(EPI_SWIGLU, wm[2], x_in, w.x_s, H, g));
+    if (f16) MBT_CUDA(tc_to_terms(nullptr, w.act_hl, 1, R, Rp, F, w.act_t, w.act_s, s));
+    MBT_CUDA(partial(wm[3], f16 ? (const void*)w.act_t : (const void*)w.act_hl, w.act_s, L.s_down, H, F, w.delta2));
   }
   if (prefill) return next_ids ? lm_head_last_row(m, w, p, next_ids, logits, s) : MBT_OK;
   MBT_CUDA(norm(w.delta2, p.ns_down, m->g_final));
@@ -452,7 +473,7 @@ int run_layers_tc(mbt_model* m, const Workspace& w, mbt_kv* kv, const Plan& p, c
   a.part = w.lm_part; a.part_ld = R; a.err = m->err;
   if (smp && smp->mode == 1) a.gum = smp->gum;
   if (smp && smp->mode == 2) a.logits = smp->z;
-  MBT_CUDA(gemm(EPI_ARGMAX, m->wmaps[(size_t)m->h.n_layers * 4], w.x_hl, H, a));
+  MBT_CUDA(gemm(EPI_ARGMAX, m->wmaps[(size_t)m->h.n_layers * 4], x_in, w.x_s, H, a));
   if (smp && smp->mode == 2) {
     MBT_CUDA(sample_from_logits(m, smp, R, next_ids, s));
     if (logits) MBT_CUDA(cudaMemcpyAsync(logits, smp->z, (size_t)R * V * 4, cudaMemcpyDeviceToDevice, s));
@@ -724,7 +745,7 @@ int model_create(const void* blob, size_t bytes, int blob_is_device, void* strea
     const int Hh = (int)h.hidden, Qd = (int)(h.n_q_heads * h.head_dim), Ff = (int)h.ffn;
     const int QKVr = (int)((h.n_q_heads + 2 * h.n_kv_heads) * h.head_dim);
     auto mk = [&](TmaMap* map, const void* base, int rows, int K) {
-      return (m->wtype == W_E4M3 ? tc_make_map_u8(map, base, rows, K) : tc_make_map(map, base, rows, K, 64)) ==
+      return (m->wtype == W_E4M3 ? tc_make_map_u8(map, base, rows, K, 64) : tc_make_map(map, base, rows, K, 64)) ==
              cudaSuccess;
     };
     m->wmaps.resize((size_t)h.n_layers * 4 + 1);

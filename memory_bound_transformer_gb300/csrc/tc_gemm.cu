@@ -26,6 +26,75 @@ __global__ void from_hl_kernel(const uint16_t* hl, int B, int Rp, int N, float* 
     out[(size_t)b * N + j] = hl16_to_f32(hl[(size_t)b * N + j], f16) + hl16_to_f32(hl[(size_t)(Rp + b) * N + j], f16);
 }
 
+// Rows (fp32 x, or 16-bit high/low rows hl [2 * Rp][K]) -> four e4m3 term rows
+// t [4][Rp][K] and the rows' power-of-two scales ts[Rp] (split_terms); rows
+// B..Rp-1 get zero codes and scale 1. One CTA per row: the largest |x| first,
+// then the split (the second read of the row comes from L1/L2).
+constexpr int kTermThreads = 512;
+__global__ void __launch_bounds__(kTermThreads) to_terms_kernel(const float* x, const uint16_t* hl, int f16, int B,
+                                                                int Rp, int K, uint8_t* t, float* ts) {
+  __shared__ float scratch[32];
+  const int b = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int n4 = K / 4;
+  if (b >= B) {
+    for (int tj = 0; tj < kTerms; ++tj)
+      for (int i = threadIdx.x; i < n4; i += blockDim.x)
+        reinterpret_cast<uint32_t*>(t + ((size_t)tj * Rp + b) * K)[i] = 0u;
+    if (threadIdx.x == 0) ts[b] = 1.f;
+    return;
+  }
+  auto load4 = [&](int i, float (&v)[4]) {
+    if (x) {
+      const float4 q = reinterpret_cast<const float4*>(x + (size_t)b * K)[i];
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
+      const uint2 h = reinterpret_cast<const uint2*>(hl + (size_t)b * K)[i];
+      const uint2 l = reinterpret_cast<const uint2*>(hl + (size_t)(Rp + b) * K)[i];
+      const uint32_t hw[4] = {h.x & 0xffffu, h.x >> 16, h.y & 0xffffu, h.y >> 16};
+      const uint32_t lw[4] = {l.x & 0xffffu, l.x >> 16, l.y & 0xffffu, l.y >> 16};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        v[e] = f16 ? __half2float(__ushort_as_half((uint16_t)hw[e])) + __half2float(__ushort_as_half((uint16_t)lw[e]))
+                   : __uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16);
+    }
+  };
+  float m = 0.f;
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    float v[4];
+    load4(i, v);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(v[e]));
+  }
+  m = block_max(m, scratch);
+  float sc, isc;
+  term_scale(m, sc, isc);
+  if (threadIdx.x == 0) ts[b] = sc;
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    float v[4];
+    load4(i, v);
+    uint32_t c[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) c[e] = split_terms(v[e], isc);
+#pragma unroll
+    for (int tj = 0; tj < kTerms; ++tj) {
+      const uint32_t w = ((c[0] >> (8 * tj)) & 255u) | (((c[1] >> (8 * tj)) & 255u) << 8) |
+                         (((c[2] >> (8 * tj)) & 255u) << 16) | (((c[3] >> (8 * tj)) & 255u) << 24);
+      reinterpret_cast<uint32_t*>(t + ((size_t)tj * Rp + b) * K)[i] = w;
+    }
+  }
+}
+
+cudaError_t tc_to_terms(const float* x, const bf16* hl, int f16, int B, int Rp, int K, uint8_t* t, float* ts,
+                        cudaStream_t s) {
+  if (K % 4 || (!x && !hl) || B < 0 || B > Rp) return cudaErrorInvalidValue;
+  void* p[] = {&x, &hl, &f16, &B, &Rp, &K, &t, &ts};
+  const uint16_t* h16 = reinterpret_cast<const uint16_t*>(hl);
+  p[1] = &h16;
+  return launch_pdl((const void*)to_terms_kernel, dim3(Rp), dim3(kTermThreads), 0, s, p);
+}
+
 cudaError_t tc_to_hl(const float* x, int B, int Rp, int K, bf16* hl, cudaStream_t s, int f16) {
   to_hl_kernel<<<Rp, 256, 0, s>>>(x, B, Rp, K, reinterpret_cast<uint16_t*>(hl), f16);
   return cudaGetLastError();
@@ -72,16 +141,15 @@ cudaError_t tc_make_map(void* map, const void* base, int rows, int K, int box_ro
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// 2-D tensor map over e4m3 codes [rows][K] (K contiguous), box of 128 codes x
-// 64 rows, 128-byte swizzle (16-byte chunk c of row r lands at chunk
-// c ^ (r % 8), so the widening threads, one row each, read shared memory
-// without bank conflicts), zero fill out of bounds.
-cudaError_t tc_make_map_u8(void* map, const void* base, int rows, int K) {
+// 2-D tensor map over e4m3 codes [rows][K] (K contiguous: weights, or the
+// activations' term rows), box of 128 codes x box_rows rows, 128-byte swizzle
+// (the layout the MMA's shared-memory descriptors read), zero fill out of bounds.
+cudaError_t tc_make_map_u8(void* map, const void* base, int rows, int K, int box_rows) {
   if (!g_encode) return cudaErrorNotSupported;
-  if (((uintptr_t)base & 15) || K % 16) return cudaErrorInvalidValue;
+  if (((uintptr_t)base & 15) || K % 16 || box_rows < 1 || box_rows > 256) return cudaErrorInvalidValue;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)K};
-  const cuuint32_t box[2] = {128u, 64u};
+  const cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode((CUtensorMap*)map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

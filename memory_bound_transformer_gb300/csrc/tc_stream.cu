@@ -1,26 +1,35 @@
 // Skinny GEMM on the tcgen05 tensor cores for decode at batch 2..64 rows per
 // launch, BF16 or e4m3 weights: y = W x with W [rows][K] the M operand
-// (swap-AB: 128 weight rows per tile) and the fp32 activation rows, split into
-// 16-bit high and low parts, the N operand. At these batches the weight-only
-// arithmetic intensity 2B / b_w ("GPU Inference Internals", "Roofline: Why
-// Decode Is Memory-Bound") is far below the ridge: the kernel must move the
-// weights at the HBM rate. Three measurements on the GB300 shape it:
+// (swap-AB: 128 weight rows per tile) and the activation rows the N operand.
+// BF16 weights: the fp32 activations split into BF16 high and low parts
+// (kind::f16). e4m3 weights: the activations split into four e4m3 terms per
+// value with a power-of-two scale per row (x = s (c0 + c1/16 + c2/256 +
+// c3/4096) to 2^-16 of |x|), multiplied with the weight codes as they are
+// (kind::f8f6f4), the 16^-j factors and s applied to the fp32 sums. At these
+// batches the weight-only arithmetic intensity 2B / b_w ("GPU Inference
+// Internals", "Roofline: Why Decode Is Memory-Bound") is far below the ridge:
+// the kernel must move the weights at the HBM rate. Measurements on the GB300
+// shape it:
 //
 // * DRAM efficiency depends on how many contiguous bytes of a weight row one
 //   copy fetches: streaming 128-row tiles with TMA boxes of 64 / 128 / 256
 //   bytes per row reached 3.9-5.2 / 6.2-6.5 / 6.7 TB/s. Every weight stage
 //   here covers 256 bytes of each of its 128 rows (128 BF16 values or 256 e4m3
 //   codes), 32 KB per stage.
+// * One thread issues a tcgen05.mma about every 100 cycles whatever its N, so
+//   the work per instruction decides the MMA rate: at M = 128, N = 128, K = 16
+//   (64 cycles of tensor-core time) the issue is the limit. The activation
+//   parts are stacked along N (one MMA per K step reads the weight tile once),
+//   and e4m3 weights take K = 32 codes per MMA at N = 4 x rows: 8 MMAs per
+//   weight stage. The earlier e4m3 design widened the codes to FP16 in TMEM
+//   for kind::f16 with FP16 high/low rows, 16 MMAs per stage, and ran at half
+//   this kernel's rate.
 // * The tensor core's fp32 accumulation drifts toward zero over long chains
 //   (a bias proportional to K: 2.3e-5 of the output rms at K = 28672, halving
 //   with each halving of the chain). The accumulator therefore lives in TMEM
-//   for at most 512 K values: TMEM accumulators rotate (three for BF16
+//   for at most 512 K values: accumulator groups rotate (three for BF16
 //   weights, two for e4m3), and the drain warps add the finished one into
 //   fp32 registers (IEEE adds) while the MMAs fill the others.
-// * The high and the low activation rows are stacked along N, so one MMA per
-//   K step reads the weight tile from shared memory once; two MMAs per step
-//   (one per part) read it twice and held each weight stage 40% longer
-//   (1,790 against 1,320 cycles per 32 KB stage and SM).
 // * Whole tiles per CTA quantise badly (224 tiles on 152 SMs run as two
 //   waves). One CTA per SM takes an equal contiguous share of the flattened
 //   (tile, K stage) work ("stream-K"). A tile whose K range spans several
@@ -34,19 +43,16 @@
 //
 // Warp roles: warp 0 (one thread) copies weight stages with TMA (it never
 // waits on the previous kernel: the weights do not depend on it); warp 1 (one
-// thread) copies activation sub-stages (64 K values, high and low rows);
-// warp 2 (one thread) issues the MMAs (M = 128, N = 2 x rows, K = 16: columns
-// [0, rows) of the accumulator take the high rows, [rows, 2 rows) the low) and
-// their commits; warp 3 owns the TMEM allocation. For e4m3 weights warps 4-7
-// widen each thread's weight row into FP16 in TMEM (the MMA reads A from
-// there; kind::f16 needs two 16-bit operands of one type; the bit pattern
-// s.0eeee.mmm0000000 is exactly the e4m3 value / 256, the 256 joining the
-// per-row scale). The last four warps drain the accumulators, finish tiles
-// and run the epilogues: split outputs, SwiGLU over 64 gate + 64 up rows
-// (written as 16-bit high/low rows for the down projection), the tile's arg-max
-// per row (or the sampling draw). Every wait is bounded (about 2 s): on a
-// timeout the kernel flags MBT_DEV_WAIT_LIMIT, lets its MMAs and copies finish
-// (bounded), frees TMEM and returns.
+// thread) copies activation sub-stages (one 128-byte row of K per activation
+// row: the high and low rows, or the four term rows); warp 2 (one thread)
+// issues the MMAs (columns [x rows, (x + 1) rows) of the accumulator take
+// activation part x) and their commits; warp 3 owns the TMEM allocation. The
+// last four warps drain the accumulators, finish tiles and run the epilogues:
+// split outputs, SwiGLU over 64 gate + 64 up rows (written as 16-bit high/low
+// rows for the down projection), the tile's arg-max per row (or the sampling
+// draw). Every wait is bounded (about 2 s): on a timeout the kernel flags
+// MBT_DEV_WAIT_LIMIT, lets its MMAs and copies finish (bounded), frees TMEM
+// and returns.
 #include <algorithm>
 
 #include "tcgen05.cuh"
@@ -54,7 +60,6 @@
 namespace mbt {
 
 constexpr int kTsRows = 64;                        // batch rows per launch (hi + lo = 128 MMA columns)
-constexpr int kTsSub = 64;                         // K values per MMA sub-stage (one 128-byte row of 16-bit values)
 constexpr int kTsFlushK = 512;                     // K values accumulated in TMEM before the fp32 drain
 constexpr uint32_t kTsAStage = 128 * 256;          // weight stage: 128 rows x 256 bytes
 constexpr uint32_t kTsRings = 192 * 1024;          // weight ring + activation ring
@@ -62,17 +67,17 @@ constexpr uint32_t kTsScratch = 32 * 128 * 4 + 4 * kTsRows * 8;  // epilogue sta
 constexpr uint32_t kTsAcc = 64;                    // TMEM columns per accumulator (one per batch row)
 constexpr uint32_t kTsTmemCols = 512;
 
-// SUBS: activation sub-stages (64 K each) per weight stage; XR: activation
-// rows per batch row in a sub-stage (high and low parts); MAXA / MAXB: ring
-// depth limits (the depths themselves depend on the batch); NACC: accumulator
-// groups in rotation, each a pair of TMEM accumulators (products with the high
-// rows, with the low rows) of 64 columns.
+// KSUB: K values per activation sub-stage (one 128-byte row: 64 BF16 values or
+// 128 e4m3 codes), SUBS of them per 32 KB weight stage; XR: activation rows per
+// batch row (BF16: high and low parts; e4m3: four terms), stacked along N, so
+// an accumulator group has XR x 64 TMEM columns; NACC groups rotate; MAXA /
+// MAXB: ring depth limits (the depths themselves depend on the batch).
 template <int WT> struct TsCfg;
 template <> struct TsCfg<W_BF16> {
-  static constexpr int SUBS = 2, XR = 2, WARPS = 8, DRAIN = 4, ST = 0, MAXA = 5, MAXB = 8, NACC = 3;
+  static constexpr int KSUB = 64, SUBS = 2, XR = 2, WARPS = 8, DRAIN = 4, MAXA = 5, MAXB = 8, NACC = 3;
 };
 template <> struct TsCfg<W_E4M3> {
-  static constexpr int SUBS = 4, XR = 2, WARPS = 12, DRAIN = 8, ST = 8, MAXA = 4, MAXB = 16, NACC = 2;
+  static constexpr int KSUB = 128, SUBS = 2, XR = 4, WARPS = 8, DRAIN = 4, MAXA = 4, MAXB = 16, NACC = 2;
 };
 
 constexpr size_t ts_smem() { return 1024 + (size_t)kTsRings + kTsScratch; }
@@ -80,8 +85,9 @@ constexpr size_t ts_smem() { return 1024 + (size_t)kTsRings + kTsScratch; }
 // Ring depths for Rc padded batch rows. Under full HBM load an activation
 // copy from L2 takes as long as a weight copy from HBM (3,400-7,000 cycles
 // measured against 6,000), so both rings are sized against that latency: the
-// activation bytes per weight byte are XR * Rc * 2 / (128 * w), and the rings
-// split the 192 KB in roughly that proportion.
+// activation bytes per weight byte are 4 Rc / (128 w) (four bytes per value:
+// two BF16 parts or four e4m3 terms), and the rings split the 192 KB in
+// roughly that proportion.
 template <int WT>
 __host__ __device__ __forceinline__ void ts_rings(int Rc, int& sa, int& sb) {
   using C = TsCfg<WT>;
@@ -118,24 +124,19 @@ __device__ __forceinline__ void split_hl16(float x, int f16, uint32_t& hi, uint3
   }
 }
 
-// Four e4m3 codes (lowest byte first) -> two FP16x2 words of value / 256.
-__device__ __forceinline__ void ts_widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t t0 = __byte_perm(w, 0u, 0x1404), t1 = __byte_perm(w, 0u, 0x3424);
-  lo = ((t0 >> 1) & 0x3F803F80u) | (t0 & 0x80008000u);
-  hi = ((t1 >> 1) & 0x3F803F80u) | (t1 & 0x80008000u);
-}
-
 template <int WT, int EPI>
 __global__ void __launch_bounds__(TsCfg<WT>::WARPS * 32, 1)
 tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const TcArgs a) {
   using C = TsCfg<WT>;
-  constexpr int SUBS = C::SUBS, ST = C::ST > 0 ? C::ST : 1;
-  constexpr int FG = kTsFlushK / (kTsSub * SUBS);    // weight stages per accumulation group
+  constexpr int SUBS = C::SUBS, KSUB = C::KSUB, XR = C::XR;
+  constexpr int ACOLS = XR * kTsAcc;                 // TMEM columns per accumulator group
+  constexpr int FG = kTsFlushK / (KSUB * SUBS);      // weight stages per accumulation group
   constexpr int DW = C::DRAIN;                       // first drain warp
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t a_full[C::MAXA], a_empty[C::MAXA], b_full[C::MAXB], b_empty[C::MAXB];
-  __shared__ __align__(8) uint64_t t_full[ST], t_empty[ST], acc_full[C::NACC], acc_empty[C::NACC], done;
+  __shared__ __align__(8) uint64_t acc_full[C::NACC], acc_empty[C::NACC], done;
+  __shared__ float xsc_s[kTsRows];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ int a_issued_s, a_used_s, b_issued_s, b_used_s, last_s;
@@ -145,12 +146,12 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   const int Rc = a.Rp;                                // padded rows of this launch (multiple of 16, <= 64)
   int SA, SB;
   ts_rings<WT>(Rc, SA, SB);
-  const uint32_t b_bytes = (uint32_t)(C::XR * Rc) * 128;    // one activation sub-stage
+  const uint32_t b_bytes = (uint32_t)(XR * Rc) * 128;       // one activation sub-stage
   unsigned char* sA = smem;                                   // [SA][K block][128 rows][128 B], 128-B swizzle
   unsigned char* sB = sA + SA * kTsAStage;                    // [SB][XR * Rc rows][128 B], 128-B swizzle
   float* scr = reinterpret_cast<float*>(smem + kTsRings);     // epilogue staging
   const int tiles = EPI == EPI_SWIGLU ? (a.N + 63) / 64 : (a.N + 127) / 128;
-  const int nA = (a.K + kTsSub * SUBS - 1) / (kTsSub * SUBS);
+  const int nA = (a.K + KSUB * SUBS - 1) / (KSUB * SUBS);
   const long long W = (long long)tiles * nA;
   const long long u0 = ts_u0(W, G, cta), u1 = ts_u0(W, G, cta + 1);
   auto rowA0 = [&](int t) { return EPI == EPI_SWIGLU ? t * 64 : t * 128; };
@@ -158,9 +159,8 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
 
   pdl_launch_dependents();
   if (tid == 0) {
-    for (int s = 0; s < SA; ++s) { mbar_init(&a_full[s], 1); mbar_init(&a_empty[s], WT == W_E4M3 ? 4 : 1); }
+    for (int s = 0; s < SA; ++s) { mbar_init(&a_full[s], 1); mbar_init(&a_empty[s], 1); }
     for (int s = 0; s < SB; ++s) { mbar_init(&b_full[s], 1); mbar_init(&b_empty[s], 1); }
-    for (int s = 0; s < ST; ++s) { mbar_init(&t_full[s], 4); mbar_init(&t_empty[s], 1); }
     for (int s = 0; s < C::NACC; ++s) { mbar_init(&acc_full[s], 1); mbar_init(&acc_empty[s], 4); }
     mbar_init(&done, 1);
     abort_flag = 0;
@@ -177,8 +177,7 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_slot;                      // accumulator pairs at columns 0, 128, ...
-  const uint32_t tmem_a = tmem + C::NACC * 2 * kTsAcc;  // e4m3: widened A sub-stages, 32 columns each
+  const uint32_t tmem = tmem_slot;                      // accumulator groups at columns 0, ACOLS, ...
 
   if (warp == 0) {
     if (lane == 0) {
@@ -206,11 +205,12 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         const int k = (int)(u % nA);
         for (int j = 0; j < SUBS; ++j, ++i, s = s + 1 == SB ? 0 : s + 1, r += s == 0) {
           if (r > 0 && (abort_flag || !mbar_wait(&b_empty[s], (uint32_t)((r - 1) & 1)))) { abort_flag = 1; break; }
-          const int kx = (k * SUBS + j) * kTsSub;
+          const int kx = (k * SUBS + j) * KSUB;
           mbar_arrive_tx(&b_full[s], b_bytes);
           unsigned char* dst = sB + (size_t)s * b_bytes;
-          tma_load_2d(dst, &tmX, kx, a.row0, &b_full[s]);                        // high rows
-          tma_load_2d(dst + (size_t)Rc * 128, &tmX, kx, a.rp_all + a.row0, &b_full[s]);   // low rows
+#pragma unroll
+          for (int x = 0; x < XR; ++x)                 // high / low rows, or the four term rows
+            tma_load_2d(dst + (size_t)x * Rc * 128, &tmX, kx, x * a.rp_all + a.row0, &b_full[s]);
           b_issued_s = i + 1;
         }
       }
@@ -218,9 +218,10 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   } else if (warp == 2) {
     if (lane == 0) {
       pdl_wait();
-      // N = Rc: the high rows and the low rows are two MMAs into one accumulator
-      const uint32_t idesc = idesc_16(128, 2 * Rc, WT == W_E4M3 ? 1 : 0);
-      int ia = 0, sa = 0, ra = 0, ib = 0, sb = 0, rb = 0, it = 0, gi = 0;   // counts, slots, rounds
+      // M = 128 weight rows, N = XR x Rc activation rows (K = 16 BF16 values or
+      // 32 e4m3 codes per MMA, four MMAs per sub-stage)
+      const uint32_t idesc = idesc_16(128, XR * Rc, WT == W_E4M3 ? 1 : 0);
+      int ia = 0, sa = 0, ra = 0, ib = 0, sb = 0, rb = 0, gi = 0;   // counts, slots, rounds
       bool ok = true;
       for (long long u = u0; u < u1 && ok;) {
         const int k0 = (int)(u % nA);
@@ -230,31 +231,24 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
           const int buf = gi % C::NACC;
           if (gi >= C::NACC && !mbar_wait(&acc_empty[buf], (uint32_t)(((gi / C::NACC) - 1) & 1))) { ok = false; break; }
           tc_fence_after();
-          const uint32_t acc = tmem + (uint32_t)buf * 2 * kTsAcc;   // columns [0, Rc): high rows, [Rc, 2 Rc): low
+          const uint32_t acc = tmem + (uint32_t)(buf * ACOLS);   // columns [x Rc, (x + 1) Rc): activation part x
           for (int x = 0; x < gn && ok; ++x, ++ia, sa = sa + 1 == SA ? 0 : sa + 1, ra += sa == 0) {
-            if (WT == W_BF16 && (abort_flag || !mbar_wait(&a_full[sa], (uint32_t)(ra & 1)))) { ok = false; break; }
+            if (abort_flag || !mbar_wait(&a_full[sa], (uint32_t)(ra & 1))) { ok = false; break; }
             for (int j = 0; j < SUBS; ++j, ++ib, sb = sb + 1 == SB ? 0 : sb + 1, rb += sb == 0) {
               if (abort_flag || !mbar_wait(&b_full[sb], (uint32_t)(rb & 1))) { ok = false; break; }
-              const int stt = it % ST;
-              if (WT == W_E4M3 && !mbar_wait(&t_full[stt], (uint32_t)((it / ST) & 1))) { ok = false; break; }
               tc_fence_after();
               const uint64_t bh = sw128_desc(smem_u32(sB + (size_t)sb * b_bytes));
+              const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)sa * kTsAStage + j * 16384));
 #pragma unroll
-              for (int kk = 0; kk < kTsSub / 16; ++kk) {
+              for (int kk = 0; kk < 4; ++kk) {             // 32 bytes of K per MMA
                 const uint32_t accum = (x > 0 || j > 0 || kk > 0) ? 1u : 0u;
-                if (WT == W_E4M3) {
-                  const uint32_t ta = tmem_a + (uint32_t)(stt * 32 + kk * 8);
-                  umma_kf16_tmem_a(acc, ta, bh + (uint64_t)(kk * 2), idesc, accum);
-                } else {
-                  const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)sa * kTsAStage + j * 16384)) + (uint64_t)(kk * 2);
-                  umma_kf16(acc, ad, bh + (uint64_t)(kk * 2), idesc, accum);
-                }
+                if (WT == W_E4M3) umma_kf8(acc, ad + (uint64_t)(kk * 2), bh + (uint64_t)(kk * 2), idesc, accum);
+                else umma_kf16(acc, ad + (uint64_t)(kk * 2), bh + (uint64_t)(kk * 2), idesc, accum);
               }
               umma_commit(&b_empty[sb]);
-              if (WT == W_E4M3) { umma_commit(&t_empty[stt]); ++it; }
               b_used_s = ib + 1;
             }
-            if (WT == W_BF16 && ok) { umma_commit(&a_empty[sa]); a_used_s = ia + 1; }
+            if (ok) { umma_commit(&a_empty[sa]); a_used_s = ia + 1; }
           }
           if (ok) umma_commit(&acc_full[buf]);
         }
@@ -263,43 +257,6 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
       if (!ok) abort_flag = 1;
       umma_commit(&done);                              // fires once every MMA issued above has completed
     }
-  } else if (WT == W_E4M3 && warp >= 4 && warp < 8) {
-    // widening: thread = weight row q * 32 + lane = TMEM lane
-    const int q = warp - 4, row = q * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    int ia = 0, sa = 0, ra = 0, it = 0;
-    for (long long u = u0; u < u1; ++u, ++ia, sa = sa + 1 == SA ? 0 : sa + 1, ra += sa == 0) {
-      if (abort_flag || !mbar_wait(&a_full[sa], (uint32_t)(ra & 1))) { abort_flag = 1; break; }
-      const unsigned char* src = sA + (size_t)sa * kTsAStage + row * 128;
-      uint4 w[16];                                     // the row's 256 codes: two 128-byte K blocks
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        w[c] = *reinterpret_cast<const uint4*>(src + (c >> 3) * 16384 + (((c & 7) ^ (row & 7)) * 16));
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&a_empty[sa]);
-      if (q == 0 && lane == 0) a_used_s = ia + 1;
-      bool ok = true;
-#pragma unroll
-      for (int j = 0; j < 4; ++j, ++it) {              // four 64-code sub-stages
-        const int stt = (int)(it % ST);
-        if (it >= ST && (abort_flag || !mbar_wait(&t_empty[stt], (uint32_t)(((it / ST) - 1) & 1)))) { ok = false; break; }
-        uint32_t h[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 v = w[j * 4 + c];
-          ts_widen4(v.x, h[8 * c + 0], h[8 * c + 1]);
-          ts_widen4(v.y, h[8 * c + 2], h[8 * c + 3]);
-          ts_widen4(v.z, h[8 * c + 4], h[8 * c + 5]);
-          ts_widen4(v.w, h[8 * c + 6], h[8 * c + 7]);
-        }
-        tmem_st32(tmem_a + lane_off + (uint32_t)(stt * 32), h);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&t_full[stt]);
-      }
-      if (!ok) { abort_flag = 1; break; }
-    }
   } else if (warp >= DW) {
     // drain, finish and epilogue: thread = weight row q * 32 + lane of the tile.
     // The tile counters and partial sums are shared with the previous launch
@@ -307,7 +264,8 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     pdl_wait();
     const int q = warp - DW, row = q * 32 + lane, et = tid - DW * 32;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    const float mul = WT == W_E4M3 ? 256.f : 1.f;
+    if (et < kTsRows) xsc_s[et] = (WT == W_E4M3 && et < Rc) ? a.x_scale[a.row0 + et] : 1.f;
+    named_bar(3, 128);
     float sum[kTsRows];
     int gi = 0;
     bool ok = true;
@@ -326,8 +284,10 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         if (abort_flag || !mbar_wait(&acc_full[buf], (uint32_t)((gi / C::NACC) & 1))) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {           // the high-row products, then the low-row ones
-          const uint32_t acc = tmem + (uint32_t)buf * 2 * kTsAcc + (uint32_t)(part * Rc) + lane_base;
+        for (int part = 0; part < XR; ++part) {          // high then low rows, or term 0..3
+          // term x carries 16^-x of the row's scale (exact power-of-two factors)
+          const float f = WT == W_E4M3 ? (part == 0 ? 1.f : part == 1 ? 0.0625f : part == 2 ? 0.00390625f : 0.000244140625f) : 1.f;
+          const uint32_t acc = tmem + (uint32_t)(buf * ACOLS) + (uint32_t)(part * Rc) + lane_base;
           // all of the row's columns in flight at once, one wait
           uint32_t v0[16], v1[16], v2[16], v3[16];
           tmem_ld16_async(acc, v0);
@@ -340,10 +300,10 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
           tmem_ld_wait16(v3);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            sum[j] += __uint_as_float(v0[j]);
-            if (Rc > 16) sum[16 + j] += __uint_as_float(v1[j]);
-            if (Rc > 32) sum[32 + j] += __uint_as_float(v2[j]);
-            if (Rc > 48) sum[48 + j] += __uint_as_float(v3[j]);
+            sum[j] += __uint_as_float(v0[j]) * f;
+            if (Rc > 16) sum[16 + j] += __uint_as_float(v1[j]) * f;
+            if (Rc > 32) sum[32 + j] += __uint_as_float(v2[j]) * f;
+            if (Rc > 48) sum[48 + j] += __uint_as_float(v3[j]) * f;
           }
         }
         tc_fence_before();
@@ -406,7 +366,6 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         const int n = t * 128 + row;
         sc = (a.scale && n < a.N) ? a.scale[n] : 1.f;
       }
-      sc *= mul;
       float* bv = scr + 32 * 128;                        // arg-max: [4 warps][kTsRows] best value, index
       int* bi = reinterpret_cast<int*>(bv + 4 * kTsRows);
 #pragma unroll
@@ -415,7 +374,7 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         if (b0 >= Rc) break;
         named_bar(2, 128);                               // the staging buffer is free
 #pragma unroll
-        for (int i = 0; i < 32; ++i) if (b0 + i < Rc) scr[i * 128 + row] = sum[b0 + i] * sc;
+        for (int i = 0; i < 32; ++i) if (b0 + i < Rc) scr[i * 128 + row] = sum[b0 + i] * (sc * xsc_s[b0 + i]);
         named_bar(2, 128);
         const int nb = min(32, Rc - b0);
         if (EPI == EPI_PARTIAL) {
@@ -547,7 +506,7 @@ size_t ts_scratch_floats(int num_sms) { return (size_t)num_sms * 128 * kTsRows; 
 cudaError_t ts_launch(int wt, int epi, const void* mapW, const void* mapX, const TcArgs& a, int num_sms,
                       cudaStream_t s) {
   if (a.Rp < 16 || a.Rp > kTsRows || a.Rp % 16 || a.R < 1 || a.R > a.Rp || a.rp_all < a.row0 + a.Rp ||
-      !a.ts_scratch || !a.ts_tickets || a.tickets_cap < ts_tiles(epi, a.N))
+      !a.ts_scratch || !a.ts_tickets || a.tickets_cap < ts_tiles(epi, a.N) || (wt == W_E4M3 && !a.x_scale))
     return cudaErrorInvalidValue;
   CUtensorMap w = *(const CUtensorMap*)mapW, x = *(const CUtensorMap*)mapX;
   TcArgs args = a;
@@ -557,8 +516,8 @@ cudaError_t ts_launch(int wt, int epi, const void* mapW, const void* mapX, const
   const size_t sm = ts_smem();
   // one CTA per SM, but never more CTAs than weight stages: every CTA's share
   // is then non-empty, so a tile's contributors are consecutive CTAs
-  const int subs = wt == W_E4M3 ? TsCfg<W_E4M3>::SUBS : TsCfg<W_BF16>::SUBS;
-  const long long units = (long long)ts_tiles(epi, a.N) * ((a.K + kTsSub * subs - 1) / (kTsSub * subs));
+  const int kst = wt == W_E4M3 ? TsCfg<W_E4M3>::SUBS * TsCfg<W_E4M3>::KSUB : TsCfg<W_BF16>::SUBS * TsCfg<W_BF16>::KSUB;
+  const long long units = (long long)ts_tiles(epi, a.N) * ((a.K + kst - 1) / kst);
   const int grid = (int)std::min<long long>(num_sms, units);
   return launch_pdl(ts_pick(wt, epi), dim3(grid), dim3(threads), sm, s, params);
 }

@@ -69,6 +69,13 @@ __device__ __forceinline__ void umma_kf16(uint32_t tmem_d, uint64_t a, uint64_t 
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
       ::"r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
+// e4m3 x e4m3 products into fp32 (kind::f8f6f4, K = 32 codes per MMA); the
+// instruction descriptor's A/B format fields hold 0 (E4M3) as for FP16 in kind::f16.
+__device__ __forceinline__ void umma_kf8(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n"
+      ::"r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
 // The same MMA with A read from tensor memory: M = 128 rows in lanes 0..127,
 // two 16-bit K elements per 32-bit column (the lower K index in the low half).
 __device__ __forceinline__ void umma_kf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
