@@ -147,6 +147,10 @@ def build_case(wl, B, steps_total, device="cuda", context=None):
     tables[tables < 0] = nb
     model = SynthModel(cfg, wl.seed, device=device, cache=False)
     blob = mblob.pack(cfg, model.tensors(), device=device)
+    # the generator's tensors are not needed once packed: free them before the
+    # engine allocates its own copy of the weights and the KV pool
+    del model
+    torch.cuda.empty_cache()
     eng = Engine(blob, nb)
     del blob
     torch.cuda.empty_cache()

@@ -118,21 +118,8 @@ __device__ __forceinline__ void mma_t(float (&d)[4], const uint32_t (&a)[4], uin
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-
-// All threads of all CTAs of the cluster: writes to shared memory before it
-// are visible to every CTA of the cluster after it.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Loads from the shared memory of CTA `rank` of the cluster, at the address
-// that p has in this CTA.
-__device__ __forceinline__ float ld_dsmem_f32(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
-  return v;
-}
+// Loads two floats from the shared memory of CTA `rank` of the cluster, at the
+// address that p has in this CTA.
 __device__ __forceinline__ float2 ld_dsmem_f2(const void* p, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
@@ -836,7 +823,17 @@ size_t attn_smem_bytes(int d, int kv8, int G) {
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
   size_t sm;
-  const int cl = a.nsplit >= 4 && a.nsplit <= kAttnCluster;
+  // the cluster merge pays off while the grid is about one wave (batch 1-4 at
+  // 8 KV heads: 2.97 / 4.07 ms per 8B step); beyond that clusters of splits
+  // packed the SMs worse than independent CTAs with the ticket merge (batch 8
+  // and 16: 4.26 / 4.41 ms against 4.59 / 4.73 ms with clusters)
+  static int nsm = 0;
+  if (!nsm) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  }
+  const int cl = a.nsplit >= 4 && a.nsplit <= kAttnCluster && a.B * a.nkv * a.nsplit <= 2 * nsm;
   void* fn = attn_pick(a.d, a.kv_fp8, (a.nq / a.nkv) > 8 ? 2 : 1, cl, &sm);
   // the merge needs the group's weights and at least one split of partials in shared memory
   const int G = a.nq / a.nkv;

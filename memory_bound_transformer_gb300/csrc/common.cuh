@@ -141,6 +141,24 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // Block-wide sum for blockDim.x a multiple of 32 (<= 1024). `scratch` holds
 // >= 32 floats. Every thread returns the total.
+// ---------------------------------------------------------------------------
+// thread-block clusters
+
+// Every thread of every CTA of the cluster arrives, then waits (release /
+// acquire: shared-memory writes before it are visible to the cluster after it).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// A float in the shared memory of the cluster's CTA `rank`, at the address
+// that `p` has in this CTA.
+__device__ __forceinline__ float ld_dsmem_f32(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float block_max(float v, float* scratch) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   v = warp_max(v);

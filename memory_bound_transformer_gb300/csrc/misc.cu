@@ -1,6 +1,8 @@
 // Small per-row kernels of the decode step: embedding + RMSNorm, fused
 // residual add + RMSNorm, RoPE fused with the paged KV-cache write, the final
 // arg-max reduction and the staging of caller inputs into graph buffers.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -124,61 +126,11 @@ __device__ __forceinline__ void norm_store_hl(const float4 (&v)[kNormMaxV], floa
   }
 }
 
-// y as four e4m3 term rows plus the row's power-of-two scale (for e4m3 x e4m3
-// tensor-core products): one pass for the largest |y|, one to split.
-__device__ __forceinline__ void norm_store_terms(const float4 (&v)[kNormMaxV], float ss, int H,
-                                                const bf16* __restrict__ gamma, float eps, uint8_t* t_row,
-                                                size_t t_stride, float* s_out, float* scratch) {
-  const float tot = block_sum(ss, scratch);
-  const float inv = 1.0f / sqrtf(tot / (float)H + eps);
-  const int nv = H / 4;
-  const uint2* g2 = reinterpret_cast<const uint2*>(gamma);
-  float o[kNormMaxV][4];
-  float m = 0.f;
-#pragma unroll
-  for (int j = 0; j < kNormMaxV; ++j) {
-    const int i = threadIdx.x + j * blockDim.x;
-    if (i < nv) {
-      const uint2 g = g2[i];
-      o[j][0] = v[j].x * inv * bf16_lo(g.x); o[j][1] = v[j].y * inv * bf16_hi(g.x);
-      o[j][2] = v[j].z * inv * bf16_lo(g.y); o[j][3] = v[j].w * inv * bf16_hi(g.y);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(o[j][e]));
-    }
-  }
-  m = block_max(m, scratch);
-  float sc, isc;
-  term_scale(m, sc, isc);
-  if (threadIdx.x == 0) *s_out = sc;
-#pragma unroll
-  for (int j = 0; j < kNormMaxV; ++j) {
-    const int i = threadIdx.x + j * blockDim.x;
-    if (i < nv) {
-      uint32_t c[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) c[e] = split_terms(o[j][e], isc);
-#pragma unroll
-      for (int tj = 0; tj < kTerms; ++tj) {
-        const uint32_t w = ((c[0] >> (8 * tj)) & 255u) | (((c[1] >> (8 * tj)) & 255u) << 8) |
-                           (((c[2] >> (8 * tj)) & 255u) << 16) | (((c[3] >> (8 * tj)) & 255u) << 24);
-        reinterpret_cast<uint32_t*>(t_row + tj * t_stride)[i] = w;
-      }
-    }
-  }
-}
-
 __global__ void __launch_bounds__(1024) add_rmsnorm_kernel(const AddNormArgs a) {
   __shared__ float scratch[32];
   const int b = blockIdx.x;
   pdl_launch_dependents();
   pdl_wait();
-  if (b >= a.B && a.y_t) {                          // padding rows of the term output
-    for (int tj = 0; tj < kTerms; ++tj)
-      for (int i = threadIdx.x; i < a.H / 4; i += blockDim.x)
-        reinterpret_cast<uint32_t*>(a.y_t + ((size_t)tj * a.rp + b) * a.H)[i] = 0u;
-    if (threadIdx.x == 0) a.y_s[b] = 1.f;
-    return;
-  }
   if (b >= a.B) {                                   // padding rows of the high/low output
     const bf16 z = __float2bfloat16_rn(0.f);
     for (int i = threadIdx.x; i < a.H; i += blockDim.x) {
@@ -211,14 +163,107 @@ __global__ void __launch_bounds__(1024) add_rmsnorm_kernel(const AddNormArgs a) 
     const int i = threadIdx.x + j * blockDim.x;
     if (i < nv) r[i] = v[j];
   }
-  if (a.y_t)
-    norm_store_terms(v, ss, a.H, a.gamma, a.eps, a.y_t + (size_t)b * a.H, (size_t)a.rp * a.H, a.y_s + b, scratch);
-  else if (a.y_hl) {
+  if (a.y_hl) {
     uint16_t* hl = reinterpret_cast<uint16_t*>(a.y_hl);
     norm_store_hl(v, ss, a.H, a.gamma, a.eps, hl + (size_t)b * a.H, hl + (size_t)(a.rp + b) * a.H, scratch, a.hl_f16);
   }
   else
     norm_store(v, ss, a.H, a.gamma, a.eps, a.y + (size_t)b * a.H, scratch);
+}
+
+// The same residual add + RMSNorm with y as four e4m3 term rows and the row's
+// power-of-two scale (split_terms), for e4m3 weights. It needs a second pass
+// over the row (its largest |y|) and the split, so a row is spread over a
+// cluster of C CTAs (one float4 of the row per thread where the row allows
+// it): a row per CTA left most SMs idle at batch 32-64 and took ~10 us. The
+// CTAs exchange their partial sums of squares, then their largest |y|,
+// through distributed shared memory, each in the same fixed order. (For the
+// 16-bit outputs the one-CTA-per-row kernel above measured faster inside the
+// replayed step: 4.34 against 4.80 ms at 8B batch 16.)
+constexpr int kNormThreads = 256;
+constexpr int kNormG = 4;          // float4 per thread: H <= 8 CTAs x 256 threads x 4 x 4
+
+__global__ void __launch_bounds__(kNormThreads) add_rmsnorm_terms_kernel(const AddNormArgs a) {
+  __shared__ float scratch[32];
+  __shared__ float part[2];        // this CTA's sum of squares, largest |y|
+  const int C = gridDim.x, c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int nv = a.H / 4, per = (nv + C - 1) / C, i0 = c * per, i1 = min(nv, i0 + per);
+  if (b >= a.B) {                  // padding rows: zero codes, scale 1 (the whole cluster)
+    for (int i = i0 + tid; i < i1; i += kNormThreads)
+      for (int tj = 0; tj < kTerms; ++tj)
+        reinterpret_cast<uint32_t*>(a.y_t + ((size_t)tj * a.rp + b) * a.H)[i] = 0u;
+    if (c == 0 && tid == 0) a.y_s[b] = 1.f;
+    return;
+  }
+  float4* __restrict__ r = reinterpret_cast<float4*>(a.r + (size_t)b * a.H);
+  const float4* __restrict__ d = reinterpret_cast<const float4*>(a.delta + (size_t)b * a.H);
+  const size_t ds = (size_t)a.delta_stride / 4;
+  float4 v[kNormG];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kNormG; ++j) {
+    const int i = i0 + tid + j * kNormThreads;
+    if (i < i1) {
+      float4 x = r[i];
+      for (int s = 0; s < a.n_delta; ++s) {
+        const float4 t = d[s * ds + i];
+        x.x += t.x; x.y += t.y; x.z += t.z; x.w += t.w;
+      }
+      v[j] = x;
+      r[i] = x;
+      ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+    }
+  }
+  float tot = block_sum(ss, scratch);
+  if (C > 1) {
+    if (tid == 0) part[0] = tot;
+    cluster_sync_all();
+    tot = 0.f;
+    for (int q = 0; q < C; ++q) tot += ld_dsmem_f32(&part[0], (uint32_t)q);
+  }
+  const float inv = 1.0f / sqrtf(tot / (float)a.H + a.eps);
+  const uint2* g2 = reinterpret_cast<const uint2*>(a.gamma);
+  float o[kNormG][4];
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < kNormG; ++j) {
+    const int i = i0 + tid + j * kNormThreads;
+    if (i < i1) {
+      const uint2 g = g2[i];
+      o[j][0] = v[j].x * inv * bf16_lo(g.x); o[j][1] = v[j].y * inv * bf16_hi(g.x);
+      o[j][2] = v[j].z * inv * bf16_lo(g.y); o[j][3] = v[j].w * inv * bf16_hi(g.y);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(o[j][e]));
+    }
+  }
+  m = block_max(m, scratch);
+  if (C > 1) {
+    if (tid == 0) part[1] = m;
+    cluster_sync_all();
+    m = 0.f;
+    for (int q = 0; q < C; ++q) m = fmaxf(m, ld_dsmem_f32(&part[1], (uint32_t)q));
+  }
+  float sc, isc;
+  term_scale(m, sc, isc);
+  if (c == 0 && tid == 0) a.y_s[b] = sc;
+#pragma unroll
+  for (int j = 0; j < kNormG; ++j) {
+    const int i = i0 + tid + j * kNormThreads;
+    if (i < i1) {
+      uint32_t cd[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) cd[e] = split_terms(o[j][e], isc);
+#pragma unroll
+      for (int tj = 0; tj < kTerms; ++tj) {
+        const uint32_t w = ((cd[0] >> (8 * tj)) & 255u) | (((cd[1] >> (8 * tj)) & 255u) << 8) |
+                           (((cd[2] >> (8 * tj)) & 255u) << 16) | (((cd[3] >> (8 * tj)) & 255u) << 24);
+        reinterpret_cast<uint32_t*>(a.y_t + ((size_t)tj * a.rp + b) * a.H)[i] = w;
+      }
+    }
+  }
+  if (C > 1) cluster_sync_all();   // no CTA leaves while the others may still read its partials
 }
 
 // One float4 per thread where the row allows it, so a CTA has the whole row
@@ -244,11 +289,18 @@ cudaError_t launch_embed_rmsnorm(const EmbedNormArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_add_rmsnorm(const AddNormArgs& a, cudaStream_t s) {
-  if (a.H % 4 || a.H > 4 * kNormMaxV * 1024) return cudaErrorInvalidValue;
   AddNormArgs args = a;
   void* p[] = {&args};
-  if (a.y_t && (!a.y_s || a.y_hl)) return cudaErrorInvalidValue;
-  const int rows = (a.y_hl || a.y_t) ? a.rp : a.B;
+  if (a.y_t) {
+    const int nv = a.H / 4;
+    const int C = std::min(8, (nv + kNormThreads - 1) / kNormThreads);
+    if (a.H % 4 || a.H < 4 || (nv + C - 1) / C > kNormThreads * kNormG || !a.y_s || a.y_hl)
+      return cudaErrorInvalidValue;
+    return launch_ex((const void*)add_rmsnorm_terms_kernel, dim3(C, a.rp), dim3(kNormThreads), 0, s, p, true, -1,
+                     C > 1 ? C : 0);
+  }
+  if (a.H % 4 || a.H > 4 * kNormMaxV * 1024 || (!a.y_hl && !a.y)) return cudaErrorInvalidValue;
+  const int rows = a.y_hl ? a.rp : a.B;
   return launch_pdl((const void*)add_rmsnorm_kernel, dim3(rows), dim3(norm_threads(a.H)), 0, s, p);
 }
 

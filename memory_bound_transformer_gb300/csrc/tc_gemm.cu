@@ -2,6 +2,8 @@
 // (looked up once through the runtime's driver entry point), the maps over
 // weights and 16-bit activation rows, and the fp32 <-> high/low row kernels the
 // kernel-level entry points use around a projection.
+#include <algorithm>
+
 #include "tcgen05.cuh"
 
 namespace mbt {
@@ -28,71 +30,86 @@ __global__ void from_hl_kernel(const uint16_t* hl, int B, int Rp, int N, float* 
 
 // Rows (fp32 x, or 16-bit high/low rows hl [2 * Rp][K]) -> four e4m3 term rows
 // t [4][Rp][K] and the rows' power-of-two scales ts[Rp] (split_terms); rows
-// B..Rp-1 get zero codes and scale 1. One CTA per row: the largest |x| first,
-// then the split (the second read of the row comes from L1/L2).
-constexpr int kTermThreads = 512;
+// B..Rp-1 get zero codes and scale 1. A row is spread over a cluster of C CTAs
+// that hold their slices in registers and exchange their largest |x| through
+// distributed shared memory, so the row is read once.
+constexpr int kTermThreads = 256;
+constexpr int kTermG = 4;          // float4 per thread: K <= 8 CTAs x 256 threads x 4 x 4
 __global__ void __launch_bounds__(kTermThreads) to_terms_kernel(const float* x, const uint16_t* hl, int f16, int B,
                                                                 int Rp, int K, uint8_t* t, float* ts) {
   __shared__ float scratch[32];
-  const int b = blockIdx.x;
+  __shared__ float part;
+  const int C = gridDim.x, c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   pdl_launch_dependents();
   pdl_wait();
-  const int n4 = K / 4;
-  if (b >= B) {
+  const int n4 = K / 4, per = (n4 + C - 1) / C, i0 = c * per, i1 = min(n4, i0 + per);
+  if (b >= B) {                    // padding rows (the whole cluster)
     for (int tj = 0; tj < kTerms; ++tj)
-      for (int i = threadIdx.x; i < n4; i += blockDim.x)
+      for (int i = i0 + tid; i < i1; i += kTermThreads)
         reinterpret_cast<uint32_t*>(t + ((size_t)tj * Rp + b) * K)[i] = 0u;
-    if (threadIdx.x == 0) ts[b] = 1.f;
+    if (c == 0 && tid == 0) ts[b] = 1.f;
     return;
   }
-  auto load4 = [&](int i, float (&v)[4]) {
-    if (x) {
-      const float4 q = reinterpret_cast<const float4*>(x + (size_t)b * K)[i];
-      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-    } else {
-      const uint2 h = reinterpret_cast<const uint2*>(hl + (size_t)b * K)[i];
-      const uint2 l = reinterpret_cast<const uint2*>(hl + (size_t)(Rp + b) * K)[i];
-      const uint32_t hw[4] = {h.x & 0xffffu, h.x >> 16, h.y & 0xffffu, h.y >> 16};
-      const uint32_t lw[4] = {l.x & 0xffffu, l.x >> 16, l.y & 0xffffu, l.y >> 16};
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        v[e] = f16 ? __half2float(__ushort_as_half((uint16_t)hw[e])) + __half2float(__ushort_as_half((uint16_t)lw[e]))
-                   : __uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16);
-    }
-  };
+  float v[kTermG][4];
   float m = 0.f;
-  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-    float v[4];
-    load4(i, v);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(v[e]));
+  for (int j = 0; j < kTermG; ++j) {
+    const int i = i0 + tid + j * kTermThreads;
+    if (i < i1) {
+      if (x) {
+        const float4 q = reinterpret_cast<const float4*>(x + (size_t)b * K)[i];
+        v[j][0] = q.x; v[j][1] = q.y; v[j][2] = q.z; v[j][3] = q.w;
+      } else {
+        const uint2 h = reinterpret_cast<const uint2*>(hl + (size_t)b * K)[i];
+        const uint2 l = reinterpret_cast<const uint2*>(hl + (size_t)(Rp + b) * K)[i];
+        const uint32_t hw[4] = {h.x & 0xffffu, h.x >> 16, h.y & 0xffffu, h.y >> 16};
+        const uint32_t lw[4] = {l.x & 0xffffu, l.x >> 16, l.y & 0xffffu, l.y >> 16};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          v[j][e] = f16 ? __half2float(__ushort_as_half((uint16_t)hw[e])) + __half2float(__ushort_as_half((uint16_t)lw[e]))
+                        : __uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(v[j][e]));
+    }
   }
   m = block_max(m, scratch);
+  if (C > 1) {
+    if (tid == 0) part = m;
+    cluster_sync_all();
+    m = 0.f;
+    for (int q = 0; q < C; ++q) m = fmaxf(m, ld_dsmem_f32(&part, (uint32_t)q));
+  }
   float sc, isc;
   term_scale(m, sc, isc);
-  if (threadIdx.x == 0) ts[b] = sc;
-  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-    float v[4];
-    load4(i, v);
-    uint32_t c[4];
+  if (c == 0 && tid == 0) ts[b] = sc;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) c[e] = split_terms(v[e], isc);
+  for (int j = 0; j < kTermG; ++j) {
+    const int i = i0 + tid + j * kTermThreads;
+    if (i < i1) {
+      uint32_t cd[4];
 #pragma unroll
-    for (int tj = 0; tj < kTerms; ++tj) {
-      const uint32_t w = ((c[0] >> (8 * tj)) & 255u) | (((c[1] >> (8 * tj)) & 255u) << 8) |
-                         (((c[2] >> (8 * tj)) & 255u) << 16) | (((c[3] >> (8 * tj)) & 255u) << 24);
-      reinterpret_cast<uint32_t*>(t + ((size_t)tj * Rp + b) * K)[i] = w;
+      for (int e = 0; e < 4; ++e) cd[e] = split_terms(v[j][e], isc);
+#pragma unroll
+      for (int tj = 0; tj < kTerms; ++tj) {
+        const uint32_t w = ((cd[0] >> (8 * tj)) & 255u) | (((cd[1] >> (8 * tj)) & 255u) << 8) |
+                           (((cd[2] >> (8 * tj)) & 255u) << 16) | (((cd[3] >> (8 * tj)) & 255u) << 24);
+        reinterpret_cast<uint32_t*>(t + ((size_t)tj * Rp + b) * K)[i] = w;
+      }
     }
   }
+  if (C > 1) cluster_sync_all();   // no CTA leaves while the others may still read its maximum
 }
 
 cudaError_t tc_to_terms(const float* x, const bf16* hl, int f16, int B, int Rp, int K, uint8_t* t, float* ts,
                         cudaStream_t s) {
-  if (K % 4 || (!x && !hl) || B < 0 || B > Rp) return cudaErrorInvalidValue;
-  void* p[] = {&x, &hl, &f16, &B, &Rp, &K, &t, &ts};
+  const int n4 = K / 4;
+  const int C = std::min(8, (n4 + kTermThreads - 1) / kTermThreads);
+  if (K % 4 || K < 4 || (!x && !hl) || B < 0 || B > Rp || (n4 + C - 1) / C > kTermThreads * kTermG)
+    return cudaErrorInvalidValue;
   const uint16_t* h16 = reinterpret_cast<const uint16_t*>(hl);
-  p[1] = &h16;
-  return launch_pdl((const void*)to_terms_kernel, dim3(Rp), dim3(kTermThreads), 0, s, p);
+  void* p[] = {&x, &h16, &f16, &B, &Rp, &K, &t, &ts};
+  return launch_ex((const void*)to_terms_kernel, dim3(C, Rp), dim3(kTermThreads), 0, s, p, true, -1, C > 1 ? C : 0);
 }
 
 cudaError_t tc_to_hl(const float* x, int B, int Rp, int K, bf16* hl, cudaStream_t s, int f16) {

@@ -92,7 +92,8 @@ template <int WT>
 __host__ __device__ __forceinline__ void ts_rings(int Rc, int& sa, int& sb) {
   using C = TsCfg<WT>;
   const int xs = C::XR * Rc * 128;
-  sa = WT == W_E4M3 ? (Rc <= 16 ? 4 : Rc <= 48 ? 3 : 2) : (Rc <= 16 ? 5 : 4);
+  sa = WT == W_E4M3 ? (Rc <= 16 ? 4 : 3) : (Rc <= 16 ? 5 : 4);
+  if (sa > C::MAXA) sa = C::MAXA;
   sb = ((int)kTsRings - sa * (int)kTsAStage) / xs;
   if (sb > C::MAXB) sb = C::MAXB;
 }
@@ -264,8 +265,10 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     pdl_wait();
     const int q = warp - DW, row = q * 32 + lane, et = tid - DW * 32;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    if (et < kTsRows) xsc_s[et] = (WT == W_E4M3 && et < Rc) ? a.x_scale[a.row0 + et] : 1.f;
-    named_bar(3, 128);
+    if (WT == W_E4M3) {                                // the term rows' scales, for the epilogue
+      if (et < kTsRows) xsc_s[et] = et < Rc ? a.x_scale[a.row0 + et] : 1.f;
+      named_bar(3, 128);
+    }
     float sum[kTsRows];
     int gi = 0;
     bool ok = true;
@@ -298,12 +301,22 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
           tmem_ld_wait16(v1);
           tmem_ld_wait16(v2);
           tmem_ld_wait16(v3);
+          if (WT == W_E4M3) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            sum[j] += __uint_as_float(v0[j]) * f;
-            if (Rc > 16) sum[16 + j] += __uint_as_float(v1[j]) * f;
-            if (Rc > 32) sum[32 + j] += __uint_as_float(v2[j]) * f;
-            if (Rc > 48) sum[48 + j] += __uint_as_float(v3[j]) * f;
+            for (int j = 0; j < 16; ++j) {
+              sum[j] += __uint_as_float(v0[j]) * f;
+              if (Rc > 16) sum[16 + j] += __uint_as_float(v1[j]) * f;
+              if (Rc > 32) sum[32 + j] += __uint_as_float(v2[j]) * f;
+              if (Rc > 48) sum[48 + j] += __uint_as_float(v3[j]) * f;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              sum[j] += __uint_as_float(v0[j]);
+              if (Rc > 16) sum[16 + j] += __uint_as_float(v1[j]);
+              if (Rc > 32) sum[32 + j] += __uint_as_float(v2[j]);
+              if (Rc > 48) sum[48 + j] += __uint_as_float(v3[j]);
+            }
           }
         }
         tc_fence_before();
@@ -374,7 +387,8 @@ tc_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         if (b0 >= Rc) break;
         named_bar(2, 128);                               // the staging buffer is free
 #pragma unroll
-        for (int i = 0; i < 32; ++i) if (b0 + i < Rc) scr[i * 128 + row] = sum[b0 + i] * (sc * xsc_s[b0 + i]);
+        for (int i = 0; i < 32; ++i)
+          if (b0 + i < Rc) scr[i * 128 + row] = sum[b0 + i] * (WT == W_E4M3 ? sc * xsc_s[b0 + i] : sc);
         named_bar(2, 128);
         const int nb = min(32, Rc - b0);
         if (EPI == EPI_PARTIAL) {

@@ -243,7 +243,7 @@ def test_gemv_full_size_sampled(cuda_lib, wt, N, K, B):
     assert np.all(np.abs(got[:, rows] - ref) <= bound)
 
 
-@pytest.mark.parametrize("H", [256, 4096, 8192, 336])
+@pytest.mark.parametrize("H", [256, 4096, 8192, 336, 5120, 1480])
 def test_norms(cuda_lib, H):
     B, V = 5, 777
     emb = _bf16_rand((V, H), 1, 0.02).to(DEV)

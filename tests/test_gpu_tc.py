@@ -1,15 +1,17 @@
 """Tensor-core (tcgen05) projections through the C ABI (op_gemm_tc for BF16
-weights, op_gemm_tc_e4m3 for e4m3 weights widened to FP16 on the way to the
-tensor core) against the oracle, and whole steps that run on them.
+weights, op_gemm_tc_e4m3 for e4m3 weights multiplied code by code) against the
+oracle, and whole steps that run on them.
 
-The activations enter as 16-bit high/low pairs (BF16: x = hi + lo to 2^-17 of
-|x|; FP16: 2^-22), the MMAs accumulate at most 512 products of a row in TMEM
-and the rest in fp32 registers, so the bound of the CUDA-core GEMV tests
-applies: |gpu - exact| <= 2e-5 * sum_k |w_k x_k| + 1e-7. The outputs are
-complete sums whatever `ksplit` says (it is accepted and ignored). A second
-test bounds the accumulation error against the output's own magnitude: the
-tensor core's fp32 accumulation truncates, and over one 28672-long chain it
-drifted 2.3e-5 of the output rms toward zero."""
+The activations enter as BF16 high/low pairs (x = hi + lo to 2^-17 of |x|) for
+BF16 weights and as four e4m3 terms with a power-of-two row scale (to 2^-16 of
+|x|, plus 2^-30 of the row's largest value) for e4m3 weights; the MMAs
+accumulate at most 512 products of a row in TMEM and the rest in fp32
+registers, so the bound of the CUDA-core GEMV tests applies: |gpu - exact| <=
+2e-5 * sum_k |w_k x_k| + 1e-7. The outputs are complete sums whatever `ksplit`
+says (it is accepted and ignored). A second test bounds the accumulation error
+against the output's own magnitude: the tensor core's fp32 accumulation
+truncates, and over one 28672-long chain it drifted 2.3e-5 of the output rms
+toward zero."""
 import numpy as np
 import pytest
 import torch
