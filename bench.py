@@ -383,7 +383,8 @@ def time_tc_swiglu(cfg, wl, B, dev, reps=3, layers=4):
     matrices. The entry-point calls are captured once in a CUDA graph and the
     graph is replayed between CUDA events, so host-side work per call (tensor
     map encoding, argument marshalling) is not in the time; the entry point's
-    fp32 -> high/low row split and act read-back kernels are (a few us)."""
+    activation split (BF16 high/low rows, or e4m3 term rows) and act
+    read-back kernels are (a few us)."""
     model = SynthModel(cfg, wl.seed + 17, device=dev, cache=False)
     mats = [model.get("w_gu", l) for l in range(min(cfg.n_layers, layers))]
     x = torch.randn((B, cfg.hidden), device=dev)
