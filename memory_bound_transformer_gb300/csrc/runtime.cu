@@ -165,7 +165,8 @@ Plan make_plan(const mbt_model* m, int R, int mbs) {
     p.ns_qkv = p.ns_o = p.ns_down = 1;
     p.g_lm = ts_tiles(EPI_ARGMAX, (int)m->h.vocab);
     const int chunks = (R + kTsMaxRows - 1) / kTsMaxRows;
-    p.kernels = 1 + (3 + 4 * chunks) * L + 2 + chunks;
+    // e4m3 weights: two term-split launches per layer (attention's and the SwiGLU's rows)
+    p.kernels = 1 + (3 + 4 * chunks + (m->wtype == W_E4M3 ? 2 : 0)) * L + 2 + chunks;
     return p;
   }
   p.ns_qkv = 1;                                          // norm prologue: whole rows per CTA

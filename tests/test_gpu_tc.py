@@ -120,6 +120,39 @@ def test_1b_batch64(cuda_lib):
     _run(case, oracle_weights(case.model), okv, 1)
 
 
+@pytest.mark.parametrize("B", [5, 20, 64])
+def test_tc8_term_split_identity(cuda_lib, B):
+    """e4m3 weights equal to the identity (code 0x38 = 1.0, scale 1): the output
+    is each activation rebuilt from its four e4m3 terms and the row's power-of-two
+    scale, which must lie within 2^-16 of |x| plus 2^-29 of the row's largest
+    value (the term split's bound), over a dynamic range of 10^-12 .. 10^3 with
+    zeros, negatives and a zero row."""
+    K = 512
+    W = torch.zeros((K, K), dtype=torch.uint8)
+    W[torch.arange(K), torch.arange(K)] = 0x38
+    W = W.to(DEV)
+    sc = torch.ones(K, device=DEV)
+    rng = np.random.default_rng(B)
+    mag = 10.0 ** rng.uniform(-12, 3, size=(B, K))
+    x = np.where(rng.random((B, K)) < 0.5, -mag, mag)
+    x[rng.random((B, K)) < 0.05] = 0.0
+    x[B // 2] = 0.0
+    xt = torch.tensor(x, dtype=torch.float32, device=DEV)
+    out = torch.full((B, K), float("nan"), device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    capi.op_gemm_tc_e4m3(capi.EPI_PARTIAL, W, sc, K, K, xt, B, 1, out=out, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    xv = xt.double().cpu().numpy()
+    got = out.double().cpu().numpy()
+    rowmax = np.abs(xv).max(axis=1, keepdims=True)
+    assert np.all(np.abs(got - xv) <= 2.0 ** -16 * np.abs(xv) + 2.0 ** -29 * rowmax)
+    assert np.all(got[B // 2] == 0.0)
+    # the bound is not loose: the split keeps more than FP16 precision but not all of fp32
+    rel = np.abs(got - xv)[xv != 0] / np.abs(xv[xv != 0])
+    assert rel.max() > 2.0 ** -24
+
+
 @pytest.mark.parametrize("B", [16, 24, 64, 128])
 @pytest.mark.parametrize("N,K,ks", [(1000, 1040, 1), (1000, 1040, 3), (6144, 4096, 3), (200, 64, 1)])
 def test_tc8_partial(cuda_lib, B, N, K, ks):
