@@ -23,9 +23,6 @@
 
 namespace mbt {
 
-#ifndef MBT_ATTN_MINB
-#define MBT_ATTN_MINB 3
-#endif
 // Fewest 64-token tiles per context split.
 #ifndef MBT_ATTN_MIN_TILES
 #define MBT_ATTN_MIN_TILES 2
@@ -43,7 +40,7 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
-template <int D, int KV8>
+template <int D, int KV8, int NT = 1, int O4 = 0>
 struct AttnShape {
   static constexpr int ESZ = KV8 ? 1 : 2;
   static constexpr int ROWB = D * ESZ;               // bytes of one token's K (or V) for one head in the cache
@@ -52,15 +49,22 @@ struct AttnShape {
   static constexpr int BNCH = BROWB / 16;            // 16-byte chunks per BF16 row (8 or 16)
   static constexpr int KSTEPS = D / 16;              // MMA k-steps over d for Q K^T
   static constexpr int MT = D / 16;                  // 16-row d tiles of O^T
-  static constexpr size_t Q_BYTES = (size_t)16 * D * 4;
   static constexpr size_t T_BYTES = (size_t)kAttnTile * BROWB;
   static constexpr size_t R_BYTES = (size_t)kAttnTile * ROWB;
-  // BF16 caches: K and V tiles double-buffered in place. e4m3 caches: three
-  // stages of raw (K, V) tiles in flight (half the bytes of a BF16 tile, so
-  // more of them to keep as many bytes moving); K is widened into MMA
-  // fragments straight from its raw tile, V into one FP16 tile.
+  // BF16 caches: K and V tiles double-buffered in place. e4m3 caches: raw
+  // (K, V) tiles in flight (half the bytes of a BF16 tile); K is widened into
+  // MMA fragments straight from its raw tile, V into one FP16 tile. The O4
+  // form of the e4m3 kernel with up to 8 query heads (one n-tile) fits four
+  // CTAs per SM (two raw stages, 8 query rows, <= 128 registers), which lets
+  // batch 64 x 8 KV heads run as one wave of single-split CTAs; small grids
+  // (batch 1-4) keep three stages, three CTAs per SM, whose deeper prologue
+  // (three tiles requested before the PDL wait) their latency wants.
+  static constexpr bool OCC4 = O4 && KV8 && NT == 1;
+  static constexpr int MINB = OCC4 ? 4 : 3;
+  static constexpr int QROWS = OCC4 ? 8 : 16;         // query rows of the tile (G <= QROWS)
+  static constexpr size_t Q_BYTES = (size_t)QROWS * D * 4;
   static constexpr int NBUF = KV8 ? 0 : 2;
-  static constexpr int NRAW = KV8 ? 3 : 0;
+  static constexpr int NRAW = KV8 ? (OCC4 ? 2 : 3) : 0;
   static constexpr int NPRO = KV8 ? NRAW : 2;          // tiles requested before the PDL wait
   static constexpr size_t SMEM = Q_BYTES + (KV8 ? T_BYTES : 2 * NBUF * T_BYTES) + (size_t)NRAW * 2 * R_BYTES;
 };
@@ -181,11 +185,26 @@ __device__ __forceinline__ void write_new_kv(const AttnArgs& a, int b, int h, in
 // before the wait on the QKV projection. The new token's row, which this CTA
 // writes after the wait, is patched into a tile already in shared memory
 // (tiles loaded later read it from the cache).
-template <int D, int KV8, int NT, int CL>
+// One element of the attention output (index oi of [B][nq * D]): fp32, and/or
+// the 16-bit high/low rows the next tensor-core projection reads.
+__device__ __forceinline__ void store_attn_out(const AttnArgs& a, size_t oi, int D, float o) {
+  if (a.out) a.out[oi] = o;
+  if (a.out_hl) {
+    const size_t row = oi / ((size_t)a.nq * D), col = oi % ((size_t)a.nq * D);
+    uint16_t* hl = reinterpret_cast<uint16_t*>(a.out_hl);
+    const float hv = a.hl_f16 ? __half2float(__float2half_rn(o)) : __bfloat162float(__float2bfloat16_rn(o));
+    hl[row * a.nq * D + col] = a.hl_f16 ? __half_as_ushort(__float2half_rn(o))
+                                        : __bfloat16_as_ushort(__float2bfloat16_rn(o));
+    hl[(a.rp_hl + row) * a.nq * D + col] = a.hl_f16 ? __half_as_ushort(__float2half_rn(o - hv))
+                                                     : __bfloat16_as_ushort(__float2bfloat16_rn(o - hv));
+  }
+}
+
+template <int D, int KV8, int NT, int CL, int O4>
 __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, int b, int h, int sp,
                                        int G, size_t head0, int seq, int blk0, int blk1, bool writer,
                                        int pos, int wblk, float2* cl_ml) {
-  using S = AttnShape<D, KV8>;
+  using S = AttnShape<D, KV8, NT, O4>;
   float* qs = reinterpret_cast<float*>(smem);                        // [16][D], rows >= G are zero
   unsigned char* kbf = smem + S::Q_BYTES;                             // BF16: [NBUF][tile][BROWB], swizzled
   unsigned char* vbf = KV8 ? kbf : kbf + S::NBUF * S::T_BYTES;        // BF16: V tiles; e4m3: the FP16 V tile
@@ -321,7 +340,7 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
   } else {
     for (int i = tid; i < G * D; i += kAttnThreads) qs[i] = a.q[head0 * D + i] * qscale;
   }
-  for (int i = G * D + tid; i < 16 * D; i += kAttnThreads) qs[i] = 0.f;
+  for (int i = G * D + tid; i < S::QROWS * D; i += kAttnThreads) qs[i] = 0.f;
   __syncthreads();                                                    // qs complete
 
   // Q^T fragments (B operand: k = d, n = query head), high and low parts, in
@@ -536,6 +555,9 @@ __device__ __forceinline__ void attend(const AttnArgs& a, unsigned char* smem, i
       // query tile, no longer needed)
       qs[hr * D + d] = acc;
       if (d == 0) cl_ml[hr] = make_float2(L > 0.f ? M : -INFINITY, L);
+    } else if (a.nsplit == 1) {
+      // one split: the output itself (the same arithmetic as the merge of one)
+      store_attn_out(a, (head0 + hr) * D + d, D, L > 0.f ? acc * (a.v_scale / L) : 0.f);
     } else {
       a.part_o[((head0 + hr) * a.nsplit + sp) * D + d] = acc;
       if (d == 0) a.part_ml[(head0 + hr) * a.nsplit + sp] = make_float2(L > 0.f ? M : -INFINITY, L);
@@ -572,18 +594,7 @@ __device__ __forceinline__ void merge_cluster(const AttnArgs& a, const float* qs
         acc += w * ov[sp];
       }
     }
-    const float o = L > 0.f ? acc * (a.v_scale / L) : 0.f;
-    const size_t oi = (head0 + hr) * D + d;
-    if (a.out) a.out[oi] = o;
-    if (a.out_hl) {                                // high/low 16-bit rows for the tensor-core GEMM
-      const size_t row = oi / ((size_t)a.nq * D), col = oi % ((size_t)a.nq * D);
-      uint16_t* hl = reinterpret_cast<uint16_t*>(a.out_hl);
-      const float hv = a.hl_f16 ? __half2float(__float2half_rn(o)) : __bfloat162float(__float2bfloat16_rn(o));
-      hl[row * a.nq * D + col] = a.hl_f16 ? __half_as_ushort(__float2half_rn(o))
-                                          : __bfloat16_as_ushort(__float2bfloat16_rn(o));
-      hl[(a.rp_hl + row) * a.nq * D + col] = a.hl_f16 ? __half_as_ushort(__float2half_rn(o - hv))
-                                                       : __bfloat16_as_ushort(__float2bfloat16_rn(o - hv));
-    }
+    store_attn_out(a, (head0 + hr) * D + d, D, L > 0.f ? acc * (a.v_scale / L) : 0.f);
   }
 }
 
@@ -595,6 +606,7 @@ __device__ __forceinline__ void merge_cluster(const AttnArgs& a, const float* qs
 // the (max, mass) pairs are read alongside; the weights then come from shared
 // memory, one warp per head.
 constexpr int kMergeMaxE = 16;     // G * D <= 16 * 128
+
 __device__ __forceinline__ void merge_splits(const AttnArgs& a, unsigned char* smem, size_t smem_bytes, int G,
                                              size_t head0, int D, int na) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -655,17 +667,7 @@ __device__ __forceinline__ void merge_splits(const AttnArgs& a, unsigned char* s
     for (; s < sc; ++s) if (wg[s] != 0.f) acc0 += wg[s] * po[(size_t)s * D];
       const float o = (acc0 + acc1) + (acc2 + acc3);
       if (!last) { run[e] = o; continue; }
-      const size_t oi = (head0 + g) * D + d;
-      if (a.out) a.out[oi] = o;
-      if (a.out_hl) {                              // high/low 16-bit rows for the tensor-core GEMM
-        const size_t row = oi / ((size_t)a.nq * D), col = oi % ((size_t)a.nq * D);
-        uint16_t* hl = reinterpret_cast<uint16_t*>(a.out_hl);
-        const float hv = a.hl_f16 ? __half2float(__float2half_rn(o)) : __bfloat162float(__float2bfloat16_rn(o));
-        hl[row * a.nq * D + col] = a.hl_f16 ? __half_as_ushort(__float2half_rn(o))
-                                            : __bfloat16_as_ushort(__float2bfloat16_rn(o));
-        hl[(a.rp_hl + row) * a.nq * D + col] = a.hl_f16 ? __half_as_ushort(__float2half_rn(o - hv))
-                                                         : __bfloat16_as_ushort(__float2bfloat16_rn(o - hv));
-      }
+      store_attn_out(a, (head0 + g) * D + d, D, o);
     }
     if (!last) {
       __syncthreads();                                               // chunk consumed
@@ -676,9 +678,9 @@ __device__ __forceinline__ void merge_splits(const AttnArgs& a, unsigned char* s
 
 // One work item: split sp of the context of (row b, KV head h), and the merge
 // of that group's splits when this is the last of them to finish.
-template <int D, int KV8, int NT, int CL>
+template <int D, int KV8, int NT, int CL, int O4>
 __device__ __forceinline__ void attn_item(const AttnArgs& a, unsigned char* smem, int sp, int h, int b) {
-  using S = AttnShape<D, KV8>;
+  using S = AttnShape<D, KV8, NT, O4>;
   const int G = a.nq / a.nkv;
   const int tid = threadIdx.x;
   const size_t head0 = (size_t)b * a.nq + (size_t)h * G;             // first query head of the group
@@ -711,17 +713,20 @@ __device__ __forceinline__ void attn_item(const AttnArgs& a, unsigned char* smem
 
   __shared__ float2 cl_ml[16];                                        // cluster merge: (max, mass) per head
   if (blk0 < nblk) {
-    attend<D, KV8, NT, CL>(a, smem, b, h, sp, G, head0, seq, blk0, blk1, writer, pos, wblk, cl_ml);
+    attend<D, KV8, NT, CL, O4>(a, smem, b, h, sp, G, head0, seq, blk0, blk1, writer, pos, wblk, cl_ml);
   } else {
     pdl_wait();
     uint32_t kc, vc;
     if (writer) write_new_kv<D, KV8>(a, b, h, pos, wblk, kc, vc);
     if (CL) {
       if (tid < G) cl_ml[tid] = make_float2(-INFINITY, 0.f);
+    } else if (a.nsplit == 1) {
+      for (int e = tid; e < G * D; e += kAttnThreads) store_attn_out(a, head0 * D + e, D, 0.f);
     } else {
       if (tid < G) a.part_ml[(head0 + tid) * a.nsplit + sp] = make_float2(-INFINITY, 0.f);
     }
   }
+  if (!CL && a.nsplit == 1) return;                                  // nothing to merge
 
   if (CL) {
     // the splits of this (row, KV head) are one cluster: merge through
@@ -754,21 +759,25 @@ __device__ __forceinline__ void attn_item(const AttnArgs& a, unsigned char* smem
 // ones finish, which already balances splits of unequal length (a persistent
 // grid claiming items from an atomic counter was measured slower: 91 vs 74 us
 // per batch-64 8B-class layer).
-template <int D, int KV8, int NT, int CL>
-__global__ void __launch_bounds__(kAttnThreads, MBT_ATTN_MINB) attn_split_kernel(const AttnArgs a) {
+template <int D, int KV8, int NT, int CL, int O4>
+__global__ void __launch_bounds__(kAttnThreads, AttnShape<D, KV8, NT, O4>::MINB) attn_split_kernel(const AttnArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   pdl_launch_dependents();
-  attn_item<D, KV8, NT, CL>(a, smem, blockIdx.x, blockIdx.y, blockIdx.z);
+  attn_item<D, KV8, NT, CL, O4>(a, smem, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
-void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nsplit) {
-  // About four CTAs per SM so that rows with long contexts do not form the
-  // tail (contexts in one batch differ by up to 8x), but at least two 64-token
-  // tiles per split so that the double buffer overlaps loads with math and
-  // the merge stays short.
-  const int target = 4 * num_sms;
+int attn_ctas_per_sm(int kv8, int G) { return kv8 && G <= 8 ? 4 : 3; }
+
+void attn_plan(int B, int nkv, int max_blocks, int num_sms, int per_sm, int* bps, int* nsplit) {
+  // Three CTAs per SM: about four CTAs per SM in all, so that rows with long
+  // contexts do not form the tail (contexts in one batch differ by up to 8x).
+  // Four per SM (e4m3 caches, up to 8 query heads): at most one wave, so that
+  // batch 64 x 8 KV heads runs one split per (row, KV head) and needs no merge
+  // (70B FP8 batch 64: 2.25 waves of two splits before). At least two 64-token
+  // tiles per split either way, so that the copies overlap the math and the
+  // merge stays short.
   const int pairs = B * nkv;
-  int want = (target + pairs - 1) / pairs;
+  int want = per_sm >= 4 ? 4 * num_sms / pairs : (4 * num_sms + pairs - 1) / pairs;
   if (want < 1) want = 1;
   int per = (max_blocks + want - 1) / want;
   const int min_per = MBT_ATTN_MIN_TILES * kAttnTile / kBlockTokens;
@@ -784,21 +793,32 @@ void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nspli
 }
 
 namespace {
-template <int D, int KV8, int NT, int CL>
-void* attn_fn() { return (void*)attn_split_kernel<D, KV8, NT, CL>; }
-template <int D, int KV8, int CL>
-void* attn_fn_nt(int nt) { return nt == 2 ? attn_fn<D, KV8, 2, CL>() : attn_fn<D, KV8, 1, CL>(); }
-template <int D, int KV8>
-void* attn_fn_cl(int nt, int cl) { return cl ? attn_fn_nt<D, KV8, 1>(nt) : attn_fn_nt<D, KV8, 0>(nt); }
+template <int D, int KV8, int NT, int CL, int O4>
+void* attn_fn() { return (void*)attn_split_kernel<D, KV8, NT, CL, O4>; }
 // query heads per KV head: up to 8 in one n-tile of the MMA, up to 16 in two;
-// cl: the splits of a (row, KV head) form one cluster
-void* attn_pick(int d, int kv8, int nt, int cl, size_t* smem) {
+// cl: the splits of a (row, KV head) form one cluster; o4: the four-per-SM
+// form (e4m3, one n-tile, no cluster)
+template <int D, int KV8, int CL>
+void* attn_fn_nt(int nt, int o4) {
+  if (nt == 2) return attn_fn<D, KV8, 2, CL, 0>();
+  return (KV8 && !CL && o4) ? attn_fn<D, KV8, 1, CL, 1>() : attn_fn<D, KV8, 1, CL, 0>();
+}
+template <int D, int KV8>
+void* attn_fn_cl(int nt, int cl, int o4) { return cl ? attn_fn_nt<D, KV8, 1>(nt, 0) : attn_fn_nt<D, KV8, 0>(nt, o4); }
+template <int D>
+size_t attn_smem_of(int kv8, int nt, int o4) {
+  if (kv8 && nt == 1 && o4) return AttnShape<D, 1, 1, 1>::SMEM;
+  return kv8 ? (nt == 2 ? AttnShape<D, 1, 2>::SMEM : AttnShape<D, 1, 1>::SMEM)
+             : (nt == 2 ? AttnShape<D, 0, 2>::SMEM : AttnShape<D, 0, 1>::SMEM);
+}
+void* attn_pick(int d, int kv8, int nt, int cl, int o4, size_t* smem) {
+  o4 = o4 && kv8 && nt == 1 && !cl;
   if (d == 64) {
-    *smem = kv8 ? AttnShape<64, 1>::SMEM : AttnShape<64, 0>::SMEM;
-    return kv8 ? attn_fn_cl<64, 1>(nt, cl) : attn_fn_cl<64, 0>(nt, cl);
+    *smem = attn_smem_of<64>(kv8, nt, o4);
+    return kv8 ? attn_fn_cl<64, 1>(nt, cl, o4) : attn_fn_cl<64, 0>(nt, cl, o4);
   }
-  *smem = kv8 ? AttnShape<128, 1>::SMEM : AttnShape<128, 0>::SMEM;
-  return kv8 ? attn_fn_cl<128, 1>(nt, cl) : attn_fn_cl<128, 0>(nt, cl);
+  *smem = attn_smem_of<128>(kv8, nt, o4);
+  return kv8 ? attn_fn_cl<128, 1>(nt, cl, o4) : attn_fn_cl<128, 0>(nt, cl, o4);
 }
 }  // namespace
 
@@ -806,18 +826,22 @@ cudaError_t attn_init() {
   for (int d : {64, 128})
     for (int kv8 = 0; kv8 < 2; ++kv8)
       for (int nt = 1; nt <= 2; ++nt)
-        for (int cl = 0; cl < 2; ++cl) {
-          size_t sm;
-          void* fn = attn_pick(d, kv8, nt, cl, &sm);
-          cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-          if (e != cudaSuccess) return e;
-        }
+        for (int cl = 0; cl < 2; ++cl)
+          for (int o4 = 0; o4 < 2; ++o4) {
+            if (o4 && !(kv8 && nt == 1 && !cl)) continue;
+            size_t sm;
+            void* fn = attn_pick(d, kv8, nt, cl, o4, &sm);
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+            // the four-per-SM form needs most of the unified L1 as shared memory
+            if (e == cudaSuccess && o4) e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+            if (e != cudaSuccess) return e;
+          }
   return cudaSuccess;
 }
 
 size_t attn_smem_bytes(int d, int kv8, int G) {
   size_t sm;
-  attn_pick(d, kv8, G > 8 ? 2 : 1, 0, &sm);
+  attn_pick(d, kv8, G > 8 ? 2 : 1, 0, 0, &sm);            // the batch-1 form
   return sm + sizeof(int) * kMaxSplitBlocks + 16;     // + the staged block ids and the ticket flag
 }
 
@@ -833,8 +857,11 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
   }
-  const int cl = a.nsplit >= 4 && a.nsplit <= kAttnCluster && a.B * a.nkv * a.nsplit <= 2 * nsm;
-  void* fn = attn_pick(a.d, a.kv_fp8, (a.nq / a.nkv) > 8 ? 2 : 1, cl, &sm);
+  const int grid = a.B * a.nkv * a.nsplit;
+  const int cl = a.nsplit >= 4 && a.nsplit <= kAttnCluster && grid <= 2 * nsm;
+  // the four-per-SM e4m3 form once three per SM would not hold the grid in one wave
+  const int o4 = grid > 3 * nsm;
+  void* fn = attn_pick(a.d, a.kv_fp8, (a.nq / a.nkv) > 8 ? 2 : 1, cl, o4, &sm);
   // the merge needs the group's weights and at least one split of partials in shared memory
   const int G = a.nq / a.nkv;
   const size_t w_bytes = (((size_t)G * a.nsplit * 8 + 15) & ~(size_t)15) + (((size_t)G * a.nsplit * 4 + 15) & ~(size_t)15);

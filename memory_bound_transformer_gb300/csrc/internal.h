@@ -210,7 +210,10 @@ struct AttnArgs {
   int carveout;             // launch carveout (percent); 0 (zero-initialised) = the default
   int no_pdl;               // ordinary launch: the previous kernel wrote this layer's cache
 };
-void attn_plan(int B, int nkv, int max_blocks, int num_sms, int* bps, int* nsplit);
+// CTAs of the attention kernel resident per SM (3, or 4 for e4m3 caches with
+// up to 8 query heads per KV head), the input of attn_plan's wave sizing.
+int attn_ctas_per_sm(int kv8, int G);
+void attn_plan(int B, int nkv, int max_blocks, int num_sms, int per_sm, int* bps, int* nsplit);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
 cudaError_t attn_init();
 size_t attn_smem_bytes(int d, int kv8, int G);   // static + dynamic shared memory of one attention CTA

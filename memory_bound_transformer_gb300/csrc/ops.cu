@@ -300,7 +300,7 @@ int op_paged_attention(int B, const float* q, int nq, int nkv, int d, const void
   a.B = B; a.q = q; a.nq = nq; a.nkv = nkv; a.d = d; a.kpool = kpool; a.vpool = vpool;
   a.kv_fp8 = kv_dtype == MBT_DTYPE_E4M3; a.k_scale = k_scale; a.v_scale = v_scale;
   a.bt = bt; a.bt_stride = bt_stride; a.seq_lens = seq_lens; a.num_blocks = num_blocks;
-  attn_plan(B, nkv, bt_stride, sm_count(), &a.bps, &a.nsplit);
+  attn_plan(B, nkv, bt_stride, sm_count(), attn_ctas_per_sm(a.kv_fp8, nq / nkv), &a.bps, &a.nsplit);
   a.out = out; a.err = err;
   const size_t heads = (size_t)B * nq * a.nsplit;
   // scratch: partial outputs, (max, sum) pairs, zeroed tickets

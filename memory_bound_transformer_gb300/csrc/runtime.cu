@@ -153,7 +153,8 @@ Plan make_plan(const mbt_model* m, int R, int mbs) {
   Plan p;
   p.R = R;
   p.mbs = mbs;
-  attn_plan(R, (int)m->h.n_kv_heads, mbs, m->num_sms, &p.attn_bps, &p.attn_nsplit);
+  attn_plan(R, (int)m->h.n_kv_heads, mbs, m->num_sms,
+            attn_ctas_per_sm(m->kv8, (int)(m->h.n_q_heads / m->h.n_kv_heads)), &p.attn_bps, &p.attn_nsplit);
   const int nb0 = std::min(R, 8);
   const int H = (int)m->h.hidden, Q = (int)(m->h.n_q_heads * m->h.head_dim), F = (int)m->h.ffn;
   const int L = (int)m->h.n_layers;

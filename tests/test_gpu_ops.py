@@ -392,6 +392,35 @@ def test_paged_attention(cuda_lib, kv, nq, nkv, d, lens):
         assert np.all(np.abs(got[b] - ref) <= 2e-5 * vmax)
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_paged_attention_one_wave_batch(cuda_lib, kv):
+    """48 rows x 8 KV heads with ~1000-token contexts: the e4m3 kernel plans one
+    wave of single-split CTAs (the output written without a merge), the BF16 one
+    two splits per (row, KV head); sampled rows against the oracle."""
+    nq, nkv, d, B = 64, 8, 128, 48
+    rng = np.random.default_rng(48)
+    lens_a = rng.integers(900, 1100, size=B).astype(np.int32)
+    nb = int(sum(-(-int(l) // 16) for l in lens_a)) + 2
+    tables = seeded_block_tables(lens_a, 16, nb, seed=5)
+    tables[tables < 0] = nb
+    cfg = ModelConfig("a", 1, 64, nq, nkv, d, 16, 16, kv_dtype=kv)
+    pool = random_kv_pool(cfg, nb, seed=9, device=DEV)
+    okv = OracleKV(kv_numpy(pool), np.array([1.0]), np.array([1.0]))
+    qd = torch.tensor(rng.normal(size=(B, nq, d)) * 0.6, dtype=torch.float32, device=DEV)
+    out = torch.zeros((B, nq * d), device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    flat = pool.view(torch.uint8).reshape(2, -1)
+    capi.op_paged_attention(qd, nkv, flat[0], flat[1], _dtype(kv), 1.0, 1.0, torch.tensor(tables, device=DEV),
+                            torch.tensor(lens_a, device=DEV), nb, out, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    got = out.double().cpu().numpy().reshape(B, nq, d)
+    for b in (0, 17, 47):
+        ref = paged_attention(qd[b].double().cpu().numpy(), okv, 0, tables[b], int(lens_a[b]))
+        vmax = np.abs(okv.decode(0, 1, tables[b][: -(-int(lens_a[b]) // 16)])).max()
+        assert np.all(np.abs(got[b] - ref) <= 2e-5 * vmax)
+
+
 def test_paged_attention_bad_seq_len(cuda_lib):
     nq, nkv, d, nb = 4, 2, 64, 4
     cfg = ModelConfig("a", 1, 64, nq, nkv, d, 16, 16)
