@@ -111,11 +111,14 @@ int op_gemm_tc(int epi, const void* W, const float* scales, int N, int K, const 
                void* stream);
 
 /* op_gemm_tc_e4m3: as op_gemm_tc for e4m3 weights W [rows][K] (codes) with
- * fp32 per-row scales (required): the codes are widened to FP16 on the way to
- * the tensor core, x is split into FP16 high/low rows, the scale is applied in
- * the epilogue ("Kernel Fusion for Large-Scale LLM Inference", section 11, FP8
- * weights and "Epilogue and dequant fusion"). K a multiple of 16, >= 64;
- * 1 <= B <= 128. */
+ * fp32 per-row scales (required): x is split internally into four e4m3 terms
+ * per value with a power-of-two scale per row (x = s (c0 + c1/16 + c2/256 +
+ * c3/4096), within 2^-16 of |x| plus 2^-29 of the row's largest value), the
+ * codes are multiplied as they are (e4m3 x e4m3 products, fp32 sums), and the
+ * row scales are applied in the epilogue ("Kernel Fusion for Large-Scale LLM
+ * Inference", section 11, FP8 weights and "Epilogue and dequant fusion"). The
+ * SWIGLU rows pass through FP16 high/low pairs before act. K a multiple of 16,
+ * >= 64; 1 <= B <= 128. */
 int op_gemm_tc_e4m3(int epi, const void* W, const float* scales, int N, int K, const float* x, int B,
                     int ksplit, float* out, float* act, float* logits, int32_t* next_ids, uint32_t* err,
                     void* stream);
