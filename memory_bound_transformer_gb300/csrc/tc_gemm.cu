@@ -8,10 +8,14 @@
 
 namespace mbt {
 
-// fp32 rows -> 16-bit (BF16, or FP16 when f16) high/low rows [2 * Rp][K] (rows B..Rp-1 zero).
+constexpr int kFromHlChunk = 1024;                 // values of a row per CTA in the two kernels below
+
+// fp32 rows -> 16-bit (BF16, or FP16 when f16) high/low rows [2 * Rp][K] (rows B..Rp-1 zero),
+// a row spread over blockIdx.y chunks of 1024 values.
 __global__ void to_hl_kernel(const float* x, int B, int Rp, int K, uint16_t* hl, int f16) {
   const int b = blockIdx.x;
-  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+  const int k1 = min(K, (int)(blockIdx.y + 1) * kFromHlChunk);
+  for (int k = blockIdx.y * kFromHlChunk + threadIdx.x; k < k1; k += blockDim.x) {
     const float v = b < B ? x[(size_t)b * K + k] : 0.f;
     store_hl16(hl + (size_t)b * K + k, hl + (size_t)(Rp + b) * K + k, v, f16);
   }
@@ -21,10 +25,12 @@ __device__ __forceinline__ float hl16_to_f32(uint16_t u, int f16) {
   return f16 ? __half2float(__ushort_as_half(u)) : __uint_as_float((uint32_t)u << 16);
 }
 
-// act[b][j] = hi + lo of the SwiGLU epilogue's high/low rows.
+// act[b][j] = hi + lo of the SwiGLU epilogue's high/low rows; a row is spread
+// over blockIdx.y chunks of 1024 values (one CTA per row left most SMs idle).
 __global__ void from_hl_kernel(const uint16_t* hl, int B, int Rp, int N, float* out, int f16) {
   const int b = blockIdx.x;
-  for (int j = threadIdx.x; j < N; j += blockDim.x)
+  const int j1 = min(N, (int)(blockIdx.y + 1) * kFromHlChunk);
+  for (int j = blockIdx.y * kFromHlChunk + threadIdx.x; j < j1; j += blockDim.x)
     out[(size_t)b * N + j] = hl16_to_f32(hl[(size_t)b * N + j], f16) + hl16_to_f32(hl[(size_t)(Rp + b) * N + j], f16);
 }
 
@@ -113,11 +119,13 @@ cudaError_t tc_to_terms(const float* x, const bf16* hl, int f16, int B, int Rp, 
 }
 
 cudaError_t tc_to_hl(const float* x, int B, int Rp, int K, bf16* hl, cudaStream_t s, int f16) {
-  to_hl_kernel<<<Rp, 256, 0, s>>>(x, B, Rp, K, reinterpret_cast<uint16_t*>(hl), f16);
+  to_hl_kernel<<<dim3(Rp, (K + kFromHlChunk - 1) / kFromHlChunk), 256, 0, s>>>(x, B, Rp, K,
+                                                                               reinterpret_cast<uint16_t*>(hl), f16);
   return cudaGetLastError();
 }
 cudaError_t tc_from_hl(const bf16* hl, int B, int Rp, int N, float* out, cudaStream_t s, int f16) {
-  from_hl_kernel<<<B, 256, 0, s>>>(reinterpret_cast<const uint16_t*>(hl), B, Rp, N, out, f16);
+  from_hl_kernel<<<dim3(B, (N + kFromHlChunk - 1) / kFromHlChunk), 256, 0, s>>>(reinterpret_cast<const uint16_t*>(hl), B,
+                                                                              Rp, N, out, f16);
   return cudaGetLastError();
 }
 
