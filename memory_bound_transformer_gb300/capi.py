@@ -137,6 +137,8 @@ def kv_alloc(model: int, num_blocks: int, mem: Optional[torch.Tensor] = None) ->
     lib = load()
     h = ctypes.c_void_p()
     _require_cuda(mem)
+    if mem is not None and mem.numel() * mem.element_size() < kv_bytes(model, num_blocks):
+        raise ValueError("kv_alloc: the caller's memory is smaller than kv_bytes(model, num_blocks)")
     _check("kv_alloc", lib.kv_alloc(model, num_blocks, _ptr(mem), ctypes.byref(h)))
     return h.value
 
